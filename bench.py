@@ -1,0 +1,389 @@
+"""Throughput benchmark of the chunkwise (Gated) DeltaNet path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input resident in
+HBM: the Gated DeltaNet forward (L2 norm, gate cumsum, Gram + UT solve, W/U, state
+scan, output, final state) on the workload B4 H16 T8192 d128 bf16 with an initial
+state, chunk 64 — or, with --workload, another of the five workloads (the
+forward+backward one runs the forward and the backward per step).
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own replica of
+the workload on its own GPU (the path shards over sequences and heads with no
+exchange), so the value is the tokens of all ranks / the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (token-by-token recurrence) on the
+host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "delta-rule chunk fwd(+bwd) tokens/s on 1 GB300; % of roofline (tensor/HBM)"
+DEFAULT_WORKLOAD = "gdn_fwd_bf16_b4h16t8192d128_h0"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_bytes(w, x) -> int:
+    """Compulsory HBM bytes of one forward: read q, k, v, beta (input dtype), g (fp32),
+    h0 (fp32 state); write o (input dtype) and the final state (fp32)."""
+    es = 2 if w.dtype == "bf16" else 4
+    tokheads = x["q"].shape[0] * x["q"].shape[1] * x["q"].shape[2]
+    d = w.d
+    n = tokheads * (3 * d * es + es + d * es)
+    if x["g"] is not None:
+        n += tokheads * 4
+    nstate = x["h0"].numel() * 4 if x["h0"] is not None else 0
+    n += nstate                                        # h0 read
+    n += (len(x["lengths"]) if x["lengths"] else x["q"].shape[0]) * x["q"].shape[1] * d * d * 4  # hT
+    return int(n)
+
+
+def algorithmic_bytes_bwd(w, x) -> int:
+    """Compulsory bytes of one backward: read q, k, v, beta, g, h0, dO, dhT; write
+    dq, dk, dv, dbeta, dg, dh0."""
+    es = 2 if w.dtype == "bf16" else 4
+    tokheads = x["q"].shape[0] * x["q"].shape[1] * x["q"].shape[2]
+    d = w.d
+    per = (4 * d * es + es) + (3 * d * es + es) + (8 if x["g"] is not None else 0)
+    nstate = x["h0"].numel() * 4 if x["h0"] is not None else 0
+    return int(tokheads * per + 3 * nstate)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clk", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunkwise_delta_rule_02_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture of this exact kernel source
+    (profiles/traffic.json), scaled to the workload; None if absent or stale."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel + "@" + workload)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def oracle_sample_fwd(x, w, items, nthreads):
+    """Run the fp64 oracle forward on `items` (batch, head) pairs of x; returns
+    (seconds, tokens) where tokens counts whole tokens (all heads of a position)."""
+    import numpy as np
+    import oracle
+    H = x["q"].shape[1]
+    f = lambda t: None if t is None else t.double().numpy()
+    if x["cu_seqlens"] is not None:
+        cu = x["cu_seqlens"].numpy().astype(np.int64)
+        seqs = sorted({s for s, _ in items})
+        t0 = time.perf_counter()
+        tok = 0
+        for s in seqs:
+            a, b = int(cu[s]), int(cu[s + 1])
+            heads = [h for ss, h in items if ss == s]
+            sl = lambda t: None if t is None else t[:, heads, a:b]
+            oracle.fwd(f(sl(x["q"])), f(sl(x["k"])), f(sl(x["v"])), f(sl(x["beta"])), f(sl(x["g"])),
+                       None, nthreads=nthreads)
+            tok += (b - a) * len(heads) / H
+        return time.perf_counter() - t0, tok
+    bs = sorted({b for b, _ in items})
+    t0 = time.perf_counter()
+    tok = 0.0
+    for b in bs:
+        heads = [h for bb, h in items if bb == b]
+        sl = lambda t: None if t is None else t[b:b + 1, heads]
+        oracle.fwd(f(sl(x["q"])), f(sl(x["k"])), f(sl(x["v"])), f(sl(x["beta"])), f(sl(x["g"])),
+                   f(sl(x["h0"])), nthreads=nthreads)
+        tok += x["q"].shape[2] * len(heads) / H
+    return time.perf_counter() - t0, tok
+
+
+def sample_items(x, n_items):
+    if x["cu_seqlens"] is not None:
+        N = x["cu_seqlens"].numel() - 1
+        H = x["q"].shape[1]
+        allitems = [(s, h) for s in range(N) for h in range(H)]
+    else:
+        allitems = [(b, h) for b in range(x["q"].shape[0]) for h in range(x["q"].shape[1])]
+    step = max(1, len(allitems) // n_items)
+    return allitems[::step][:n_items]
+
+
+def cpu_baseline(x, w, budget_items=None):
+    nthreads = os.cpu_count() or 1
+    items = sample_items(x, budget_items or max(nthreads, 16))
+    secs, tok = oracle_sample_fwd(x, w, items, nthreads)
+    return {"value": tok / secs, "unit": "tokens/s", "cores": min(nthreads, len(items)),
+            "kind": "oracle",
+            "sample": "fp64 oracle forward on %d of the workload's (sequence, head) items, whole "
+                      "sequences; tokens counted as whole tokens (items / heads)" % len(items),
+            "seconds": secs}
+
+
+def run_reference(args, w, x):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    nthreads = os.cpu_count() or 1
+    items = sample_items(x, max(nthreads, 8))
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample_fwd(x, w, items[:1], nthreads)
+    times, toks = [], 0.0
+    for _ in range(args.steps):
+        s, t = oracle_sample_fwd(x, w, items, nthreads)
+        times.append(s)
+        toks = t
+    ms = 1000.0 * sum(times) / len(times)
+    value = toks / (ms / 1000.0)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "chunk": w.chunk,
+                       "pass": "forward", "sample_items": len(items)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(nthreads, len(items)),
+                             "kind": "oracle",
+                             "sample": "per step: fp64 oracle forward on %d (sequence, head) items "
+                                       "of the workload, whole sequences" % len(items)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import torch
+    from chunkwise_delta_rule_02_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.generate(w)
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, w, x)
+        return
+
+    import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    shape = gdn.make_shape(d["q"], d["v"], w.chunk, d["cu_seqlens"])
+    ws = binding.alloc_workspace(shape, w.backward, dev)
+    o = torch.empty_like(d["v"])
+    N = shape.num_seqs if d["cu_seqlens"] is not None else w.B
+    hT = torch.empty((N, w.H, w.d, w.d), dtype=torch.float32, device=dev)
+    if w.backward:
+        grads = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]), dv=torch.empty_like(d["v"]),
+                     dbeta=torch.empty_like(d["beta"]), dg=torch.empty_like(d["g"]),
+                     dh0=torch.empty_like(d["h0"]))
+    stream = torch.cuda.current_stream(dev)
+    fast = binding.dn_uses_fast_path(shape, False) == 1
+
+    def step():
+        if d["g"] is None:
+            binding.dn_chunk_fwd(shape, d["q"], d["k"], d["v"], d["beta"], d["h0"], o, hT, ws, stream)
+        else:
+            binding.gdn_chunk_fwd(shape, d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], o, hT, ws,
+                                  stream)
+        if w.backward:
+            binding.gdn_chunk_bwd(shape, d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["do"],
+                                  d["dhT"], grads["dq"], grads["dk"], grads["dv"], grads["dbeta"],
+                                  grads["dg"], grads["dh0"], ws, stream)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    if binding.dn_device_status(ws, stream) != binding.DN_OK:
+        raise RuntimeError("device status error after warm-up")
+
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    barrier()
+    clocks = clk.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = sum(per) / len(per)
+    if pg is not None:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = w.tokens
+    value = tokens * world / (ms / 1000.0)
+
+    # end to end through the host-buffer entry point (forward workloads)
+    e2e = None
+    if not w.backward:
+        hx = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("q", "k", "v", "beta", "g", "h0")
+                  else v) for k, v in x.items()}
+        ho = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+        hhT = torch.empty((N, w.H, w.d, w.d), dtype=torch.float32).pin_memory()
+        arena = torch.empty(binding.dn_host_arena_size(shape, hx["g"] is not None, hx["h0"] is not None),
+                            dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            binding.gdn_chunk_fwd_host(shape, hx["q"], hx["k"], hx["v"], hx["beta"], hx["g"], hx["h0"], ho,
+                                       hhT, arena, ws, stream)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        t1.record(stream)
+        barrier()
+        ms_e2e = t0.elapsed_time(t1) / n_e2e
+        h2d = sum(hx[k].numel() * hx[k].element_size() for k in ("q", "k", "v", "beta", "g", "h0")
+                  if hx[k] is not None)
+        d2h = ho.numel() * ho.element_size() + hhT.numel() * hhT.element_size()
+        e2e = {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
+    pk, src = peaks()
+    abytes = algorithmic_bytes(w, x) + (algorithmic_bytes_bwd(w, x) if w.backward else 0)
+    achieved = abytes / (ms / 1000.0) / 1e9
+    kname = "gdn_fast_fwd" if fast else "general_fwd"
+    launches_per_step = (1 if fast else 3) + (1 if d["cu_seqlens"] is not None else 0)
+    if w.backward:
+        launches_per_step += 4
+    roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": recorded_traffic(kname, w.name),
+            "kernel": kname if fast else "whole step (3 general kernels)",
+            "algorithmic_bytes_per_launch": abytes, "peak_source": src}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "chunk": w.chunk,
+                       "pass": "forward+backward" if w.backward else "forward",
+                       "path": "tcgen05 fast path" if fast else "general fp32 path",
+                       "l2": "no flush: inputs %.2f GB per step > 129 MB L2" % (abytes / 1e9),
+                       "parallelism": "replicas over ranks" if world > 1 else "single GPU"},
+            "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, w)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+"""Thin ctypes binding of libgdn_gb300.so (include/gdn.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, and every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if the library is missing, or a
+call returns an error status, these functions raise.
+
+The names match the C ABI: dn_workspace_size, dn_chunk_fwd, gdn_chunk_fwd,
+gdn_chunk_bwd, dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status,
+dn_uses_fast_path.  ``forward`` / ``backward`` additionally allocate outputs
+and the workspace with torch (device memory only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from ._build import LIB
+
+DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_WORKSPACE, DN_ERR_CUDA, DN_ERR_TIMEOUT = range(6)
+DN_F32, DN_BF16 = 0, 1
+
+EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
+           "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
+           "dn_uses_fast_path"]
+
+
+class DnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
+                ("num_seqs", ctypes.c_int32), ("qk_l2norm", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (where, status_str(status), status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB
+
+
+def lib():
+    """Load libgdn_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError("libgdn_gb300.so is not built (call __graft_entry__.build() or "
+                                   "chunkwise_delta_rule_02_gb300._build.build()); there is no fallback")
+            L = ctypes.CDLL(LIB)
+            P, S, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            SP = ctypes.POINTER(DnShape)
+            L.dn_workspace_size.argtypes = [SP, I]
+            L.dn_workspace_size.restype = S
+            L.dn_uses_fast_path.argtypes = [SP, I]
+            L.dn_uses_fast_path.restype = I
+            L.dn_chunk_fwd.argtypes = [SP, P, P, P, P, P, P, P, P, S, P]
+            L.dn_chunk_fwd.restype = I
+            L.gdn_chunk_fwd.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P]
+            L.gdn_chunk_fwd.restype = I
+            L.gdn_chunk_bwd.argtypes = [SP, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
+            L.gdn_chunk_bwd.restype = I
+            L.dn_host_arena_size.argtypes = [SP, I, I]
+            L.dn_host_arena_size.restype = S
+            L.gdn_chunk_fwd_host.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P, S, P]
+            L.gdn_chunk_fwd_host.restype = I
+            L.dn_device_status.argtypes = [P, P]
+            L.dn_device_status.restype = I
+            L.dn_status_str.argtypes = [I]
+            L.dn_status_str.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_str(s: int) -> str:
+    try:
+        return lib().dn_status_str(int(s)).decode()
+    except Exception:
+        return "status %d" % s
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != DN_OK:
+        raise GdnError(rc, where)
+
+
+def make_shape(q: torch.Tensor, v: torch.Tensor, chunk: int = 64, cu_seqlens=None,
+               scale: float = 1.0, qk_l2norm: bool = True, eps: float = 1e-6) -> DnShape:
+    """Shape record for q [B,H,T,dk], v [B,H,T,dv]; cu_seqlens a device int32 tensor."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if q.dtype == torch.float32:
+        dt = DN_F32
+    elif q.dtype == torch.bfloat16:
+        dt = DN_BF16
+    else:
+        raise TypeError("q must be float32 or bfloat16")
+    s = DnShape(B, H, T, dk, dv, chunk, dt, None, 0, int(bool(qk_l2norm)), float(scale), float(eps))
+    if cu_seqlens is not None:
+        s.cu_seqlens = _p(cu_seqlens)
+        s.num_seqs = int(cu_seqlens.numel()) - 1
+    return s
+
+
+def dn_workspace_size(shape: DnShape, for_backward: bool = False) -> int:
+    return int(lib().dn_workspace_size(ctypes.byref(shape), int(bool(for_backward))))
+
+
+def dn_uses_fast_path(shape: DnShape, for_backward: bool = False) -> int:
+    return int(lib().dn_uses_fast_path(ctypes.byref(shape), int(bool(for_backward))))
+
+
+def dn_host_arena_size(shape: DnShape, gated: bool, with_h0: bool) -> int:
+    return int(lib().dn_host_arena_size(ctypes.byref(shape), int(gated), int(with_h0)))
+
+
+def dn_chunk_fwd(shape, q, k, v, beta, h0, o, hT, ws, stream=None):
+    rc = lib().dn_chunk_fwd(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(h0), _p(o),
+                            _p(hT), _p(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "dn_chunk_fwd")
+
+
+def gdn_chunk_fwd(shape, q, k, v, beta, g, h0, o, hT, ws, stream=None):
+    rc = lib().gdn_chunk_fwd(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g), _p(h0),
+                             _p(o), _p(hT), _p(ws), ws.numel() * ws.element_size(),
+                             _stream(stream))
+    _check(rc, "gdn_chunk_fwd")
+
+
+def gdn_chunk_bwd(shape, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws,
+                  stream=None):
+    rc = lib().gdn_chunk_bwd(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g), _p(h0),
+                             _p(dO), _p(dhT), _p(dq), _p(dk), _p(dv), _p(dbeta), _p(dg),
+                             _p(dh0), _p(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "gdn_chunk_bwd")
+
+
+def gdn_chunk_fwd_host(shape, q, k, v, beta, g, h0, o, hT, arena, ws, stream=None):
+    """Host (pinned CPU) tensors in and out; arena and ws are device tensors."""
+    rc = lib().gdn_chunk_fwd_host(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g),
+                                  _p(h0), _p(o), _p(hT), _p(arena),
+                                  arena.numel() * arena.element_size(), _p(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "gdn_chunk_fwd_host")
+
+
+def dn_device_status(ws, stream=None) -> int:
+    return int(lib().dn_device_status(_p(ws), _stream(stream)))
+
+
+def alloc_workspace(shape: DnShape, for_backward: bool, device) -> torch.Tensor:
+    n = dn_workspace_size(shape, for_backward)
+    if n == 0:
+        raise GdnError(DN_ERR_INVALID_ARG, "dn_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _nseq(q, cu_seqlens):
+    return q.shape[0] if cu_seqlens is None else int(cu_seqlens.numel()) - 1
+
+
+def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0,
+            qk_l2norm=True, eps=1e-6, want_state=True, ws=None):
+    """Allocate o (and hT) and run gdn_chunk_fwd / dn_chunk_fwd.  Returns (o, hT)."""
+    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps)
+    o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    N = _nseq(q, cu_seqlens)
+    hT = torch.empty((N, q.shape[1], q.shape[-1], v.shape[-1]), dtype=torch.float32,
+                     device=q.device) if want_state else None
+    if ws is None:
+        ws = alloc_workspace(shape, False, q.device)
+    if g is None:
+        dn_chunk_fwd(shape, q, k, v, beta, h0, o, hT, ws)
+    else:
+        gdn_chunk_fwd(shape, q, k, v, beta, g, h0, o, hT, ws)
+    return o, hT
+
+
+def backward(q, k, v, beta, g, h0, dO, dhT, cu_seqlens=None, chunk=64, scale=1.0,
+             qk_l2norm=True, eps=1e-6, ws=None):
+    """Allocate the gradients and run gdn_chunk_bwd.  Returns a dict."""
+    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps)
+    out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+               dbeta=torch.empty_like(beta),
+               dg=torch.empty_like(g) if g is not None else None,
+               dh0=torch.empty((_nseq(q, cu_seqlens), q.shape[1], q.shape[-1], v.shape[-1]),
+                               dtype=torch.float32, device=q.device))
+    if ws is None:
+        ws = alloc_workspace(shape, True, q.device)
+    gdn_chunk_bwd(shape, q, k, v, beta, g, h0, dO, dhT, out["dq"], out["dk"], out["dv"],
+                  out["dbeta"], out["dg"], out["dh0"], ws)
+    return out

@@ -1,0 +1,334 @@
+// C ABI of libgdn_gb300.so: argument validation, workspace layout, dispatch
+// between the tcgen05 fast path and the general fp32 path, host-buffer entry
+// point and the device status word.
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "fast.h"
+#include "general.h"
+
+namespace gdn {
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool is_aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validates the shape; on success fills the geometry (without device pointers).
+dn_status check_shape(const dn_shape *s, Geo *g)
+{
+    if (!s) return DN_ERR_INVALID_ARG;
+    if (s->B < 1 || s->H < 1 || s->T < 0 || s->dk < 1 || s->dv < 1) return DN_ERR_INVALID_ARG;
+    if (s->dtype != DN_F32 && s->dtype != DN_BF16) return DN_ERR_INVALID_ARG;
+    if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return DN_ERR_UNSUPPORTED;
+    if (s->dk > kMaxD || s->dv > kMaxD) return DN_ERR_UNSUPPORTED;
+    if (!(s->eps >= 0.f) || !(s->scale == s->scale)) return DN_ERR_INVALID_ARG;
+    if (s->cu_seqlens) {
+        if (s->B != 1 || s->num_seqs < 0) return DN_ERR_INVALID_ARG;
+        if ((uintptr_t)s->cu_seqlens & 3u) return DN_ERR_INVALID_ARG;
+    }
+    // keep every element index inside 63 bits comfortably
+    double elems = (double)s->B * s->H * (double)(s->T + 1) * (s->dk > s->dv ? s->dk : s->dv);
+    if (elems > 4.0e15) return DN_ERR_INVALID_ARG;
+    Geo x;
+    memset(&x, 0, sizeof(x));
+    x.B = s->B; x.H = s->H; x.T = s->T; x.dk = s->dk; x.dv = s->dv; x.C = s->chunk;
+    x.varlen = s->cu_seqlens != nullptr;
+    x.N = x.varlen ? s->num_seqs : s->B;
+    x.NC = x.varlen ? (s->T + x.C - 1) / x.C + x.N : x.B * ((s->T + x.C - 1) / x.C);
+    x.l2norm = s->qk_l2norm != 0;
+    x.scale = s->scale;
+    x.eps = s->eps;
+    x.cu = s->cu_seqlens;
+    *g = x;
+    return DN_OK;
+}
+
+struct Layout {
+    size_t status, cstart, fast;
+    size_t Kn, Qn, W, U, Unew, Tm, gam, Sin, dSo, dUn, dQ, dK, dW;
+    size_t total;
+};
+
+Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast)
+{
+    Layout L;
+    memset(&L, 0, sizeof(L));
+    size_t off = 0;
+    L.status = off; off += 256;
+    L.cstart = off; off += align256(sizeof(int32_t) * (size_t)(g.N + 1));
+    if (fast && !for_backward) {
+        L.fast = off; off += align256(fast::workspace_bytes(g));
+        L.total = off;
+        return L;
+    }
+    const size_t slots = (size_t)g.NC * g.H, C = g.C, dk = g.dk, dv = g.dv;
+    auto take = [&](size_t nfloat) { size_t o = off; off += align256(nfloat * sizeof(float)); return o; };
+    L.Kn = take(slots * C * dk);
+    L.Qn = take(slots * C * dk);
+    L.W = take(slots * C * dk);
+    L.U = take(slots * C * dv);
+    L.Unew = take(slots * C * dv);
+    L.Tm = take(slots * C * C);
+    L.gam = take(slots * C);
+    L.Sin = take(slots * dk * dv);
+    if (for_backward) {
+        L.dSo = take(slots * dk * dv);
+        L.dUn = take(slots * C * dv);
+        L.dQ = take(slots * C * dk);
+        L.dK = take(slots * C * dk);
+        L.dW = take(slots * C * dk);
+    }
+    (void)s;
+    L.total = off;
+    return L;
+}
+
+gen::Ws general_ws(const Layout &L, char *base)
+{
+    gen::Ws w;
+    auto F = [&](size_t o) { return o ? (float *)(base + o) : (float *)nullptr; };
+    w.Kn = F(L.Kn); w.Qn = F(L.Qn); w.W = F(L.W); w.U = F(L.U); w.Unew = F(L.Unew);
+    w.Tm = F(L.Tm); w.gam = F(L.gam); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
+    w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
+    return w;
+}
+
+// First chunk slot of every packed sequence; flags malformed offsets (which are
+// then treated as empty sequences) in the status word.
+__global__ void k_cstart(const int32_t *cu, int N, int T, int C, int32_t *cstart, uint32_t *status)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    bool ok = cu[0] == 0 && cu[N] == T;
+    for (int s = 0; s < N && ok; ++s) ok = cu[s + 1] >= cu[s];
+    int acc = 0;
+    cstart[0] = 0;
+    for (int s = 0; s < N; ++s) {
+        int L = ok ? cu[s + 1] - cu[s] : 0;
+        acc += (L + C - 1) / C;
+        cstart[s + 1] = acc;
+    }
+    if (!ok) raise_status(status, kStatusBadOffsets);
+}
+
+// GDN_FORCE_GENERAL=1 in the environment routes every call to the general fp32
+// kernels (used by the tests to compare the two kernel families).
+bool force_general()
+{
+    const char *e = getenv("GDN_FORCE_GENERAL");
+    return e && e[0] && e[0] != '0';
+}
+
+bool fast_ok(const dn_shape *s, const Geo &g, int for_backward)
+{
+    return !for_backward && !force_general() && fast::supports(g, s->dtype);
+}
+
+dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size_t ws_bytes,
+                     cudaStream_t st, Layout &L, bool &fast)
+{
+    fast = fast_ok(s, g, for_backward);
+    L = make_layout(g, s, for_backward, fast);
+    if (!ws || !is_aligned16(ws)) return DN_ERR_WORKSPACE;
+    if (ws_bytes < L.total) return DN_ERR_WORKSPACE;
+    char *base = (char *)ws;
+    if (cudaMemsetAsync(base + L.status, 0, sizeof(uint32_t), st) != cudaSuccess) return DN_ERR_CUDA;
+    if (g.varlen) {
+        g.cstart = (const int32_t *)(base + L.cstart);
+        k_cstart<<<1, 32, 0, st>>>(g.cu, g.N, g.T, g.C, (int32_t *)(base + L.cstart),
+                                   (uint32_t *)(base + L.status));
+        if (cudaPeekAtLastError() != cudaSuccess) return DN_ERR_CUDA;
+    }
+    return DN_OK;
+}
+
+dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *v,
+                   const void *beta, const float *gate, const float *h0, void *o, float *hT,
+                   void *ws, size_t ws_bytes, void *stream)
+{
+    Geo g;
+    dn_status rc = check_shape(s, &g);
+    if (rc != DN_OK) return rc;
+    const bool any = g.T > 0;
+    if (any && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, gate, h0, o, hT};
+    for (const void *p : ptrs)
+        if (p && !is_aligned16(p)) return DN_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    Layout L;
+    bool fast;
+    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast)) != DN_OK) return rc;
+    char *base = (char *)ws;
+    cudaError_t e;
+    if (fast) {
+        e = fast::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                      (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
+                      (__nv_bfloat16 *)o, hT, base + L.fast, (uint32_t *)(base + L.status), st);
+    } else {
+        gen::Ws w = general_ws(L, base);
+        if (s->dtype == DN_F32)
+            e = gen::fwd<float>(g, (const float *)q, (const float *)k, (const float *)v,
+                                (const float *)beta, gate, h0, (float *)o, hT, w, st);
+        else
+            e = gen::fwd<__nv_bfloat16>(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                                        (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta,
+                                        gate, h0, (__nv_bfloat16 *)o, hT, w, st);
+    }
+    return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+size_t dn_workspace_size(const dn_shape *shape, int for_backward)
+{
+    Geo g;
+    if (check_shape(shape, &g) != DN_OK) return 0;
+    bool fast = fast_ok(shape, g, for_backward);
+    return make_layout(g, shape, for_backward, fast).total;
+}
+
+int dn_uses_fast_path(const dn_shape *shape, int for_backward)
+{
+    Geo g;
+    if (check_shape(shape, &g) != DN_OK) return -1;
+    return fast_ok(shape, g, for_backward) ? 1 : 0;
+}
+
+dn_status dn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                       const void *beta, const float *h0, void *o, float *hT, void *ws,
+                       size_t ws_bytes, void *stream)
+{
+    return fwd_impl(shape, q, k, v, beta, nullptr, h0, o, hT, ws, ws_bytes, stream);
+}
+
+dn_status gdn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *beta, const float *g, const float *h0, void *o, float *hT,
+                        void *ws, size_t ws_bytes, void *stream)
+{
+    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, ws_bytes, stream);
+}
+
+dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *beta, const float *gate, const float *h0, const void *dO,
+                        const float *dhT, void *dq, void *dk, void *dv, void *dbeta, float *dg,
+                        float *dh0, void *ws, size_t ws_bytes, void *stream)
+{
+    Geo g;
+    dn_status rc = check_shape(shape, &g);
+    if (rc != DN_OK) return rc;
+    if (dg && !gate) return DN_ERR_INVALID_ARG;
+    if (g.T > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
+        return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, gate, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0};
+    for (const void *p : ptrs)
+        if (p && !is_aligned16(p)) return DN_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    Layout L;
+    bool fast;
+    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, fast)) != DN_OK) return rc;
+    gen::Ws w = general_ws(L, (char *)ws);
+    cudaError_t e;
+    if (shape->dtype == DN_F32)
+        e = gen::bwd<float>(g, (const float *)q, (const float *)k, (const float *)v,
+                            (const float *)beta, gate, h0, (const float *)dO, dhT, (float *)dq,
+                            (float *)dk, (float *)dv, (float *)dbeta, dg, dh0, w, st);
+    else
+        e = gen::bwd<__nv_bfloat16>(
+            g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
+            (const __nv_bfloat16 *)beta, gate, h0, (const __nv_bfloat16 *)dO, dhT,
+            (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
+            (__nv_bfloat16 *)dbeta, dg, dh0, w, st);
+    return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+size_t dn_host_arena_size(const dn_shape *s, int gated, int with_h0)
+{
+    Geo g;
+    if (check_shape(s, &g) != DN_OK) return 0;
+    const size_t es = s->dtype == DN_BF16 ? 2 : 4;
+    const size_t tok = (size_t)g.B * g.H * g.T;
+    const size_t st = (size_t)g.N * g.H * g.dk * g.dv * sizeof(float);
+    size_t n = 0;
+    n += align256(tok * g.dk * es) * 2;           // q, k
+    n += align256(tok * g.dv * es) * 2;           // v, o
+    n += align256(tok * es);                      // beta
+    if (gated) n += align256(tok * sizeof(float));
+    if (with_h0) n += align256(st);
+    n += align256(st);                            // hT
+    return n;
+}
+
+dn_status gdn_chunk_fwd_host(const dn_shape *s, const void *q, const void *k, const void *v,
+                             const void *beta, const float *gate, const float *h0, void *o,
+                             float *hT, void *arena, size_t arena_bytes, void *ws,
+                             size_t ws_bytes, void *stream)
+{
+    Geo g;
+    dn_status rc = check_shape(s, &g);
+    if (rc != DN_OK) return rc;
+    if (!arena || !is_aligned16(arena)) return DN_ERR_INVALID_ARG;
+    if (arena_bytes < dn_host_arena_size(s, gate != nullptr, h0 != nullptr)) return DN_ERR_INVALID_ARG;
+    if (g.T > 0 && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t es = s->dtype == DN_BF16 ? 2 : 4;
+    const size_t tok = (size_t)g.B * g.H * g.T;
+    const size_t sbytes = (size_t)g.N * g.H * g.dk * g.dv * sizeof(float);
+    char *p = (char *)arena;
+    auto carve = [&](size_t bytes) { char *r = p; p += align256(bytes); return r; };
+    char *dq = carve(tok * g.dk * es), *dk = carve(tok * g.dk * es);
+    char *dvv = carve(tok * g.dv * es), *dout = carve(tok * g.dv * es);
+    char *db = carve(tok * es);
+    char *dgate = gate ? carve(tok * sizeof(float)) : nullptr;
+    char *dh0 = h0 ? carve(sbytes) : nullptr;
+    char *dhT = carve(sbytes);
+    struct { void *dst; const void *src; size_t n; } cp[] = {
+        {dq, q, tok * g.dk * es}, {dk, k, tok * g.dk * es}, {dvv, v, tok * g.dv * es},
+        {db, beta, tok * es}, {dgate, gate, tok * sizeof(float)}, {dh0, h0, sbytes}};
+    for (auto &c : cp) {
+        if (!c.dst || !c.src || c.n == 0) continue;
+        if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return DN_ERR_CUDA;
+    }
+    rc = fwd_impl(s, dq, dk, dvv, db, (const float *)dgate, (const float *)dh0, dout,
+                  (float *)dhT, ws, ws_bytes, stream);
+    if (rc != DN_OK) return rc;
+    if (o && tok && cudaMemcpyAsync(o, dout, tok * g.dv * es, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return DN_ERR_CUDA;
+    if (hT && sbytes && cudaMemcpyAsync(hT, dhT, sbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return DN_ERR_CUDA;
+    return DN_OK;
+}
+
+dn_status dn_device_status(void *ws, void *stream)
+{
+    if (!ws) return DN_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DN_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DN_ERR_CUDA;
+    if (word == 0) return DN_OK;
+    if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return DN_ERR_CUDA;
+    if (word & kStatusTimeout) return DN_ERR_TIMEOUT;
+    return DN_ERR_INVALID_ARG;
+}
+
+const char *dn_status_str(dn_status s)
+{
+    switch (s) {
+    case DN_OK: return "ok";
+    case DN_ERR_INVALID_ARG: return "invalid argument";
+    case DN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case DN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DN_ERR_CUDA: return "CUDA error";
+    case DN_ERR_TIMEOUT: return "a bounded device wait ran out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// Host launchers of the general (fp32 CUDA-core) chunk kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace gdn {
+namespace gen {
+
+// Workspace arrays, all float32, indexed by slot = chunk_slot * H + head.
+struct Ws {
+    float *Kn, *Qn, *W;        // [slots][C][dk]  normalised K, Q; WY factor W
+    float *U, *Unew;           // [slots][C][dv]
+    float *Tm;                 // [slots][C][C]   UT transform T
+    float *gam;                // [slots][C]      within-chunk cumulative log-gate
+    float *Sin;                // [slots][dk][dv] state entering the chunk
+    float *dSo, *dUn;          // backward: dS leaving the chunk, dUnew
+    float *dQ, *dK, *dW;       // backward scratch [slots][C][dk]
+};
+
+template <class Tin>
+cudaError_t fwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,
+                const float *gate, const float *h0, Tin *o, float *hT, const Ws &w,
+                cudaStream_t st);
+
+template <class Tin>
+cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,
+                const float *gate, const float *h0, const Tin *dO, const float *dhT, Tin *dq,
+                Tin *dk, Tin *dv, Tin *dbeta, float *dg, float *dh0, const Ws &w,
+                cudaStream_t st);
+
+}  // namespace gen
+}  // namespace gdn

@@ -1,0 +1,146 @@
+/*
+ * gdn.h — C ABI of libgdn_gb300.so: chunkwise-parallel DeltaNet and Gated
+ * DeltaNet on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence and head, state S stored d_k x d_v, key index
+ * outer):
+ *     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ * — "Gated DeltaNet: Improving Mamba2 with Delta Rule", rebuttal Table 1,
+ * rows "DeltaNet" (alpha_t = 1) and "Gated DeltaNet" (there written with the
+ * d_v x d_k transpose, S_t = S_{t-1}(alpha_t(I - beta_t k_t k_t^T)) +
+ * beta_t v_t k_t^T).  alpha_t = exp(g_t) for a per-token, per-head log-gate g.
+ * q and k are L2-normalised per token inside the kernels when
+ * shape->qk_l2norm is set: x / sqrt(sum x^2 + eps).
+ *
+ * The kernels evaluate it chunk by chunk ("Parallelizing Linear Transformers
+ * with the Delta Rule over Sequence Length": WY representation of the
+ * Householder-like products, chunkwise parallel form; GDN page: the same
+ * algorithm extended with gating).  Per chunk of C tokens, with gamma the
+ * within-chunk cumulative log-gate and D_ri = exp(gamma_r - gamma_i):
+ *     T = (I + strict_lower(diag(beta)(K K^T o D)))^-1 diag(beta)
+ *     W = T diag(exp gamma) K,  U = T V,  Unew = U - W S
+ *     O = diag(exp gamma) Q S + lower(Q K^T o D) Unew
+ *     S <- exp(gamma_C) S + (diag(exp(gamma_C - gamma)) K)^T Unew
+ *
+ * Layouts.  Token arrays are [B][H][T][d] row-major (time axis of one batch
+ * row and head contiguous); beta, g are [B][H][T]; states are
+ * [N][H][dk][dv] float32 where N = B, or the number of packed sequences.
+ * Packed variable-length input: B == 1, T = total tokens,
+ * shape->cu_seqlens = device int32 offsets [num_seqs + 1] (first 0, last T,
+ * non-decreasing); chunks never cross a sequence boundary.
+ *
+ * Dtypes.  shape->dtype fixes q, k, v, beta, o (forward) and dO, dq, dk, dv,
+ * dbeta (backward): DN_F32 (float) or DN_BF16 (bfloat16).  g, h0, hT, dhT,
+ * dg, dh0 are always float32.  Arithmetic is float32 (bf16 tensor-core
+ * operands with float32 accumulation on the bf16 fast path).
+ *
+ * Ownership.  The caller owns every buffer and the stream; the library
+ * allocates nothing, keeps no state between calls and never synchronises
+ * the stream (except dn_device_status, which says so).  All device pointers
+ * must be 16-byte aligned.  Calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL = legacy default stream).
+ *
+ * Errors.  Every entry point returns a dn_status and never aborts or throws.
+ * Argument errors are found on the host before anything is launched.  Launch
+ * errors return DN_ERR_CUDA.  Every device-side wait in the kernels is
+ * bounded; a wait that runs out records DN_ERR_TIMEOUT in the workspace's
+ * status word, which dn_device_status reads back.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DN_OK = 0,
+    DN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad sizes or offsets */
+    DN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. dk > 128)     */
+    DN_ERR_WORKSPACE = 3,     /* ws == NULL or ws_bytes < dn_workspace_size     */
+    DN_ERR_CUDA = 4,          /* a CUDA call or kernel launch failed            */
+    DN_ERR_TIMEOUT = 5        /* a bounded device wait ran out (see above)      */
+} dn_status;
+
+typedef enum { DN_F32 = 0, DN_BF16 = 1 } dn_dtype;
+
+typedef struct {
+    int32_t B, H, T;              /* batch rows, heads, tokens per row (packed: B = 1) */
+    int32_t dk, dv;               /* head dims, 1..128                                  */
+    int32_t chunk;                /* C: 16, 32 or 64 (64 is the tuned size)             */
+    int32_t dtype;                /* dn_dtype                                           */
+    const int32_t *cu_seqlens;    /* device, [num_seqs + 1], or NULL for fixed length   */
+    int32_t num_seqs;             /* packed sequences (ignored when cu_seqlens == NULL) */
+    int32_t qk_l2norm;            /* 1: normalise q and k per token inside the kernels  */
+    float scale;                  /* o = scale * S^T q                                  */
+    float eps;                    /* normalisation epsilon (1e-6 is the default)        */
+} dn_shape;
+
+/* Bytes of device workspace the calls below need for `shape` (0 on bad
+ * arguments).  for_backward = 1 sizes it for gdn_chunk_bwd. */
+size_t dn_workspace_size(const dn_shape *shape, int for_backward);
+
+/* DeltaNet forward (alpha = 1; Table 1 row "DeltaNet").
+ *   q, k [B,H,T,dk], v [B,H,T,dv], beta [B,H,T]   (dtype)
+ *   h0   [N,H,dk,dv] float32 initial state, NULL = zero
+ *   o    [B,H,T,dv] (dtype) output
+ *   hT   [N,H,dk,dv] float32 final state, NULL = not written
+ *   ws   device workspace of ws_bytes >= dn_workspace_size(shape, 0)      */
+dn_status dn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                       const void *beta, const float *h0, void *o, float *hT, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Gated DeltaNet forward (Table 1 row "Gated DeltaNet"): as dn_chunk_fwd plus
+ *   g [B,H,T] float32 log-gate, alpha = exp(g); g must be <= 0 (alpha <= 1).
+ *   g == NULL is the same as g = 0 (alpha = 1).                               */
+dn_status gdn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *beta, const float *g, const float *h0, void *o,
+                        float *hT, void *ws, size_t ws_bytes, void *stream);
+
+/* Gated DeltaNet backward: gradients of L = <o, dO> + <hT, dhT>.
+ * Recomputes the chunk states from q, k, v, beta, g, h0 (chunk states are
+ * recomputed in the backward rather than kept — DeltaNet page, reply Q2).
+ *   dO  [B,H,T,dv] (dtype), dhT [N,H,dk,dv] float32 or NULL (= 0)
+ *   dq, dk [B,H,T,dk], dv [B,H,T,dv], dbeta [B,H,T]   (dtype), with respect to
+ *   the raw q and k given (chained through the normalisation)
+ *   dg  [B,H,T] float32 or NULL (not written; must be NULL when g is NULL)
+ *   dh0 [N,H,dk,dv] float32 or NULL (not written)
+ *   ws  >= dn_workspace_size(shape, 1) bytes                                   */
+dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *beta, const float *g, const float *h0, const void *dO,
+                        const float *dhT, void *dq, void *dk, void *dv, void *dbeta,
+                        float *dg, float *dh0, void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of the device staging arena gdn_chunk_fwd_host needs (0 on bad args). */
+size_t dn_host_arena_size(const dn_shape *shape, int gated, int with_h0);
+
+/* Gated DeltaNet forward on HOST buffers: copies q, k, v, beta, g, h0 (host,
+ * pinned for asynchronous copies) into `arena` (device, >= dn_host_arena_size
+ * bytes), runs gdn_chunk_fwd on `stream`, and copies o and hT back into the
+ * host buffers.  Returns once the work is enqueued: synchronise `stream`
+ * before reading o / hT.  g, h0, hT may be NULL as in gdn_chunk_fwd; for
+ * packed input shape->cu_seqlens must still be a DEVICE pointer.            */
+dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k,
+                             const void *v, const void *beta, const float *g,
+                             const float *h0, void *o, float *hT, void *arena,
+                             size_t arena_bytes, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the status word that bounded
+ * device waits write into `ws` (DN_OK or DN_ERR_TIMEOUT). */
+dn_status dn_device_status(void *ws, void *stream);
+
+/* Static description of a status code. */
+const char *dn_status_str(dn_status s);
+
+/* Which kernel family `shape` runs on: 1 = tcgen05/TMA fast path, 0 = the
+ * general fp32 path, -1 = invalid shape.  for_backward as above. */
+int dn_uses_fast_path(const dn_shape *shape, int for_backward);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_GB300_H */

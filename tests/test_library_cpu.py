@@ -1,0 +1,111 @@
+"""Host-side checks that need no GPU: the C ABI library loads, exports every
+function include/gdn.h declares, sizes its workspace, and rejects bad arguments
+with a status code before touching the device.  Also the seeded input
+generators."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    import __graft_entry__
+    __graft_entry__.build()
+    from chunkwise_delta_rule_02_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z][a-z0-9_]+)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd", "dn_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(gdn):
+    lib = ctypes.CDLL(gdn.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    for name in gdn.EXPORTS:
+        assert hasattr(lib, name), name
+
+
+def _shape(gdn, B=2, H=3, T=100, d=64, dtype=1, chunk=64, cu=None, N=0):
+    s = gdn.DnShape(B, H, T, d, d, chunk, dtype, cu, N, 1, 1.0, 1e-6)
+    return s
+
+
+def test_workspace_size_and_validation(gdn):
+    s = _shape(gdn)
+    n_f = gdn.dn_workspace_size(s, False)
+    n_b = gdn.dn_workspace_size(s, True)
+    assert 0 < n_f < n_b
+    assert n_f % 256 == 0
+    bad = [_shape(gdn, B=0), _shape(gdn, d=129), _shape(gdn, chunk=48), _shape(gdn, dtype=7),
+           _shape(gdn, H=0), _shape(gdn, T=-1)]
+    for b in bad:
+        assert gdn.dn_workspace_size(b, False) == 0
+        assert gdn.dn_uses_fast_path(b, False) == -1
+    assert gdn.dn_workspace_size(_shape(gdn, B=2, cu=16, N=3), False) == 0   # packed needs B == 1
+    assert gdn.dn_workspace_size(_shape(gdn, B=1, cu=16, N=3), False) > 0
+
+
+def test_status_codes_without_device_work(gdn):
+    L = gdn.lib()
+    s = _shape(gdn)
+    # null shape
+    assert L.gdn_chunk_fwd(None, 16, 16, 16, 16, None, None, 16, None, 16, 1 << 40, None) == gdn.DN_ERR_INVALID_ARG
+    # null input pointer
+    assert L.gdn_chunk_fwd(ctypes.byref(s), None, 16, 16, 16, None, None, 16, None, 16, 1 << 40, None) == gdn.DN_ERR_INVALID_ARG
+    # misaligned pointer
+    assert L.gdn_chunk_fwd(ctypes.byref(s), 18, 16, 16, 16, None, None, 16, None, 16, 1 << 40, None) == gdn.DN_ERR_INVALID_ARG
+    # workspace missing / too small
+    assert L.gdn_chunk_fwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, None, 0, None) == gdn.DN_ERR_WORKSPACE
+    assert L.gdn_chunk_fwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, 16, 64, None) == gdn.DN_ERR_WORKSPACE
+    # unsupported head dim
+    s2 = _shape(gdn, d=256)
+    assert L.dn_chunk_fwd(ctypes.byref(s2), 16, 16, 16, 16, None, 16, None, 16, 1 << 40, None) == gdn.DN_ERR_UNSUPPORTED
+    # backward: dg without g
+    assert L.gdn_chunk_bwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, 16, 16, 16, 16,
+                           16, None, 16, 1 << 40, None) == gdn.DN_ERR_INVALID_ARG
+    for code in range(6):
+        assert gdn.status_str(code)
+
+
+def test_workloads_are_seeded_and_shaped():
+    from chunkwise_delta_rule_02_gb300 import workloads as W
+    for name, w in W.WORKLOADS.items():
+        x = W.generate(w, B=1 if not w.varlen_total else None, H=2, T=70 if not w.varlen_total else None,
+                       lengths=[5, 70, 0, 9] if w.varlen_total else None)
+        y = W.generate(w, B=1 if not w.varlen_total else None, H=2, T=70 if not w.varlen_total else None,
+                       lengths=[5, 70, 0, 9] if w.varlen_total else None)
+        for key in ("q", "k", "v", "beta", "g", "h0", "do", "dhT"):
+            if x[key] is not None:
+                assert torch.equal(x[key], y[key]), (name, key)
+        assert (x["g"] is not None) == w.gated
+        if x["g"] is not None:
+            assert float(x["g"].max()) < 0.0
+        want = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        assert x["q"].dtype == want and x["beta"].dtype == want
+    lens = W.varlen_lengths(65536, 8, 3)
+    assert sum(lens) == 65536 and len(lens) == 8
+    assert all(1024 <= L <= 16384 for L in lens)
+    full = W.generate(W.WORKLOADS["gdn_fwd_bf16_varlen_h32_n8_t65536"])
+    assert full["q"].shape == (1, 32, 65536, 128)
+    assert full["cu_seqlens"].tolist()[-1] == 65536
