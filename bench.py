@@ -126,6 +126,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, pg, device) -> float:
+    """The slowest rank's time (every rank runs its own replica; no data exchange)."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Tokens of all ranks per second of the slowest rank."""
+    return tokens_per_rank * world / (ms / 1000.0)
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunkwise_delta_rule_02_gb300", "csrc")
@@ -312,13 +327,9 @@ def main():
     barrier()
     clocks = clk.stop()
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    ms = sum(per) / len(per)
-    if pg is not None:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(per) / len(per), pg, dev)
     tokens = w.tokens
-    value = tokens * world / (ms / 1000.0)
+    value = whole_job_value(tokens, world, ms)
 
     # end to end through the host-buffer entry point (forward workloads)
     e2e = None
