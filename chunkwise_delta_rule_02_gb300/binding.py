@@ -26,7 +26,7 @@ DN_F32, DN_BF16 = 0, 1
 
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
-           "dn_uses_fast_path"]
+           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc"]
 
 
 class DnShape(ctypes.Structure):
@@ -76,6 +76,8 @@ def lib():
             L.dn_host_arena_size.restype = S
             L.gdn_chunk_fwd_host.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P, S, P]
             L.gdn_chunk_fwd_host.restype = I
+            L.gdn_chunk_fwd_noalloc.argtypes = [SP, P, P, P, P, P, P, P, P, P]
+            L.gdn_chunk_fwd_noalloc.restype = I
             L.dn_device_status.argtypes = [P, P]
             L.dn_device_status.restype = I
             L.dn_status_str.argtypes = [I]
@@ -170,6 +172,14 @@ def gdn_chunk_fwd_host(shape, q, k, v, beta, g, h0, o, hT, arena, ws, stream=Non
                                   arena.numel() * arena.element_size(), _p(ws),
                                   ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "gdn_chunk_fwd_host")
+
+
+def gdn_chunk_fwd_noalloc(shape, q, k, v, beta, g, h0, o, hT, stream=None):
+    """Forward without workspace or allocation (scratch in the library's static
+    device array; bf16, d = 128, chunk 64 only)."""
+    rc = lib().gdn_chunk_fwd_noalloc(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g),
+                                     _p(h0), _p(o), _p(hT), _stream(stream))
+    _check(rc, "gdn_chunk_fwd_noalloc")
 
 
 def dn_device_status(ws, stream=None) -> int:

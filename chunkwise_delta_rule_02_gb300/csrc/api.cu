@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "fast.h"
 #include "general.h"
@@ -303,6 +305,49 @@ dn_status gdn_chunk_fwd_host(const dn_shape *s, const void *q, const void *k, co
     if (hT && sbytes && cudaMemcpyAsync(hT, dhT, sbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return DN_ERR_CUDA;
     return DN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free forward.  The scratch it needs (the status word and, for
+// packed input, the per-sequence chunk starts and longest-first order) lives in
+// this file-scope array instead of a caller-provided workspace.  Every GPU that
+// loads the library holds the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = 256 * 1024;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of the array on the current device, looked up once per device
+// (with that device current) and cached.  Returns null on failure.
+void *noalloc_scratch()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void *k, const void *v,
+                                const void *beta, const float *g, const float *h0, void *o,
+                                float *hT, void *stream)
+{
+    Geo geo;
+    dn_status rc = check_shape(shape, &geo);
+    if (rc != DN_OK) return rc;
+    if (!fast_ok(shape, geo, 0)) return DN_ERR_UNSUPPORTED;
+    if (make_layout(geo, shape, 0, true).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
+    void *ws = noalloc_scratch();
+    if (!ws) return DN_ERR_CUDA;
+    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, kNoAllocScratchBytes, stream);
 }
 
 dn_status dn_device_status(void *ws, void *stream)

@@ -129,6 +129,27 @@ dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k
                              const float *h0, void *o, float *hT, void *arena,
                              size_t arena_bytes, void *ws, size_t ws_bytes, void *stream);
 
+/* Gated DeltaNet forward that allocates nothing and takes no workspace.
+ * (The pages have no counterpart: this is a deployment variant.)  It is for
+ * callers that cannot allocate device memory or hand the library a scratch
+ * buffer: operator / plugin interfaces whose call signature carries no
+ * workspace argument, and code running inside a host framework that owns all
+ * device memory or forbids allocation on its hot path.
+ * It runs the same fused kernel as gdn_chunk_fwd, with that kernel's scratch
+ * (the device status word and, for packed input, per-sequence chunk offsets
+ * and a longest-first order) in a 256 KiB array of static device memory that
+ * every GPU loading the library keeps until the process exits.  Limits:
+ * the fast-path shapes only (dtype DN_BF16, dk = dv = 128, chunk 64;
+ * otherwise DN_ERR_UNSUPPORTED), and at most about 32,000 packed sequences
+ * (larger returns DN_ERR_WORKSPACE).  The first call on each device looks up
+ * the array's device address with that device current; make that first call
+ * before any stream capture.  All calls share the one array, so calls whose
+ * work overlaps on the GPU race on it: serialise them (one stream, or events).
+ * Arguments, layouts and the other errors are those of gdn_chunk_fwd. */
+dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void *k,
+                                const void *v, const void *beta, const float *g,
+                                const float *h0, void *o, float *hT, void *stream);
+
 /* Synchronises `stream`, then reads and clears the status word that bounded
  * device waits write into `ws` (DN_OK or DN_ERR_TIMEOUT). */
 dn_status dn_device_status(void *ws, void *stream);
