@@ -47,13 +47,25 @@ dn_status check_shape(const dn_shape *s, Geo *g)
     return DN_OK;
 }
 
+// SM count of the current device (0 when there is no device, e.g. when sizing on a
+// build machine; the workspace is then sized for an upper bound).
+int device_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
 struct Layout {
     size_t status, cstart, fast;
     size_t Kn, Qn, W, U, Unew, Tm, gam, Sin, dSo, dUn, dQ, dK, dW;
     size_t total;
 };
 
-Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast)
+// with_ring: the fused forward will be the cooperative kernel (its package ring
+// lives in the workspace); otherwise the one-CTA-per-item fused kernel.
+Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast, bool with_ring)
 {
     Layout L;
     memset(&L, 0, sizeof(L));
@@ -61,7 +73,11 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast)
     L.status = off; off += 256;
     L.cstart = off; off += align256(sizeof(int32_t) * (size_t)(g.N + 1));
     if (fast && !for_backward) {
-        L.fast = off; off += align256(fast::workspace_bytes(g));
+        // room for either fused forward: the cooperative one (ring of packages) or,
+        // where a cooperative launch is not available, the one-CTA-per-item kernel
+        const size_t a = fast::workspace_bytes(g);
+        const size_t b = with_ring ? coop::workspace_bytes(g, device_sms()) : 0;
+        L.fast = off; off += align256(a > b ? a : b);
         L.total = off;
         return L;
     }
@@ -122,16 +138,25 @@ bool force_general()
     return e && e[0] && e[0] != '0';
 }
 
+// The cooperative forward is used where the device supports it, unless
+// GDN_FUSED_PER_ITEM=1 asks for the one-CTA-per-(sequence, head) fused kernel.
+bool use_coop()
+{
+    const char *e = getenv("GDN_FUSED_PER_ITEM");
+    if (e && e[0] && e[0] != '0') return false;
+    return coop::available();
+}
+
 bool fast_ok(const dn_shape *s, const Geo &g, int for_backward)
 {
     return !for_backward && !force_general() && fast::supports(g, s->dtype);
 }
 
 dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size_t ws_bytes,
-                     cudaStream_t st, Layout &L, bool &fast)
+                     cudaStream_t st, Layout &L, bool &fast, bool with_ring)
 {
     fast = fast_ok(s, g, for_backward);
-    L = make_layout(g, s, for_backward, fast);
+    L = make_layout(g, s, for_backward, fast, with_ring);
     if (!ws || !is_aligned16(ws)) return DN_ERR_WORKSPACE;
     if (ws_bytes < L.total) return DN_ERR_WORKSPACE;
     char *base = (char *)ws;
@@ -147,7 +172,7 @@ dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size
 
 dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *v,
                    const void *beta, const float *gate, const float *h0, void *o, float *hT,
-                   void *ws, size_t ws_bytes, void *stream)
+                   void *ws, size_t ws_bytes, void *stream, bool allow_coop = true)
 {
     Geo g;
     dn_status rc = check_shape(s, &g);
@@ -160,10 +185,16 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
     bool fast;
-    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast)) != DN_OK) return rc;
+    const bool coop_run = allow_coop && use_coop();
+    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast, coop_run)) != DN_OK) return rc;
     char *base = (char *)ws;
     cudaError_t e;
-    if (fast) {
+    if (fast && coop_run) {
+        e = coop::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                      (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
+                      (__nv_bfloat16 *)o, hT, base + L.fast, ws_bytes - L.fast,
+                      (uint32_t *)(base + L.status), st);
+    } else if (fast) {
         e = fast::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                       (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
                       (__nv_bfloat16 *)o, hT, base + L.fast, (uint32_t *)(base + L.status), st);
@@ -192,7 +223,7 @@ size_t dn_workspace_size(const dn_shape *shape, int for_backward)
     Geo g;
     if (check_shape(shape, &g) != DN_OK) return 0;
     bool fast = fast_ok(shape, g, for_backward);
-    return make_layout(g, shape, for_backward, fast).total;
+    return make_layout(g, shape, for_backward, fast, fast && !for_backward && use_coop()).total;
 }
 
 int dn_uses_fast_path(const dn_shape *shape, int for_backward)
@@ -233,7 +264,7 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
     bool fast;
-    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, fast)) != DN_OK) return rc;
+    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, fast, false)) != DN_OK) return rc;
     gen::Ws w = general_ws(L, (char *)ws);
     cudaError_t e;
     if (shape->dtype == DN_F32)
@@ -344,10 +375,11 @@ dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void
     dn_status rc = check_shape(shape, &geo);
     if (rc != DN_OK) return rc;
     if (!fast_ok(shape, geo, 0)) return DN_ERR_UNSUPPORTED;
-    if (make_layout(geo, shape, 0, true).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
+    if (make_layout(geo, shape, 0, true, false).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
     void *ws = noalloc_scratch();
     if (!ws) return DN_ERR_CUDA;
-    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, kNoAllocScratchBytes, stream);
+    // the one-CTA-per-item fused kernel: its scratch fits the static array
+    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, kNoAllocScratchBytes, stream, false);
 }
 
 dn_status dn_device_status(void *ws, void *stream)

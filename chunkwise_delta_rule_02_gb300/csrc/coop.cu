@@ -1,0 +1,1059 @@
+// Cooperative persistent forward of the (gated) delta rule for bf16 inputs with
+// d_k = d_v = 128 and chunk C = 64: one launch whose CTAs take one of two roles.
+//
+//   preparation CTAs (two independent pipelines each): for a chunk, compute
+//     everything that does not depend on the state -- norms, gates, the Gram and
+//     Q K^T masks, the UT transform T = (I + A)^-1 diag(beta), T' = T diag(exp(gamma) n),
+//     -W = -T' K, Qt = diag(exp(gamma) m) Q, P = lower(Q K^T o D) with the norms --
+//     and publish them as one 50 KB package into an L2-resident ring slot of the
+//     chain CTA that owns the chunk;
+//   chain CTAs (one per SM, persistent over their (sequence, head) items): keep
+//     the state in TMEM and run, per chunk, only
+//       U^T            = V^T T^T                       (4 tcgen05 MMAs)
+//       [Unew^T | O^T] += S^T [-W | Qt]^T              (8, shared-memory operands, N = 128)
+//       S_hat^T        += (f o Unew)^T K               (4)
+//       O^T            += Unew^T P^T                   (4)
+//     with bf16 copies of S (the A operand above), Unew and f o Unew written to
+//     shared memory by the warpgroups that read the accumulators.
+//
+// (Chunk form: "Parallelizing Linear Transformers with the Delta Rule over
+// Sequence Length", WY / UT representation and the chunk-state scan;
+// "Gated DeltaNet", gates folded in as within-chunk cumulative log-decays.)
+//
+// The launch is cooperative, so every CTA is resident and the producer /
+// consumer flags in the workspace cannot deadlock on scheduling.  Tasks are
+// handed out in order (chunk index major), a preparation pipeline waits for its
+// ring slot to be consumed (RING slots per chain CTA), and a chain CTA waits for
+// its next package; every such wait, like every mbarrier wait, is bounded and
+// reports a timeout through the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fast.h"
+#include "prep_math.cuh"
+#include "sm100.cuh"
+
+// Optional event timeline of chain CTA 0 and of the preparation of its chunks
+// (compiled only with -DGDN_TRACE).
+#ifdef GDN_TRACE
+__device__ unsigned long long g_coop_trace[256][24];
+#define CTR(n, e)                                                                \
+    do {                                                                         \
+        if ((n) < 256) {                                                         \
+            unsigned long long t_;                                               \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));               \
+            g_coop_trace[(n)][(e)] = t_;                                         \
+        }                                                                        \
+    } while (0)
+#else
+#define CTR(n, e) \
+    do {          \
+    } while (0)
+#endif
+
+namespace gdn {
+namespace coop {
+using namespace sm100;
+using namespace prep;
+
+namespace {
+
+constexpr int C = 64;
+constexpr int D = 128;
+constexpr int NTHREADS = 512;
+constexpr int RING = 4;
+constexpr long long BUDGET = 4000000000LL;                 // clock cycles (about 2 s)
+constexpr float RENORM_BELOW = 9.313225746154785e-10f;      // 2^-30
+
+// package (ring slot in global memory and its copy in a chain CTA's shared memory)
+constexpr uint32_t PK_WQ = 0;          // 32 KB: per 64-column half [-W rows | Qt rows], bf16, 128B swizzle
+constexpr uint32_t PK_T = 32768;       // 8 KB : T bf16 [r][i]
+constexpr uint32_t PK_P = 40960;       // 8 KB : P bf16 [r][i]
+constexpr uint32_t PK_VEC = 49152;     // f0[64] = exp(gamma_C - gamma_r) n_r, then exp(gamma_C)
+constexpr uint32_t PK_BYTES = 50176;
+constexpr uint32_t PK_STRIDE = 51200;
+
+// chain CTA shared memory
+constexpr uint32_t CH_K = 0;                        // 2 x 16 KB K tiles
+constexpr uint32_t CH_V = 32768;                    // 16 KB V tile
+constexpr uint32_t CH_PK = 49152;                   // 2 package slots
+constexpr uint32_t CH_SB = CH_PK + 2 * PK_STRIDE;   // S^T bf16 [dv][dk], two 64-column halves (32 KB)
+constexpr uint32_t CH_U1 = CH_SB + 32768;           // Unew^T bf16 [dv][token] (16 KB)
+constexpr uint32_t CH_U2 = CH_U1 + 16384;           // (f o Unew)^T bf16 (16 KB)
+constexpr uint32_t CH_BAR = CH_U2 + 16384;
+constexpr uint32_t CH_END = CH_BAR + 32 * 8 + 64;
+
+// preparation CTA shared memory, per pipeline
+constexpr uint32_t AST = 68;                        // row stride (floats) of the solve matrices
+constexpr uint32_t PP_TL = 0;                       // 32 KB K|Q tiles, become -W|Qt (package WQ)
+constexpr uint32_t PP_AF = 32768;                   // A fp32 [64][68]; then T|P|vec (package tail)
+constexpr uint32_t PP_XF = PP_AF + 64 * AST * 4;    // X fp32 [64][68]
+constexpr uint32_t PP_TP = PP_XF + 64 * AST * 4;    // T' bf16 [r][i] 8 KB
+constexpr uint32_t PP_VEC = PP_TP + 8192;           // vectors, 12 x 64 floats
+constexpr uint32_t PP_BAR = PP_VEC + 12 * 256;      // barriers + task word
+constexpr uint32_t PP_STRIDE = 80896;               // 79 KB
+static_assert(PP_BAR + 64 <= PP_STRIDE, "pipeline layout");
+static_assert(PP_AF + PK_BYTES - PK_T <= PP_XF, "package tail must fit in A's space");
+constexpr uint32_t SMEM_USED = (CH_END > 2 * PP_STRIDE ? CH_END : 2 * PP_STRIDE);
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+// chain TMEM columns
+constexpr uint32_t TM_S = 0;        // S_hat^T fp32 (lane = dv, column = dk)
+constexpr uint32_t TM_XO = 128;     // 2 x 128: [X (64) | O (64)] per chunk parity
+
+// chain barriers
+enum {
+    B_KFULL = 0, B_KEMPTY = 2, B_VFULL = 4, B_VEMPTY = 5, B_PFULL = 6, B_PEMPTY = 8, B_X = 10,
+    B_S = 12, B_O = 13, B_U2READY = 15, B_SNAP = 16, B_OFREE = 17, B_ABORTED = 19, NBAR_CH = 20
+};
+// preparation barriers (per pipeline)
+enum { P_FULL = 0, P_G = 1, P_W = 2, P_DONE = 3, NBAR_PP = 4 };
+
+constexpr uint32_t ID_SS_N128 = idesc(1, 128, 128, false, false);
+constexpr uint32_t ID_SS_N64 = idesc(1, 128, 64, false, false);
+constexpr uint32_t ID_SS_N64_AMN = idesc(1, 128, 64, true, false);
+constexpr uint32_t ID_SS_N128_BMN = idesc(1, 128, 128, false, true);
+
+struct Params {
+    const __nv_bfloat16 *beta;
+    const float *gate;
+    const float *h0;
+    __nv_bfloat16 *o;
+    float *hT;
+    uint32_t *status;
+    const int32_t *cu;       // packed offsets or null
+    const int32_t *order;    // packed: sequences longest first (or null)
+    uint32_t *ctl;           // [0] task counter, [1] Jmax, [2..2+Nc) consumed, then ready[Nc][RING]
+    uint8_t *ring;           // Nc x RING package slots
+    int H, T, N, items, Nc, Jmax_fixed;
+    float scale, eps;
+    int l2norm;
+};
+
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+struct Item {
+    int seq, h, L, nch;
+    long long rowbase;
+};
+
+__device__ __forceinline__ Item item_of(const Params &p, int it)
+{
+    Item r;
+    r.h = it % p.H;
+    const int rank = it / p.H;
+    if (p.cu) {
+        r.seq = p.order ? p.order[rank] : rank;
+        int t0 = p.cu[r.seq], t1 = p.cu[r.seq + 1];
+        if (t0 < 0 || t1 < t0 || t1 > p.T) t0 = t1 = 0;   // malformed offsets: empty (flagged elsewhere)
+        r.L = t1 - t0;
+        r.rowbase = (long long)r.h * p.T + t0;
+    } else {
+        r.seq = rank;
+        r.L = p.T;
+        r.rowbase = ((long long)r.seq * p.H + r.h) * p.T;
+    }
+    r.nch = (r.L + C - 1) / C;
+    return r;
+}
+
+// Walks the chunk stream of chain CTA c: its items c, c + Nc, ... (empty ones skipped),
+// each chunk in order.
+struct Stream {
+    int it, n;
+    Item cur;
+    bool valid;
+    __device__ void start(const Params &p, int c)
+    {
+        it = c - p.Nc;
+        advance_item(p);
+    }
+    __device__ void advance_item(const Params &p)
+    {
+        while (true) {
+            it += p.Nc;
+            if (it >= p.items) { valid = false; return; }
+            cur = item_of(p, it);
+            if (cur.nch > 0) break;
+        }
+        n = 0;
+        valid = true;
+    }
+    __device__ void next(const Params &p)
+    {
+        if (++n >= cur.nch) advance_item(p);
+    }
+    __device__ bool first() const { return n == 0; }
+    __device__ bool last() const { return n == cur.nch - 1; }
+    __device__ int len() const { return min(C, cur.L - n * C); }
+    __device__ long long row0() const { return cur.rowbase + (long long)n * C; }
+};
+
+__device__ __forceinline__ int stream_length(const Params &p, int c)
+{
+    int J = 0;
+    for (int it = c; it < p.items; it += p.Nc) J += item_of(p, it).nch;
+    return J;
+}
+
+}  // namespace
+
+// ================================================================================= chain role
+__device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm_k,
+                                          const CUtensorMap *tm_v, uint8_t *sm, int c)
+{
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *bar = (uint64_t *)(sm + CH_BAR);
+    volatile int *abort_flag = (volatile int *)(sm + CH_BAR + 32 * 8);
+    uint32_t *tmem_slot = (uint32_t *)(sm + CH_BAR + 32 * 8 + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t *consumed = p.ctl + 2 + c;
+    uint32_t *ready = p.ctl + 2 + p.Nc + c * RING;
+    const uint8_t *ring = p.ring + (size_t)c * RING * PK_STRIDE;
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int i = 0; i < NBAR_CH; ++i) {
+            uint32_t cnt = 1;
+            if (i == B_U2READY || i == B_SNAP || i == B_OFREE || i == B_OFREE + 1) cnt = 4;
+            mbar_init(&bar[i], cnt);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(tm_k);
+        prefetch_tmap(tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int J = stream_length(p, c);
+
+    auto fail = [&]() {
+        if (!*abort_flag) {
+            *abort_flag = 1;
+            raise_status(p.status, kStatusTimeout);
+        }
+    };
+    auto wait = [&](int b, uint32_t k) -> bool {
+        if (mbar_wait(&bar[b], k & 1u, BUDGET, abort_flag)) return true;
+        fail();
+        return false;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- K / V tiles (TMA)
+        if (lane == 0) {
+            Stream st;
+            st.start(p, c);
+            int jk = -1, jv = -1;   // last chunk whose K / V copy was issued
+            for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
+                const int s = j & 1;
+                const int row = (int)st.row0();
+                if (j >= 2 && !wait(B_KEMPTY + s, (uint32_t)((j >> 1) - 1))) break;
+                mbar_expect_tx(&bar[B_KFULL + s], 16384);
+                tma_load_2d(sm + CH_K + s * 16384, tm_k, &bar[B_KFULL + s], 0, row);
+                tma_load_2d(sm + CH_K + s * 16384 + 8192, tm_k, &bar[B_KFULL + s], 64, row);
+                jk = j;
+                if (j >= 1 && !wait(B_VEMPTY, (uint32_t)(j - 1))) break;
+                mbar_expect_tx(&bar[B_VFULL], 16384);
+                tma_load_2d(sm + CH_V, tm_v, &bar[B_VFULL], 0, row);
+                tma_load_2d(sm + CH_V + 8192, tm_v, &bar[B_VFULL], 64, row);
+                jv = j;
+            }
+            if (*abort_flag) {
+                // let copies in flight land before shared memory goes away
+                for (int jj = (jk > 0 ? jk - 1 : 0); jj <= jk; ++jj)
+                    mbar_wait(&bar[B_KFULL + (jj & 1)], (uint32_t)(jj >> 1) & 1u, BUDGET, nullptr);
+                if (jv >= 0) mbar_wait(&bar[B_VFULL], (uint32_t)jv & 1u, BUDGET, nullptr);
+            }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- packages (bulk copies)
+        if (lane == 0) {
+            for (int j = 0; j < J; ++j) {
+                const int s = j & 1, slot = j % RING;
+                // wait for the producer's flag
+                const long long t0 = clock64();
+                bool ok = true;
+                while (ld_acquire_gpu(&ready[slot]) != (uint32_t)(j + 1)) {
+                    if (*abort_flag || clock64() - t0 > BUDGET) { ok = false; break; }
+                    __nanosleep(64);
+                }
+                if (!ok) { fail(); break; }
+                fence_async_global();
+                if (c == 0) CTR(j, 0);
+                if (j >= 2 && !wait(B_PEMPTY + s, (uint32_t)((j >> 1) - 1))) break;
+                mbar_expect_tx(&bar[B_PFULL + s], PK_BYTES);
+                bulk_load(sm + CH_PK + s * PK_STRIDE, ring + (size_t)slot * PK_STRIDE, PK_BYTES,
+                          &bar[B_PFULL + s]);
+                if (!wait(B_PFULL + s, (uint32_t)(j >> 1))) {
+                    mbar_wait(&bar[B_PFULL + s], (uint32_t)(j >> 1) & 1u, BUDGET, nullptr);
+                    break;
+                }
+                st_release_gpu(consumed, (uint32_t)(j + 1));   // the ring slot may be refilled
+                if (c == 0) CTR(j, 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0 && J > 0) {
+            const uint64_t dSB = sdesc(sb + CH_SB, 16, 1024);
+            const uint64_t dU1 = sdesc(sb + CH_U1, 16, 1024), dU2 = sdesc(sb + CH_U2, 16, 1024);
+            const uint64_t dK0 = sdesc(sb + CH_K, 8192, 1024), dK1 = sdesc(sb + CH_K + 16384, 8192, 1024);
+            const uint64_t dV = sdesc(sb + CH_V, 8192, 1024);
+            const uint64_t dPK0 = sdesc(sb + CH_PK, 16, 1024), dPK1 = sdesc(sb + CH_PK + PK_STRIDE, 16, 1024);
+            auto issue_U = [&](int m) {
+                // U^T = V^T T^T into X[m & 1]
+                tc_fence_after();
+                const uint64_t dpk = (m & 1) ? dPK1 : dPK0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_ss(tmem + TM_XO + (m & 1) * 128, dadd(dV, k * 2048), dadd(dpk, PK_T + k * 32),
+                                ID_SS_N64_AMN, k > 0);
+                mma_commit(&bar[B_VEMPTY]);
+            };
+            bool ok = wait(B_VFULL, 0) && wait(B_PFULL, 0);
+            if (ok) issue_U(0);
+            for (int j = 0; j < J && ok; ++j) {
+                const int s = j & 1;
+                const uint64_t dpk = s ? dPK1 : dPK0;
+                // [Unew^T | O^T] += S^T [-W | Qt]^T
+                if (!(ok = wait(B_PFULL + s, (uint32_t)(j >> 1)))) break;
+                if (!(ok = wait(B_SNAP, (uint32_t)j))) break;
+                if (!(ok = wait(B_OFREE + s, (uint32_t)(j >> 1)))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    mma_bf16_ss(tmem + TM_XO + s * 128, dadd(dSB, off), dadd(dpk, PK_WQ + off), ID_SS_N128, 1);
+                }
+                mma_commit(&bar[B_X + s]);
+                if (c == 0) CTR(j, 2);
+                // S_hat^T += U2^T K ; O^T += U1^T P^T
+                if (!(ok = wait(B_U2READY, (uint32_t)j))) break;
+                if (c == 0) CTR(j, 3);
+                if (!(ok = wait(B_KFULL + s, (uint32_t)(j >> 1)))) break;
+                tc_fence_after();
+                {
+                    const uint64_t dk = s ? dK1 : dK0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16_ss(tmem + TM_S, dadd(dU2, k * 32), dadd(dk, k * 2048), ID_SS_N128_BMN, 1);
+                }
+                mma_commit(&bar[B_S]);
+                mma_commit(&bar[B_KEMPTY + s]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_ss(tmem + TM_XO + s * 128 + 64, dadd(dU1, k * 32), dadd(dpk, PK_P + k * 32),
+                                ID_SS_N64, 1);
+                mma_commit(&bar[B_O + s]);
+                mma_commit(&bar[B_PEMPTY + s]);
+                if (c == 0) CTR(j, 4);
+                // U of the next chunk
+                if (j + 1 < J) {
+                    if (!(ok = wait(B_VFULL, (uint32_t)(j + 1)))) break;
+                    if (!(ok = wait(B_PFULL + ((j + 1) & 1), (uint32_t)((j + 1) >> 1)))) break;
+                    issue_U(j + 1);
+                    if (c == 0) CTR(j, 5);
+                }
+            }
+            mma_commit(&bar[B_ABORTED]);
+            mbar_wait(&bar[B_ABORTED], 0, BUDGET, nullptr);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- Unew -> U1, U2 (shared)
+        const int dv = (warp & 3) * 32 + lane;
+        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+        Stream st;
+        st.start(p, c);
+        float Gpend = 1.f;
+        for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
+            const int s = j & 1;
+            if (st.first()) Gpend = 1.f;
+            if (!__all_sync(0xffffffffu, wait(B_X + s, (uint32_t)(j >> 1)))) break;
+            if (c == 0 && tid == 128) CTR(j, 6);
+            tc_fence_after();
+            uint32_t x[64];
+            tmem_ld32(tmem + lrow + TM_XO + s * 128, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tmem_ld_wait();
+            const float *vec = (const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC);
+            const float GC = vec[64];
+            const float Gnext = Gpend * GC;
+            const bool renorm = Gnext < RENORM_BELOW;
+            const float fdiv = renorm ? 1.f : 1.f / Gnext;
+            Gpend = renorm ? 1.f : Gnext;
+            uint8_t *u1 = sm + CH_U1, *u2 = sm + CH_U2;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t w1[4], w2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = c8 * 8 + 2 * e;
+                    const float a = __uint_as_float(x[i0]), b = __uint_as_float(x[i0 + 1]);
+                    w1[e] = pack_bf16(a, b);
+                    w2[e] = pack_bf16(a * vec[i0] * fdiv, b * vec[i0 + 1] * fdiv);
+                }
+                const uint32_t off = sw128(dv, c8 * 16);
+                *(uint4 *)(u1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_U2READY]);
+            if (c == 0 && tid == 128) CTR(j, 7);
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ---------------------------------------------------------------- state: h0, snapshot, renorm, h_T
+        const int dv = (warp & 3) * 32 + lane;
+        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+        // items without chunks pass their initial state straight through
+        for (int it = c; it < p.items; it += p.Nc) {
+            const Item I = item_of(p, it);
+            if (I.nch == 0 && p.hT) {
+                const size_t sidx = ((size_t)I.seq * p.H + I.h) * D * D;
+                for (int k = 0; k < D; ++k) p.hT[sidx + (size_t)k * D + dv] = p.h0 ? p.h0[sidx + (size_t)k * D + dv] : 0.f;
+            }
+        }
+        Stream st;
+        st.start(p, c);
+        float Gpend = 1.f;
+        uint8_t *sbp = sm + CH_SB;
+        for (int j = 0; j < J && st.valid; ++j) {
+            const int s = j & 1;
+            const size_t sidx = ((size_t)st.cur.seq * p.H + st.cur.h) * D * D;
+            if (st.first()) {
+                // S^T[dv][dk] = h0[dk][dv] into TMEM, pending scale 1
+                Gpend = 1.f;
+                for (int k0 = 0; k0 < D; k0 += 32) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        r[k] = __float_as_uint(p.h0 ? p.h0[sidx + (size_t)(k0 + k) * D + dv] : 0.f);
+                    tmem_st32(tmem + lrow + TM_S + k0, r);
+                }
+                tmem_st_wait();
+            } else {
+                wait(B_S, (uint32_t)(j - 1));
+            }
+            wait(B_PFULL + s, (uint32_t)(j >> 1));
+            tc_fence_after();
+            const float GC = ((const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC))[64];
+            if (c == 0 && tid == 256) CTR(j, 8);
+            const float Gn = Gpend;
+            const float Gnext = Gn * GC;
+            const bool renorm = Gnext < RENORM_BELOW;
+            // bf16 snapshot of the true state S = G S_hat (A operand of the next MMA);
+            // a renormalising chunk also rescales S_hat in TMEM to exp(gamma_C) S
+            for (int k0 = 0; k0 < D; k0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lrow + TM_S + k0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(Gn * __uint_as_float(r[c8 * 8 + 2 * e]), Gn * __uint_as_float(r[c8 * 8 + 2 * e + 1]));
+                    const int kk = k0 + c8 * 8;   // first dk of this 16-byte group
+                    *(uint4 *)(sbp + (kk >> 6) * 16384 + sw128(dv, (kk & 63) * 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                if (renorm) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * Gnext);
+                    tmem_st32(tmem + lrow + TM_S + k0, r);
+                }
+            }
+            if (renorm) tmem_st_wait();
+            Gpend = renorm ? 1.f : Gnext;
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_SNAP]);
+            if (c == 0 && tid == 256) CTR(j, 9);
+            if (st.last()) {
+                // h_T = G S_hat once the chunk's state update has landed
+                wait(B_S, (uint32_t)j);
+                tc_fence_after();
+                if (p.hT && !*abort_flag) {
+                    for (int k0 = 0; k0 < D; k0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + lrow + TM_S + k0, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            p.hT[sidx + (size_t)(k0 + k) * D + dv] = Gpend * __uint_as_float(r[k]);
+                    }
+                }
+            }
+            st.next(p);
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        }
+    } else if (warp >= 12) {
+        // ---------------------------------------------------------------- output
+        const int dv = (warp & 3) * 32 + lane;
+        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+        {
+            uint32_t z[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) z[k] = 0u;
+            for (int s = 0; s < 2; ++s) {
+                tmem_st32(tmem + lrow + TM_XO + s * 128 + 64, z);
+                tmem_st32(tmem + lrow + TM_XO + s * 128 + 96, z);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar[B_OFREE]);
+                mbar_arrive(&bar[B_OFREE + 1]);
+            }
+        }
+        Stream st;
+        st.start(p, c);
+        for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
+            const int s = j & 1;
+            if (!__all_sync(0xffffffffu, wait(B_O + s, (uint32_t)(j >> 1)))) break;
+            if (c == 0 && tid == 384) CTR(j, 10);
+            tc_fence_after();
+            uint32_t ov[64];
+            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+            tmem_ld_wait();
+            uint32_t z[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) z[k] = 0u;
+            tmem_st32(tmem + lrow + TM_XO + s * 128 + 64, z);
+            tmem_st32(tmem + lrow + TM_XO + s * 128 + 96, z);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_OFREE + s]);
+            const int len = st.len();
+            __nv_bfloat16 *orow = p.o + st.row0() * D + dv;
+#pragma unroll
+            for (int r = 0; r < 64; ++r)
+                if (r < len) orow[(size_t)r * D] = __float2bfloat16_rn(p.scale * __uint_as_float(ov[r]));
+            if (c == 0 && tid == 384) CTR(j, 11);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ================================================================================= preparation role
+__device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_q,
+                                         const CUtensorMap *tm_k, uint8_t *sm)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    if (tid == 0) s_abort = 0;
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    const int pipe = (warp >> 2) - 1;   // warps 4..7 -> 0, 8..11 -> 1
+    uint8_t *base = sm + (pipe >= 0 ? pipe : 0) * PP_STRIDE;
+    uint64_t *bar = (uint64_t *)(base + PP_BAR);
+    if (pipe >= 0 && pipe < 2 && (warp & 3) == 0 && lane == 0) {
+        for (int i = 0; i < NBAR_PP; ++i) mbar_init(&bar[i], 1);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int *abort_flag = &s_abort;
+
+    if (pipe >= 0 && pipe < 2) {
+        const int t = tid - (pipe + 1) * 128;   // 0..127 within the pipeline
+        const int q4 = warp & 3;
+        const int bar_id = 1 + pipe;
+        const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
+        const uint32_t tg = tmem + pipe * 256;          // [K;Q][K;Q]^T (128 columns)
+        const uint32_t tw = tmem + pipe * 256 + 128;    // W^T (64 columns)
+        const uint32_t sbase = smem_u32(base);
+        volatile int *task_word = (volatile int *)(base + PP_BAR + NBAR_PP * 8);
+        float *vb = (float *)(base + PP_VEC);
+        float *s_beta = vb, *s_gl = vb + 64, *s_nk = vb + 128, *s_nq = vb + 192, *s_tc = vb + 256;
+        float *s_qs = vb + 320, *s_ra = vb + 384, *s_cb = vb + 448, *s_f0 = vb + 512, *s_g = vb + 576;
+        int *s_safe = (int *)(vb + 640);
+        float *Af = (float *)(base + PP_AF);
+        float *Xf = (float *)(base + PP_XF);
+        const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
+        const long long ntasks = (long long)p.Nc * Jmax;
+        auto fail = [&]() {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                raise_status(p.status, kStatusTimeout);
+            }
+        };
+        auto wait = [&](int b, uint32_t k) -> bool {
+            if (mbar_wait(&bar[b], k & 1u, BUDGET, abort_flag)) return true;
+            fail();
+            return false;
+        };
+        uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
+        bool tma_pending = false, mma_issued = false;
+        while (true) {
+            if (t == 0) {
+                const int tk = (int)atomicAdd(&p.ctl[0], 1u);
+                *task_word = *abort_flag ? 0x7fffffff : tk;   // one decision for the whole pipeline
+            }
+            named_bar(bar_id, 128);
+            const int task = *task_word;
+            named_bar(bar_id, 128);
+            if (task >= ntasks) break;
+            const int c = task % p.Nc, j = task / p.Nc;
+            // find chunk j of chain CTA c
+            Item I;
+            int n = j, it = c;
+            bool found = false;
+            for (; it < p.items; it += p.Nc) {
+                I = item_of(p, it);
+                if (n < I.nch) { found = true; break; }
+                n -= I.nch;
+            }
+            if (!found) continue;
+            if (c == 0 && t == 0) CTR(j, 12);
+            const int len = min(C, I.L - n * C);
+            const long long row0 = I.rowbase + (long long)n * C;
+            const int slot = j % RING;
+            uint32_t *consumed = p.ctl + 2 + c;
+            uint32_t *ready = p.ctl + 2 + p.Nc + c * RING + slot;
+            uint8_t *dst = p.ring + ((size_t)c * RING + slot) * PK_STRIDE;
+            if (t == 0) {
+                // the ring slot must have been copied out by the chain CTA
+                const long long t0 = clock64();
+                while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
+                    if (clock64() - t0 > BUDGET) { fail(); break; }
+                    __nanosleep(128);
+                }
+                if (!*abort_flag) {
+                    mbar_expect_tx(&bar[P_FULL], 32768);
+                    tma_load_2d(base + PP_TL, tm_k, &bar[P_FULL], 0, (int)row0);
+                    tma_load_2d(base + PP_TL + 16384, tm_k, &bar[P_FULL], 64, (int)row0);
+                    tma_load_2d(base + PP_TL + 8192, tm_q, &bar[P_FULL], 0, (int)row0);
+                    tma_load_2d(base + PP_TL + 24576, tm_q, &bar[P_FULL], 64, (int)row0);
+                    tma_pending = true;
+                    if (c == 0) CTR(j, 13);
+                }
+            }
+            if (q4 == 0) {
+                // beta and g (zero past the chunk), gates scanned in log2 units
+                float g0 = 0.f, g1 = 0.f;
+                s_beta[lane] = lane < len ? __bfloat162float(p.beta[row0 + lane]) : 0.f;
+                s_beta[lane + 32] = lane + 32 < len ? __bfloat162float(p.beta[row0 + lane + 32]) : 0.f;
+                if (p.gate) {
+                    g0 = lane < len ? p.gate[row0 + lane] : 0.f;
+                    g1 = lane + 32 < len ? p.gate[row0 + lane + 32] : 0.f;
+                }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+                    float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+                    if (lane >= o) { g0 += a0; g1 += a1; }
+                }
+                g1 += __shfl_sync(0xffffffffu, g0, 31);
+                g0 *= 1.4426950408889634f;
+                g1 *= 1.4426950408889634f;
+                s_gl[lane] = g0;
+                s_gl[lane + 32] = g1;
+                float mx = fmaxf(fabsf(g0), fabsf(g1));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) *s_safe = mx < 100.f;
+            }
+            if (wait(P_FULL, k_task) && t == 0) tma_pending = false;
+            if (c == 0 && t == 0) CTR(j, 14);
+            if (t == 0) {
+                // [K;Q][K;Q]^T: Gram rows, Q K^T rows and both norms on the diagonals
+                mma_issued = true;
+                tc_fence_after();
+                const uint64_t d = sdesc(sbase + PP_TL, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t dk = dadd(d, (k >> 2) * 16384 + (k & 3) * 32);
+                    mma_bf16_ss(tg, dk, dk, ID_SS_N128, k > 0);
+                }
+                mma_commit(&bar[P_G]);
+            }
+            wait(P_G, k_task);
+            tc_fence_after();
+            if (c == 0 && t == 0) CTR(j, 15);
+            {
+                // diagonal element of this lane's row: column 32 q4 + lane
+                uint32_t v[32];
+                tmem_ld32(tg + lrow + 32 * q4, v);
+                tmem_ld_wait();
+                float dg = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) dg = (i == lane) ? __uint_as_float(v[i]) : dg;
+                const int r = (q4 & 1) * 32 + lane;
+                const float nrm = r < len ? (p.l2norm ? rsqrtf(dg + p.eps) : 1.f) : 0.f;
+                if (q4 < 2) s_nk[r] = nrm; else s_nq[r] = nrm;
+            }
+            named_bar(bar_id, 128);
+            const bool safe = *s_safe != 0;
+            const float glC = s_gl[len - 1];
+            if (t < 64) {
+                const float gl = s_gl[t];
+                const float e = ex2f(gl);
+                s_tc[t] = s_beta[t] * e * s_nk[t];
+                s_qs[t] = e * s_nq[t];
+                s_ra[t] = s_beta[t] * s_nk[t] * e;
+                s_cb[t] = safe ? s_nk[t] * ex2f(-gl) : 0.f;
+                s_f0[t] = ex2f(glC - gl) * s_nk[t];
+                if (t == 0) s_g[0] = ex2f(glC);
+            }
+            named_bar(bar_id, 128);
+            // A = strict_lower(diag(beta n) (K K^T o D) diag(n))
+            if (q4 < 2) {
+                const int r = q4 * 32 + lane;
+                uint32_t v[64];
+                tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_ld_wait();
+                float4 *arow = reinterpret_cast<float4 *>(Af + r * AST);
+                const float ra = s_ra[r], br = s_beta[r] * s_nk[r], gr = s_gl[r];
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * c4 + e;
+                        const float gv = __uint_as_float(v[i]);
+                        a[e] = (i < r) ? (safe ? ra * s_cb[i] * gv : br * s_nk[i] * gv * ex2f(gr - s_gl[i])) : 0.f;
+                    }
+                    arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
+                }
+            }
+            named_bar(bar_id, 128);
+            solve_unit_lower_64<AST>(Af, Xf, lane, q4, bar_id);
+            if (c == 0 && t == 0) CTR(j, 16);
+            // A is dead: its space now takes the package tail (T | P | vectors)
+            uint8_t *pt = base + PP_AF;
+            if (q4 >= 2) {
+                // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i]
+                const int r = (q4 - 2) * 32 + lane;
+                uint32_t v[64];
+                tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_ld_wait();
+                const float mr = s_nq[r], gr = s_gl[r], rp = mr * ex2f(gr);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = c8 * 8 + 2 * e, i1 = i0 + 1;
+                        const float v0 = __uint_as_float(v[i0]), v1 = __uint_as_float(v[i1]);
+                        float a0, a1;
+                        if (safe) {
+                            a0 = (i0 <= r) ? rp * s_cb[i0] * v0 : 0.f;
+                            a1 = (i1 <= r) ? rp * s_cb[i1] * v1 : 0.f;
+                        } else {
+                            a0 = (i0 <= r) ? mr * s_nk[i0] * v0 * ex2f(gr - s_gl[i0]) : 0.f;
+                            a1 = (i1 <= r) ? mr * s_nk[i1] * v1 * ex2f(gr - s_gl[i1]) : 0.f;
+                        }
+                        w[e] = pack_bf16(a0, a1);
+                    }
+                    *(uint4 *)(pt + (PK_P - PK_T) + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            {
+                // T = X diag(beta) (package) and T' = X diag(beta exp(gamma) n) (local), bf16 [r][i]
+                const int r = t >> 1, hh = t & 1;
+                const float4 *xr = reinterpret_cast<const float4 *>(Xf + r * AST + hh * 32);
+                const float4 *b4 = reinterpret_cast<const float4 *>(s_beta + hh * 32);
+                const float4 *c4 = reinterpret_cast<const float4 *>(s_tc + hh * 32);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t wt[4], wp[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const int q = c8 * 2 + e2;
+                        float4 x = xr[q];
+                        const int i0 = hh * 32 + 4 * q;
+                        if (i0 > r) x.x = 0.f;
+                        if (i0 + 1 > r) x.y = 0.f;
+                        if (i0 + 2 > r) x.z = 0.f;
+                        if (i0 + 3 > r) x.w = 0.f;
+                        const float4 bb = b4[q], cc = c4[q];
+                        wt[2 * e2] = pack_bf16(x.x * bb.x, x.y * bb.y);
+                        wt[2 * e2 + 1] = pack_bf16(x.z * bb.z, x.w * bb.w);
+                        wp[2 * e2] = pack_bf16(x.x * cc.x, x.y * cc.y);
+                        wp[2 * e2 + 1] = pack_bf16(x.z * cc.z, x.w * cc.w);
+                    }
+                    const uint32_t off = sw128(r, (hh * 4 + c8) * 16);
+                    *(uint4 *)(pt + off) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+                    *(uint4 *)(base + PP_TP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                }
+                if (t < 64) ((float *)(pt + (PK_VEC - PK_T)))[t] = s_f0[t];
+                if (t == 0) ((float *)(pt + (PK_VEC - PK_T)))[64] = s_g[0];
+            }
+            fence_async_smem();
+            named_bar(bar_id, 128);
+            if (t == 0) {
+                // W^T = K^T T'^T
+                tc_fence_after();
+                const uint64_t dk = sdesc(sbase + PP_TL, 16384, 1024);
+                const uint64_t dtp = sdesc(sbase + PP_TP, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16_ss(tw, dadd(dk, k * 2048), dadd(dtp, k * 32), ID_SS_N64_AMN, k > 0);
+                mma_commit(&bar[P_W]);
+            }
+            {
+                // Qt = diag(exp(gamma) m) Q in place (the Q rows of the package's WQ block)
+                const int r = t >> 1, hh = t & 1;
+                const float f = s_qs[r];
+                uint8_t *qr = base + PP_TL + hh * 16384 + 8192 + r * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint4 a = *(uint4 *)(qr + q * 16);
+                    a.x = scale_pair(a.x, f); a.y = scale_pair(a.y, f);
+                    a.z = scale_pair(a.z, f); a.w = scale_pair(a.w, f);
+                    *(uint4 *)(qr + q * 16) = a;
+                }
+            }
+            wait(P_W, k_task);
+            tc_fence_after();
+            if (c == 0 && t == 0) CTR(j, 17);
+            {
+                // -W rows over the K rows (K is no longer needed): element (token r, dk)
+                uint32_t v[64];
+                tmem_ld32(tw + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(tw + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_ld_wait();
+                const int dk = q4 * 32 + lane;
+                uint8_t *wb = base + PP_TL + (dk >> 6) * 16384;
+#pragma unroll
+                for (int r = 0; r < 64; ++r)
+                    *(__nv_bfloat16 *)(wb + sw128(r, (dk & 63) * 2)) = __float2bfloat16_rn(-__uint_as_float(v[r]));
+            }
+            tc_fence_before();
+            fence_async_smem();
+            named_bar(bar_id, 128);
+            if (t == 0 && !*abort_flag) {
+                // publish: package -> ring slot, then the ready flag
+                fence_async_global();
+                bulk_store(dst + PK_WQ, base + PP_TL, 32768);
+                bulk_store(dst + PK_T, base + PP_AF, PK_BYTES - PK_T);
+                bulk_commit();
+                bulk_wait_all();
+                fence_async_global();
+                __threadfence();
+                st_release_gpu(ready, (uint32_t)(j + 1));
+                if (c == 0) CTR(j, 18);
+            }
+            ++k_task;
+            named_bar(bar_id, 128);
+        }
+        if (t == 0) {
+            // nothing of this pipeline may still be in flight when the block exits
+            if (tma_pending) mbar_wait(&bar[P_FULL], k_task & 1u, BUDGET, nullptr);
+            if (mma_issued) {
+                mma_commit(&bar[P_DONE]);
+                mbar_wait(&bar[P_DONE], 0, BUDGET, nullptr);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ================================================================================= kernel
+__global__ void __launch_bounds__(NTHREADS, 1)
+k_coop_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    if ((int)blockIdx.x < p.Nc) chain_cta(p, &tm_k, &tm_v, sm, blockIdx.x);
+    else prep_cta(p, &tm_q, &tm_k, sm);
+}
+
+// Packed input: longest-first order of the sequences and the longest chunk stream of
+// any chain CTA (written to ctl[1]).  One block.
+__global__ void k_plan(const int32_t *cu, int N, int T, int H, int Nc, int32_t *order, uint32_t *ctl)
+{
+    __shared__ int s_max;
+    if (threadIdx.x == 0) s_max = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < N; s += blockDim.x) {
+        int a = cu[s], b = cu[s + 1];
+        if (a < 0 || b < a || b > T) a = b = 0;
+        const int Ls = b - a;
+        int rank = 0;
+        if (N <= 4096) {
+            for (int o = 0; o < N; ++o) {
+                int a2 = cu[o], b2 = cu[o + 1];
+                if (a2 < 0 || b2 < a2 || b2 > T) a2 = b2 = 0;
+                const int Lo = b2 - a2;
+                rank += (Lo > Ls) || (Lo == Ls && o < s);
+            }
+        } else {
+            rank = s;
+        }
+        order[rank] = s;
+    }
+    __syncthreads();
+    const int items = N * H;
+    for (int c = threadIdx.x; c < Nc; c += blockDim.x) {
+        int Jc = 0;
+        for (int it = c; it < items; it += Nc) {
+            const int sq = order[it / H];
+            int a = cu[sq], b = cu[sq + 1];
+            if (a < 0 || b < a || b > T) a = b = 0;
+            Jc += (b - a + C - 1) / C;
+        }
+        atomicMax(&s_max, Jc);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) ctl[1] = (uint32_t)s_max;
+}
+
+// ================================================================================= host
+#ifdef GDN_TRACE
+extern "C" int gdn_coop_trace_fetch(unsigned long long *host, size_t count)
+{
+    return cudaMemcpyFromSymbol(host, g_coop_trace, count * sizeof(unsigned long long)) == cudaSuccess ? 0 : 1;
+}
+#endif
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *base, long long rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t gstr[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim, gstr, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+// Split of the SMs: chain CTAs (at most 64, at most one per item), the rest prepare.
+int chain_ctas(const Geo &g, int sms)
+{
+    const int items = g.N * g.H;
+    int nc = (sms * 27 + 32) / 64;   // 64 of 152
+    if (nc > items) nc = items;
+    if (nc < 1) nc = 1;
+    return nc;
+}
+
+size_t workspace_bytes(const Geo &g, int sms)
+{
+    if (sms <= 0) sms = 160;   // sizing without a device: an upper bound
+    const int nc = chain_ctas(g, sms);
+    const size_t ctl = (size_t)(2 + nc + nc * RING) * sizeof(uint32_t);
+    const size_t order = g.varlen ? sizeof(int32_t) * (size_t)(g.N + 1) : 0;
+    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    return al(ctl) + al(order) + (size_t)nc * RING * PK_STRIDE;
+}
+
+bool available()
+{
+    static int ok = -1;
+    if (ok < 0) {
+        int dev = 0, coop = 0;
+        ok = cudaGetDevice(&dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+             encode_fn() != nullptr && num_sms() >= 2;
+    }
+    return ok == 1;
+}
+
+cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                const __nv_bfloat16 *v, const __nv_bfloat16 *beta, const float *gate,
+                const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
+                uint32_t *status, cudaStream_t st)
+{
+    const int sms = num_sms();
+    if (sms < 2) return cudaErrorNotSupported;
+    if (ws_bytes < workspace_bytes(g, sms)) return cudaErrorInvalidValue;
+    const int items = g.N * g.H;
+    if (items == 0) return cudaSuccess;
+    const int nc = chain_ctas(g, sms);
+    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    uint8_t *w = (uint8_t *)ws;
+    const size_t ctl_bytes = (size_t)(2 + nc + nc * RING) * sizeof(uint32_t);
+    Params p;
+    p.beta = beta; p.gate = gate; p.h0 = h0; p.o = o; p.hT = hT; p.status = status;
+    p.cu = g.varlen ? g.cu : nullptr;
+    p.ctl = (uint32_t *)w;
+    p.order = g.varlen ? (const int32_t *)(w + al(ctl_bytes)) : nullptr;
+    p.ring = w + al(ctl_bytes) + (g.varlen ? al(sizeof(int32_t) * (size_t)(g.N + 1)) : 0);
+    p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc;
+    p.Jmax_fixed = g.varlen ? 0 : ((items + nc - 1) / nc) * ((g.T + C - 1) / C);
+    p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm;
+    cudaError_t e = cudaMemsetAsync(p.ctl, 0, ctl_bytes, st);
+    if (e != cudaSuccess) return e;
+    if (g.varlen) {
+        k_plan<<<1, 1024, 0, st>>>(g.cu, g.N, g.T, g.H, nc, (int32_t *)p.order, p.ctl);
+        if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    }
+    const long long rows = (long long)g.B * g.H * g.T;
+    CUtensorMap mq, mk, mv;
+    const long long maprows = rows > 0 ? rows : 1;
+    if (!make_map(&mq, q, maprows) || !make_map(&mk, k, maprows) || !make_map(&mv, v, maprows))
+        return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(k_coop_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)) !=
+        cudaSuccess)
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_coop_fwd, NTHREADS, SMEM_BYTES)) !=
+        cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    void *args[] = {(void *)&mq, (void *)&mk, (void *)&mv, (void *)&p};
+    e = cudaLaunchCooperativeKernel((const void *)k_coop_fwd, dim3(sms), dim3(NTHREADS), args, SMEM_BYTES, st);
+    if (e != cudaSuccess) return e;
+    return cudaPeekAtLastError();
+}
+
+}  // namespace coop
+}  // namespace gdn

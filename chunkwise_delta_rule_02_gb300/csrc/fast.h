@@ -18,4 +18,21 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                 cudaStream_t st);
 
 }  // namespace fast
+
+// Cooperative persistent forward (preparation CTAs + chain CTAs); same shapes as fast.
+namespace coop {
+
+// Whether this device can run it (cooperative launch, tensor-map encoder).
+bool available();
+
+// Workspace it needs: control words, packed order, package ring.  sms <= 0 sizes
+// for an upper bound on the SM count.
+size_t workspace_bytes(const Geo &g, int sms);
+
+cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                const __nv_bfloat16 *v, const __nv_bfloat16 *beta, const float *gate,
+                const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
+                uint32_t *status, cudaStream_t st);
+
+}  // namespace coop
 }  // namespace gdn

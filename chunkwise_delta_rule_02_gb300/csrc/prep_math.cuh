@@ -1,0 +1,121 @@
+// Device helpers shared by the fused kernels' chunk preparation: bf16 pair
+// handling, 2^x, tf32 conversion, a 16x8x8 tf32 tensor-core tile, and the
+// 64x64 unit-lower-triangular inverse of the UT transform.
+#pragma once
+
+#include <stdint.h>
+
+#include "sm100.cuh"
+
+namespace gdn {
+namespace prep {
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t scale_pair(uint32_t w, float s)
+{
+    return sm100::pack_bf16(bf_lo(w) * s, bf_hi(w) * s);
+}
+
+// 2^x on the special-function unit (results may flush to 0)
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D += A B for one 16x8x8 tile (A row-major 16x8, B 8x8, tf32 in, fp32 accumulate)
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// X = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row stride
+// AST floats), called by the 128 threads of one warpgroup (warp q4 = 0..3 in the
+// group, lane = lane id).  Diagonal 16 x 16 blocks by substitution (warp w:
+// block w, lane c: column c); then block column j (warp j):
+//     X_ij = -sum_{m=j}^{i-1} (X_ii A_im) X_mj,
+// as 16 x 16 products on the tensor cores (tf32 mma.sync, fp32 accumulate) with
+// the product X_ii A_im kept in registers as the A operand of the next one.
+// Synchronises the warpgroup (named barrier bar_id) between the two phases and
+// at the end; X's strictly upper part is not written.
+template <int AST>
+__device__ __forceinline__ void solve_unit_lower_64(const float *Af, float *Xf, int lane, int q4,
+                                                    int bar_id)
+{
+    {
+        const int base = 16 * q4, c = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float acc = (i == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int l = 0; l < i; ++l) acc = fmaf(-Af[(base + i) * AST + base + l], x[l], acc);
+            x[i] = (i < c) ? 0.f : acc;
+        }
+        if (lane < 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Xf[(base + i) * AST + base + c] = x[i];
+        }
+    }
+    sm100::named_bar(bar_id, 128);
+    const int g8 = lane >> 2, t4 = lane & 3;
+    if (q4 < 3) {
+        const int j = q4;
+        for (int i = j + 1; i < 4; ++i) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int m = j; m < i; ++m) {
+                float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *xa = Xf + (16 * i) * AST + 16 * i + 8 * ks;
+                    uint32_t a[4] = {tf32(xa[g8 * AST + t4]), tf32(xa[(g8 + 8) * AST + t4]),
+                                     tf32(xa[g8 * AST + t4 + 4]), tf32(xa[(g8 + 8) * AST + t4 + 4])};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float *ab = Af + (16 * i + 8 * ks) * AST + 16 * m + 8 * nt + g8;
+                        uint32_t b[2] = {tf32(ab[t4 * AST]), tf32(ab[(t4 + 4) * AST])};
+                        mma_tf32_16x8x8(z[nt], a, b);
+                    }
+                }
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4] = {tf32(z[ks][0]), tf32(z[ks][2]), tf32(z[ks][1]), tf32(z[ks][3])};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float *xb = Xf + (16 * m + 8 * ks) * AST + 16 * j + 8 * nt + g8;
+                        uint32_t b[2] = {tf32(xb[(2 * t4) * AST]), tf32(xb[(2 * t4 + 1) * AST])};
+                        mma_tf32_16x8x8(acc[nt], a, b);
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float *xo = Xf + (16 * i + g8) * AST + 16 * j + 8 * nt + 2 * t4;
+                xo[0] = -acc[nt][0];
+                xo[1] = -acc[nt][1];
+                xo[8 * AST] = -acc[nt][2];
+                xo[8 * AST + 1] = -acc[nt][3];
+            }
+            __syncwarp();
+        }
+    }
+    sm100::named_bar(bar_id, 128);
+}
+
+}  // namespace prep
+}  // namespace gdn

@@ -135,10 +135,12 @@ dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k
  * buffer: operator / plugin interfaces whose call signature carries no
  * workspace argument, and code running inside a host framework that owns all
  * device memory or forbids allocation on its hot path.
- * It runs the same fused kernel as gdn_chunk_fwd, with that kernel's scratch
- * (the device status word and, for packed input, per-sequence chunk offsets
- * and a longest-first order) in a 256 KiB array of static device memory that
- * every GPU loading the library keeps until the process exits.  Limits:
+ * It runs the fused forward with one CTA per (sequence, head) -- the
+ * cooperative forward gdn_chunk_fwd prefers needs a multi-megabyte package
+ * ring in its workspace -- with that kernel's scratch (the device status word
+ * and, for packed input, per-sequence chunk offsets and a longest-first order)
+ * in a 256 KiB array of static device memory that every GPU loading the
+ * library keeps until the process exits.  Limits:
  * the fast-path shapes only (dtype DN_BF16, dk = dv = 128, chunk 64;
  * otherwise DN_ERR_UNSUPPORTED), and at most about 32,000 packed sequences
  * (larger returns DN_ERR_WORKSPACE).  The first call on each device looks up
