@@ -370,13 +370,13 @@ def main():
     pk, src = peaks()
     abytes = algorithmic_bytes(w, x) + (algorithmic_bytes_bwd(w, x) if w.backward else 0)
     achieved = abytes / (ms / 1000.0) / 1e9
-    kname = "gdn_fast_fwd" if fast else "general_fwd"
-    launches_per_step = (1 if fast else 3) + (1 if d["cu_seqlens"] is not None else 0)
+    path, launches_per_step = binding.dn_plan(shape, False)
+    kname = {binding.DN_PATH_COOP: "k_coop_fwd", binding.DN_PATH_FUSED: "k_fast_fwd"}.get(path, "general_fwd")
     if w.backward:
-        launches_per_step += 4
+        launches_per_step += binding.dn_plan(shape, True)[1]
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / pk["hbm_gbs"], "traffic": recorded_traffic(kname, w.name),
-            "kernel": kname if fast else "whole step (3 general kernels)",
+            "kernel": kname if fast else "whole step (general kernels)",
             "algorithmic_bytes_per_launch": abytes, "peak_source": src}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -384,7 +384,9 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "chunk": w.chunk,
                        "pass": "forward+backward" if w.backward else "forward",
-                       "path": "tcgen05 fast path" if fast else "general fp32 path",
+                       "path": {binding.DN_PATH_COOP: "cooperative tcgen05 kernel",
+                                binding.DN_PATH_FUSED: "fused tcgen05 kernel per (sequence, head)"}.get(
+                                    path, "general fp32 kernels"),
                        "l2": "no flush: inputs %.2f GB per step > 129 MB L2" % (abytes / 1e9),
                        "parallelism": "replicas over ranks" if world > 1 else "single GPU"},
             "roofline": roof, "clocks": clocks, "e2e": e2e,

@@ -7,7 +7,7 @@ call returns an error status, these functions raise.
 
 The names match the C ABI: dn_workspace_size, dn_chunk_fwd, gdn_chunk_fwd,
 gdn_chunk_bwd, dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status,
-dn_uses_fast_path.  ``forward`` / ``backward`` additionally allocate outputs
+dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc.  ``forward`` / ``backward`` additionally allocate outputs
 and the workspace with torch (device memory only).
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ DN_F32, DN_BF16 = 0, 1
 
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
-           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc"]
+           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_plan"]
 
 
 class DnShape(ctypes.Structure):
@@ -66,6 +66,8 @@ def lib():
             L.dn_workspace_size.restype = S
             L.dn_uses_fast_path.argtypes = [SP, I]
             L.dn_uses_fast_path.restype = I
+            L.dn_plan.argtypes = [SP, I, ctypes.POINTER(ctypes.c_int)]
+            L.dn_plan.restype = I
             L.dn_chunk_fwd.argtypes = [SP, P, P, P, P, P, P, P, P, S, P]
             L.dn_chunk_fwd.restype = I
             L.gdn_chunk_fwd.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P]
@@ -138,6 +140,17 @@ def dn_workspace_size(shape: DnShape, for_backward: bool = False) -> int:
 
 def dn_uses_fast_path(shape: DnShape, for_backward: bool = False) -> int:
     return int(lib().dn_uses_fast_path(ctypes.byref(shape), int(bool(for_backward))))
+
+
+DN_PATH_GENERAL, DN_PATH_FUSED, DN_PATH_COOP = 0, 1, 2
+PATH_NAMES = {DN_PATH_GENERAL: "general", DN_PATH_FUSED: "fused", DN_PATH_COOP: "coop"}
+
+
+def dn_plan(shape: DnShape, for_backward: bool = False):
+    """(path, kernels per call): DN_PATH_* and the number of library kernels one call launches."""
+    n = ctypes.c_int(0)
+    path = int(lib().dn_plan(ctypes.byref(shape), int(bool(for_backward)), ctypes.byref(n)))
+    return path, int(n.value)
 
 
 def dn_host_arena_size(shape: DnShape, gated: bool, with_h0: bool) -> int:

@@ -233,6 +233,29 @@ int dn_uses_fast_path(const dn_shape *shape, int for_backward)
     return fast_ok(shape, g, for_backward) ? 1 : 0;
 }
 
+int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
+{
+    Geo g;
+    if (check_shape(shape, &g) != DN_OK) return -1;
+    const int offsets = g.varlen ? 1 : 0;   // k_cstart
+    int path, n;
+    if (for_backward) {
+        path = DN_PATH_GENERAL;
+        n = 4 + offsets;                    // k_prep, k_scan, k_bscan, k_bchunk
+    } else if (!fast_ok(shape, g, 0)) {
+        path = DN_PATH_GENERAL;
+        n = 3 + offsets;                    // k_prep, k_scan, k_out
+    } else if (use_coop()) {
+        path = DN_PATH_COOP;
+        n = 1 + 2 * offsets;                // k_coop_fwd (+ k_cstart, k_plan)
+    } else {
+        path = DN_PATH_FUSED;
+        n = 1 + 2 * offsets;                // k_fast_fwd (+ k_cstart, k_order)
+    }
+    if (kernels) *kernels = n;
+    return path;
+}
+
 dn_status dn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
                        const void *beta, const float *h0, void *o, float *hT, void *ws,
                        size_t ws_bytes, void *stream)

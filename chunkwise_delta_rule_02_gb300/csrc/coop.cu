@@ -719,6 +719,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 if (t == 0) s_g[0] = ex2f(glC);
             }
             named_bar(bar_id, 128);
+            if (c == 0 && t == 0) CTR(j, 19);
             // A = strict_lower(diag(beta n) (K K^T o D) diag(n))
             if (q4 < 2) {
                 const int r = q4 * 32 + lane;
@@ -741,6 +742,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 }
             }
             named_bar(bar_id, 128);
+            if (c == 0 && t == 0) CTR(j, 20);
             solve_unit_lower_64<AST>(Af, Xf, lane, q4, bar_id);
             if (c == 0 && t == 0) CTR(j, 16);
             // A is dead: its space now takes the package tail (T | P | vectors)
@@ -806,6 +808,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             }
             fence_async_smem();
             named_bar(bar_id, 128);
+            if (c == 0 && t == 0) CTR(j, 21);
             if (t == 0) {
                 // W^T = K^T T'^T
                 tc_fence_after();
@@ -829,6 +832,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                     *(uint4 *)(qr + q * 16) = a;
                 }
             }
+            if (c == 0 && t == 0) CTR(j, 22);
             wait(P_W, k_task);
             tc_fence_after();
             if (c == 0 && t == 0) CTR(j, 17);
@@ -847,6 +851,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             tc_fence_before();
             fence_async_smem();
             named_bar(bar_id, 128);
+            if (c == 0 && t == 0) CTR(j, 23);
             if (t == 0 && !*abort_flag) {
                 // publish: package -> ring slot, then the ready flag
                 fence_async_global();

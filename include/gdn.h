@@ -163,6 +163,16 @@ const char *dn_status_str(dn_status s);
  * general fp32 path, -1 = invalid shape.  for_backward as above. */
 int dn_uses_fast_path(const dn_shape *shape, int for_backward);
 
+/* Which kernels one call with `shape` runs, for launch accounting and CUDA
+ * graph planning.  Returns DN_PATH_GENERAL (fp32 CUDA-core kernels),
+ * DN_PATH_FUSED (one fused tcgen05 CTA per (sequence, head)) or DN_PATH_COOP
+ * (the cooperative persistent tcgen05 kernel), or -1 for an invalid shape.  If
+ * `kernels` is not null it receives the number of the library's own kernels the
+ * call launches (memsets of the workspace are not counted).  for_backward as
+ * above; the gdn_chunk_fwd_noalloc entry point never takes DN_PATH_COOP. */
+enum { DN_PATH_GENERAL = 0, DN_PATH_FUSED = 1, DN_PATH_COOP = 2 };
+int dn_plan(const dn_shape *shape, int for_backward, int *kernels);
+
 #ifdef __cplusplus
 }
 #endif

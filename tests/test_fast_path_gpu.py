@@ -26,14 +26,21 @@ def _wl(**kw):
     return workloads.Workload(**base)
 
 
-def _run(x, force_general=False):
+def _run(x, force_general=False, kernel="coop"):
+    """Forward through the C ABI on the general kernels, the cooperative kernel
+    (kernel="coop", the default path) or the one-CTA-per-item fused kernel."""
     import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding
     d = to_dev(x, DEV)
-    old = os.environ.get("GDN_FORCE_GENERAL")
+    old = {k: os.environ.get(k) for k in ("GDN_FORCE_GENERAL", "GDN_FUSED_PER_ITEM")}
     os.environ["GDN_FORCE_GENERAL"] = "1" if force_general else "0"
+    os.environ["GDN_FUSED_PER_ITEM"] = "1" if kernel == "fused" else "0"
     try:
         shape = gdn.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])
         assert gdn.dn_uses_fast_path(shape) == (0 if force_general else 1)
+        want = binding.DN_PATH_GENERAL if force_general else (
+            binding.DN_PATH_FUSED if kernel == "fused" else binding.DN_PATH_COOP)
+        assert binding.dn_plan(shape)[0] == want
         ws = gdn.binding.alloc_workspace(shape, False, DEV)
         o = torch.empty_like(d["v"])
         N = x["cu_seqlens"].numel() - 1 if x["cu_seqlens"] is not None else x["q"].shape[0]
@@ -44,30 +51,33 @@ def _run(x, force_general=False):
             gdn.gdn_chunk_fwd(shape, d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], o, hT, ws)
         assert gdn.dn_device_status(ws) == 0
     finally:
-        if old is None:
-            del os.environ["GDN_FORCE_GENERAL"]
-        else:
-            os.environ["GDN_FORCE_GENERAL"] = old
+        for k, v in old.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
     return o.float().cpu().numpy(), hT.cpu().numpy()
 
 
+@pytest.mark.parametrize("kernel", ["coop", "fused"])
 @pytest.mark.parametrize("T", [64, 1, 65, 200, 1000])
 @pytest.mark.parametrize("gated,h0", [(True, True), (False, False)])
-def test_fast_forward_small(T, gated, h0):
+def test_fast_forward_small(T, gated, h0, kernel):
     from chunkwise_delta_rule_02_gb300 import workloads
     x = workloads.generate(_wl(T=T, gated=gated, with_h0=h0, seed=T))
-    o, hT = _run(x)
+    o, hT = _run(x, kernel=kernel)
     ro, rh = oracle_fwd(x)
     assert np.isfinite(o).all() and np.isfinite(hT).all()
     assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
     assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
 
 
-def test_fast_forward_varlen_ragged():
+@pytest.mark.parametrize("kernel", ["coop", "fused"])
+def test_fast_forward_varlen_ragged(kernel):
     from chunkwise_delta_rule_02_gb300 import workloads
     w = _wl(B=1, H=3, T=0, with_h0=True, varlen_total=1, varlen_n=1, seed=9)
     x = workloads.generate(w, lengths=[5, 64, 0, 130, 300, 1, 63])
-    o, hT = _run(x)
+    o, hT = _run(x, kernel=kernel)
     ro, rh = oracle_fwd(x)
     assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
     assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
@@ -87,7 +97,9 @@ def test_fast_strong_decay_and_unit_beta():
     x = workloads.generate(_wl(T=256, seed=3))
     x["g"] = x["g"] * 40.0            # mean about -2 per token: chunk decays ~exp(-130)
     x["beta"] = torch.ones_like(x["beta"])
-    o, hT = _run(x)
     ro, rh = oracle_fwd(x)
-    assert np.isfinite(o).all() and np.isfinite(hT).all()
-    assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+    for kernel in ("coop", "fused"):
+        o, hT = _run(x, kernel=kernel)
+        assert np.isfinite(o).all() and np.isfinite(hT).all()
+        assert rel(o, ro) <= TOL["bf16"], (kernel, rel(o, ro))
+        assert rel(hT, rh) <= TOL["bf16"], (kernel, rel(hT, rh))

@@ -66,6 +66,21 @@ def test_workspace_size_and_validation(gdn):
     assert gdn.dn_workspace_size(_shape(gdn, B=1, cu=16, N=3), False) > 0
 
 
+def test_plan_reports_path_and_kernel_count(gdn):
+    # fp32 runs the three general kernels, the backward four; packed input adds k_cstart
+    assert gdn.dn_plan(_shape(gdn, dtype=0), False) == (gdn.DN_PATH_GENERAL, 3)
+    assert gdn.dn_plan(_shape(gdn, d=128), True) == (gdn.DN_PATH_GENERAL, 4)
+    assert gdn.dn_plan(_shape(gdn, B=1, dtype=0, cu=16, N=3), False) == (gdn.DN_PATH_GENERAL, 4)
+    # bf16 d = 128 takes one of the tcgen05 kernels on an sm_103 device (one launch, plus
+    # two for packed input); without such a device it falls to the general kernels
+    fused = (gdn.DN_PATH_FUSED, gdn.DN_PATH_COOP)
+    path, n = gdn.dn_plan(_shape(gdn, d=128), False)
+    assert (path in fused and n == 1) or (path == gdn.DN_PATH_GENERAL and n == 3)
+    path, n = gdn.dn_plan(_shape(gdn, B=1, d=128, cu=16, N=3), False)
+    assert (path in fused and n == 3) or (path == gdn.DN_PATH_GENERAL and n == 4)
+    assert gdn.dn_plan(_shape(gdn, B=0), False)[0] == -1
+
+
 def test_status_codes_without_device_work(gdn):
     L = gdn.lib()
     s = _shape(gdn)
