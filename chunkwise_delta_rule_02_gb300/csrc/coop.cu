@@ -36,7 +36,7 @@
 // Optional event timeline of chain CTA 0 and of the preparation of its chunks
 // (compiled only with -DGDN_TRACE).
 #ifdef GDN_TRACE
-__device__ unsigned long long g_coop_trace[256][24];
+__device__ unsigned long long g_coop_trace[256][32];
 #define CTR(n, e)                                                                \
     do {                                                                         \
         if ((n) < 256) {                                                         \
@@ -61,7 +61,7 @@ namespace {
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NTHREADS = 512;
-constexpr int RING = 4;
+constexpr int RING = 8;
 constexpr long long BUDGET = 4000000000LL;                 // clock cycles (about 2 s)
 constexpr float RENORM_BELOW = 9.313225746154785e-10f;      // 2^-30
 
@@ -83,18 +83,19 @@ constexpr uint32_t CH_U2 = CH_U1 + 16384;           // (f o Unew)^T bf16 (16 KB)
 constexpr uint32_t CH_BAR = CH_U2 + 16384;
 constexpr uint32_t CH_END = CH_BAR + 32 * 8 + 64;
 
-// preparation CTA shared memory, per pipeline
-constexpr uint32_t AST = 68;                        // row stride (floats) of the solve matrices
-constexpr uint32_t PP_TL = 0;                       // 32 KB K|Q tiles, become -W|Qt (package WQ)
-constexpr uint32_t PP_AF = 32768;                   // A fp32 [64][68]; then T|P|vec (package tail)
-constexpr uint32_t PP_XF = PP_AF + 64 * AST * 4;    // X fp32 [64][68]
-constexpr uint32_t PP_TP = PP_XF + 64 * AST * 4;    // T' bf16 [r][i] 8 KB
-constexpr uint32_t PP_VEC = PP_TP + 8192;           // vectors, 12 x 64 floats
+// preparation CTA shared memory, per pipeline (four pipelines of four warps)
+constexpr int PIPES = 4;
+constexpr uint32_t AST = 72;                        // row stride (floats) of the solve buffer
+constexpr uint32_t PP_TL = 0;                       // 32 KB: per 64-column half [K rows | Q rows];
+                                                    //   K becomes -W, Q becomes Qt and then T (half 0) | P (half 1)
+constexpr uint32_t PP_AX = 32768;                   // fp32 [64][72]: A below the diagonal, X^T on and
+                                                    //   above it; then T' (bf16, first 8 KB)
+constexpr uint32_t PP_VEC = PP_AX + 64 * AST * 4;   // vectors, 12 x 64 floats
 constexpr uint32_t PP_BAR = PP_VEC + 12 * 256;      // barriers + task word
-constexpr uint32_t PP_STRIDE = 80896;               // 79 KB
+constexpr uint32_t PP_STRIDE = 55296;               // 54 KB, a multiple of 1 KB (128-byte swizzle)
 static_assert(PP_BAR + 64 <= PP_STRIDE, "pipeline layout");
-static_assert(PP_AF + PK_BYTES - PK_T <= PP_XF, "package tail must fit in A's space");
-constexpr uint32_t SMEM_USED = (CH_END > 2 * PP_STRIDE ? CH_END : 2 * PP_STRIDE);
+static_assert(PP_STRIDE % 1024 == 0 && PP_AX % 1024 == 0, "swizzled operands need 1 KB alignment");
+constexpr uint32_t SMEM_USED = (CH_END > PIPES * PP_STRIDE ? CH_END : PIPES * PP_STRIDE);
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
@@ -553,6 +554,12 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
 }
 
 // ================================================================================= preparation role
+// Four independent pipelines (warps 4p .. 4p + 3) take chunk tasks from a global
+// counter.  One task, for chunk n of item (seq, head):
+//   TMA K, Q -> [K;Q][K;Q]^T on the tensor cores (Gram rows, Q K^T rows, both
+//   norms on the diagonal) -> gates, scale vectors -> Qt in place, published at
+//   once -> A (warps 0, 1) while P is built (warps 2, 3) -> (I + A)^-1 in place ->
+//   T, T' -> -(T' K) on the tensor cores -> -W over K -> publish, ready flag.
 __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, uint8_t *sm)
 {
@@ -564,10 +571,10 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
-    const int pipe = (warp >> 2) - 1;   // warps 4..7 -> 0, 8..11 -> 1
-    uint8_t *base = sm + (pipe >= 0 ? pipe : 0) * PP_STRIDE;
+    const int pipe = warp >> 2;
+    uint8_t *base = sm + pipe * PP_STRIDE;
     uint64_t *bar = (uint64_t *)(base + PP_BAR);
-    if (pipe >= 0 && pipe < 2 && (warp & 3) == 0 && lane == 0) {
+    if ((warp & 3) == 0 && lane == 0) {
         for (int i = 0; i < NBAR_PP; ++i) mbar_init(&bar[i], 1);
         fence_barrier_init();
     }
@@ -577,305 +584,330 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
     const uint32_t tmem = s_tmem;
     volatile int *abort_flag = &s_abort;
 
-    if (pipe >= 0 && pipe < 2) {
-        const int t = tid - (pipe + 1) * 128;   // 0..127 within the pipeline
-        const int q4 = warp & 3;
-        const int bar_id = 1 + pipe;
-        const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
-        const uint32_t tg = tmem + pipe * 256;          // [K;Q][K;Q]^T (128 columns)
-        const uint32_t tw = tmem + pipe * 256 + 128;    // W^T (64 columns)
-        const uint32_t sbase = smem_u32(base);
-        volatile int *task_word = (volatile int *)(base + PP_BAR + NBAR_PP * 8);
-        float *vb = (float *)(base + PP_VEC);
-        float *s_beta = vb, *s_gl = vb + 64, *s_nk = vb + 128, *s_nq = vb + 192, *s_tc = vb + 256;
-        float *s_qs = vb + 320, *s_ra = vb + 384, *s_cb = vb + 448, *s_f0 = vb + 512, *s_g = vb + 576;
-        int *s_safe = (int *)(vb + 640);
-        float *Af = (float *)(base + PP_AF);
-        float *Xf = (float *)(base + PP_XF);
-        const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
-        const long long ntasks = (long long)p.Nc * Jmax;
-        auto fail = [&]() {
+    const int t = tid & 127;   // thread within the pipeline
+    const int q4 = warp & 3;   // warp within the pipeline = its TMEM lane quarter
+    const int bar_id = 1 + pipe;            // the pipeline's four warps
+    const int bar_hi = 1 + PIPES + pipe;    // its warps 2 and 3
+    const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tg = tmem + pipe * 128;  // [K;Q][K;Q]^T (128 columns), later T' K
+    const uint32_t sbase = smem_u32(base);
+    volatile int *task_word = (volatile int *)(base + PP_BAR + NBAR_PP * 8);
+    float *vb = (float *)(base + PP_VEC);
+    float *s_beta = vb, *s_gl = vb + 64, *s_nk = vb + 128, *s_nq = vb + 192, *s_tc = vb + 256;
+    float *s_qs = vb + 320, *s_ra = vb + 384, *s_cb = vb + 448, *s_f0 = vb + 512, *s_g = vb + 576;
+    int *s_safe = (int *)(vb + 640);
+    float *AX = (float *)(base + PP_AX);
+    uint8_t *tl = base + PP_TL;
+    const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
+    const long long ntasks = (long long)p.Nc * Jmax;
+    auto fail = [&]() {
+        if (!*abort_flag) {
+            *abort_flag = 1;
+            raise_status(p.status, kStatusTimeout);
+        }
+    };
+    auto wait = [&](int b, uint32_t k) -> bool {
+        if (mbar_wait(&bar[b], k & 1u, BUDGET, abort_flag)) return true;
+        fail();
+        return false;
+    };
+    uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
+    bool tma_pending = false, mma_issued = false;
+    while (true) {
+        if (t == 0) {
+            const int tk = (int)atomicAdd(&p.ctl[0], 1u);
+            *task_word = *abort_flag ? 0x7fffffff : tk;   // one decision for the whole pipeline
+        }
+        named_bar(bar_id, 128);
+        const int task = *task_word;
+        named_bar(bar_id, 128);
+        if (task >= ntasks) break;
+        const int c = task % p.Nc, j = task / p.Nc;
+        // find chunk j of chain CTA c
+        Item I;
+        int n = j, it = c;
+        bool found = false;
+        for (; it < p.items; it += p.Nc) {
+            I = item_of(p, it);
+            if (n < I.nch) { found = true; break; }
+            n -= I.nch;
+        }
+        if (!found) continue;
+        if (c == 0 && t == 0) CTR(j, 12);
+        const int len = min(C, I.L - n * C);
+        const long long row0 = I.rowbase + (long long)n * C;
+        const int slot = j % RING;
+        uint32_t *consumed = p.ctl + 2 + c;
+        uint32_t *ready = p.ctl + 2 + p.Nc + c * RING + slot;
+        uint8_t *dst = p.ring + ((size_t)c * RING + slot) * PK_STRIDE;
+        if (t == 0) {
+            // the ring slot must have been copied out by the chain CTA
+            const long long t0 = clock64();
+            while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
+                if (clock64() - t0 > BUDGET) { fail(); break; }
+                __nanosleep(128);
+            }
             if (!*abort_flag) {
-                *abort_flag = 1;
-                raise_status(p.status, kStatusTimeout);
+                mbar_expect_tx(&bar[P_FULL], 32768);
+                tma_load_2d(tl, tm_k, &bar[P_FULL], 0, (int)row0);
+                tma_load_2d(tl + 16384, tm_k, &bar[P_FULL], 64, (int)row0);
+                tma_load_2d(tl + 8192, tm_q, &bar[P_FULL], 0, (int)row0);
+                tma_load_2d(tl + 24576, tm_q, &bar[P_FULL], 64, (int)row0);
+                tma_pending = true;
+                if (c == 0) CTR(j, 13);
             }
-        };
-        auto wait = [&](int b, uint32_t k) -> bool {
-            if (mbar_wait(&bar[b], k & 1u, BUDGET, abort_flag)) return true;
-            fail();
-            return false;
-        };
-        uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
-        bool tma_pending = false, mma_issued = false;
-        while (true) {
-            if (t == 0) {
-                const int tk = (int)atomicAdd(&p.ctl[0], 1u);
-                *task_word = *abort_flag ? 0x7fffffff : tk;   // one decision for the whole pipeline
+        }
+        if (q4 == 0) {
+            // beta and g (zero past the chunk), gates scanned in log2 units
+            float g0 = 0.f, g1 = 0.f;
+            s_beta[lane] = lane < len ? __bfloat162float(p.beta[row0 + lane]) : 0.f;
+            s_beta[lane + 32] = lane + 32 < len ? __bfloat162float(p.beta[row0 + lane + 32]) : 0.f;
+            if (p.gate) {
+                g0 = lane < len ? p.gate[row0 + lane] : 0.f;
+                g1 = lane + 32 < len ? p.gate[row0 + lane + 32] : 0.f;
             }
-            named_bar(bar_id, 128);
-            const int task = *task_word;
-            named_bar(bar_id, 128);
-            if (task >= ntasks) break;
-            const int c = task % p.Nc, j = task / p.Nc;
-            // find chunk j of chain CTA c
-            Item I;
-            int n = j, it = c;
-            bool found = false;
-            for (; it < p.items; it += p.Nc) {
-                I = item_of(p, it);
-                if (n < I.nch) { found = true; break; }
-                n -= I.nch;
-            }
-            if (!found) continue;
-            if (c == 0 && t == 0) CTR(j, 12);
-            const int len = min(C, I.L - n * C);
-            const long long row0 = I.rowbase + (long long)n * C;
-            const int slot = j % RING;
-            uint32_t *consumed = p.ctl + 2 + c;
-            uint32_t *ready = p.ctl + 2 + p.Nc + c * RING + slot;
-            uint8_t *dst = p.ring + ((size_t)c * RING + slot) * PK_STRIDE;
-            if (t == 0) {
-                // the ring slot must have been copied out by the chain CTA
-                const long long t0 = clock64();
-                while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
-                    if (clock64() - t0 > BUDGET) { fail(); break; }
-                    __nanosleep(128);
-                }
-                if (!*abort_flag) {
-                    mbar_expect_tx(&bar[P_FULL], 32768);
-                    tma_load_2d(base + PP_TL, tm_k, &bar[P_FULL], 0, (int)row0);
-                    tma_load_2d(base + PP_TL + 16384, tm_k, &bar[P_FULL], 64, (int)row0);
-                    tma_load_2d(base + PP_TL + 8192, tm_q, &bar[P_FULL], 0, (int)row0);
-                    tma_load_2d(base + PP_TL + 24576, tm_q, &bar[P_FULL], 64, (int)row0);
-                    tma_pending = true;
-                    if (c == 0) CTR(j, 13);
-                }
-            }
-            if (q4 == 0) {
-                // beta and g (zero past the chunk), gates scanned in log2 units
-                float g0 = 0.f, g1 = 0.f;
-                s_beta[lane] = lane < len ? __bfloat162float(p.beta[row0 + lane]) : 0.f;
-                s_beta[lane + 32] = lane + 32 < len ? __bfloat162float(p.beta[row0 + lane + 32]) : 0.f;
-                if (p.gate) {
-                    g0 = lane < len ? p.gate[row0 + lane] : 0.f;
-                    g1 = lane + 32 < len ? p.gate[row0 + lane + 32] : 0.f;
-                }
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    float a0 = __shfl_up_sync(0xffffffffu, g0, o);
-                    float a1 = __shfl_up_sync(0xffffffffu, g1, o);
-                    if (lane >= o) { g0 += a0; g1 += a1; }
-                }
-                g1 += __shfl_sync(0xffffffffu, g0, 31);
-                g0 *= 1.4426950408889634f;
-                g1 *= 1.4426950408889634f;
-                s_gl[lane] = g0;
-                s_gl[lane + 32] = g1;
-                float mx = fmaxf(fabsf(g0), fabsf(g1));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (lane == 0) *s_safe = mx < 100.f;
+            for (int o = 1; o < 32; o <<= 1) {
+                float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+                float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+                if (lane >= o) { g0 += a0; g1 += a1; }
             }
-            if (wait(P_FULL, k_task) && t == 0) tma_pending = false;
-            if (c == 0 && t == 0) CTR(j, 14);
-            if (t == 0) {
-                // [K;Q][K;Q]^T: Gram rows, Q K^T rows and both norms on the diagonals
-                mma_issued = true;
-                tc_fence_after();
-                const uint64_t d = sdesc(sbase + PP_TL, 16, 1024);
+            g1 += __shfl_sync(0xffffffffu, g0, 31);
+            g0 *= 1.4426950408889634f;
+            g1 *= 1.4426950408889634f;
+            s_gl[lane] = g0;
+            s_gl[lane + 32] = g1;
+            float mx = fmaxf(fabsf(g0), fabsf(g1));
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t dk = dadd(d, (k >> 2) * 16384 + (k & 3) * 32);
-                    mma_bf16_ss(tg, dk, dk, ID_SS_N128, k > 0);
-                }
-                mma_commit(&bar[P_G]);
-            }
-            wait(P_G, k_task);
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) *s_safe = mx < 100.f;
+        }
+        if (wait(P_FULL, k_task) && t == 0) tma_pending = false;
+        if (c == 0 && t == 0) CTR(j, 14);
+        if (t == 0) {
+            // [K;Q][K;Q]^T: Gram rows, Q K^T rows and both norms on the diagonals
+            mma_issued = true;
             tc_fence_after();
-            if (c == 0 && t == 0) CTR(j, 15);
-            {
-                // diagonal element of this lane's row: column 32 q4 + lane
-                uint32_t v[32];
-                tmem_ld32(tg + lrow + 32 * q4, v);
-                tmem_ld_wait();
-                float dg = 0.f;
+            const uint64_t d = sdesc(sbase + PP_TL, 16, 1024);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) dg = (i == lane) ? __uint_as_float(v[i]) : dg;
-                const int r = (q4 & 1) * 32 + lane;
-                const float nrm = r < len ? (p.l2norm ? rsqrtf(dg + p.eps) : 1.f) : 0.f;
-                if (q4 < 2) s_nk[r] = nrm; else s_nq[r] = nrm;
+            for (int k = 0; k < 8; ++k) {
+                const uint64_t dk = dadd(d, (k >> 2) * 16384 + (k & 3) * 32);
+                mma_bf16_ss(tg, dk, dk, ID_SS_N128, k > 0);
             }
-            named_bar(bar_id, 128);
-            const bool safe = *s_safe != 0;
-            const float glC = s_gl[len - 1];
-            if (t < 64) {
-                const float gl = s_gl[t];
-                const float e = ex2f(gl);
-                s_tc[t] = s_beta[t] * e * s_nk[t];
-                s_qs[t] = e * s_nq[t];
-                s_ra[t] = s_beta[t] * s_nk[t] * e;
-                s_cb[t] = safe ? s_nk[t] * ex2f(-gl) : 0.f;
-                s_f0[t] = ex2f(glC - gl) * s_nk[t];
-                if (t == 0) s_g[0] = ex2f(glC);
+            mma_commit(&bar[P_G]);
+        }
+        wait(P_G, k_task);
+        tc_fence_after();
+        if (c == 0 && t == 0) CTR(j, 15);
+        {
+            // diagonal element of this lane's row: column 32 q4 + lane
+            uint32_t v[32];
+            tmem_ld32(tg + lrow + 32 * q4, v);
+            tmem_ld_wait();
+            float dg = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dg = (i == lane) ? __uint_as_float(v[i]) : dg;
+            const int r = (q4 & 1) * 32 + lane;
+            const float nrm = r < len ? (p.l2norm ? rsqrtf(dg + p.eps) : 1.f) : 0.f;
+            if (q4 < 2) s_nk[r] = nrm; else s_nq[r] = nrm;
+        }
+        named_bar(bar_id, 128);
+        const bool safe = *s_safe != 0;
+        const float glC = s_gl[len - 1];
+        if (t < 64) {
+            const float gl = s_gl[t];
+            const float e = ex2f(gl);
+            s_tc[t] = s_beta[t] * e * s_nk[t];
+            s_qs[t] = e * s_nq[t];
+            s_ra[t] = s_beta[t] * s_nk[t] * e;
+            s_cb[t] = safe ? s_nk[t] * ex2f(-gl) : 0.f;
+            s_f0[t] = ex2f(glC - gl) * s_nk[t];
+            if (t == 0) s_g[0] = ex2f(glC);
+        }
+        named_bar(bar_id, 128);
+        if (c == 0 && t == 0) CTR(j, 19);
+        {
+            // Qt = diag(exp(gamma) m) Q in place: 16-byte pieces, a warp covers 4 whole rows
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int idx = u * 128 + t;
+                const int hh = idx >> 9, r = (idx >> 3) & 63;
+                uint4 *qp = (uint4 *)(tl + hh * 16384 + 8192 + r * 128 + (idx & 7) * 16);
+                const float f = s_qs[r];
+                uint4 a = *qp;
+                a.x = scale_pair(a.x, f); a.y = scale_pair(a.y, f);
+                a.z = scale_pair(a.z, f); a.w = scale_pair(a.w, f);
+                *qp = a;
             }
-            named_bar(bar_id, 128);
-            if (c == 0 && t == 0) CTR(j, 19);
-            // A = strict_lower(diag(beta n) (K K^T o D) diag(n))
-            if (q4 < 2) {
-                const int r = q4 * 32 + lane;
-                uint32_t v[64];
-                tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tmem_ld_wait();
-                float4 *arow = reinterpret_cast<float4 *>(Af + r * AST);
-                const float ra = s_ra[r], br = s_beta[r] * s_nk[r], gr = s_gl[r];
+        }
+        fence_async_smem();
+        named_bar(bar_id, 128);
+        if (q4 < 2) {
+            // A = strict_lower(diag(beta n) (K K^T o D) diag(n)), full rows (zeros on and above the diagonal)
+            const int r = q4 * 32 + lane;
+            uint32_t v[64];
+            tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+            float4 *arow = reinterpret_cast<float4 *>(AX + r * AST);
+            const float ra = s_ra[r], br = s_beta[r] * s_nk[r], gr = s_gl[r];
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    float a[4];
+            for (int c4 = 0; c4 < 16; ++c4) {
+                float a[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 4 * c4 + e;
-                        const float gv = __uint_as_float(v[i]);
-                        a[e] = (i < r) ? (safe ? ra * s_cb[i] * gv : br * s_nk[i] * gv * ex2f(gr - s_gl[i])) : 0.f;
-                    }
-                    arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 4 * c4 + e;
+                    const float gv = __uint_as_float(v[i]);
+                    a[e] = (i < r) ? (safe ? ra * s_cb[i] * gv : br * s_nk[i] * gv * ex2f(gr - s_gl[i])) : 0.f;
                 }
+                arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
             }
-            named_bar(bar_id, 128);
-            if (c == 0 && t == 0) CTR(j, 20);
-            solve_unit_lower_64<AST>(Af, Xf, lane, q4, bar_id);
-            if (c == 0 && t == 0) CTR(j, 16);
-            // A is dead: its space now takes the package tail (T | P | vectors)
-            uint8_t *pt = base + PP_AF;
-            if (q4 >= 2) {
-                // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i]
-                const int r = (q4 - 2) * 32 + lane;
+        } else {
+            // publish Qt now; once the copy has read it, its space takes T and P
+            if (t == 64 && !*abort_flag) {
+                bulk_store(dst + PK_WQ + 8192, tl + 8192, 8192);
+                bulk_store(dst + PK_WQ + 24576, tl + 24576, 8192);
+                bulk_commit();
+                bulk_wait_read();
+            }
+            named_bar(bar_hi, 64);
+            // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i], into Qt's second half
+            const int r = (q4 - 2) * 32 + lane;
+            uint32_t v[64];
+            tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+            const float mr = s_nq[r], gr = s_gl[r], rp = mr * ex2f(gr);
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = c8 * 8 + 2 * e, i1 = i0 + 1;
+                    const float v0 = __uint_as_float(v[i0]), v1 = __uint_as_float(v[i1]);
+                    float a0, a1;
+                    if (safe) {
+                        a0 = (i0 <= r) ? rp * s_cb[i0] * v0 : 0.f;
+                        a1 = (i1 <= r) ? rp * s_cb[i1] * v1 : 0.f;
+                    } else {
+                        a0 = (i0 <= r) ? mr * s_nk[i0] * v0 * ex2f(gr - s_gl[i0]) : 0.f;
+                        a1 = (i1 <= r) ? mr * s_nk[i1] * v1 * ex2f(gr - s_gl[i1]) : 0.f;
+                    }
+                    w[e] = pack_bf16(a0, a1);
+                }
+                *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (c == 0 && t == 64) CTR(j, 28);
+        }
+        tc_fence_before();   // G's last reads precede the MMA that reuses its columns
+        named_bar(bar_id, 128);
+        if (c == 0 && t == 0) CTR(j, 20);
+        solve_unit_lower_64_packed<AST>(AX, lane, q4, bar_id);
+        if (c == 0 && t == 0) CTR(j, 16);
+        {
+            // T = X diag(beta) (package, into Qt's first half) and T' = X diag(beta exp(gamma) n)
+            // (operand of the next MMA, over the solve buffer); X[r][i] = AX[i][r] for i <= r
+            const int r = t & 63, hh = t >> 6;
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int i = 32 * hh + e;
+                x[e] = (i <= r) ? AX[i * AST + r] : 0.f;
+            }
+            named_bar(bar_id, 128);   // all of X has been read before T' overwrites it
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t wt[4], wp[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = 32 * hh + 8 * c8 + 2 * e;
+                    const float x0 = x[8 * c8 + 2 * e], x1 = x[8 * c8 + 2 * e + 1];
+                    wt[e] = pack_bf16(x0 * s_beta[i0], x1 * s_beta[i0 + 1]);
+                    wp[e] = pack_bf16(x0 * s_tc[i0], x1 * s_tc[i0 + 1]);
+                }
+                const uint32_t off = sw128(r, (hh * 4 + c8) * 16);
+                *(uint4 *)(tl + 8192 + off) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+                *(uint4 *)(base + PP_AX + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+            }
+            if (c == 0 && t == 0) CTR(j, 29);
+        }
+        fence_async_smem();
+        named_bar(bar_id, 128);
+        if (c == 0 && t == 0) CTR(j, 21);
+        if (t == 0) {
+            // (T' K)[r][dk] with r on TMEM lanes 0..63 (A rows 64..127 are don't-care)
+            tc_fence_after();
+            const uint64_t da = sdesc(sbase + PP_AX, 16, 1024);
+            const uint64_t db = sdesc(sbase + PP_TL, 16384, 1024);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_ss(tg, dadd(da, k * 32), dadd(db, k * 2048), ID_SS_N128_BMN, k > 0);
+            mma_commit(&bar[P_W]);
+            if (c == 0) CTR(j, 24);
+            if (!*abort_flag) {
+                bulk_store(dst + PK_T, tl + 8192, 8192);
+                bulk_store(dst + PK_P, tl + 24576, 8192);
+                bulk_store(dst + PK_VEC, s_f0, 272);   // f0[64], exp(gamma_C)
+                bulk_commit();
+            }
+        }
+        wait(P_W, k_task);
+        tc_fence_after();
+        if (c == 0 && t == 0) CTR(j, 17);
+        if (q4 < 2) {
+            // -W rows over the K rows: token r, 128 columns
+            const int r = q4 * 32 + lane;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
                 uint32_t v[64];
-                tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_ld32(tg + lrow + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(tg + lrow + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                 tmem_ld_wait();
-                const float mr = s_nq[r], gr = s_gl[r], rp = mr * ex2f(gr);
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i0 = c8 * 8 + 2 * e, i1 = i0 + 1;
-                        const float v0 = __uint_as_float(v[i0]), v1 = __uint_as_float(v[i1]);
-                        float a0, a1;
-                        if (safe) {
-                            a0 = (i0 <= r) ? rp * s_cb[i0] * v0 : 0.f;
-                            a1 = (i1 <= r) ? rp * s_cb[i1] * v1 : 0.f;
-                        } else {
-                            a0 = (i0 <= r) ? mr * s_nk[i0] * v0 * ex2f(gr - s_gl[i0]) : 0.f;
-                            a1 = (i1 <= r) ? mr * s_nk[i1] * v1 * ex2f(gr - s_gl[i1]) : 0.f;
-                        }
-                        w[e] = pack_bf16(a0, a1);
-                    }
-                    *(uint4 *)(pt + (PK_P - PK_T) + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(-__uint_as_float(v[8 * c8 + 2 * e]), -__uint_as_float(v[8 * c8 + 2 * e + 1]));
+                    *(uint4 *)(tl + h * 16384 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-            }
-            {
-                // T = X diag(beta) (package) and T' = X diag(beta exp(gamma) n) (local), bf16 [r][i]
-                const int r = t >> 1, hh = t & 1;
-                const float4 *xr = reinterpret_cast<const float4 *>(Xf + r * AST + hh * 32);
-                const float4 *b4 = reinterpret_cast<const float4 *>(s_beta + hh * 32);
-                const float4 *c4 = reinterpret_cast<const float4 *>(s_tc + hh * 32);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t wt[4], wp[4];
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const int q = c8 * 2 + e2;
-                        float4 x = xr[q];
-                        const int i0 = hh * 32 + 4 * q;
-                        if (i0 > r) x.x = 0.f;
-                        if (i0 + 1 > r) x.y = 0.f;
-                        if (i0 + 2 > r) x.z = 0.f;
-                        if (i0 + 3 > r) x.w = 0.f;
-                        const float4 bb = b4[q], cc = c4[q];
-                        wt[2 * e2] = pack_bf16(x.x * bb.x, x.y * bb.y);
-                        wt[2 * e2 + 1] = pack_bf16(x.z * bb.z, x.w * bb.w);
-                        wp[2 * e2] = pack_bf16(x.x * cc.x, x.y * cc.y);
-                        wp[2 * e2 + 1] = pack_bf16(x.z * cc.z, x.w * cc.w);
-                    }
-                    const uint32_t off = sw128(r, (hh * 4 + c8) * 16);
-                    *(uint4 *)(pt + off) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
-                    *(uint4 *)(base + PP_TP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-                }
-                if (t < 64) ((float *)(pt + (PK_VEC - PK_T)))[t] = s_f0[t];
-                if (t == 0) ((float *)(pt + (PK_VEC - PK_T)))[64] = s_g[0];
-            }
-            fence_async_smem();
-            named_bar(bar_id, 128);
-            if (c == 0 && t == 0) CTR(j, 21);
-            if (t == 0) {
-                // W^T = K^T T'^T
-                tc_fence_after();
-                const uint64_t dk = sdesc(sbase + PP_TL, 16384, 1024);
-                const uint64_t dtp = sdesc(sbase + PP_TP, 16, 1024);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ss(tw, dadd(dk, k * 2048), dadd(dtp, k * 32), ID_SS_N64_AMN, k > 0);
-                mma_commit(&bar[P_W]);
-            }
-            {
-                // Qt = diag(exp(gamma) m) Q in place (the Q rows of the package's WQ block)
-                const int r = t >> 1, hh = t & 1;
-                const float f = s_qs[r];
-                uint8_t *qr = base + PP_TL + hh * 16384 + 8192 + r * 128;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint4 a = *(uint4 *)(qr + q * 16);
-                    a.x = scale_pair(a.x, f); a.y = scale_pair(a.y, f);
-                    a.z = scale_pair(a.z, f); a.w = scale_pair(a.w, f);
-                    *(uint4 *)(qr + q * 16) = a;
-                }
-            }
-            if (c == 0 && t == 0) CTR(j, 22);
-            wait(P_W, k_task);
-            tc_fence_after();
-            if (c == 0 && t == 0) CTR(j, 17);
-            {
-                // -W rows over the K rows (K is no longer needed): element (token r, dk)
-                uint32_t v[64];
-                tmem_ld32(tw + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tw + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tmem_ld_wait();
-                const int dk = q4 * 32 + lane;
-                uint8_t *wb = base + PP_TL + (dk >> 6) * 16384;
-#pragma unroll
-                for (int r = 0; r < 64; ++r)
-                    *(__nv_bfloat16 *)(wb + sw128(r, (dk & 63) * 2)) = __float2bfloat16_rn(-__uint_as_float(v[r]));
-            }
-            tc_fence_before();
-            fence_async_smem();
-            named_bar(bar_id, 128);
-            if (c == 0 && t == 0) CTR(j, 23);
-            if (t == 0 && !*abort_flag) {
-                // publish: package -> ring slot, then the ready flag
-                fence_async_global();
-                bulk_store(dst + PK_WQ, base + PP_TL, 32768);
-                bulk_store(dst + PK_T, base + PP_AF, PK_BYTES - PK_T);
-                bulk_commit();
-                bulk_wait_all();
-                fence_async_global();
-                __threadfence();
-                st_release_gpu(ready, (uint32_t)(j + 1));
-                if (c == 0) CTR(j, 18);
-            }
-            ++k_task;
-            named_bar(bar_id, 128);
-        }
-        if (t == 0) {
-            // nothing of this pipeline may still be in flight when the block exits
-            if (tma_pending) mbar_wait(&bar[P_FULL], k_task & 1u, BUDGET, nullptr);
-            if (mma_issued) {
-                mma_commit(&bar[P_DONE]);
-                mbar_wait(&bar[P_DONE], 0, BUDGET, nullptr);
             }
         }
+        tc_fence_before();
+        fence_async_smem();
+        if (t == 64) {
+            // Qt's copy has landed before the ready flag goes up
+            bulk_wait_all();
+            fence_async_global();
+            __threadfence();
+        }
+        named_bar(bar_id, 128);
+        if (c == 0 && t == 0) CTR(j, 23);
+        if (t == 0 && !*abort_flag) {
+            // publish -W, then the ready flag
+            bulk_store(dst + PK_WQ, tl, 8192);
+            bulk_store(dst + PK_WQ + 16384, tl + 16384, 8192);
+            bulk_commit();
+            bulk_wait_all();
+            fence_async_global();
+            __threadfence();
+            st_release_gpu(ready, (uint32_t)(j + 1));
+            if (c == 0) CTR(j, 18);
+        }
+        if (t == 0) bulk_wait_all();   // nothing may still read this pipeline's buffers
+        ++k_task;
+        named_bar(bar_id, 128);
     }
+    if (t == 0) {
+        // nothing of this pipeline may still be in flight when the block exits
+        if (tma_pending) mbar_wait(&bar[P_FULL], k_task & 1u, BUDGET, nullptr);
+        if (mma_issued) {
+            mma_commit(&bar[P_DONE]);
+            mbar_wait(&bar[P_DONE], 0, BUDGET, nullptr);
+        }
+        bulk_wait_all();
+    }
+    if (t == 64) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

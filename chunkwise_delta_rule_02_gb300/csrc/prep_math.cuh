@@ -117,5 +117,86 @@ __device__ __forceinline__ void solve_unit_lower_64(const float *Af, float *Xf, 
     sm100::named_bar(bar_id, 128);
 }
 
+// The same inverse computed in one buffer.  On entry AX holds the strictly lower
+// triangular A below its diagonal (fp32, row stride AST floats; what lies on and
+// above the diagonal is ignored).  On return the strictly lower blocks still hold
+// A, and X is stored transposed on and above the diagonal:
+//     AX[c * AST + r] = X[r][c]   for every r >= c,
+// with each diagonal 16 x 16 block rewritten in full as X_ii^T (unit diagonal,
+// zeros for the upper part of X_ii).  The off-diagonal blocks X_ij (i > j) go to
+// block (j, i); nothing reads or writes A's blocks after the diagonal phase, so
+// the column-parallel schedule of solve_unit_lower_64 carries over unchanged.
+// Called by the 128 threads of one warpgroup; synchronises it (named barrier
+// bar_id) between the phases and at the end.
+template <int AST>
+__device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, int q4, int bar_id)
+{
+    {
+        const int base = 16 * q4, c = lane & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float acc = (i == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int l = 0; l < i; ++l) acc = fmaf(-AX[(base + i) * AST + base + l], x[l], acc);
+            x[i] = (i < c) ? 0.f : acc;
+        }
+        __syncwarp();   // every lane has read A_ii before its block is overwritten
+        if (lane < 16) {
+            float4 *dst = reinterpret_cast<float4 *>(AX + (base + c) * AST + base);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        }
+    }
+    sm100::named_bar(bar_id, 128);
+    const int g8 = lane >> 2, t4 = lane & 3;
+    if (q4 < 3) {
+        const int j = q4;
+        for (int i = j + 1; i < 4; ++i) {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int m = j; m < i; ++m) {
+                // Z = X_ii A_im
+                float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const float *xa = AX + (16 * i + 8 * ks) * AST + 16 * i;   // X_ii[r][8ks + k] = xa[k * AST + r]
+                    uint32_t a[4] = {tf32(xa[t4 * AST + g8]), tf32(xa[t4 * AST + g8 + 8]),
+                                     tf32(xa[(t4 + 4) * AST + g8]), tf32(xa[(t4 + 4) * AST + g8 + 8])};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float *ab = AX + (16 * i + 8 * ks) * AST + 16 * m + 8 * nt + g8;
+                        uint32_t b[2] = {tf32(ab[t4 * AST]), tf32(ab[(t4 + 4) * AST])};
+                        mma_tf32_16x8x8(z[nt], a, b);
+                    }
+                }
+                // acc += Z X_mj, with Z's accumulator layout reused as the A operand
+                // (k order permuted: k = t4 <-> column 2 t4, k = t4 + 4 <-> 2 t4 + 1)
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4] = {tf32(z[ks][0]), tf32(z[ks][2]), tf32(z[ks][1]), tf32(z[ks][3])};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float2 xb = *reinterpret_cast<const float2 *>(
+                            AX + (16 * j + 8 * nt + g8) * AST + 16 * m + 8 * ks + 2 * t4);
+                        uint32_t b[2] = {tf32(xb.x), tf32(xb.y)};
+                        mma_tf32_16x8x8(acc[nt], a, b);
+                    }
+                }
+            }
+            // X_ij = -acc, transposed into block (j, i)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float *xo = AX + (16 * j + 8 * nt + 2 * t4) * AST + 16 * i + g8;
+                xo[0] = -acc[nt][0];
+                xo[AST] = -acc[nt][1];
+                xo[8] = -acc[nt][2];
+                xo[AST + 8] = -acc[nt][3];
+            }
+            __syncwarp();
+        }
+    }
+    sm100::named_bar(bar_id, 128);
+}
+
 }  // namespace prep
 }  // namespace gdn

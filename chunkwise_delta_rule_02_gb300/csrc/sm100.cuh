@@ -116,6 +116,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until every committed bulk group of this thread has completed its writes.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Wait until every committed bulk group of this thread has finished reading its
+// shared-memory source (the writes may still be in flight).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // async-proxy global accesses <-> generic-proxy global accesses
 __device__ __forceinline__ void fence_async_global()
 {
