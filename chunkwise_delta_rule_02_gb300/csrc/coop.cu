@@ -62,6 +62,14 @@ constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NTHREADS = 512;
 constexpr int RING = 8;
+// control block, in 32-bit words: line 0 holds the task counter [0] and Jmax [1];
+// then one 128-byte line per chain CTA for its consumed count and one for its
+// RING ready flags, so that pollers and the task counter do not share lines
+constexpr int CTL_LINE = 32;
+static_assert(RING <= CTL_LINE, "ready flags of one chain CTA fit one line");
+__host__ __device__ constexpr size_t ctl_words(int nc) { return (size_t)CTL_LINE * (1 + 2 * (size_t)nc); }
+__device__ __forceinline__ uint32_t *consumed_word(uint32_t *ctl, int c) { return ctl + CTL_LINE * (1 + c); }
+__device__ __forceinline__ uint32_t *ready_words(uint32_t *ctl, int nc, int c) { return ctl + CTL_LINE * (1 + nc + c); }
 constexpr long long BUDGET = 4000000000LL;                 // clock cycles (about 2 s)
 constexpr float RENORM_BELOW = 9.313225746154785e-10f;      // 2^-30
 
@@ -125,7 +133,7 @@ struct Params {
     uint32_t *status;
     const int32_t *cu;       // packed offsets or null
     const int32_t *order;    // packed: sequences longest first (or null)
-    uint32_t *ctl;           // [0] task counter, [1] Jmax, [2..2+Nc) consumed, then ready[Nc][RING]
+    uint32_t *ctl;           // control block (ctl_words(Nc) words, see CTL_LINE)
     uint8_t *ring;           // Nc x RING package slots
     int H, T, N, items, Nc, Jmax_fixed;
     float scale, eps;
@@ -209,15 +217,16 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     volatile int *abort_flag = (volatile int *)(sm + CH_BAR + 32 * 8);
     uint32_t *tmem_slot = (uint32_t *)(sm + CH_BAR + 32 * 8 + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint32_t *consumed = p.ctl + 2 + c;
-    uint32_t *ready = p.ctl + 2 + p.Nc + c * RING;
+    uint32_t *consumed = consumed_word(p.ctl, c);
+    uint32_t *ready = ready_words(p.ctl, p.Nc, c);
     const uint8_t *ring = p.ring + (size_t)c * RING * PK_STRIDE;
 
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < NBAR_CH; ++i) {
             uint32_t cnt = 1;
-            if (i == B_U2READY || i == B_SNAP || i == B_OFREE || i == B_OFREE + 1) cnt = 4;
+            if (i == B_U2READY || i == B_SNAP) cnt = 8;
+            if (i == B_OFREE || i == B_OFREE + 1) cnt = 4;
             mbar_init(&bar[i], cnt);
         }
         fence_barrier_init();
@@ -283,9 +292,11 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 // wait for the producer's flag
                 const long long t0 = clock64();
                 bool ok = true;
+                unsigned ns = 32;
                 while (ld_acquire_gpu(&ready[slot]) != (uint32_t)(j + 1)) {
                     if (*abort_flag || clock64() - t0 > BUDGET) { ok = false; break; }
-                    __nanosleep(64);
+                    __nanosleep(ns);
+                    ns = ns < 256 ? 2 * ns : ns;
                 }
                 if (!ok) { fail(); break; }
                 fence_async_global();
@@ -368,73 +379,35 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             mma_commit(&bar[B_ABORTED]);
             mbar_wait(&bar[B_ABORTED], 0, BUDGET, nullptr);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- Unew -> U1, U2 (shared)
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------- state and Unew, split in halves over two warpgroups
+        // warpgroup `half` owns S columns (d_k) [64 half, 64 half + 64) and chunk
+        // tokens [32 half, 32 half + 32); per chunk: state snapshot for the next
+        // MMA, then Unew -> U1, U2 once X is in TMEM; h0 in and h_T out at item ends
+        const int half = (warp >> 2) - 1;
         const int dv = (warp & 3) * 32 + lane;
         const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
-        Stream st;
-        st.start(p, c);
-        float Gpend = 1.f;
-        for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
-            const int s = j & 1;
-            if (st.first()) Gpend = 1.f;
-            if (!__all_sync(0xffffffffu, wait(B_X + s, (uint32_t)(j >> 1)))) break;
-            if (c == 0 && tid == 128) CTR(j, 6);
-            tc_fence_after();
-            uint32_t x[64];
-            tmem_ld32(tmem + lrow + TM_XO + s * 128, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-            tmem_ld_wait();
-            const float *vec = (const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC);
-            const float GC = vec[64];
-            const float Gnext = Gpend * GC;
-            const bool renorm = Gnext < RENORM_BELOW;
-            const float fdiv = renorm ? 1.f : 1.f / Gnext;
-            Gpend = renorm ? 1.f : Gnext;
-            uint8_t *u1 = sm + CH_U1, *u2 = sm + CH_U2;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t w1[4], w2[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i0 = c8 * 8 + 2 * e;
-                    const float a = __uint_as_float(x[i0]), b = __uint_as_float(x[i0 + 1]);
-                    w1[e] = pack_bf16(a, b);
-                    w2[e] = pack_bf16(a * vec[i0] * fdiv, b * vec[i0 + 1] * fdiv);
-                }
-                const uint32_t off = sw128(dv, c8 * 16);
-                *(uint4 *)(u1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[B_U2READY]);
-            if (c == 0 && tid == 128) CTR(j, 7);
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ---------------------------------------------------------------- state: h0, snapshot, renorm, h_T
-        const int dv = (warp & 3) * 32 + lane;
-        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+        const int tid_trace = 128 + 128 * half;
         // items without chunks pass their initial state straight through
         for (int it = c; it < p.items; it += p.Nc) {
             const Item I = item_of(p, it);
             if (I.nch == 0 && p.hT) {
                 const size_t sidx = ((size_t)I.seq * p.H + I.h) * D * D;
-                for (int k = 0; k < D; ++k) p.hT[sidx + (size_t)k * D + dv] = p.h0 ? p.h0[sidx + (size_t)k * D + dv] : 0.f;
+                for (int k = 64 * half; k < 64 * half + 64; ++k)
+                    p.hT[sidx + (size_t)k * D + dv] = p.h0 ? p.h0[sidx + (size_t)k * D + dv] : 0.f;
             }
         }
         Stream st;
         st.start(p, c);
         float Gpend = 1.f;
-        uint8_t *sbp = sm + CH_SB;
+        uint8_t *sbp = sm + CH_SB + half * 16384;
         for (int j = 0; j < J && st.valid; ++j) {
             const int s = j & 1;
             const size_t sidx = ((size_t)st.cur.seq * p.H + st.cur.h) * D * D;
             if (st.first()) {
                 // S^T[dv][dk] = h0[dk][dv] into TMEM, pending scale 1
                 Gpend = 1.f;
-                for (int k0 = 0; k0 < D; k0 += 32) {
+                for (int k0 = 64 * half; k0 < 64 * half + 64; k0 += 32) {
                     uint32_t r[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
@@ -447,45 +420,78 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             }
             wait(B_PFULL + s, (uint32_t)(j >> 1));
             tc_fence_after();
-            const float GC = ((const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC))[64];
-            if (c == 0 && tid == 256) CTR(j, 8);
+            const float *vec = (const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC);
+            const float GC = vec[64];
+            if (c == 0 && tid == tid_trace) CTR(j, 8);
             const float Gn = Gpend;
             const float Gnext = Gn * GC;
             const bool renorm = Gnext < RENORM_BELOW;
             // bf16 snapshot of the true state S = G S_hat (A operand of the next MMA);
             // a renormalising chunk also rescales S_hat in TMEM to exp(gamma_C) S
-            for (int k0 = 0; k0 < D; k0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lrow + TM_S + k0, r);
+            {
+                uint32_t r[64];
+                tmem_ld32(tmem + lrow + TM_S + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(tmem + lrow + TM_S + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_ld_wait();
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < 8; ++c8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         w[e] = pack_bf16(Gn * __uint_as_float(r[c8 * 8 + 2 * e]), Gn * __uint_as_float(r[c8 * 8 + 2 * e + 1]));
-                    const int kk = k0 + c8 * 8;   // first dk of this 16-byte group
-                    *(uint4 *)(sbp + (kk >> 6) * 16384 + sw128(dv, (kk & 63) * 2)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(sbp + sw128(dv, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 if (renorm) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * Gnext);
-                    tmem_st32(tmem + lrow + TM_S + k0, r);
+                    for (int e = 0; e < 64; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * Gnext);
+                    tmem_st32(tmem + lrow + TM_S + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_st32(tmem + lrow + TM_S + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_st_wait();
                 }
             }
-            if (renorm) tmem_st_wait();
             Gpend = renorm ? 1.f : Gnext;
+            const float fdiv = renorm ? 1.f : 1.f / Gnext;
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_SNAP]);
-            if (c == 0 && tid == 256) CTR(j, 9);
+            if (c == 0 && tid == tid_trace) CTR(j, 9);
+            // Unew (this warpgroup's 32 tokens) -> U1 = Unew^T, U2 = (f o Unew)^T / G, bf16
+            if (!__all_sync(0xffffffffu, wait(B_X + s, (uint32_t)(j >> 1)))) break;
+            if (c == 0 && tid == tid_trace) CTR(j, 6);
+            tc_fence_after();
+            {
+                uint32_t x[32];
+                tmem_ld32(tmem + lrow + TM_XO + s * 128 + 32 * half, x);
+                tmem_ld_wait();
+                uint8_t *u1 = sm + CH_U1, *u2 = sm + CH_U2;
+                const float *f0 = vec + 32 * half;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t w1[4], w2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = c8 * 8 + 2 * e;
+                        const float a = __uint_as_float(x[i0]), b = __uint_as_float(x[i0 + 1]);
+                        w1[e] = pack_bf16(a, b);
+                        w2[e] = pack_bf16(a * f0[i0] * fdiv, b * f0[i0 + 1] * fdiv);
+                    }
+                    const uint32_t off = sw128(dv, (4 * half + c8) * 16);
+                    *(uint4 *)(u1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_U2READY]);
+            if (c == 0 && tid == tid_trace) CTR(j, 7);
             if (st.last()) {
                 // h_T = G S_hat once the chunk's state update has landed
                 wait(B_S, (uint32_t)j);
                 tc_fence_after();
                 if (p.hT && !*abort_flag) {
-                    for (int k0 = 0; k0 < D; k0 += 32) {
+                    for (int k0 = 64 * half; k0 < 64 * half + 64; k0 += 32) {
                         uint32_t r[32];
                         tmem_ld32(tmem + lrow + TM_S + k0, r);
                         tmem_ld_wait();
@@ -611,9 +617,29 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         fail();
         return false;
     };
+    // chunk j of chain CTA c: item and chunk within it (false if the stream is shorter)
+    auto locate = [&](int c, int j, Item &I, int &n) -> bool {
+        n = j;
+        for (int it = c; it < p.items; it += p.Nc) {
+            I = item_of(p, it);
+            if (n < I.nch) return true;
+            n -= I.nch;
+        }
+        return false;
+    };
     uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
     bool tma_pending = false, mma_issued = false;
+    uint32_t *pend_ready = nullptr;     // (t == 64) flag of a package still being written
+    uint32_t pend_val = 0;
     while (true) {
+        if (t == 64 && pend_ready) {
+            // the previous package has landed: raise its ready flag (while thread 0 fetches a task)
+            bulk_wait_all();
+            fence_async_global();
+            __threadfence();
+            st_release_gpu(pend_ready, pend_val);
+            pend_ready = nullptr;
+        }
         if (t == 0) {
             const int tk = (int)atomicAdd(&p.ctl[0], 1u);
             *task_word = *abort_flag ? 0x7fffffff : tk;   // one decision for the whole pipeline
@@ -623,29 +649,24 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         named_bar(bar_id, 128);
         if (task >= ntasks) break;
         const int c = task % p.Nc, j = task / p.Nc;
-        // find chunk j of chain CTA c
         Item I;
-        int n = j, it = c;
-        bool found = false;
-        for (; it < p.items; it += p.Nc) {
-            I = item_of(p, it);
-            if (n < I.nch) { found = true; break; }
-            n -= I.nch;
-        }
-        if (!found) continue;
+        int n;
+        if (!locate(c, j, I, n)) continue;
         if (c == 0 && t == 0) CTR(j, 12);
         const int len = min(C, I.L - n * C);
         const long long row0 = I.rowbase + (long long)n * C;
         const int slot = j % RING;
-        uint32_t *consumed = p.ctl + 2 + c;
-        uint32_t *ready = p.ctl + 2 + p.Nc + c * RING + slot;
+        uint32_t *consumed = consumed_word(p.ctl, c);
+        uint32_t *ready = ready_words(p.ctl, p.Nc, c) + slot;
         uint8_t *dst = p.ring + ((size_t)c * RING + slot) * PK_STRIDE;
         if (t == 0) {
             // the ring slot must have been copied out by the chain CTA
             const long long t0 = clock64();
+            unsigned ns = 64;
             while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
                 if (clock64() - t0 > BUDGET) { fail(); break; }
-                __nanosleep(128);
+                __nanosleep(ns);
+                ns = ns < 2048 ? 2 * ns : ns;
             }
             if (!*abort_flag) {
                 mbar_expect_tx(&bar[P_FULL], 32768);
@@ -742,6 +763,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         }
         fence_async_smem();
         named_bar(bar_id, 128);
+        if (c == 0 && t == 0) CTR(j, 22);
         if (q4 < 2) {
             // A = strict_lower(diag(beta n) (K K^T o D) diag(n)), full rows (zeros on and above the diagonal)
             const int r = q4 * 32 + lane;
@@ -750,18 +772,32 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tmem_ld_wait();
             float4 *arow = reinterpret_cast<float4 *>(AX + r * AST);
-            const float ra = s_ra[r], br = s_beta[r] * s_nk[r], gr = s_gl[r];
+            if (safe) {
+                // exp(gamma_r - gamma_i) factored as exp(gamma_r) * exp(-gamma_i)
+                const float ra = s_ra[r];
+                const float4 *cb4 = reinterpret_cast<const float4 *>(s_cb);
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
-                float a[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 4 * c4 + e;
-                    const float gv = __uint_as_float(v[i]);
-                    a[e] = (i < r) ? (safe ? ra * s_cb[i] * gv : br * s_nk[i] * gv * ex2f(gr - s_gl[i])) : 0.f;
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const float4 cb = cb4[c4];
+                    const int i = 4 * c4;
+                    arow[c4] = make_float4(i < r ? ra * cb.x * __uint_as_float(v[i]) : 0.f,
+                                           i + 1 < r ? ra * cb.y * __uint_as_float(v[i + 1]) : 0.f,
+                                           i + 2 < r ? ra * cb.z * __uint_as_float(v[i + 2]) : 0.f,
+                                           i + 3 < r ? ra * cb.w * __uint_as_float(v[i + 3]) : 0.f);
                 }
-                arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
+            } else {
+                const float br = s_beta[r] * s_nk[r], gr = s_gl[r];
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * c4 + e;
+                        a[e] = (i < r) ? br * s_nk[i] * __uint_as_float(v[i]) * ex2f(gr - s_gl[i]) : 0.f;
+                    }
+                    arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
+                }
             }
+            if (c == 0 && t == 0) CTR(j, 25);
         } else {
             // publish Qt now; once the copy has read it, its space takes T and P
             if (t == 64 && !*abort_flag) {
@@ -771,31 +807,43 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 bulk_wait_read();
             }
             named_bar(bar_hi, 64);
+            if (c == 0 && t == 64) CTR(j, 26);
             // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i], into Qt's second half
             const int r = (q4 - 2) * 32 + lane;
             uint32_t v[64];
             tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
             tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tmem_ld_wait();
-            const float mr = s_nq[r], gr = s_gl[r], rp = mr * ex2f(gr);
+            const float mr = s_nq[r], gr = s_gl[r];
+            if (safe) {
+                const float rp = mr * ex2f(gr);
+                const float4 *cb4 = reinterpret_cast<const float4 *>(s_cb);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t w[4];
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const float4 ca = cb4[2 * c8], cc = cb4[2 * c8 + 1];
+                    const float cbv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
+                    uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i0 = c8 * 8 + 2 * e, i1 = i0 + 1;
-                    const float v0 = __uint_as_float(v[i0]), v1 = __uint_as_float(v[i1]);
-                    float a0, a1;
-                    if (safe) {
-                        a0 = (i0 <= r) ? rp * s_cb[i0] * v0 : 0.f;
-                        a1 = (i1 <= r) ? rp * s_cb[i1] * v1 : 0.f;
-                    } else {
-                        a0 = (i0 <= r) ? mr * s_nk[i0] * v0 * ex2f(gr - s_gl[i0]) : 0.f;
-                        a1 = (i1 <= r) ? mr * s_nk[i1] * v1 * ex2f(gr - s_gl[i1]) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = c8 * 8 + 2 * e;
+                        const float a0 = (i0 <= r) ? rp * cbv[2 * e] * __uint_as_float(v[i0]) : 0.f;
+                        const float a1 = (i0 + 1 <= r) ? rp * cbv[2 * e + 1] * __uint_as_float(v[i0 + 1]) : 0.f;
+                        w[e] = pack_bf16(a0, a1);
                     }
-                    w[e] = pack_bf16(a0, a1);
+                    *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = c8 * 8 + 2 * e, i1 = i0 + 1;
+                        const float a0 = (i0 <= r) ? mr * s_nk[i0] * __uint_as_float(v[i0]) * ex2f(gr - s_gl[i0]) : 0.f;
+                        const float a1 = (i1 <= r) ? mr * s_nk[i1] * __uint_as_float(v[i1]) * ex2f(gr - s_gl[i1]) : 0.f;
+                        w[e] = pack_bf16(a0, a1);
+                    }
+                    *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
             }
             if (c == 0 && t == 64) CTR(j, 28);
         }
@@ -844,12 +892,12 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 mma_bf16_ss(tg, dadd(da, k * 32), dadd(db, k * 2048), ID_SS_N128_BMN, k > 0);
             mma_commit(&bar[P_W]);
             if (c == 0) CTR(j, 24);
-            if (!*abort_flag) {
-                bulk_store(dst + PK_T, tl + 8192, 8192);
-                bulk_store(dst + PK_P, tl + 24576, 8192);
-                bulk_store(dst + PK_VEC, s_f0, 272);   // f0[64], exp(gamma_C)
-                bulk_commit();
-            }
+        }
+        if (t == 64 && !*abort_flag) {
+            bulk_store(dst + PK_T, tl + 8192, 8192);
+            bulk_store(dst + PK_P, tl + 24576, 8192);
+            bulk_store(dst + PK_VEC, s_f0, 272);   // f0[64], exp(gamma_C)
+            bulk_commit();
         }
         wait(P_W, k_task);
         tc_fence_after();
@@ -875,28 +923,31 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         }
         tc_fence_before();
         fence_async_smem();
-        if (t == 64) {
-            // Qt's copy has landed before the ready flag goes up
-            bulk_wait_all();
-            fence_async_global();
-            __threadfence();
-        }
         named_bar(bar_id, 128);
         if (c == 0 && t == 0) CTR(j, 23);
-        if (t == 0 && !*abort_flag) {
-            // publish -W, then the ready flag
-            bulk_store(dst + PK_WQ, tl, 8192);
-            bulk_store(dst + PK_WQ + 16384, tl + 16384, 8192);
-            bulk_commit();
-            bulk_wait_all();
-            fence_async_global();
-            __threadfence();
-            st_release_gpu(ready, (uint32_t)(j + 1));
-            if (c == 0) CTR(j, 18);
+        if (t == 64) {
+            // publish -W; the ready flag goes up at the top of the next round, once
+            // every copy of the package has landed
+            if (!*abort_flag) {
+                bulk_store(dst + PK_WQ, tl, 8192);
+                bulk_store(dst + PK_WQ + 16384, tl + 16384, 8192);
+                bulk_commit();
+                pend_ready = ready;
+                pend_val = (uint32_t)(j + 1);
+                if (c == 0) CTR(j, 18);
+            }
+            bulk_wait_read();   // the buffers may be refilled
         }
-        if (t == 0) bulk_wait_all();   // nothing may still read this pipeline's buffers
         ++k_task;
         named_bar(bar_id, 128);
+    }
+    if (t == 64) {
+        bulk_wait_all();
+        if (pend_ready && !*abort_flag) {
+            fence_async_global();
+            __threadfence();
+            st_release_gpu(pend_ready, pend_val);
+        }
     }
     if (t == 0) {
         // nothing of this pipeline may still be in flight when the block exits
@@ -907,7 +958,6 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         }
         bulk_wait_all();
     }
-    if (t == 64) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1026,7 +1076,7 @@ size_t workspace_bytes(const Geo &g, int sms)
 {
     if (sms <= 0) sms = 160;   // sizing without a device: an upper bound
     const int nc = chain_ctas(g, sms);
-    const size_t ctl = (size_t)(2 + nc + nc * RING) * sizeof(uint32_t);
+    const size_t ctl = ctl_words(nc) * sizeof(uint32_t);
     const size_t order = g.varlen ? sizeof(int32_t) * (size_t)(g.N + 1) : 0;
     auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
     return al(ctl) + al(order) + (size_t)nc * RING * PK_STRIDE;
@@ -1057,7 +1107,7 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     const int nc = chain_ctas(g, sms);
     auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
     uint8_t *w = (uint8_t *)ws;
-    const size_t ctl_bytes = (size_t)(2 + nc + nc * RING) * sizeof(uint32_t);
+    const size_t ctl_bytes = ctl_words(nc) * sizeof(uint32_t);
     Params p;
     p.beta = beta; p.gate = gate; p.h0 = h0; p.o = o; p.hT = hT; p.status = status;
     p.cu = g.varlen ? g.cu : nullptr;

@@ -67,8 +67,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes
+// or about `ns` nanoseconds pass, instead of spinning on issue slots that the
+// working warps of the SM need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (after roughly `budget` clock cycles) if it never does, or as soon as *abort
+// (after roughly `budget` clock cycles) if it never does, or soon after *abort
 // is set by another thread of the block.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget,
                                           volatile int *abort)
@@ -76,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
         if (abort && *abort) return false;
         if (clock64() - t0 > budget) return false;
     }
@@ -136,6 +152,14 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Prefetch one tile of a 2D tensor map into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x),
+                 "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
