@@ -59,7 +59,7 @@ int device_sms()
 
 struct Layout {
     size_t status, cstart, fast;
-    size_t Kn, Qn, W, U, Unew, Tm, gam, Sin, dSo, dUn, dQ, dK, dW;
+    size_t Kn, Qn, W, U, Unew, gam, Sin, dSo, dUn, dQ, dK, dW, P, aux;
     size_t total;
 };
 
@@ -88,10 +88,11 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast,
     L.W = take(slots * C * dk);
     L.U = take(slots * C * dv);
     L.Unew = take(slots * C * dv);
-    L.Tm = take(slots * C * C);
     L.gam = take(slots * C);
     L.Sin = take(slots * dk * dv);
+    L.P = take(slots * C * C);
     if (for_backward) {
+        L.aux = take(slots * (2 * C + 4));
         L.dSo = take(slots * dk * dv);
         L.dUn = take(slots * C * dv);
         L.dQ = take(slots * C * dk);
@@ -108,8 +109,9 @@ gen::Ws general_ws(const Layout &L, char *base)
     gen::Ws w;
     auto F = [&](size_t o) { return o ? (float *)(base + o) : (float *)nullptr; };
     w.Kn = F(L.Kn); w.Qn = F(L.Qn); w.W = F(L.W); w.U = F(L.U); w.Unew = F(L.Unew);
-    w.Tm = F(L.Tm); w.gam = F(L.gam); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
+    w.gam = F(L.gam); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
     w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
+    w.P = F(L.P); w.aux = F(L.aux);
     return w;
 }
 
@@ -241,7 +243,7 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
     int path, n;
     if (for_backward) {
         path = DN_PATH_GENERAL;
-        n = 4 + offsets;                    // k_prep, k_scan, k_bscan, k_bchunk
+        n = 5 + offsets;                    // k_prep, k_scan, k_bscan, k_bbig, k_bchunk
     } else if (!fast_ok(shape, g, 0)) {
         path = DN_PATH_GENERAL;
         n = 3 + offsets;                    // k_prep, k_scan, k_out

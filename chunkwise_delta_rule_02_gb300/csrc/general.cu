@@ -2,18 +2,27 @@
 // 128, chunk 16/32/64, float32 or bfloat16 inputs, gated or not, packed or not.
 //
 // These kernels carry the fp32 workload (whose 1e-4 tolerance tensor-core
-// operands cannot meet) and every shape the tcgen05 fast path does not take.
-// They follow the chunk form of "Parallelizing Linear Transformers with the
-// Delta Rule over Sequence Length" (WY / UT representation, chunk-state scan)
-// with the gates of "Gated DeltaNet" folded in as within-chunk cumulative
+// operands cannot meet), every shape the tcgen05 kernels do not take, and the
+// backward.  They follow the chunk form of "Parallelizing Linear Transformers
+// with the Delta Rule over Sequence Length" (WY / UT representation, chunk-state
+// scan) with the gates of "Gated DeltaNet" folded in as within-chunk cumulative
 // log-decays:
-//   prep  : per chunk, parallel       normalise q,k; gamma; A; T; W; U
+//   prep  : per chunk, parallel       normalise q,k; gamma; A; T; W; U; P
 //   scan  : per (seq, head, dv-slice) Unew = U - W S; S <- Gamma_C S + Kt^T Unew
-//   out   : per chunk, parallel       O = diag(Gamma) Q S + lower(QK^T o D) Unew
-// and the backward (chunk states recomputed by prep+scan, then):
+//   out   : per chunk, parallel       O = diag(Gamma) Q S + P Unew
+// and the backward (chunk states recomputed by prep + scan, then):
 //   bscan : per (seq, head, dv-slice), last chunk first:
-//           dUnew = lower(..)^T dO + Kt dS;  dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
+//           dUnew = P^T dO + Kt dS;  dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
+//   bbig  : per chunk, parallel       the three products with the d_k x d_v states
 //   bchunk: per chunk, parallel       every input gradient of the chunk.
+// (P = lower(Q K^T o D) with the diagonal kept; D_ri = exp(gamma_r - gamma_i).)
+//
+// Every matrix product is a register-tiled block product (rgemm): each thread
+// owns TM consecutive rows and TN columns spread across the threads, so an
+// operand that is contiguous along the output columns is read coalesced (from
+// L1) or without bank conflicts (from shared memory).  Operands that would be
+// read across rows instead are first staged in shared memory with an odd row
+// stride.
 #include "common.cuh"
 #include "general.h"
 
@@ -27,22 +36,58 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// Block-cooperative small GEMM: out(m, n) = sum_k A(m, k) B(k, n), handed to St.
-template <class FA, class FB, class FS>
-__device__ __forceinline__ void bgemm(int M, int N, int K, FA A, FB B, FS St)
+// St(m, n, sum_k A(m, k) B(k, n)) for m < M, n < N.  Thread tile: rows
+// m0 .. m0 + TM - 1 and columns tn, tn + nt, .., tn + (TN - 1) nt, where nt is
+// the number of column tiles.  Accessors are called only inside the bounds.
+template <int TM, int TN, class FA, class FB, class FS>
+__device__ __forceinline__ void rgemm(int M, int N, int K, FA A, FB B, FS St)
 {
-    for (int idx = threadIdx.x; idx < M * N; idx += blockDim.x) {
-        int m = idx / N, n = idx - m * N;
-        float s = 0.f;
-        for (int k = 0; k < K; ++k) s = fmaf(A(m, k), B(k, n), s);
-        St(m, n, s);
+    const int mt = (M + TM - 1) / TM, nt = (N + TN - 1) / TN;
+    for (int t = threadIdx.x; t < mt * nt; t += blockDim.x) {
+        const int m0 = (t / nt) * TM, tn = t - (t / nt) * nt;
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        if (m0 + TM <= M && tn + (TN - 1) * nt < N) {
+#pragma unroll 2
+            for (int k = 0; k < K; ++k) {
+                float a[TM], b[TN];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) a[i] = A(m0 + i, k);
+#pragma unroll
+                for (int j = 0; j < TN; ++j) b[j] = B(k, tn + j * nt);
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+        } else {
+            for (int k = 0; k < K; ++k) {
+                float a[TM], b[TN];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) a[i] = (m0 + i < M) ? A(m0 + i, k) : 0.f;
+#pragma unroll
+                for (int j = 0; j < TN; ++j) b[j] = (tn + j * nt < N) ? B(k, tn + j * nt) : 0.f;
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                if (m0 + i < M && tn + j * nt < N) St(m0 + i, tn + j * nt, acc[i][j]);
     }
 }
 
 // Column-parallel forward substitution: X = (I + A)^-1 diag(d), A strictly lower
-// (len x len, row stride C).  Thread j solves column j on its own.
+// (len x len, row stride ld).  Thread j solves column j on its own.
 __device__ __forceinline__ void unit_lower_solve(const float *A, float *X, const float *d,
-                                                 int len, int C)
+                                                 int len, int ld)
 {
     for (int jc = threadIdx.x; jc < len; jc += blockDim.x) {
         for (int r = 0; r < len; ++r) {
@@ -53,10 +98,10 @@ __device__ __forceinline__ void unit_lower_solve(const float *A, float *X, const
                 x = d ? d[jc] : 1.f;
             } else {
                 float s = 0.f;
-                for (int i = jc; i < r; ++i) s = fmaf(A[r * C + i], X[i * C + jc], s);
+                for (int i = jc; i < r; ++i) s = fmaf(A[r * ld + i], X[i * ld + jc], s);
                 x = -s;
             }
-            X[r * C + jc] = x;
+            X[r * ld + jc] = x;
         }
     }
 }
@@ -72,14 +117,15 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
     const int j = blockIdx.x, h = blockIdx.y;
     int b, t0, len, seq, local;
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
-    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int C = g.C, dk = g.dk, dv = g.dv, LK = dk + 1, LC = C + 1;
     extern __shared__ float sm[];
-    float *sK = sm;               // [C][dk] normalised keys
-    float *sA = sK + C * dk;      // [C][C]
-    float *sT = sA + C * C;       // [C][C]
-    float *sb = sT + C * C;       // [C] beta
-    float *sg = sb + C;           // [C] gamma
-    float *sG = sg + C;           // [C] exp(gamma)
+    float *sK = sm;                                 // [C][LK] normalised keys
+    float *sQ = sK + C * LK;                        // [C][LK] normalised queries, then V [C][dv]
+    float *sA = sQ + C * (LK > dv ? LK : dv);       // [C][LC]
+    float *sT = sA + C * LC;                        // [C][LC]
+    float *sb = sT + C * LC;                        // [C] beta
+    float *sg = sb + C;                             // [C] gamma
+    float *sG = sg + C;                             // [C] exp(gamma)
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -98,43 +144,61 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
         float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
         float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
         for (int c = lane; c < dk; c += 32) {
-            float x = ld_in(kr + c) * rk;
-            sK[r * dk + c] = x;
+            float x = ld_in(kr + c) * rk, y = ld_in(qr + c) * rq;
+            sK[r * LK + c] = x;
+            sQ[r * LK + c] = y;
             w.Kn[slot * C * dk + r * dk + c] = x;
-            w.Qn[slot * C * dk + r * dk + c] = ld_in(qr + c) * rq;
+            w.Qn[slot * C * dk + r * dk + c] = y;
         }
     }
-    if (threadIdx.x == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < len; ++r) {
-            acc += gate ? gate[row + r] : 0.f;
-            sg[r] = acc;
-            sG[r] = expf(acc);
-            sb[r] = ld_in(beta + row + r);
-            w.gam[slot * C + r] = acc;
+    if (warp == 0) {
+        // within-chunk cumulative log-gate, two rows per lane (C <= 64)
+        float x0 = (gate && lane < len) ? gate[row + lane] : 0.f;
+        float x1 = (gate && lane + 32 < len) ? gate[row + lane + 32] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        if (lane < len) {
+            sg[lane] = x0;
+            sG[lane] = expf(x0);
+            sb[lane] = ld_in(beta + row + lane);
+            w.gam[slot * C + lane] = x0;
+        }
+        if (lane + 32 < len) {
+            sg[lane + 32] = x1;
+            sG[lane + 32] = expf(x1);
+            sb[lane + 32] = ld_in(beta + row + lane + 32);
+            w.gam[slot * C + lane + 32] = x1;
         }
     }
     __syncthreads();
-    // A = strict_lower(diag(beta) (K K^T o D))
-    bgemm(len, len, dk, [&](int m, int kk) { return sK[m * dk + kk]; },
-          [&](int kk, int n) { return sK[n * dk + kk]; },
-          [&](int m, int n, float s) {
-              sA[m * C + n] = (n < m) ? sb[m] * s * expf(sg[m] - sg[n]) : 0.f;
-          });
+    // A = strict_lower(diag(beta) (K K^T o D)),  P = lower(Q K^T o D)
+    rgemm<4, 4>(len, len, dk, [&](int m, int kk) { return sK[m * LK + kk]; },
+                [&](int kk, int n) { return sK[n * LK + kk]; },
+                [&](int m, int n, float s) {
+                    sA[m * LC + n] = (n < m) ? sb[m] * s * expf(sg[m] - sg[n]) : 0.f;
+                });
+    float *Pg = w.P + slot * C * C;
+    rgemm<4, 4>(len, len, dk, [&](int m, int kk) { return sQ[m * LK + kk]; },
+                [&](int kk, int n) { return sK[n * LK + kk]; },
+                [&](int m, int n, float s) { Pg[m * C + n] = (n <= m) ? s * expf(sg[m] - sg[n]) : 0.f; });
     __syncthreads();
-    unit_lower_solve(sA, sT, sb, len, C);   // T = (I + A)^-1 diag(beta)
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
-        int r = idx / len, c = idx - r * len;
-        w.Tm[slot * C * C + r * C + c] = sT[r * C + c];
+    unit_lower_solve(sA, sT, sb, len, LC);   // T = (I + A)^-1 diag(beta)
+    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
+        int r = idx / dv, c = idx - r * dv;
+        sQ[r * dv + c] = ld_in(v + (row + r) * dv + c);
     }
+    __syncthreads();
     // W = T diag(Gamma) K,  U = T V
-    bgemm(len, dk, len, [&](int m, int i) { return sT[m * C + i]; },
-          [&](int i, int n) { return sG[i] * sK[i * dk + n]; },
-          [&](int m, int n, float s) { w.W[slot * C * dk + m * dk + n] = s; });
-    bgemm(len, dv, len, [&](int m, int i) { return sT[m * C + i]; },
-          [&](int i, int n) { return ld_in(v + (row + i) * dv + n); },
-          [&](int m, int n, float s) { w.U[slot * C * dv + m * dv + n] = s; });
+    rgemm<4, 8>(len, dk, len, [&](int m, int i) { return sT[m * LC + i]; },
+                [&](int i, int n) { return sG[i] * sK[i * LK + n]; },
+                [&](int m, int n, float s) { w.W[slot * C * dk + m * dk + n] = s; });
+    rgemm<4, 8>(len, dv, len, [&](int m, int i) { return sT[m * LC + i]; },
+                [&](int i, int n) { return sQ[i * dv + n]; },
+                [&](int m, int n, float s) { w.U[slot * C * dv + m * dv + n] = s; });
 }
 
 // ----------------------------------------------------------------------------- scan
@@ -169,19 +233,19 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
         const float *W = w.W + slot * C * dk;
         const float *U = w.U + slot * C * dv;
         float *Un = w.Unew + slot * C * dv;
-        bgemm(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
-              [&](int kk, int n) { return sS[kk * BV + n]; },
-              [&](int r, int n, float acc) {
-                  float u = U[r * dv + n0 + n] - acc;
-                  sU[r * BV + n] = u;
-                  Un[r * dv + n0 + n] = u;
-              });
+        rgemm<4, 2>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
+                    [&](int kk, int n) { return sS[kk * BV + n]; },
+                    [&](int r, int n, float acc) {
+                        float u = U[r * dv + n0 + n] - acc;
+                        sU[r * BV + n] = u;
+                        Un[r * dv + n0 + n] = u;
+                    });
         __syncthreads();
         const float *Kn = w.Kn + slot * C * dk;
         const float GC = expf(gC);
-        bgemm(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
-              [&](int r, int n) { return sU[r * BV + n]; },
-              [&](int kk, int n, float acc) { sS[kk * BV + n] = fmaf(GC, sS[kk * BV + n], acc); });
+        rgemm<8, 2>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
+                    [&](int r, int n) { return sU[r * BV + n]; },
+                    [&](int kk, int n, float acc) { sS[kk * BV + n] = fmaf(GC, sS[kk * BV + n], acc); });
         __syncthreads();
     }
     if (hT) {
@@ -201,27 +265,21 @@ __global__ void __launch_bounds__(256) k_out(Geo g, Tout *__restrict__ o, Ws w)
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
     const int C = g.C, dk = g.dk, dv = g.dv;
     extern __shared__ float sm[];
-    float *sP = sm;            // [C][C]
-    float *sG = sP + C * C;    // [C]
+    float *sG = sm;            // [C] exp(gamma)
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
     const float *gam = w.gam + slot * C;
     const float *Qn = w.Qn + slot * C * dk;
-    const float *Kn = w.Kn + slot * C * dk;
     const float *Sin = w.Sin + slot * dk * dv;
     const float *Un = w.Unew + slot * C * dv;
+    const float *Pg = w.P + slot * C * C;
     for (int r = threadIdx.x; r < len; r += blockDim.x) sG[r] = expf(gam[r]);
-    bgemm(len, len, dk, [&](int r, int kk) { return Qn[r * dk + kk]; },
-          [&](int kk, int i) { return Kn[i * dk + kk]; },
-          [&](int r, int i, float s) { sP[r * C + i] = (i <= r) ? s * expf(gam[r] - gam[i]) : 0.f; });
     __syncthreads();
-    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
-        int r = idx / dv, n = idx - r * dv;
-        float a = 0.f, bsum = 0.f;
-        for (int kk = 0; kk < dk; ++kk) a = fmaf(Qn[r * dk + kk], Sin[(size_t)kk * dv + n], a);
-        for (int i = 0; i <= r; ++i) bsum = fmaf(sP[r * C + i], Un[i * dv + n], bsum);
-        st_out(o + (row + r) * dv + n, g.scale * fmaf(sG[r], a, bsum));
-    }
+    const float sc = g.scale;
+    rgemm<4, 8>(len, dv, dk + len,
+                [&](int r, int x) { return x < dk ? sG[r] * Qn[r * dk + x] : Pg[r * C + (x - dk)]; },
+                [&](int x, int n) { return x < dk ? Sin[(size_t)x * dv + n] : Un[(x - dk) * dv + n]; },
+                [&](int r, int n, float acc) { st_out(o + (row + r) * dv + n, sc * acc); });
 }
 
 // ----------------------------------------------------------------------------- backward scan
@@ -239,8 +297,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
     float *sdS = sm;               // [dk][BV]
     float *sdU = sdS + dk * BV;    // [C][BV]
     float *sdO = sdU + C * BV;     // [C][BV]  scale * dO
-    float *sP = sdO + C * BV;      // [C][C]
-    float *sE = sP + C * C;        // [C]
+    float *sE = sdO + C * BV;      // [C]
     float *sG = sE + C;            // [C]
     const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
     for (int idx = threadIdx.x; idx < dk * nb; idx += blockDim.x) {
@@ -257,6 +314,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
         const float *Qn = w.Qn + slot * C * dk;
         const float *Kn = w.Kn + slot * C * dk;
         const float *W = w.W + slot * C * dk;
+        const float *Pg = w.P + slot * C * C;
         for (int r = threadIdx.x; r < len; r += blockDim.x) {
             sE[r] = expf(gC - gam[r]);
             sG[r] = expf(gam[r]);
@@ -269,33 +327,23 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
             int r = idx / nb, n = idx - r * nb;
             sdO[r * BV + n] = g.scale * ld_in(dO + (row + r) * dv + n0 + n);
         }
-        bgemm(len, len, dk, [&](int r, int kk) { return Qn[r * dk + kk]; },
-              [&](int kk, int i) { return Kn[i * dk + kk]; },
-              [&](int r, int i, float v) { sP[r * C + i] = (i <= r) ? v * expf(gam[r] - gam[i]) : 0.f; });
         __syncthreads();
-        // dUnew(i, n) = sum_r P(r, i) dO(r, n) + sum_kk exp(gC - gam_i) K(i, kk) dS(kk, n)
+        // dUnew(i, n) = sum_r P(r, i) dO(r, n) + exp(gC - gam_i) sum_kk K(i, kk) dS(kk, n)
         float *dUg = w.dUn + slot * C * dv;
-        for (int idx = threadIdx.x; idx < len * nb; idx += blockDim.x) {
-            int i = idx / nb, n = idx - i * nb;
-            float a = 0.f, e = 0.f;
-            for (int r = i; r < len; ++r) a = fmaf(sP[r * C + i], sdO[r * BV + n], a);
-            for (int kk = 0; kk < dk; ++kk) e = fmaf(Kn[i * dk + kk], sdS[kk * BV + n], e);
-            float u = fmaf(sE[i], e, a);
-            sdU[i * BV + n] = u;
-            dUg[i * dv + n0 + n] = u;
-        }
+        rgemm<4, 2>(len, nb, len + dk,
+                    [&](int i, int x) { return x < len ? Pg[x * C + i] : sE[i] * Kn[i * dk + (x - len)]; },
+                    [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdS[(x - len) * BV + n]; },
+                    [&](int i, int n, float u) {
+                        sdU[i * BV + n] = u;
+                        dUg[i * dv + n0 + n] = u;
+                    });
         __syncthreads();
         // dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
         const float GC = expf(gC);
-        for (int idx = threadIdx.x; idx < dk * nb; idx += blockDim.x) {
-            int kk = idx / nb, n = idx - kk * nb;
-            float acc = GC * sdS[kk * BV + n];
-            for (int r = 0; r < len; ++r) {
-                acc = fmaf(sG[r] * Qn[r * dk + kk], sdO[r * BV + n], acc);
-                acc = fmaf(-W[r * dk + kk], sdU[r * BV + n], acc);
-            }
-            sdS[kk * BV + n] = acc;
-        }
+        rgemm<8, 2>(dk, nb, 2 * len,
+                    [&](int kk, int x) { return x < len ? sG[x] * Qn[x * dk + kk] : -W[(x - len) * dk + kk]; },
+                    [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdU[(x - len) * BV + n]; },
+                    [&](int kk, int n, float acc) { sdS[kk * BV + n] = fmaf(GC, sdS[kk * BV + n], acc); });
         __syncthreads();
     }
     if (dh0) {
@@ -304,6 +352,87 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
             dh0[sidx + (size_t)kk * dv + n0 + n] = sdS[kk * BV + n];
         }
     }
+}
+
+// ----------------------------------------------------------------------------- backward: state products
+// Per chunk: Y = scale dO S_in^T (dQ = diag(Gamma) Y), dW = -dUnew S_in^T and
+// Kt = Unew dS_out^T (dK = diag(exp(gamma_C - gamma)) Kt); plus the row sums
+// <Q_r, Y_r>, <Kt_r, K_r> and <dS_out, S_in> that the gate gradient needs.
+template <class Tin>
+__global__ void __launch_bounds__(256) k_bbig(Geo g, const Tin *__restrict__ dO, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv, LK = dk + 1;
+    extern __shared__ float sm[];
+    float *sT = sm;                 // [dv][LK] a state, transposed
+    float *sE = sT + dv * LK;       // [C]
+    float *sG = sE + C;             // [C]
+    float *sqt = sG + C;            // [C] <Q_r, Y_r>
+    float *set = sqt + C;           // [C] <Kt_r, K_r>
+    float *sred = set + C;          // [1] <dS_out, S_in>
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const float *gam = w.gam + slot * C;
+    const float *Sin = w.Sin + slot * dk * dv;
+    const float *dSo = w.dSo + slot * dk * dv;
+    const float *Un = w.Unew + slot * C * dv;
+    const float *dUn = w.dUn + slot * C * dv;
+    const float *Qn = w.Qn + slot * C * dk;
+    const float *Kn = w.Kn + slot * C * dk;
+    float *dQ = w.dQ + slot * C * dk;
+    float *dK = w.dK + slot * C * dk;
+    float *dW = w.dW + slot * C * dk;
+    const float gC = gam[len - 1], sc = g.scale;
+    const int lane = threadIdx.x & 31;
+    for (int r = threadIdx.x; r < C; r += blockDim.x) {
+        sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
+        sG[r] = r < len ? expf(gam[r]) : 0.f;
+        sqt[r] = 0.f;
+        set[r] = 0.f;
+    }
+    if (threadIdx.x == 0) sred[0] = 0.f;
+    __syncthreads();
+    {
+        float p = 0.f;
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) p = fmaf(dSo[idx], Sin[idx], p);
+        p = warp_sum(p);
+        if (lane == 0) atomicAdd(sred, p);
+    }
+    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+        int kk = idx / dv, n = idx - kk * dv;
+        sT[n * LK + kk] = Sin[idx];
+    }
+    __syncthreads();
+    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
+                [&](int n, int kk) { return sT[n * LK + kk]; },
+                [&](int r, int kk, float y) {
+                    dQ[r * dk + kk] = sG[r] * y;
+                    atomicAdd(&sqt[r], Qn[r * dk + kk] * y);
+                });
+    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return -dUn[r * dv + n]; },
+                [&](int n, int kk) { return sT[n * LK + kk]; },
+                [&](int r, int kk, float s) { dW[r * dk + kk] = s; });
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+        int kk = idx / dv, n = idx - kk * dv;
+        sT[n * LK + kk] = dSo[idx];
+    }
+    __syncthreads();
+    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return Un[r * dv + n]; },
+                [&](int n, int kk) { return sT[n * LK + kk]; },
+                [&](int r, int kk, float s) {
+                    dK[r * dk + kk] = sE[r] * s;
+                    atomicAdd(&set[r], s * Kn[r * dk + kk]);
+                });
+    __syncthreads();
+    float *aux = w.aux + slot * (2 * C + 4);
+    for (int r = threadIdx.x; r < len; r += blockDim.x) {
+        aux[r] = sqt[r];
+        aux[C + r] = set[r];
+    }
+    if (threadIdx.x == 0) aux[2 * C] = sred[0];
 }
 
 // ----------------------------------------------------------------------------- backward per chunk
@@ -321,35 +450,36 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
     const int j = blockIdx.x, h = blockIdx.y;
     int b, t0, len, seq, local;
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
-    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int C = g.C, dk = g.dk, dv = g.dv, LC = C + 1;
+    const int LS = (dk > dv ? dk : dv) + 1;
     extern __shared__ float sm[];
-    float *sD = sm;                 // D_ri = exp(gam_r - gam_i), i <= r
-    float *sKK = sD + C * C;        // K K^T
-    float *sQK = sKK + C * C;       // Q K^T
-    float *sLi = sQK + C * C;       // (I + A)^-1
-    float *sdP = sLi + C * C;       // lower(dO Unew^T)
-    float *sdT = sdP + C * C;       // dT
-    float *sX = sdT + C * C;        // A, later Linv^T dT diag(beta)
-    float *sY = sX + C * C;         // dA, then dKK
-    float *sb = sY + C * C;         // beta
+    float *sKK = sm;                // K K^T
+    float *sP = sKK + C * LC;       // lower(Q K^T o D)
+    float *sdP = sP + C * LC;       // lower(dO Unew^T)
+    float *sDP = sdP + C * LC;      // dP o D, later X = Linv^T dT diag(beta)
+    float *sLi = sDP + C * LC;      // (I + A)^-1
+    float *sdT = sLi + C * LC;      // dT
+    float *sY = sdT + C * LC;       // A, then dA, then dKK
+    float *sS = sY + C * LC;        // [C][LS] staged rows (K, Unew, V)
+    float *sb = sS + C * LS;        // beta
     float *sg = sb + C;             // gamma
     float *sG = sg + C;             // exp(gamma)
     float *sE = sG + C;             // exp(gamma_C - gamma)
     float *sdg = sE + C;            // d gamma
     float *sdb = sdg + C;           // d beta
     float *se = sdb + C;            // e_r (K~ gate term)
-    float *sred = se + C;           // [1] <dS_out, S_in>
+    float *sk2 = se + C;            // <dGK_r, K_r>
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
     const float *Qn = w.Qn + slot * C * dk;
     const float *Kn = w.Kn + slot * C * dk;
-    const float *Sin = w.Sin + slot * dk * dv;
-    const float *dSo = w.dSo + slot * dk * dv;
     const float *Un = w.Unew + slot * C * dv;
     const float *dUn = w.dUn + slot * C * dv;
+    const float *Pg = w.P + slot * C * C;
+    const float *aux = w.aux + slot * (2 * C + 4);
     float *dQ = w.dQ + slot * C * dk;
     float *dK = w.dK + slot * C * dk;
-    float *dW = w.dW + slot * C * dk;
+    const float *dW = w.dW + slot * C * dk;
     const float *gam = w.gam + slot * C;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const float gC = gam[len - 1];
@@ -360,150 +490,123 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
         sg[r] = gam[r];
         sG[r] = expf(gam[r]);
         sE[r] = expf(gC - gam[r]);
-        sdg[r] = 0.f;
+        sdg[r] = sG[r] * aux[r];      // q-term of d gamma
+        se[r] = sE[r] * aux[C + r];   // K~ gate term
         sdb[r] = 0.f;
+        sk2[r] = 0.f;
     }
-    if (threadIdx.x == 0) sred[0] = 0.f;
-    __syncthreads();
+    for (int idx = threadIdx.x; idx < len * dk; idx += blockDim.x) {
+        int r = idx / dk, c = idx - r * dk;
+        sS[r * LS + c] = Kn[idx];
+    }
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
-        sD[r * C + i] = (i <= r) ? expf(sg[r] - sg[i]) : 0.f;
+        sP[r * LC + i] = Pg[r * C + i];
     }
-    bgemm(len, len, dk, [&](int r, int kk) { return Kn[r * dk + kk]; },
-          [&](int kk, int i) { return Kn[i * dk + kk]; },
-          [&](int r, int i, float s) { sKK[r * C + i] = s; });
-    bgemm(len, len, dk, [&](int r, int kk) { return Qn[r * dk + kk]; },
-          [&](int kk, int i) { return Kn[i * dk + kk]; },
-          [&](int r, int i, float s) { sQK[r * C + i] = s; });
-    bgemm(len, len, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
-          [&](int n, int i) { return Un[i * dv + n]; },
-          [&](int r, int i, float s) { sdP[r * C + i] = (i <= r) ? s : 0.f; });
     __syncthreads();
+    auto Dm = [&](int r, int i) { return i <= r ? expf(sg[r] - sg[i]) : 0.f; };
+    // K K^T and the first half of dT = dW (diag(Gamma) K)^T + dUnew V^T
+    rgemm<4, 4>(len, len, dk, [&](int r, int kk) { return sS[r * LS + kk]; },
+                [&](int kk, int i) { return sS[i * LS + kk]; },
+                [&](int r, int i, float s) { sKK[r * LC + i] = s; });
+    rgemm<4, 4>(len, len, dk, [&](int r, int kk) { return dW[r * dk + kk]; },
+                [&](int kk, int i) { return sG[i] * sS[i * LS + kk]; },
+                [&](int r, int i, float s) { sdT[r * LC + i] = s; });
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
+        int r = idx / dv, c = idx - r * dv;
+        sS[r * LS + c] = Un[idx];
+    }
+    __syncthreads();
+    // dP = lower(scale dO Unew^T)
+    rgemm<4, 4>(len, len, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
+                [&](int n, int i) { return sS[i * LS + n]; },
+                [&](int r, int i, float s) {
+                    sdP[r * LC + i] = (i <= r) ? s : 0.f;
+                    sDP[r * LC + i] = (i <= r) ? s * expf(sg[r] - sg[i]) : 0.f;
+                });
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
-        sX[r * C + i] = (i < r) ? sb[r] * sKK[r * C + i] * sD[r * C + i] : 0.f;
+        sY[r * LC + i] = (i < r) ? sb[r] * sKK[r * LC + i] * expf(sg[r] - sg[i]) : 0.f;
     }
     __syncthreads();
-    unit_lower_solve(sX, sLi, nullptr, len, C);
-    // Rows of dQ / dK / dW: one warp per row; also the q-term of d gamma and e_r.
-    for (int r = warp; r < len; r += nw) {
-        float qterm = 0.f, eterm = 0.f;
-        for (int kk = lane; kk < dk; kk += 32) {
-            float y = 0.f, kt = 0.f, wv = 0.f;
-            for (int n = 0; n < dv; ++n) {
-                float sin_kn = Sin[(size_t)kk * dv + n];
-                y = fmaf(sc * ld_in(dO + (row + r) * dv + n), sin_kn, y);
-                kt = fmaf(Un[r * dv + n], dSo[(size_t)kk * dv + n], kt);
-                wv = fmaf(-dUn[r * dv + n], sin_kn, wv);
-            }
-            float a = 0.f, c2 = 0.f;
-            for (int i = 0; i <= r; ++i) a = fmaf(sdP[r * C + i] * sD[r * C + i], Kn[i * dk + kk], a);
-            for (int i = r; i < len; ++i) c2 = fmaf(sdP[i * C + r] * sD[i * C + r], Qn[i * dk + kk], c2);
-            dQ[r * dk + kk] = fmaf(sG[r], y, a);
-            dK[r * dk + kk] = fmaf(sE[r], kt, c2);
-            dW[r * dk + kk] = wv;
-            qterm = fmaf(Qn[r * dk + kk], y, qterm);
-            eterm = fmaf(kt, Kn[r * dk + kk], eterm);
-        }
-        qterm = warp_sum(qterm);
-        eterm = warp_sum(eterm);
-        if (lane == 0) {
-            sdg[r] += sG[r] * qterm;
-            se[r] = sE[r] * eterm;
-        }
-    }
-    // <dS_out, S_in>
-    {
-        float p = 0.f;
-        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) p = fmaf(dSo[idx], Sin[idx], p);
-        p = warp_sum(p);
-        if (lane == 0) atomicAdd(sred, p);
+    unit_lower_solve(sY, sLi, nullptr, len, LC);
+    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
+        int r = idx / dv, c = idx - r * dv;
+        sS[r * LS + c] = ld_in(v + (row + r) * dv + c);
     }
     __syncthreads();
-    // dT = dW (diag(Gamma) K)^T + dUnew V^T
-    bgemm(len, len, dk + dv,
-          [&](int r, int x) { return x < dk ? dW[r * dk + x] : dUn[r * dv + (x - dk)]; },
-          [&](int x, int i) {
-              return x < dk ? sG[i] * Kn[i * dk + x] : ld_in(v + (row + i) * dv + (x - dk));
-          },
-          [&](int r, int i, float s) { sdT[r * C + i] = s; });
+    // dT += dUnew V^T;  dQ += (dP o D) K;  dK += (dP o D)^T Q
+    rgemm<4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
+                [&](int n, int i) { return sS[i * LS + n]; },
+                [&](int r, int i, float s) { sdT[r * LC + i] += s; });
+    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sDP[r * LC + i]; },
+                [&](int i, int kk) { return Kn[i * dk + kk]; },
+                [&](int r, int kk, float s) { dQ[r * dk + kk] += s; });
+    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sDP[i * LC + r]; },
+                [&](int i, int kk) { return Qn[i * dk + kk]; },
+                [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
     __syncthreads();
-    // dGK = T^T dW (T = Linv diag(beta)); dK += Gamma dGK; d gamma += Gamma <dGK, K>
-    for (int r = warp; r < len; r += nw) {
-        float s2 = 0.f;
-        for (int kk = lane; kk < dk; kk += 32) {
-            float a = 0.f;
-            for (int i = r; i < len; ++i) a = fmaf(sLi[i * C + r], dW[i * dk + kk], a);
-            a *= sb[r];
-            dK[r * dk + kk] += sG[r] * a;
-            s2 = fmaf(a, Kn[r * dk + kk], s2);
-        }
-        s2 = warp_sum(s2);
-        if (lane == 0) sdg[r] += sG[r] * s2;
-        // dV = T^T dUnew
-        for (int n = lane; n < dv; n += 32) {
-            float a = 0.f;
-            for (int i = r; i < len; ++i) a = fmaf(sLi[i * C + r], dUn[i * dv + n], a);
-            st_out(dvout + (row + r) * dv + n, sb[r] * a);
-        }
-    }
-    // d beta (through T = Linv diag(beta)) and X = Linv^T (dT diag(beta))
+    // dGK = T^T dW (T = Linv diag(beta)); dK += Gamma dGK; d gamma += Gamma <dGK, K>;  dV = T^T dUnew
+    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sLi[i * LC + r]; },
+                [&](int i, int kk) { return dW[i * dk + kk]; },
+                [&](int r, int kk, float s) {
+                    const float a = sb[r] * s;
+                    dK[r * dk + kk] += sG[r] * a;
+                    atomicAdd(&sk2[r], a * Kn[r * dk + kk]);
+                });
+    rgemm<4, 8>(len, dv, len, [&](int r, int i) { return sLi[i * LC + r]; },
+                [&](int i, int n) { return dUn[i * dv + n]; },
+                [&](int r, int n, float s) { st_out(dvout + (row + r) * dv + n, sb[r] * s); });
+    // d beta through T = Linv diag(beta)
     for (int i = threadIdx.x; i < len; i += blockDim.x) {
         float a = 0.f;
-        for (int r = i; r < len; ++r) a = fmaf(sLi[r * C + i], sdT[r * C + i], a);
+        for (int r = i; r < len; ++r) a = fmaf(sLi[r * LC + i], sdT[r * LC + i], a);
         sdb[i] += a;
     }
-    bgemm(len, len, len, [&](int a, int r) { return sLi[r * C + a]; },
-          [&](int r, int bb) { return sdT[r * C + bb] * sb[bb]; },
-          [&](int a, int bb, float s) { sX[a * C + bb] = s; });
+    // X = Linv^T (dT diag(beta))
+    rgemm<4, 4>(len, len, len, [&](int a, int r) { return sLi[r * LC + a]; },
+                [&](int r, int bb) { return sdT[r * LC + bb] * sb[bb]; },
+                [&](int a, int bb, float s) { sDP[a * LC + bb] = s; });
     __syncthreads();
     // dA = strict_lower(-X Linv^T)
-    bgemm(len, len, len, [&](int a, int c) { return sX[a * C + c]; },
-          [&](int c, int bb) { return sLi[bb * C + c]; },
-          [&](int a, int bb, float s) { sY[a * C + bb] = (bb < a) ? -s : 0.f; });
+    rgemm<4, 4>(len, len, len, [&](int a, int c) { return sDP[a * LC + c]; },
+                [&](int c, int bb) { return sLi[bb * LC + c]; },
+                [&](int a, int bb, float s) { sY[a * LC + bb] = (bb < a) ? -s : 0.f; });
     __syncthreads();
-    // d beta from A, E = dD o D, d gamma row/col sums;  Y <- dKK = dA o beta_r o D
+    // d beta from A, E = dD o D, d gamma row / column sums;  then Y <- dKK = dA o beta_r o D
     for (int r = warp; r < len; r += nw) {
         float db = 0.f, rs = 0.f;
         for (int i = lane; i < len; i += 32) {
-            float dA = sY[r * C + i];
-            float Dri = sD[r * C + i];
-            db = fmaf(dA * sKK[r * C + i], Dri, db);
-            float E = (dA * sb[r] * sKK[r * C + i] + (i <= r ? sdP[r * C + i] * sQK[r * C + i] : 0.f)) * Dri;
-            rs += E;
+            const float dA = sY[r * LC + i], Dri = Dm(r, i);
+            db = fmaf(dA * sKK[r * LC + i], Dri, db);
+            rs += dA * sb[r] * sKK[r * LC + i] * Dri + (i <= r ? sdP[r * LC + i] * sP[r * LC + i] : 0.f);
         }
         db = warp_sum(db);
         rs = warp_sum(rs);
         if (lane == 0) {
             sdb[r] += db;
-            sdg[r] += rs;
+            sdg[r] += rs + sG[r] * sk2[r];
         }
     }
     for (int i = warp; i < len; i += nw) {
         float cs = 0.f;
-        for (int r = lane; r < len; r += 32) {
-            float Dri = sD[r * C + i];
-            float E = (sY[r * C + i] * sb[r] * sKK[r * C + i] + (i <= r ? sdP[r * C + i] * sQK[r * C + i] : 0.f)) * Dri;
-            cs += E;
-        }
+        for (int r = lane; r < len; r += 32)
+            cs += sY[r * LC + i] * sb[r] * sKK[r * LC + i] * Dm(r, i) +
+                  (i <= r ? sdP[r * LC + i] * sP[r * LC + i] : 0.f);
         cs = warp_sum(cs);
-        if (lane == 0) sdg[i] -= cs;
+        if (lane == 0) atomicAdd(&sdg[i], -cs);
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
-        sY[r * C + i] = sY[r * C + i] * sb[r] * sD[r * C + i];
+        sY[r * LC + i] = sY[r * LC + i] * sb[r] * Dm(r, i);
     }
     __syncthreads();
-    // dK += dKK K + dKK^T K;  then the normalisation chain rule for dq, dk
-    for (int r = warp; r < len; r += nw) {
-        for (int kk = lane; kk < dk; kk += 32) {
-            float a = 0.f;
-            for (int i = 0; i < len; ++i)
-                a = fmaf(sY[r * C + i] + sY[i * C + r], Kn[i * dk + kk], a);
-            dK[r * dk + kk] += a;
-        }
-    }
+    // dK += (dKK + dKK^T) K
+    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sY[r * LC + i] + sY[i * LC + r]; },
+                [&](int i, int kk) { return Kn[i * dk + kk]; },
+                [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
     __syncthreads();
     if (threadIdx.x == 0) {
         float es = 0.f;
@@ -511,7 +614,7 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
             sdg[r] -= se[r];
             es += se[r];
         }
-        sdg[len - 1] += es + expf(gC) * sred[0];
+        sdg[len - 1] += es + expf(gC) * aux[2 * C];
         // d g = reverse cumulative sum of d gamma within the chunk
         float acc = 0.f;
         for (int r = len - 1; r >= 0; --r) {
@@ -519,6 +622,7 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
             if (dg) dg[row + r] = acc;
         }
     }
+    // the normalisation chain rule for dq, dk
     for (int r = warp; r < len; r += nw) {
         const Tin *qr = q + (row + r) * dk;
         const Tin *kr = k + (row + r) * dk;
@@ -547,14 +651,20 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
 }
 
 // ----------------------------------------------------------------------------- host launchers
-static size_t smem_prep(const Geo &g) { return sizeof(float) * (g.C * g.dk + 2 * g.C * g.C + 3 * g.C); }
-static size_t smem_scan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + g.C * BV + g.C); }
-static size_t smem_out(const Geo &g) { return sizeof(float) * (g.C * g.C + g.C); }
-static size_t smem_bscan(const Geo &g, int BV)
+static size_t smem_prep(const Geo &g)
 {
-    return sizeof(float) * (g.dk * BV + 2 * g.C * BV + g.C * g.C + 2 * g.C);
+    const size_t LK = g.dk + 1, LC = g.C + 1;
+    return sizeof(float) * (g.C * LK + g.C * (LK > (size_t)g.dv ? LK : g.dv) + 2 * g.C * LC + 3 * g.C);
 }
-static size_t smem_bchunk(const Geo &g) { return sizeof(float) * (8 * g.C * g.C + 7 * g.C + 1); }
+static size_t smem_scan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + g.C * BV + g.C); }
+static size_t smem_out(const Geo &g) { return sizeof(float) * g.C; }
+static size_t smem_bscan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + 2 * g.C * BV + 2 * g.C); }
+static size_t smem_bbig(const Geo &g) { return sizeof(float) * (g.dv * (g.dk + 1) + 4 * g.C + 4); }
+static size_t smem_bchunk(const Geo &g)
+{
+    const size_t LC = g.C + 1, LS = (g.dk > g.dv ? g.dk : g.dv) + 1;
+    return sizeof(float) * (7 * g.C * LC + g.C * LS + 8 * g.C);
+}
 
 static int slice_width(const Geo &g) { return g.dv < 32 ? g.dv : 32; }
 
@@ -606,6 +716,9 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     if (g.N > 0)
         k_bscan<Tin><<<dim3(g.N, g.H, (g.dv + BV - 1) / BV), 256, smem_bscan(g, BV), st>>>(
             g, dO, dhT, dh0, w, BV);
+    if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
+    if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 256, smem_bbig(g), st>>>(g, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bchunk<Tin>, smem_bchunk(g))) != cudaSuccess) return e;
     if (g.NC > 0)

@@ -10,11 +10,12 @@ namespace gen {
 struct Ws {
     float *Kn, *Qn, *W;        // [slots][C][dk]  normalised K, Q; WY factor W
     float *U, *Unew;           // [slots][C][dv]
-    float *Tm;                 // [slots][C][C]   UT transform T
     float *gam;                // [slots][C]      within-chunk cumulative log-gate
     float *Sin;                // [slots][dk][dv] state entering the chunk
     float *dSo, *dUn;          // backward: dS leaving the chunk, dUnew
     float *dQ, *dK, *dW;       // backward scratch [slots][C][dk]
+    float *P;                  // [slots][C][C]   lower(Q K^T o D), diagonal kept
+    float *aux;                // backward [slots][2C + 4]: row sums and <dS_out, S_in>
 };
 
 template <class Tin>
