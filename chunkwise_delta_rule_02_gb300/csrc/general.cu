@@ -8,7 +8,7 @@
 // scan) with the gates of "Gated DeltaNet" folded in as within-chunk cumulative
 // log-decays:
 //   prep  : per chunk, parallel       normalise q,k; gamma; A; T; W; U; P
-//   scan  : per (seq, head, dv-slice) Unew = U - W S; S <- Gamma_C S + Kt^T Unew
+//   scan  : per (seq, head, 64-column dv-slice) Unew = U - W S; S <- Gamma_C S + Kt^T Unew
 //   out   : per chunk, parallel       O = diag(Gamma) Q S + P Unew
 // and the backward (chunk states recomputed by prep + scan, then):
 //   bscan : per (seq, head, dv-slice), last chunk first:
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
         const float *W = w.W + slot * C * dk;
         const float *U = w.U + slot * C * dv;
         float *Un = w.Unew + slot * C * dv;
-        rgemm<4, 2>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
+        rgemm<4, 4>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
                     [&](int kk, int n) { return sS[kk * BV + n]; },
                     [&](int r, int n, float acc) {
                         float u = U[r * dv + n0 + n] - acc;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
         __syncthreads();
         const float *Kn = w.Kn + slot * C * dk;
         const float GC = expf(gC);
-        rgemm<8, 2>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
+        rgemm<8, 4>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
                     [&](int r, int n) { return sU[r * BV + n]; },
                     [&](int kk, int n, float acc) { sS[kk * BV + n] = fmaf(GC, sS[kk * BV + n], acc); });
         __syncthreads();
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
         __syncthreads();
         // dUnew(i, n) = sum_r P(r, i) dO(r, n) + exp(gC - gam_i) sum_kk K(i, kk) dS(kk, n)
         float *dUg = w.dUn + slot * C * dv;
-        rgemm<4, 2>(len, nb, len + dk,
+        rgemm<4, 4>(len, nb, len + dk,
                     [&](int i, int x) { return x < len ? Pg[x * C + i] : sE[i] * Kn[i * dk + (x - len)]; },
                     [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdS[(x - len) * BV + n]; },
                     [&](int i, int n, float u) {
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
         __syncthreads();
         // dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
         const float GC = expf(gC);
-        rgemm<8, 2>(dk, nb, 2 * len,
+        rgemm<8, 4>(dk, nb, 2 * len,
                     [&](int kk, int x) { return x < len ? sG[x] * Qn[x * dk + kk] : -W[(x - len) * dk + kk]; },
                     [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdU[(x - len) * BV + n]; },
                     [&](int kk, int n, float acc) { sdS[kk * BV + n] = fmaf(GC, sdS[kk * BV + n], acc); });
@@ -666,7 +666,7 @@ static size_t smem_bchunk(const Geo &g)
     return sizeof(float) * (7 * g.C * LC + g.C * LS + 8 * g.C);
 }
 
-static int slice_width(const Geo &g) { return g.dv < 32 ? g.dv : 32; }
+static int slice_width(const Geo &g) { return g.dv < 64 ? g.dv : 64; }
 
 template <class K>
 static cudaError_t set_smem(K kernel, size_t bytes)
