@@ -1,0 +1,77 @@
+"""gdn_chunk_fwd_host: the forward on host (pinned) buffers, against the oracle and
+against gdn_chunk_fwd on the same inputs, with and without gate, initial and
+final state, on the tcgen05 kernels (bf16, d = 128) and the general kernels
+(fp32)."""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL, oracle_fwd, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _host_forward(x, want_hT=True):
+    """Run gdn_chunk_fwd_host on pinned copies of x; returns (o, hT) as numpy."""
+    from chunkwise_delta_rule_02_gb300 import binding
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("q", "k", "v", "beta", "g", "h0")
+               else v) for k, v in x.items()}
+    shape = binding.make_shape(pin["q"], pin["v"])
+    B, H, T, d = x["q"].shape
+    o = torch.full(tuple(x["v"].shape), float("nan"), dtype=x["v"].dtype).pin_memory()
+    hT = torch.full((B, H, d, x["v"].shape[-1]), float("nan")).pin_memory() if want_hT else None
+    arena = torch.empty(binding.dn_host_arena_size(shape, pin["g"] is not None, pin["h0"] is not None),
+                        dtype=torch.uint8, device=DEV)
+    ws = binding.alloc_workspace(shape, False, DEV)
+    stream = torch.cuda.current_stream()
+    binding.gdn_chunk_fwd_host(shape, pin["q"], pin["k"], pin["v"], pin["beta"], pin["g"], pin["h0"], o,
+                               hT, arena, ws, stream)
+    stream.synchronize()
+    assert binding.dn_device_status(ws) == binding.DN_OK
+    return o.float().numpy(), (hT.numpy() if hT is not None else None)
+
+
+def _device_forward(x):
+    import chunkwise_delta_rule_02_gb300 as gdn
+    d = to_dev(x, DEV)
+    o, hT = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), hT.cpu().numpy()
+
+
+def _inputs(B, H, T, d, dtype, gated, with_h0, seed):
+    from chunkwise_delta_rule_02_gb300 import workloads
+    w = workloads.Workload("host", B, H, T, d, dtype, gated, with_h0, seed)
+    return workloads.generate(w)
+
+
+@pytest.mark.parametrize("B,H,T,d,dtype,gated,with_h0", [
+    (2, 3, 4133, 128, "bf16", True, True),     # ragged last chunk
+    (1, 2, 2048, 128, "bf16", False, False),   # DeltaNet, zero initial state
+    (2, 2, 300, 128, "bf16", True, True),
+    (1, 2, 2100, 64, "f32", True, True),       # general fp32 kernels
+])
+def test_host_forward_matches_oracle_and_device_path(B, H, T, d, dtype, gated, with_h0):
+    x = _inputs(B, H, T, d, dtype, gated, with_h0, seed=T + d)
+    ho, hh = _host_forward(x)
+    do, dh = _device_forward(x)
+    assert np.isfinite(ho).all() and np.isfinite(hh).all()
+    assert rel(ho, do) <= TOL[dtype] and rel(hh, dh) <= TOL[dtype]
+    sel = [(0, 0), (B - 1, H - 1)]
+    for (b, h), (ro, rh) in zip(sel, oracle_fwd(x, sel=sel)):
+        assert rel(ho[b, h], ro[0, 0]) <= TOL[dtype], rel(ho[b, h], ro[0, 0])
+        assert rel(hh[b, h], rh[0, 0]) <= TOL[dtype], rel(hh[b, h], rh[0, 0])
+
+
+def test_host_forward_without_final_state():
+    x = _inputs(1, 2, 2048, 128, "bf16", True, True, seed=5)
+    ho, _ = _host_forward(x, want_hT=False)
+    do, _ = _device_forward(x)
+    assert rel(ho, do) <= TOL["bf16"]
