@@ -250,6 +250,76 @@ def run_reference(args, w, x):
     print(json.dumps(line), flush=True)
 
 
+DECODE_WORKLOAD = "gdn_decode_bf16_n256h16d128"
+
+
+def run_decode(args):
+    """Recurrent decode step (one token for each of 256 sequences x 16 heads, d = 128,
+    bf16, gated, state updated in place): tokens/s and the HBM roofline of its
+    compulsory bytes (the fp32 state read and written, q, k, v, beta, g in, o out)."""
+    import torch
+    import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding
+    rank, world, local = dist_env()
+    N, H, d = 256, 16, 128
+    gen = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(N, H, d, generator=gen).to(torch.bfloat16) for _ in range(3))
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).to(torch.bfloat16)
+    g = -torch.nn.functional.softplus(torch.randn(N, H, generator=gen)) / 16
+    S = 0.02 * torch.randn(N, H, d, d, generator=gen)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    qd, kd, vd, bd, gd, Sd = (t.to(dev) for t in (q, k, v, beta, g, S))
+    o = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
+    shape = binding.make_shape(qd.view(N, H, 1, d), vd.view(N, H, 1, d))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.gdn_decode_step(shape, qd, kd, vd, bd, gd, Sd, Sd, o, stream)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    clk = ClockSampler(local)
+    clk.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    barrier()
+    clocks = clk.stop()
+    ms = max_over_ranks(sum(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)) / args.steps, pg, dev)
+    if rank == 0:
+        pk, src = peaks()
+        nbytes = N * H * (2 * d * d * 4 + 4 * d * 2 + 2 + 4)
+        achieved = nbytes / (ms / 1000.0) / 1e9
+        line = {"metric": "recurrent decode step tokens/s on 1 GB300; % of HBM roofline",
+                "value": N * world / (ms / 1000.0), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": DECODE_WORKLOAD, "N": N, "H": H, "d": d,
+                           "l2": "no flush: the 268 MB state read and written per step > 129 MB L2"},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                             "frac": achieved / pk["hbm_gbs"], "traffic": None, "kernel": "k_decode",
+                             "algorithmic_bytes_per_launch": nbytes, "peak_source": src},
+                "clocks": clocks, "e2e": None, "gpu_launches": args.steps}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -260,6 +330,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
+    if args.workload == DECODE_WORKLOAD and args.impl == "ours":
+        run_decode(args)
+        return
     import torch
     from chunkwise_delta_rule_02_gb300 import workloads
     w = workloads.WORKLOADS[args.workload]

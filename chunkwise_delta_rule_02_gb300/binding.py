@@ -7,7 +7,7 @@ call returns an error status, these functions raise.
 
 The names match the C ABI: dn_workspace_size, dn_chunk_fwd, gdn_chunk_fwd,
 gdn_chunk_bwd, dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status,
-dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc.  ``forward`` / ``backward`` additionally allocate outputs
+dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc, gdn_decode_step.  ``forward`` / ``backward`` additionally allocate outputs
 and the workspace with torch (device memory only).
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ DN_F32, DN_BF16 = 0, 1
 
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
-           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_plan"]
+           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_plan", "gdn_decode_step"]
 
 
 class DnShape(ctypes.Structure):
@@ -80,6 +80,8 @@ def lib():
             L.gdn_chunk_fwd_host.restype = I
             L.gdn_chunk_fwd_noalloc.argtypes = [SP, P, P, P, P, P, P, P, P, P]
             L.gdn_chunk_fwd_noalloc.restype = I
+            L.gdn_decode_step.argtypes = [SP, P, P, P, P, P, P, P, P, P]
+            L.gdn_decode_step.restype = I
             L.dn_device_status.argtypes = [P, P]
             L.dn_device_status.restype = I
             L.dn_status_str.argtypes = [I]
@@ -193,6 +195,28 @@ def gdn_chunk_fwd_noalloc(shape, q, k, v, beta, g, h0, o, hT, stream=None):
     rc = lib().gdn_chunk_fwd_noalloc(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g),
                                      _p(h0), _p(o), _p(hT), _stream(stream))
     _check(rc, "gdn_chunk_fwd_noalloc")
+
+
+def gdn_decode_step(shape, q, k, v, beta, g, state_in, state_out, o, stream=None):
+    """One recurrent step per sequence: q, k [N,H,dk], v [N,H,dv], beta [N,H], g [N,H] or
+    None, states [N,H,dk,dv] float32 (state_out may be state_in), o [N,H,dv]."""
+    rc = lib().gdn_decode_step(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g),
+                               _p(state_in), _p(state_out), _p(o), _stream(stream))
+    _check(rc, "gdn_decode_step")
+
+
+def decode_step(q, k, v, beta, g=None, state=None, out_state=None, scale=1.0, qk_l2norm=True,
+                eps=1e-6):
+    """Allocate o (and the new state unless out_state is given; pass out_state=state for an
+    in-place update) and run gdn_decode_step.  q, k [N,H,dk].  Returns (o, new_state)."""
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    shape = make_shape(q.view(N, H, 1, dk), v.view(N, H, 1, dv), 64, None, scale, qk_l2norm, eps)
+    o = torch.empty((N, H, dv), dtype=v.dtype, device=v.device)
+    if out_state is None:
+        out_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    gdn_decode_step(shape, q, k, v, beta, g, state, out_state, o)
+    return o, out_state
 
 
 def dn_device_status(ws, stream=None) -> int:

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode.h"
 #include "fast.h"
 #include "general.h"
 
@@ -302,6 +303,34 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
             (const __nv_bfloat16 *)beta, gate, h0, (const __nv_bfloat16 *)dO, dhT,
             (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
             (__nv_bfloat16 *)dbeta, dg, dh0, w, st);
+    return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, const void *v,
+                          const void *beta, const float *g, const float *state_in, float *state_out,
+                          void *o, void *stream)
+{
+    Geo gg;
+    dn_status rc = check_shape(shape, &gg);
+    if (rc != DN_OK) return rc;
+    if (shape->cu_seqlens || shape->T != 1) return DN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !beta || !state_out || !o) return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, g, state_in, state_out, o};
+    for (const void *p : ptrs)
+        if (p && ((uintptr_t)p & 3u)) return DN_ERR_INVALID_ARG;
+    dec::Args a;
+    a.N = shape->B; a.H = shape->H; a.dk = shape->dk; a.dv = shape->dv;
+    a.l2norm = shape->qk_l2norm != 0; a.scale = shape->scale; a.eps = shape->eps;
+    a.gate = g; a.state_in = state_in; a.state_out = state_out;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (shape->dtype == DN_F32)
+        e = dec::step<float>(a, (const float *)q, (const float *)k, (const float *)v,
+                             (const float *)beta, (float *)o, st);
+    else
+        e = dec::step<__nv_bfloat16>(a, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                                     (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta,
+                                     (__nv_bfloat16 *)o, st);
     return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
 }
 

@@ -1,0 +1,141 @@
+// Recurrent decode step of the (gated) delta rule: one new token per sequence,
+// the state updated in place or into a second buffer.
+//
+// Per (sequence, head), with the state S stored d_k x d_v (key index outer) and
+// the token's normalised q, k:
+//     S' = alpha (I - beta k k^T) S + beta k v^T,   o = scale S'^T q
+// ("Gated DeltaNet", Table 1, row Gated DeltaNet; alpha = 1 is DeltaNet).
+// Each column n of S evolves on its own:
+//     r_n = sum_i S[i][n] k_i,   u_n = beta (v_n - alpha r_n),
+//     S'[i][n] = alpha S[i][n] + k_i u_n,
+//     o_n = scale (alpha sum_i S[i][n] q_i + u_n (k . q)),
+// so one pass reads the state once, keeps it in registers, and writes it once:
+// the step moves the compulsory 2 d_k d_v fp32 state bytes per head and is
+// bound by HBM bandwidth.
+#include "common.cuh"
+#include "decode.h"
+
+namespace gdn {
+namespace dec {
+
+namespace {
+
+constexpr int kCols = 32;            // d_v columns per CTA (one warp's width)
+constexpr int kGroups = 8;           // row groups: 256 threads
+constexpr int kRows = kMaxD / kGroups;
+
+template <class Tin>
+__global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *__restrict__ q,
+                                                          const Tin *__restrict__ k,
+                                                          const Tin *__restrict__ v,
+                                                          const Tin *__restrict__ beta,
+                                                          Tin *__restrict__ o)
+{
+    const int nsl = (a.dv + kCols - 1) / kCols;
+    const int seq = blockIdx.x / nsl, sl = blockIdx.x - seq * nsl, h = blockIdx.y;
+    const int col = threadIdx.x & 31, rg = threadIdx.x >> 5;
+    const int n = sl * kCols + col;
+    const size_t item = (size_t)seq * a.H + h;
+    __shared__ float sk[kMaxD], sq[kMaxD];
+    __shared__ float sr[kGroups][kCols], sp[kGroups][kCols];
+    __shared__ float su[kCols];
+    __shared__ float sscal[2];   // k . q, alpha
+
+    for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
+        sk[i] = ld_in(k + item * a.dk + i);
+        sq[i] = ld_in(q + item * a.dk + i);
+    }
+    __syncthreads();
+    if (rg == 0) {
+        float kk = 0.f, qq = 0.f;
+        for (int i = col; i < a.dk; i += 32) {
+            kk = fmaf(sk[i], sk[i], kk);
+            qq = fmaf(sq[i], sq[i], qq);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, o2);
+            qq += __shfl_xor_sync(0xffffffffu, qq, o2);
+        }
+        const float rk = a.l2norm ? rsqrtf(kk + a.eps) : 1.f;
+        const float rq = a.l2norm ? rsqrtf(qq + a.eps) : 1.f;
+        float kq = 0.f;
+        for (int i = col; i < a.dk; i += 32) {
+            sk[i] *= rk;
+            sq[i] *= rq;
+            kq = fmaf(sk[i], sq[i], kq);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o2);
+        if (col == 0) {
+            sscal[0] = kq;
+            sscal[1] = a.gate ? expf(a.gate[item]) : 1.f;
+        }
+    }
+    __syncthreads();
+    const float alpha = sscal[1];
+    // this thread's rows rg, rg + 8, ... of column n: read once, kept in registers
+    float s[kRows];
+    float r = 0.f, p = 0.f;
+    const float *Sin = a.state_in ? a.state_in + item * a.dk * a.dv : nullptr;
+    float *Sout = a.state_out + item * a.dk * a.dv;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const int i = rg + kGroups * j;
+        s[j] = (n < a.dv && i < a.dk && Sin) ? Sin[(size_t)i * a.dv + n] : 0.f;
+        if (i < a.dk) {
+            r = fmaf(s[j], sk[i], r);
+            p = fmaf(s[j], sq[i], p);
+        }
+    }
+    sr[rg][col] = r;
+    sp[rg][col] = p;
+    __syncthreads();
+    if (rg == 0) {
+        float rt = 0.f, pt = 0.f;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            rt += sr[g][col];
+            pt += sp[g][col];
+        }
+        float u = 0.f;
+        if (n < a.dv) {
+            const float b = ld_in(beta + item);
+            u = b * (ld_in(v + item * a.dv + n) - alpha * rt);
+            st_out(o + item * a.dv + n, a.scale * fmaf(alpha, pt, u * sscal[0]));
+        }
+        su[col] = u;
+    }
+    __syncthreads();
+    if (n < a.dv) {
+        const float u = su[col];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            const int i = rg + kGroups * j;
+            if (i < a.dk) Sout[(size_t)i * a.dv + n] = fmaf(alpha, s[j], sk[i] * u);
+        }
+    }
+}
+
+}  // namespace
+
+template <class Tin>
+cudaError_t step(const Args &a, const Tin *q, const Tin *k, const Tin *v, const Tin *beta, Tin *o,
+                 cudaStream_t st)
+{
+    if (a.N == 0) return cudaSuccess;
+    const int nsl = (a.dv + kCols - 1) / kCols;
+    const long long blocks = (long long)a.N * nsl;
+    if (blocks > 0x7fffffffLL || a.H > 65535) return cudaErrorInvalidValue;
+    k_decode<Tin><<<dim3((unsigned)blocks, a.H), kCols * kGroups, 0, st>>>(a, q, k, v, beta, o);
+    return cudaPeekAtLastError();
+}
+
+template cudaError_t step<float>(const Args &, const float *, const float *, const float *,
+                                 const float *, float *, cudaStream_t);
+template cudaError_t step<__nv_bfloat16>(const Args &, const __nv_bfloat16 *, const __nv_bfloat16 *,
+                                         const __nv_bfloat16 *, const __nv_bfloat16 *, __nv_bfloat16 *,
+                                         cudaStream_t);
+
+}  // namespace dec
+}  // namespace gdn

@@ -115,6 +115,25 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
                         const float *dhT, void *dq, void *dk, void *dv, void *dbeta,
                         float *dg, float *dh0, void *ws, size_t ws_bytes, void *stream);
 
+/* Recurrent decode step (one new token per sequence; the recurrence itself, as
+ * in Table 1 of the Gated DeltaNet page, row "Gated DeltaNet", and the
+ * Gated DeltaNet page's reply on decoding with a fixed-size state):
+ *   S' = alpha (I - beta k k^T) S + beta k v^T,   o = scale S'^T q,
+ * q, k normalised in the kernel when shape->qk_l2norm.  Shape: B = number of
+ * sequences, H heads, T must be 1, dk, dv <= 128, cu_seqlens NULL; chunk is
+ * ignored (any accepted value).  Layouts (dtype = shape->dtype unless noted):
+ *   q, k [B,H,dk], v [B,H,dv], beta [B,H]; g [B,H] float32 log-gate or NULL
+ *   (alpha = 1); state_in [B,H,dk,dv] float32 or NULL (zero state);
+ *   state_out [B,H,dk,dv] float32, may be the same buffer as state_in (the
+ *   update is then in place); o [B,H,dv].
+ * Needs no workspace, allocates nothing, does not synchronise.  Errors:
+ * DN_ERR_INVALID_ARG for a bad shape, T != 1, packed input, a missing buffer or
+ * a pointer that is not 4-byte aligned; DN_ERR_UNSUPPORTED for head dims above
+ * 128; DN_ERR_CUDA if the launch fails. */
+dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, const void *v,
+                          const void *beta, const float *g, const float *state_in,
+                          float *state_out, void *o, void *stream);
+
 /* Bytes of the device staging arena gdn_chunk_fwd_host needs (0 on bad args). */
 size_t dn_host_arena_size(const dn_shape *shape, int gated, int with_h0);
 

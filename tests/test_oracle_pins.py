@@ -220,6 +220,23 @@ def test_output_uses_state_after_own_write():
                                rtol=1e-13)
 
 
+def test_single_step_from_a_state_is_the_matrix_update():
+    """The decode step: from a non-zero state, one token gives S' = alpha (I - beta k k^T) S
+    + beta k v^T with the normalised key, and o = scale S'^T q_hat ([GDN] Table 1 row
+    Gated DeltaNet, written out as matrices)."""
+    rng = RNG(26)
+    q, k, v, beta, g, S0 = _rand_inputs(rng, 2, 3, 1, 7, 5)
+    o, hT = oracle.fwd(q, k, v, beta, g, S0, scale=0.7)
+    for b in range(2):
+        for h in range(3):
+            kn = k[b, h, 0] / np.sqrt((k[b, h, 0] ** 2).sum() + oracle.EPS)
+            qn = q[b, h, 0] / np.sqrt((q[b, h, 0] ** 2).sum() + oracle.EPS)
+            a, bt = np.exp(g[b, h, 0]), beta[b, h, 0]
+            Sp = a * (np.eye(7) - bt * np.outer(kn, kn)) @ S0[b, h] + bt * np.outer(kn, v[b, h, 0])
+            np.testing.assert_allclose(hT[b, h], Sp, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(o[b, h, 0], 0.7 * Sp.T @ qn, rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------- [GDN-SP], packing
 def test_state_passing_split_equals_whole():
     rng = RNG(16)
