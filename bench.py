@@ -292,6 +292,8 @@ def run_decode(args):
     barrier()
     clk = ClockSampler(local)
     clk.start()
+    time.sleep(0.3)
+    barrier()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     ev[0].record(stream)
     for i in range(args.steps):

@@ -9,7 +9,9 @@
 //     r_n = sum_i S[i][n] k_i,   u_n = beta (v_n - alpha r_n),
 //     S'[i][n] = alpha S[i][n] + k_i u_n,
 //     o_n = scale (alpha sum_i S[i][n] q_i + u_n (k . q)),
-// so one pass reads the state once, keeps it in registers, and writes it once:
+// so one pass reads the state once, keeps it in registers, and writes it once
+// (16-byte accesses, one CTA per (sequence, head), when d_v % 4 == 0; else
+// 4-byte accesses, one CTA per 32-column slice):
 // the step moves the compulsory 2 d_k d_v fp32 state bytes per head and is
 // bound by HBM bandwidth.
 #include "common.cuh"
@@ -117,6 +119,107 @@ __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *_
     }
 }
 
+// The same step with 16-byte state accesses: one CTA per (sequence, head), lane
+// l of every warp owns columns 4l .. 4l + 3, so a warp moves one 512-byte state
+// row per instruction (needs d_v % 4 == 0 and 16-byte aligned states).
+template <class Tin>
+__global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__ q,
+                                                 const Tin *__restrict__ k,
+                                                 const Tin *__restrict__ v,
+                                                 const Tin *__restrict__ beta,
+                                                 Tin *__restrict__ o)
+{
+    const int seq = blockIdx.x, h = blockIdx.y;
+    const int lane = threadIdx.x & 31, rg = threadIdx.x >> 5;
+    const int n4 = 4 * lane;
+    const bool live = n4 < a.dv;
+    const size_t item = (size_t)seq * a.H + h;
+    __shared__ float sk[kMaxD], sq[kMaxD];
+    __shared__ float4 sr[kGroups][32], sp[kGroups][32];
+    __shared__ float4 su[32];
+    __shared__ float sscal[2];
+
+    for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
+        sk[i] = ld_in(k + item * a.dk + i);
+        sq[i] = ld_in(q + item * a.dk + i);
+    }
+    __syncthreads();
+    if (rg == 0) {
+        float kk = 0.f, qq = 0.f;
+        for (int i = lane; i < a.dk; i += 32) {
+            kk = fmaf(sk[i], sk[i], kk);
+            qq = fmaf(sq[i], sq[i], qq);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, o2);
+            qq += __shfl_xor_sync(0xffffffffu, qq, o2);
+        }
+        const float rk = a.l2norm ? rsqrtf(kk + a.eps) : 1.f;
+        const float rq = a.l2norm ? rsqrtf(qq + a.eps) : 1.f;
+        float kq = 0.f;
+        for (int i = lane; i < a.dk; i += 32) {
+            sk[i] *= rk;
+            sq[i] *= rq;
+            kq = fmaf(sk[i], sq[i], kq);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o2);
+        if (lane == 0) {
+            sscal[0] = kq;
+            sscal[1] = a.gate ? expf(a.gate[item]) : 1.f;
+        }
+    }
+    __syncthreads();
+    const float alpha = sscal[1];
+    const float4 *Sin = a.state_in ? reinterpret_cast<const float4 *>(a.state_in + item * a.dk * a.dv) : nullptr;
+    float4 *Sout = reinterpret_cast<float4 *>(a.state_out + item * a.dk * a.dv);
+    const int dv4 = a.dv >> 2;
+    float4 s[kRows];
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f), p = r;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const int i = rg + kGroups * j;
+        s[j] = (live && i < a.dk && Sin) ? Sin[(size_t)i * dv4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < a.dk) {
+            const float ki = sk[i], qi = sq[i];
+            r.x = fmaf(s[j].x, ki, r.x); r.y = fmaf(s[j].y, ki, r.y);
+            r.z = fmaf(s[j].z, ki, r.z); r.w = fmaf(s[j].w, ki, r.w);
+            p.x = fmaf(s[j].x, qi, p.x); p.y = fmaf(s[j].y, qi, p.y);
+            p.z = fmaf(s[j].z, qi, p.z); p.w = fmaf(s[j].w, qi, p.w);
+        }
+    }
+    sr[rg][lane] = r;
+    sp[rg][lane] = p;
+    __syncthreads();
+    if (threadIdx.x < a.dv) {
+        // column c = threadIdx.x: component c & 3 of lane c >> 2
+        const int c = threadIdx.x, L = c >> 2, e = c & 3;
+        float rt = 0.f, pt = 0.f;
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            rt += reinterpret_cast<const float *>(&sr[g][L])[e];
+            pt += reinterpret_cast<const float *>(&sp[g][L])[e];
+        }
+        const float u = ld_in(beta + item) * (ld_in(v + item * a.dv + c) - alpha * rt);
+        st_out(o + item * a.dv + c, a.scale * fmaf(alpha, pt, u * sscal[0]));
+        reinterpret_cast<float *>(&su[L])[e] = u;
+    }
+    __syncthreads();
+    if (live) {
+        const float4 u = su[lane];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            const int i = rg + kGroups * j;
+            if (i < a.dk) {
+                const float ki = sk[i];
+                Sout[(size_t)i * dv4 + lane] = make_float4(fmaf(alpha, s[j].x, ki * u.x), fmaf(alpha, s[j].y, ki * u.y),
+                                                           fmaf(alpha, s[j].z, ki * u.z), fmaf(alpha, s[j].w, ki * u.w));
+            }
+        }
+    }
+}
+
 }  // namespace
 
 template <class Tin>
@@ -124,6 +227,12 @@ cudaError_t step(const Args &a, const Tin *q, const Tin *k, const Tin *v, const 
                  cudaStream_t st)
 {
     if (a.N == 0) return cudaSuccess;
+    const bool aligned = ((uintptr_t)a.state_out & 15u) == 0 && ((uintptr_t)a.state_in & 15u) == 0;
+    if (a.dv % 4 == 0 && aligned) {
+        if (a.N > 0x7fffffff || a.H > 65535) return cudaErrorInvalidValue;
+        k_decode4<Tin><<<dim3((unsigned)a.N, a.H), kCols * kGroups, 0, st>>>(a, q, k, v, beta, o);
+        return cudaPeekAtLastError();
+    }
     const int nsl = (a.dv + kCols - 1) / kCols;
     const long long blocks = (long long)a.N * nsl;
     if (blocks > 0x7fffffffLL || a.H > 65535) return cudaErrorInvalidValue;

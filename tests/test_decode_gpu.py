@@ -46,6 +46,7 @@ def _oracle(q, k, v, beta, g, S0, scale=1.0):
     (3, 2, 64, 96, "f32", True, False),      # d_v not a multiple of the 32-column slice
     (2, 4, 128, 128, "bf16", True, True),    # no initial state
     (1, 1, 16, 20, "f32", True, False),
+    (2, 2, 32, 30, "f32", True, False),      # d_v % 4 != 0: the 4-byte-access kernel
 ])
 def test_one_step_matches_oracle(N, H, dk, dv, dtype, gated, zero_state):
     import chunkwise_delta_rule_02_gb300 as gdn
