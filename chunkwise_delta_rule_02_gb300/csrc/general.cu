@@ -17,12 +17,16 @@
 //   bchunk: per chunk, parallel       every input gradient of the chunk.
 // (P = lower(Q K^T o D) with the diagonal kept; D_ri = exp(gamma_r - gamma_i).)
 //
-// Every matrix product is a register-tiled block product (rgemm): each thread
+// Every matrix product is a register-tiled block product (rgemm) -- in the
+// backward with bf16 inputs, a warp-level tensor-core product (mgemm) instead,
+// except for the two small products of the solve's adjoint: each thread
 // owns TM consecutive rows and TN columns spread across the threads, so an
 // operand that is contiguous along the output columns is read coalesced (from
 // L1) or without bank conflicts (from shared memory).  Operands that would be
 // read across rows instead are first staged in shared memory with an odd row
 // stride.
+#include <type_traits>
+
 #include "common.cuh"
 #include "general.h"
 
@@ -82,6 +86,94 @@ __device__ __forceinline__ void rgemm(int M, int N, int K, FA A, FB B, FS St)
             for (int j = 0; j < TN; ++j)
                 if (m0 + i < M && tn + j * nt < N) St(m0 + i, tn + j * nt, acc[i][j]);
     }
+}
+
+// bf16 pair for a tensor-core fragment: lo in the low half
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// D += A B for one 16 x 8 x 16 tile: A row-major, B column-major, bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// The block product of rgemm on the tensor cores (warp-level mma, bf16 operands
+// rounded from the accessors' fp32 values, fp32 accumulation): each warp owns
+// 16 x 8 NT output tiles in turn.  Used by the backward when the inputs are bf16,
+// where the 2e-2 tolerance leaves room for bf16 operands.
+template <int NT, class FA, class FB, class FS>
+__device__ __forceinline__ void mgemm(int M, int N, int K, FA A, FB B, FS St)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int mt = (M + 15) / 16, ntl = (N + 8 * NT - 1) / (8 * NT);
+    for (int tile = warp; tile < mt * ntl; tile += nw) {
+        const int m0 = (tile / ntl) * 16, n0 = (tile - (tile / ntl) * ntl) * 8 * NT;
+        float acc[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const bool mn_in = m0 + 16 <= M && n0 + 8 * NT <= N;
+        for (int k0 = 0; k0 < K; k0 += 16) {
+            uint32_t a[4];
+            uint32_t b[NT][2];
+            if (mn_in && k0 + 16 <= K) {
+                const int ka = k0 + 2 * t;
+                a[0] = bf16x2(A(m0 + g, ka), A(m0 + g, ka + 1));
+                a[1] = bf16x2(A(m0 + g + 8, ka), A(m0 + g + 8, ka + 1));
+                a[2] = bf16x2(A(m0 + g, ka + 8), A(m0 + g, ka + 9));
+                a[3] = bf16x2(A(m0 + g + 8, ka + 8), A(m0 + g + 8, ka + 9));
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int n = n0 + 8 * j + g;
+                    b[j][0] = bf16x2(B(ka, n), B(ka + 1, n));
+                    b[j][1] = bf16x2(B(ka + 8, n), B(ka + 9, n));
+                }
+            } else {
+                auto ga = [&](int m, int k) { return (m < M && k < K) ? A(m, k) : 0.f; };
+                auto gb = [&](int k, int n) { return (k < K && n < N) ? B(k, n) : 0.f; };
+                const int ka = k0 + 2 * t;
+                a[0] = bf16x2(ga(m0 + g, ka), ga(m0 + g, ka + 1));
+                a[1] = bf16x2(ga(m0 + g + 8, ka), ga(m0 + g + 8, ka + 1));
+                a[2] = bf16x2(ga(m0 + g, ka + 8), ga(m0 + g, ka + 9));
+                a[3] = bf16x2(ga(m0 + g + 8, ka + 8), ga(m0 + g + 8, ka + 9));
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int n = n0 + 8 * j + g;
+                    b[j][0] = bf16x2(gb(ka, n), gb(ka + 1, n));
+                    b[j][1] = bf16x2(gb(ka + 8, n), gb(ka + 9, n));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma_bf16_16816(acc[j], a, b[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int m = m0 + g, n = n0 + 8 * j + 2 * t;
+            if (m < M && n < N) St(m, n, acc[j][0]);
+            if (m < M && n + 1 < N) St(m, n + 1, acc[j][1]);
+            if (m + 8 < M && n < N) St(m + 8, n, acc[j][2]);
+            if (m + 8 < M && n + 1 < N) St(m + 8, n + 1, acc[j][3]);
+        }
+    }
+}
+
+// Block product for the backward: tensor cores for bf16 inputs, fp32 otherwise.
+template <class Tin, int TM, int TN, class FA, class FB, class FS>
+__device__ __forceinline__ void bgemm(int M, int N, int K, FA A, FB B, FS St)
+{
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value)
+        mgemm<4>(M, N, K, A, B, St);
+    else
+        rgemm<TM, TN>(M, N, K, A, B, St);
 }
 
 // Column-parallel forward substitution: X = (I + A)^-1 diag(d), A strictly lower
@@ -330,7 +422,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
         __syncthreads();
         // dUnew(i, n) = sum_r P(r, i) dO(r, n) + exp(gC - gam_i) sum_kk K(i, kk) dS(kk, n)
         float *dUg = w.dUn + slot * C * dv;
-        rgemm<4, 4>(len, nb, len + dk,
+        bgemm<Tin, 4, 4>(len, nb, len + dk,
                     [&](int i, int x) { return x < len ? Pg[x * C + i] : sE[i] * Kn[i * dk + (x - len)]; },
                     [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdS[(x - len) * BV + n]; },
                     [&](int i, int n, float u) {
@@ -340,7 +432,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
         __syncthreads();
         // dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
         const float GC = expf(gC);
-        rgemm<8, 4>(dk, nb, 2 * len,
+        bgemm<Tin, 8, 4>(dk, nb, 2 * len,
                     [&](int kk, int x) { return x < len ? sG[x] * Qn[x * dk + kk] : -W[(x - len) * dk + kk]; },
                     [&](int x, int n) { return x < len ? sdO[x * BV + n] : sdU[(x - len) * BV + n]; },
                     [&](int kk, int n, float acc) { sdS[kk * BV + n] = fmaf(GC, sdS[kk * BV + n], acc); });
@@ -405,13 +497,13 @@ __global__ void __launch_bounds__(256) k_bbig(Geo g, const Tin *__restrict__ dO,
         sT[n * LK + kk] = Sin[idx];
     }
     __syncthreads();
-    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
+    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
                 [&](int n, int kk) { return sT[n * LK + kk]; },
                 [&](int r, int kk, float y) {
                     dQ[r * dk + kk] = sG[r] * y;
                     atomicAdd(&sqt[r], Qn[r * dk + kk] * y);
                 });
-    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return -dUn[r * dv + n]; },
+    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return -dUn[r * dv + n]; },
                 [&](int n, int kk) { return sT[n * LK + kk]; },
                 [&](int r, int kk, float s) { dW[r * dk + kk] = s; });
     __syncthreads();
@@ -420,7 +512,7 @@ __global__ void __launch_bounds__(256) k_bbig(Geo g, const Tin *__restrict__ dO,
         sT[n * LK + kk] = dSo[idx];
     }
     __syncthreads();
-    rgemm<4, 8>(len, dk, dv, [&](int r, int n) { return Un[r * dv + n]; },
+    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return Un[r * dv + n]; },
                 [&](int n, int kk) { return sT[n * LK + kk]; },
                 [&](int r, int kk, float s) {
                     dK[r * dk + kk] = sE[r] * s;
@@ -506,10 +598,10 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
     __syncthreads();
     auto Dm = [&](int r, int i) { return i <= r ? expf(sg[r] - sg[i]) : 0.f; };
     // K K^T and the first half of dT = dW (diag(Gamma) K)^T + dUnew V^T
-    rgemm<4, 4>(len, len, dk, [&](int r, int kk) { return sS[r * LS + kk]; },
+    bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return sS[r * LS + kk]; },
                 [&](int kk, int i) { return sS[i * LS + kk]; },
                 [&](int r, int i, float s) { sKK[r * LC + i] = s; });
-    rgemm<4, 4>(len, len, dk, [&](int r, int kk) { return dW[r * dk + kk]; },
+    bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return dW[r * dk + kk]; },
                 [&](int kk, int i) { return sG[i] * sS[i * LS + kk]; },
                 [&](int r, int i, float s) { sdT[r * LC + i] = s; });
     __syncthreads();
@@ -519,7 +611,7 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
     }
     __syncthreads();
     // dP = lower(scale dO Unew^T)
-    rgemm<4, 4>(len, len, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
+    bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
                 [&](int n, int i) { return sS[i * LS + n]; },
                 [&](int r, int i, float s) {
                     sdP[r * LC + i] = (i <= r) ? s : 0.f;
@@ -537,25 +629,25 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
     }
     __syncthreads();
     // dT += dUnew V^T;  dQ += (dP o D) K;  dK += (dP o D)^T Q
-    rgemm<4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
+    bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
                 [&](int n, int i) { return sS[i * LS + n]; },
                 [&](int r, int i, float s) { sdT[r * LC + i] += s; });
-    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sDP[r * LC + i]; },
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[r * LC + i]; },
                 [&](int i, int kk) { return Kn[i * dk + kk]; },
                 [&](int r, int kk, float s) { dQ[r * dk + kk] += s; });
-    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sDP[i * LC + r]; },
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[i * LC + r]; },
                 [&](int i, int kk) { return Qn[i * dk + kk]; },
                 [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
     __syncthreads();
     // dGK = T^T dW (T = Linv diag(beta)); dK += Gamma dGK; d gamma += Gamma <dGK, K>;  dV = T^T dUnew
-    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sLi[i * LC + r]; },
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sLi[i * LC + r]; },
                 [&](int i, int kk) { return dW[i * dk + kk]; },
                 [&](int r, int kk, float s) {
                     const float a = sb[r] * s;
                     dK[r * dk + kk] += sG[r] * a;
                     atomicAdd(&sk2[r], a * Kn[r * dk + kk]);
                 });
-    rgemm<4, 8>(len, dv, len, [&](int r, int i) { return sLi[i * LC + r]; },
+    bgemm<Tin, 4, 8>(len, dv, len, [&](int r, int i) { return sLi[i * LC + r]; },
                 [&](int i, int n) { return dUn[i * dv + n]; },
                 [&](int r, int n, float s) { st_out(dvout + (row + r) * dv + n, sb[r] * s); });
     // d beta through T = Linv diag(beta)
@@ -604,7 +696,7 @@ __global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q
     }
     __syncthreads();
     // dK += (dKK + dKK^T) K
-    rgemm<4, 8>(len, dk, len, [&](int r, int i) { return sY[r * LC + i] + sY[i * LC + r]; },
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sY[r * LC + i] + sY[i * LC + r]; },
                 [&](int i, int kk) { return Kn[i * dk + kk]; },
                 [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
     __syncthreads();
