@@ -18,8 +18,9 @@
 // (P = lower(Q K^T o D) with the diagonal kept; D_ri = exp(gamma_r - gamma_i).)
 //
 // Every matrix product is a register-tiled block product (rgemm) -- in the
-// backward with bf16 inputs, a warp-level tensor-core product (mgemm) instead,
-// except for the two small products of the solve's adjoint: each thread
+// kernels with bf16 inputs, a warp-level tensor-core product (mgemm) instead,
+// except for the two small products of the solve's adjoint and the output
+// kernel: each thread
 // owns TM consecutive rows and TN columns spread across the threads, so an
 // operand that is contiguous along the output columns is read coalesced (from
 // L1) or without bank conflicts (from shared memory).  Operands that would be
@@ -268,13 +269,13 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
     }
     __syncthreads();
     // A = strict_lower(diag(beta) (K K^T o D)),  P = lower(Q K^T o D)
-    rgemm<4, 4>(len, len, dk, [&](int m, int kk) { return sK[m * LK + kk]; },
+    bgemm<Tin, 4, 4>(len, len, dk, [&](int m, int kk) { return sK[m * LK + kk]; },
                 [&](int kk, int n) { return sK[n * LK + kk]; },
                 [&](int m, int n, float s) {
                     sA[m * LC + n] = (n < m) ? sb[m] * s * expf(sg[m] - sg[n]) : 0.f;
                 });
     float *Pg = w.P + slot * C * C;
-    rgemm<4, 4>(len, len, dk, [&](int m, int kk) { return sQ[m * LK + kk]; },
+    bgemm<Tin, 4, 4>(len, len, dk, [&](int m, int kk) { return sQ[m * LK + kk]; },
                 [&](int kk, int n) { return sK[n * LK + kk]; },
                 [&](int m, int n, float s) { Pg[m * C + n] = (n <= m) ? s * expf(sg[m] - sg[n]) : 0.f; });
     __syncthreads();
@@ -285,15 +286,16 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
     }
     __syncthreads();
     // W = T diag(Gamma) K,  U = T V
-    rgemm<4, 8>(len, dk, len, [&](int m, int i) { return sT[m * LC + i]; },
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int m, int i) { return sT[m * LC + i]; },
                 [&](int i, int n) { return sG[i] * sK[i * LK + n]; },
                 [&](int m, int n, float s) { w.W[slot * C * dk + m * dk + n] = s; });
-    rgemm<4, 8>(len, dv, len, [&](int m, int i) { return sT[m * LC + i]; },
+    bgemm<Tin, 4, 8>(len, dv, len, [&](int m, int i) { return sT[m * LC + i]; },
                 [&](int i, int n) { return sQ[i * dv + n]; },
                 [&](int m, int n, float s) { w.U[slot * C * dv + m * dv + n] = s; });
 }
 
 // ----------------------------------------------------------------------------- scan
+template <class Tin>
 __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h0,
                                               float *__restrict__ hT, Ws w, int BV)
 {
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
         const float *W = w.W + slot * C * dk;
         const float *U = w.U + slot * C * dv;
         float *Un = w.Unew + slot * C * dv;
-        rgemm<4, 4>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
+        bgemm<Tin, 4, 4>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
                     [&](int kk, int n) { return sS[kk * BV + n]; },
                     [&](int r, int n, float acc) {
                         float u = U[r * dv + n0 + n] - acc;
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
         __syncthreads();
         const float *Kn = w.Kn + slot * C * dk;
         const float GC = expf(gC);
-        rgemm<8, 4>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
+        bgemm<Tin, 8, 4>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
                     [&](int r, int n) { return sU[r * BV + n]; },
                     [&](int kk, int n, float acc) { sS[kk * BV + n] = fmaf(GC, sS[kk * BV + n], acc); });
         __syncthreads();
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
 // Kt = Unew dS_out^T (dK = diag(exp(gamma_C - gamma)) Kt); plus the row sums
 // <Q_r, Y_r>, <Kt_r, K_r> and <dS_out, S_in> that the gate gradient needs.
 template <class Tin>
-__global__ void __launch_bounds__(256) k_bbig(Geo g, const Tin *__restrict__ dO, Ws w)
+__global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO, Ws w)
 {
     const int j = blockIdx.x, h = blockIdx.y;
     int b, t0, len, seq, local;
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(256) k_bbig(Geo g, const Tin *__restrict__ dO,
 
 // ----------------------------------------------------------------------------- backward per chunk
 template <class Tin>
-__global__ void __launch_bounds__(256) k_bchunk(Geo g, const Tin *__restrict__ q,
+__global__ void __launch_bounds__(512) k_bchunk(Geo g, const Tin *__restrict__ q,
                                                 const Tin *__restrict__ k,
                                                 const Tin *__restrict__ v,
                                                 const Tin *__restrict__ beta,
@@ -777,9 +779,9 @@ static cudaError_t forward_states(const Geo &g, const Tin *q, const Tin *k, cons
     if (g.NC > 0) k_prep<Tin><<<dim3(g.NC, g.H), 256, smem_prep(g), st>>>(g, q, k, v, beta, gate, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     const int BV = slice_width(g);
-    if ((e = set_smem(k_scan, smem_scan(g, BV))) != cudaSuccess) return e;
+    if ((e = set_smem(k_scan<Tin>, smem_scan(g, BV))) != cudaSuccess) return e;
     if (g.N > 0)
-        k_scan<<<dim3(g.N, g.H, (g.dv + BV - 1) / BV), 256, smem_scan(g, BV), st>>>(g, h0, hT, w, BV);
+        k_scan<Tin><<<dim3(g.N, g.H, (g.dv + BV - 1) / BV), 256, smem_scan(g, BV), st>>>(g, h0, hT, w, BV);
     return cudaPeekAtLastError();
 }
 
@@ -810,11 +812,11 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
             g, dO, dhT, dh0, w, BV);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
-    if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 256, smem_bbig(g), st>>>(g, dO, w);
+    if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bchunk<Tin>, smem_bchunk(g))) != cudaSuccess) return e;
     if (g.NC > 0)
-        k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk(g), st>>>(g, q, k, v, beta, dO, dq, dk,
+        k_bchunk<Tin><<<dim3(g.NC, g.H), 512, smem_bchunk(g), st>>>(g, q, k, v, beta, dO, dq, dk,
                                                                      dv, dbeta, dg, w);
     return cudaPeekAtLastError();
 }
