@@ -10,7 +10,7 @@
 
 namespace gdn {
 
-constexpr int kMaxD = 128;       // largest head dim supported
+constexpr int kMaxD = 256;       // largest head dim supported (tcgen05 kernels: 128)
 constexpr int kMaxC = 64;        // largest chunk
 
 // Geometry of one call, passed by value to every kernel.

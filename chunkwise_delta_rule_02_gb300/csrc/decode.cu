@@ -10,7 +10,8 @@
 //     S'[i][n] = alpha S[i][n] + k_i u_n,
 //     o_n = scale (alpha sum_i S[i][n] q_i + u_n (k . q)),
 // so one pass reads the state once, keeps it in registers, and writes it once
-// (16-byte accesses, one CTA per (sequence, head), when d_v % 4 == 0; else
+// (16-byte accesses, one CTA per (sequence, head), when d_v % 4 == 0 and
+// d_k, d_v <= 128; else
 // 4-byte accesses, one CTA per 32-column slice):
 // the step moves the compulsory 2 d_k d_v fp32 state bytes per head and is
 // bound by HBM bandwidth.
@@ -24,7 +25,8 @@ namespace {
 
 constexpr int kCols = 32;            // d_v columns per CTA (one warp's width)
 constexpr int kGroups = 8;           // row groups: 256 threads
-constexpr int kRows = kMaxD / kGroups;
+constexpr int kRows = kMaxD / kGroups;   // rows per thread, 4-byte kernel
+constexpr int kRows4 = 128 / kGroups;    // rows per thread, 16-byte kernel (d_k <= 128)
 
 template <class Tin>
 __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *__restrict__ q,
@@ -175,10 +177,10 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     const float4 *Sin = a.state_in ? reinterpret_cast<const float4 *>(a.state_in + item * a.dk * a.dv) : nullptr;
     float4 *Sout = reinterpret_cast<float4 *>(a.state_out + item * a.dk * a.dv);
     const int dv4 = a.dv >> 2;
-    float4 s[kRows];
+    float4 s[kRows4];
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f), p = r;
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
+    for (int j = 0; j < kRows4; ++j) {
         const int i = rg + kGroups * j;
         s[j] = (live && i < a.dk && Sin) ? Sin[(size_t)i * dv4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < a.dk) {
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     if (live) {
         const float4 u = su[lane];
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) {
+        for (int j = 0; j < kRows4; ++j) {
             const int i = rg + kGroups * j;
             if (i < a.dk) {
                 const float ki = sk[i];
@@ -228,7 +230,7 @@ cudaError_t step(const Args &a, const Tin *q, const Tin *k, const Tin *v, const 
 {
     if (a.N == 0) return cudaSuccess;
     const bool aligned = ((uintptr_t)a.state_out & 15u) == 0 && ((uintptr_t)a.state_in & 15u) == 0;
-    if (a.dv % 4 == 0 && aligned) {
+    if (a.dv % 4 == 0 && a.dv <= 128 && a.dk <= 128 && aligned) {
         if (a.N > 0x7fffffff || a.H > 65535) return cudaErrorInvalidValue;
         k_decode4<Tin><<<dim3((unsigned)a.N, a.H), kCols * kGroups, 0, st>>>(a, q, k, v, beta, o);
         return cudaPeekAtLastError();

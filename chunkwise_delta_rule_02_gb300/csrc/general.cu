@@ -460,8 +460,8 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
     const int C = g.C, dk = g.dk, dv = g.dv, LK = dk + 1;
     extern __shared__ float sm[];
-    float *sT = sm;                 // [dv][LK] a state, transposed
-    float *sE = sT + dv * LK;       // [C]
+    float *sT = sm;                 // [<= 128][LK] d_v columns of a state, transposed
+    float *sE = sT + (dv < 128 ? dv : 128) * LK;   // [C]
     float *sG = sE + C;             // [C]
     float *sqt = sG + C;            // [C] <Q_r, Y_r>
     float *set = sqt + C;           // [C] <Kt_r, K_r>
@@ -494,32 +494,43 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
         p = warp_sum(p);
         if (lane == 0) atomicAdd(sred, p);
     }
-    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
-        int kk = idx / dv, n = idx - kk * dv;
-        sT[n * LK + kk] = Sin[idx];
+    // the states are staged transposed, at most 128 of their d_v columns at a time
+    const int NB = dv < 128 ? dv : 128;
+    for (int nb0 = 0; nb0 < dv; nb0 += NB) {
+        const int nbn = min(NB, dv - nb0);
+        const bool first = nb0 == 0;
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < dk * nbn; idx += blockDim.x) {
+            int kk = idx / nbn, n = idx - kk * nbn;
+            sT[n * LK + kk] = Sin[(size_t)kk * dv + nb0 + n];
+        }
+        __syncthreads();
+        bgemm<Tin, 4, 8>(len, dk, nbn, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + nb0 + n); },
+                         [&](int n, int kk) { return sT[n * LK + kk]; },
+                         [&](int r, int kk, float y) {
+                             dQ[r * dk + kk] = (first ? 0.f : dQ[r * dk + kk]) + sG[r] * y;
+                             atomicAdd(&sqt[r], Qn[r * dk + kk] * y);
+                         });
+        bgemm<Tin, 4, 8>(len, dk, nbn, [&](int r, int n) { return -dUn[r * dv + nb0 + n]; },
+                         [&](int n, int kk) { return sT[n * LK + kk]; },
+                         [&](int r, int kk, float s) { dW[r * dk + kk] = (first ? 0.f : dW[r * dk + kk]) + s; });
     }
-    __syncthreads();
-    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
-                [&](int n, int kk) { return sT[n * LK + kk]; },
-                [&](int r, int kk, float y) {
-                    dQ[r * dk + kk] = sG[r] * y;
-                    atomicAdd(&sqt[r], Qn[r * dk + kk] * y);
-                });
-    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return -dUn[r * dv + n]; },
-                [&](int n, int kk) { return sT[n * LK + kk]; },
-                [&](int r, int kk, float s) { dW[r * dk + kk] = s; });
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
-        int kk = idx / dv, n = idx - kk * dv;
-        sT[n * LK + kk] = dSo[idx];
+    for (int nb0 = 0; nb0 < dv; nb0 += NB) {
+        const int nbn = min(NB, dv - nb0);
+        const bool first = nb0 == 0;
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < dk * nbn; idx += blockDim.x) {
+            int kk = idx / nbn, n = idx - kk * nbn;
+            sT[n * LK + kk] = dSo[(size_t)kk * dv + nb0 + n];
+        }
+        __syncthreads();
+        bgemm<Tin, 4, 8>(len, dk, nbn, [&](int r, int n) { return Un[r * dv + nb0 + n]; },
+                         [&](int n, int kk) { return sT[n * LK + kk]; },
+                         [&](int r, int kk, float s) {
+                             dK[r * dk + kk] = (first ? 0.f : dK[r * dk + kk]) + sE[r] * s;
+                             atomicAdd(&set[r], s * Kn[r * dk + kk]);
+                         });
     }
-    __syncthreads();
-    bgemm<Tin, 4, 8>(len, dk, dv, [&](int r, int n) { return Un[r * dv + n]; },
-                [&](int n, int kk) { return sT[n * LK + kk]; },
-                [&](int r, int kk, float s) {
-                    dK[r * dk + kk] = sE[r] * s;
-                    atomicAdd(&set[r], s * Kn[r * dk + kk]);
-                });
     __syncthreads();
     float *aux = w.aux + slot * (2 * C + 4);
     for (int r = threadIdx.x; r < len; r += blockDim.x) {
@@ -753,7 +764,10 @@ static size_t smem_prep(const Geo &g)
 static size_t smem_scan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + g.C * BV + g.C); }
 static size_t smem_out(const Geo &g) { return sizeof(float) * g.C; }
 static size_t smem_bscan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + 2 * g.C * BV + 2 * g.C); }
-static size_t smem_bbig(const Geo &g) { return sizeof(float) * (g.dv * (g.dk + 1) + 4 * g.C + 4); }
+static size_t smem_bbig(const Geo &g)
+{
+    return sizeof(float) * ((g.dv < 128 ? g.dv : 128) * (g.dk + 1) + 4 * g.C + 4);
+}
 static size_t smem_bchunk(const Geo &g)
 {
     const size_t LC = g.C + 1, LS = (g.dk > g.dv ? g.dk : g.dv) + 1;

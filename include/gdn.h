@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
     DN_OK = 0,
     DN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad sizes or offsets */
-    DN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. dk > 128)     */
+    DN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. dk > 256)     */
     DN_ERR_WORKSPACE = 3,     /* ws == NULL or ws_bytes < dn_workspace_size     */
     DN_ERR_CUDA = 4,          /* a CUDA call or kernel launch failed            */
     DN_ERR_TIMEOUT = 5        /* a bounded device wait ran out (see above)      */
@@ -70,7 +70,7 @@ typedef enum { DN_F32 = 0, DN_BF16 = 1 } dn_dtype;
 
 typedef struct {
     int32_t B, H, T;              /* batch rows, heads, tokens per row (packed: B = 1) */
-    int32_t dk, dv;               /* head dims, 1..128                                  */
+    int32_t dk, dv;               /* head dims, 1..256 (tcgen05 kernels: 128)           */
     int32_t chunk;                /* C: 16, 32 or 64 (64 is the tuned size)             */
     int32_t dtype;                /* dn_dtype                                           */
     const int32_t *cu_seqlens;    /* device, [num_seqs + 1], or NULL for fixed length   */
@@ -120,7 +120,7 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
  * Gated DeltaNet page's reply on decoding with a fixed-size state):
  *   S' = alpha (I - beta k k^T) S + beta k v^T,   o = scale S'^T q,
  * q, k normalised in the kernel when shape->qk_l2norm.  Shape: B = number of
- * sequences, H heads, T must be 1, dk, dv <= 128, cu_seqlens NULL; chunk is
+ * sequences, H heads, T must be 1, dk, dv <= 256, cu_seqlens NULL; chunk is
  * ignored (any accepted value).  Layouts (dtype = shape->dtype unless noted):
  *   q, k [B,H,dk], v [B,H,dv], beta [B,H]; g [B,H] float32 log-gate or NULL
  *   (alpha = 1); state_in [B,H,dk,dv] float32 or NULL (zero state);
@@ -129,7 +129,7 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
  * Needs no workspace, allocates nothing, does not synchronise.  Errors:
  * DN_ERR_INVALID_ARG for a bad shape, T != 1, packed input, a missing buffer or
  * a pointer that is not 4-byte aligned; DN_ERR_UNSUPPORTED for head dims above
- * 128; DN_ERR_CUDA if the launch fails. */
+ * 256; DN_ERR_CUDA if the launch fails. */
 dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, const void *v,
                           const void *beta, const float *g, const float *state_in,
                           float *state_out, void *o, void *stream);

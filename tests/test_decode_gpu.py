@@ -47,6 +47,7 @@ def _oracle(q, k, v, beta, g, S0, scale=1.0):
     (2, 4, 128, 128, "bf16", True, True),    # no initial state
     (1, 1, 16, 20, "f32", True, False),
     (2, 2, 32, 30, "f32", True, False),      # d_v % 4 != 0: the 4-byte-access kernel
+    (2, 2, 256, 256, "bf16", True, False),   # head dim 256: the 4-byte-access kernel
 ])
 def test_one_step_matches_oracle(N, H, dk, dv, dtype, gated, zero_state):
     import chunkwise_delta_rule_02_gb300 as gdn

@@ -57,7 +57,7 @@ def test_workspace_size_and_validation(gdn):
     n_b = gdn.dn_workspace_size(s, True)
     assert 0 < n_f < n_b
     assert n_f % 256 == 0
-    bad = [_shape(gdn, B=0), _shape(gdn, d=129), _shape(gdn, chunk=48), _shape(gdn, dtype=7),
+    bad = [_shape(gdn, B=0), _shape(gdn, d=257), _shape(gdn, chunk=48), _shape(gdn, dtype=7),
            _shape(gdn, H=0), _shape(gdn, T=-1)]
     for b in bad:
         assert gdn.dn_workspace_size(b, False) == 0
@@ -94,7 +94,7 @@ def test_status_codes_without_device_work(gdn):
     assert L.gdn_chunk_fwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, None, 0, None) == gdn.DN_ERR_WORKSPACE
     assert L.gdn_chunk_fwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, 16, 64, None) == gdn.DN_ERR_WORKSPACE
     # unsupported head dim
-    s2 = _shape(gdn, d=256)
+    s2 = _shape(gdn, d=512)
     assert L.dn_chunk_fwd(ctypes.byref(s2), 16, 16, 16, 16, None, 16, None, 16, 1 << 40, None) == gdn.DN_ERR_UNSUPPORTED
     # backward: dg without g
     assert L.gdn_chunk_bwd(ctypes.byref(s), 16, 16, 16, 16, None, None, 16, None, 16, 16, 16, 16,

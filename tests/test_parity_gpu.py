@@ -213,6 +213,31 @@ def test_backward_small(dtype, T, d):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,dk,dv,chunk", [(130, 256, 256, 64), (97, 256, 192, 32), (64, 160, 256, 16)])
+def test_head_dim_256_forward_and_backward(dtype, T, dk, dv, chunk):
+    """Head dims up to 256 (the Gated DeltaNet head size) on the general kernels,
+    including d_k != d_v, ragged chunks and the smaller chunk sizes."""
+    from chunkwise_delta_rule_02_gb300 import workloads
+    import oracle as orc
+    w = workloads.Workload("d256", 1, 2, T, dk, dtype, True, True, seed=T + dk + dv, chunk=chunk,
+                           backward=True)
+    x = workloads.generate(w)
+    if dv != dk:   # the generator draws square heads: cut v, h0, do, dhT to d_v columns
+        for key in ("v", "do"):
+            x[key] = x[key][..., :dv].contiguous()
+        for key in ("h0", "dhT"):
+            x[key] = x[key][..., :dv].contiguous()
+    o, hT = _run_fwd(x, chunk=chunk)
+    ro, rh = oracle_fwd(x)
+    _assert_close("o", o, ro, TOL[dtype])
+    _assert_close("hT", hT, rh, TOL[dtype])
+    got = _run_bwd(x, chunk=chunk)
+    ref = oracle_bwd(x)
+    for n in GRADS:
+        _assert_close(n, got[n], ref[n], TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_backward_varlen_small(dtype):
     from chunkwise_delta_rule_02_gb300 import workloads
     w = workloads.Workload("bwv", 1, 2, 0, 32, dtype, True, True, seed=21, varlen_total=1,
