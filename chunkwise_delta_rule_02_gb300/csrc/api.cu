@@ -60,7 +60,7 @@ int device_sms()
 
 struct Layout {
     size_t status, cstart, fast;
-    size_t Kn, Qn, W, U, Unew, gam, Sin, dSo, dUn, dQ, dK, dW, P, aux;
+    size_t Kn, Qn, W, U, Unew, gam, Sin, dSo, dUn, dQ, dK, dW, P, aux, M3;
     size_t total;
 };
 
@@ -93,7 +93,8 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast,
     L.Sin = take(slots * dk * dv);
     L.P = take(slots * C * C);
     if (for_backward) {
-        L.aux = take(slots * (2 * C + 4));
+        L.aux = take(slots * (4 * C + 4));
+        L.M3 = take(slots * 3 * C * C);
         L.dSo = take(slots * dk * dv);
         L.dUn = take(slots * C * dv);
         L.dQ = take(slots * C * dk);
@@ -112,7 +113,7 @@ gen::Ws general_ws(const Layout &L, char *base)
     w.Kn = F(L.Kn); w.Qn = F(L.Qn); w.W = F(L.W); w.U = F(L.U); w.Unew = F(L.Unew);
     w.gam = F(L.gam); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
     w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
-    w.P = F(L.P); w.aux = F(L.aux);
+    w.P = F(L.P); w.aux = F(L.aux); w.M3 = F(L.M3);
     return w;
 }
 
@@ -244,7 +245,7 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
     int path, n;
     if (for_backward) {
         path = DN_PATH_GENERAL;
-        n = 5 + offsets;                    // k_prep, k_scan, k_bscan, k_bbig, k_bchunk
+        n = 6 + offsets;                    // k_prep, k_scan, k_bscan, k_bbig, k_bchunk, k_bgrad
     } else if (!fast_ok(shape, g, 0)) {
         path = DN_PATH_GENERAL;
         n = 3 + offsets;                    // k_prep, k_scan, k_out

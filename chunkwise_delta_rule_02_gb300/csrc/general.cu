@@ -14,7 +14,8 @@
 //   bscan : per (seq, head, dv-slice), last chunk first:
 //           dUnew = P^T dO + Kt dS;  dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
 //   bbig  : per chunk, parallel       the three products with the d_k x d_v states
-//   bchunk: per chunk, parallel       every input gradient of the chunk.
+//   bchunk: per chunk, parallel       the C x C part: solve adjoint, gate / beta terms
+//   bgrad : per chunk, parallel       the C x d part: dq, dk, dv, dg, the norm chain rule.
 // (P = lower(Q K^T o D) with the diagonal kept; D_ri = exp(gamma_r - gamma_i).)
 //
 // Every matrix product is a register-tiled block product (rgemm) -- in the
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
                          });
     }
     __syncthreads();
-    float *aux = w.aux + slot * (2 * C + 4);
+    float *aux = w.aux + slot * (4 * C + 4);
     for (int r = threadIdx.x; r < len; r += blockDim.x) {
         aux[r] = sqt[r];
         aux[C + r] = set[r];
@@ -541,17 +542,19 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
 }
 
 // ----------------------------------------------------------------------------- backward per chunk
+// Two kernels per chunk.  k_bchunk: K K^T, dP, the solve (I + A)^-1 and its
+// adjoint, dT, and the gate / beta terms that need the C x C matrices; it hands
+// dP o D, (I + A)^-1 and dKK to k_bgrad through the workspace, together with its
+// partial d gamma and d beta.  k_bgrad: the C x d products into dq, dk, dv, the
+// gate's reverse cumsum and the normalisation chain rule.  The split keeps each
+// kernel's shared memory small enough for two (k_bchunk, bf16) or three (k_bgrad)
+// 256-thread CTAs per SM.
 template <class Tin>
-__global__ void __launch_bounds__(512) k_bchunk(Geo g, const Tin *__restrict__ q,
-                                                const Tin *__restrict__ k,
-                                                const Tin *__restrict__ v,
+__global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict__ v,
                                                 const Tin *__restrict__ beta,
-                                                const Tin *__restrict__ dO,
-                                                Tin *__restrict__ dq, Tin *__restrict__ dkout,
-                                                Tin *__restrict__ dvout,
-                                                Tin *__restrict__ dbeta,
-                                                float *__restrict__ dg, Ws w)
+                                                const Tin *__restrict__ dO, Ws w)
 {
+    constexpr bool kStage = !std::is_same<Tin, __nv_bfloat16>::value;   // fp32: stage row operands
     const int j = blockIdx.x, h = blockIdx.y;
     int b, t0, len, seq, local;
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
@@ -559,110 +562,89 @@ __global__ void __launch_bounds__(512) k_bchunk(Geo g, const Tin *__restrict__ q
     const int LS = (dk > dv ? dk : dv) + 1;
     extern __shared__ float sm[];
     float *sKK = sm;                // K K^T
-    float *sP = sKK + C * LC;       // lower(Q K^T o D)
-    float *sdP = sP + C * LC;       // lower(dO Unew^T)
+    float *sdP = sKK + C * LC;      // lower(dO Unew^T)
     float *sDP = sdP + C * LC;      // dP o D, later X = Linv^T dT diag(beta)
     float *sLi = sDP + C * LC;      // (I + A)^-1
     float *sdT = sLi + C * LC;      // dT
     float *sY = sdT + C * LC;       // A, then dA, then dKK
-    float *sS = sY + C * LC;        // [C][LS] staged rows (K, Unew, V)
-    float *sb = sS + C * LS;        // beta
+    float *sb = sY + C * LC;        // beta
     float *sg = sb + C;             // gamma
     float *sG = sg + C;             // exp(gamma)
-    float *sE = sG + C;             // exp(gamma_C - gamma)
-    float *sdg = sE + C;            // d gamma
-    float *sdb = sdg + C;           // d beta
-    float *se = sdb + C;            // e_r (K~ gate term)
-    float *sk2 = se + C;            // <dGK_r, K_r>
+    float *sdg = sG + C;            // d gamma (partial)
+    float *sdb = sdg + C;           // d beta (partial)
+    float *sS = sdb + C;            // fp32 only: [C][LS] staged rows (K, Unew, V)
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
-    const float *Qn = w.Qn + slot * C * dk;
     const float *Kn = w.Kn + slot * C * dk;
     const float *Un = w.Unew + slot * C * dv;
     const float *dUn = w.dUn + slot * C * dv;
     const float *Pg = w.P + slot * C * C;
-    const float *aux = w.aux + slot * (2 * C + 4);
-    float *dQ = w.dQ + slot * C * dk;
-    float *dK = w.dK + slot * C * dk;
+    float *aux = w.aux + slot * (4 * C + 4);
+    float *M3 = w.M3 + slot * 3 * C * C;   // dP o D | (I + A)^-1 | dKK
     const float *dW = w.dW + slot * C * dk;
     const float *gam = w.gam + slot * C;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const float gC = gam[len - 1];
     const float sc = g.scale;
 
     for (int r = threadIdx.x; r < len; r += blockDim.x) {
         sb[r] = ld_in(beta + row + r);
         sg[r] = gam[r];
         sG[r] = expf(gam[r]);
-        sE[r] = expf(gC - gam[r]);
         sdg[r] = sG[r] * aux[r];      // q-term of d gamma
-        se[r] = sE[r] * aux[C + r];   // K~ gate term
         sdb[r] = 0.f;
-        sk2[r] = 0.f;
     }
-    for (int idx = threadIdx.x; idx < len * dk; idx += blockDim.x) {
-        int r = idx / dk, c = idx - r * dk;
-        sS[r * LS + c] = Kn[idx];
-    }
-    for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
-        int r = idx / len, i = idx - r * len;
-        sP[r * LC + i] = Pg[r * C + i];
+    if (kStage) {
+        for (int idx = threadIdx.x; idx < len * dk; idx += blockDim.x) {
+            int r = idx / dk, c = idx - r * dk;
+            sS[r * LS + c] = Kn[idx];
+        }
     }
     __syncthreads();
     auto Dm = [&](int r, int i) { return i <= r ? expf(sg[r] - sg[i]) : 0.f; };
+    auto Kt = [&](int kk, int i) { return kStage ? sS[i * LS + kk] : Kn[i * dk + kk]; };
     // K K^T and the first half of dT = dW (diag(Gamma) K)^T + dUnew V^T
-    bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return sS[r * LS + kk]; },
-                [&](int kk, int i) { return sS[i * LS + kk]; },
-                [&](int r, int i, float s) { sKK[r * LC + i] = s; });
+    bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return Kn[r * dk + kk]; }, Kt,
+                     [&](int r, int i, float s) { sKK[r * LC + i] = s; });
     bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return dW[r * dk + kk]; },
-                [&](int kk, int i) { return sG[i] * sS[i * LS + kk]; },
-                [&](int r, int i, float s) { sdT[r * LC + i] = s; });
+                     [&](int kk, int i) { return sG[i] * Kt(kk, i); },
+                     [&](int r, int i, float s) { sdT[r * LC + i] = s; });
     __syncthreads();
-    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
-        int r = idx / dv, c = idx - r * dv;
-        sS[r * LS + c] = Un[idx];
+    if (kStage) {
+        for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
+            int r = idx / dv, c = idx - r * dv;
+            sS[r * LS + c] = Un[idx];
+        }
+        __syncthreads();
     }
-    __syncthreads();
     // dP = lower(scale dO Unew^T)
     bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return sc * ld_in(dO + (row + r) * dv + n); },
-                [&](int n, int i) { return sS[i * LS + n]; },
-                [&](int r, int i, float s) {
-                    sdP[r * LC + i] = (i <= r) ? s : 0.f;
-                    sDP[r * LC + i] = (i <= r) ? s * expf(sg[r] - sg[i]) : 0.f;
-                });
+                     [&](int n, int i) { return kStage ? sS[i * LS + n] : Un[i * dv + n]; },
+                     [&](int r, int i, float s) {
+                         sdP[r * LC + i] = (i <= r) ? s : 0.f;
+                         sDP[r * LC + i] = (i <= r) ? s * expf(sg[r] - sg[i]) : 0.f;
+                     });
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
         sY[r * LC + i] = (i < r) ? sb[r] * sKK[r * LC + i] * expf(sg[r] - sg[i]) : 0.f;
     }
     __syncthreads();
     unit_lower_solve(sY, sLi, nullptr, len, LC);
-    for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
-        int r = idx / dv, c = idx - r * dv;
-        sS[r * LS + c] = ld_in(v + (row + r) * dv + c);
+    if (kStage) {
+        for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
+            int r = idx / dv, c = idx - r * dv;
+            sS[r * LS + c] = ld_in(v + (row + r) * dv + c);
+        }
+    }
+    for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
+        int r = idx / len, i = idx - r * len;
+        M3[r * C + i] = sDP[r * LC + i];
     }
     __syncthreads();
-    // dT += dUnew V^T;  dQ += (dP o D) K;  dK += (dP o D)^T Q
+    // dT += dUnew V^T
     bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
-                [&](int n, int i) { return sS[i * LS + n]; },
-                [&](int r, int i, float s) { sdT[r * LC + i] += s; });
-    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[r * LC + i]; },
-                [&](int i, int kk) { return Kn[i * dk + kk]; },
-                [&](int r, int kk, float s) { dQ[r * dk + kk] += s; });
-    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[i * LC + r]; },
-                [&](int i, int kk) { return Qn[i * dk + kk]; },
-                [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
+                     [&](int n, int i) { return kStage ? sS[i * LS + n] : ld_in(v + (row + i) * dv + n); },
+                     [&](int r, int i, float s) { sdT[r * LC + i] += s; });
     __syncthreads();
-    // dGK = T^T dW (T = Linv diag(beta)); dK += Gamma dGK; d gamma += Gamma <dGK, K>;  dV = T^T dUnew
-    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sLi[i * LC + r]; },
-                [&](int i, int kk) { return dW[i * dk + kk]; },
-                [&](int r, int kk, float s) {
-                    const float a = sb[r] * s;
-                    dK[r * dk + kk] += sG[r] * a;
-                    atomicAdd(&sk2[r], a * Kn[r * dk + kk]);
-                });
-    bgemm<Tin, 4, 8>(len, dv, len, [&](int r, int i) { return sLi[i * LC + r]; },
-                [&](int i, int n) { return dUn[i * dv + n]; },
-                [&](int r, int n, float s) { st_out(dvout + (row + r) * dv + n, sb[r] * s); });
     // d beta through T = Linv diag(beta)
     for (int i = threadIdx.x; i < len; i += blockDim.x) {
         float a = 0.f;
@@ -685,38 +667,116 @@ __global__ void __launch_bounds__(512) k_bchunk(Geo g, const Tin *__restrict__ q
         for (int i = lane; i < len; i += 32) {
             const float dA = sY[r * LC + i], Dri = Dm(r, i);
             db = fmaf(dA * sKK[r * LC + i], Dri, db);
-            rs += dA * sb[r] * sKK[r * LC + i] * Dri + (i <= r ? sdP[r * LC + i] * sP[r * LC + i] : 0.f);
+            rs += dA * sb[r] * sKK[r * LC + i] * Dri + (i <= r ? sdP[r * LC + i] * Pg[r * C + i] : 0.f);
         }
         db = warp_sum(db);
         rs = warp_sum(rs);
         if (lane == 0) {
             sdb[r] += db;
-            sdg[r] += rs + sG[r] * sk2[r];
+            sdg[r] += rs;
         }
     }
     for (int i = warp; i < len; i += nw) {
         float cs = 0.f;
         for (int r = lane; r < len; r += 32)
             cs += sY[r * LC + i] * sb[r] * sKK[r * LC + i] * Dm(r, i) +
-                  (i <= r ? sdP[r * LC + i] * sP[r * LC + i] : 0.f);
+                  (i <= r ? sdP[r * LC + i] * Pg[r * C + i] : 0.f);
         cs = warp_sum(cs);
         if (lane == 0) atomicAdd(&sdg[i], -cs);
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
-        sY[r * LC + i] = sY[r * LC + i] * sb[r] * Dm(r, i);
+        M3[C * C + r * C + i] = sLi[r * LC + i];
+        M3[2 * C * C + r * C + i] = sY[r * LC + i] * sb[r] * Dm(r, i);
     }
+    for (int r = threadIdx.x; r < len; r += blockDim.x) {
+        aux[2 * C + 4 + r] = sdg[r];
+        aux[3 * C + 4 + r] = sdb[r];
+    }
+}
+
+template <class Tin>
+__global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__ q,
+                                               const Tin *__restrict__ k,
+                                               Tin *__restrict__ dq, Tin *__restrict__ dkout,
+                                               Tin *__restrict__ dvout,
+                                               Tin *__restrict__ dbeta,
+                                               float *__restrict__ dg,
+                                               const Tin *__restrict__ beta, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv, LC = C + 1;
+    extern __shared__ float sm[];
+    float *sDP = sm;                // dP o D
+    float *sLi = sDP + C * LC;      // (I + A)^-1
+    float *sY = sLi + C * LC;       // dKK
+    float *sb = sY + C * LC;        // beta
+    float *sG = sb + C;             // exp(gamma)
+    float *sdg = sG + C;            // d gamma
+    float *sdb = sdg + C;           // d beta
+    float *se = sdb + C;            // e_r (K~ gate term)
+    float *sk2 = se + C;            // <dGK_r, K_r>
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const float *Qn = w.Qn + slot * C * dk;
+    const float *Kn = w.Kn + slot * C * dk;
+    const float *dUn = w.dUn + slot * C * dv;
+    const float *aux = w.aux + slot * (4 * C + 4);
+    const float *M3 = w.M3 + slot * 3 * C * C;
+    float *dQ = w.dQ + slot * C * dk;
+    float *dK = w.dK + slot * C * dk;
+    const float *dW = w.dW + slot * C * dk;
+    const float *gam = w.gam + slot * C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const float gC = gam[len - 1];
+
+    for (int r = threadIdx.x; r < len; r += blockDim.x) {
+        sb[r] = ld_in(beta + row + r);
+        sG[r] = expf(gam[r]);
+        se[r] = expf(gC - gam[r]) * aux[C + r];
+        sdg[r] = aux[2 * C + 4 + r];
+        sdb[r] = aux[3 * C + 4 + r];
+        sk2[r] = 0.f;
+    }
+    for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
+        int r = idx / len, i = idx - r * len;
+        sDP[r * LC + i] = M3[r * C + i];
+        sLi[r * LC + i] = M3[C * C + r * C + i];
+        sY[r * LC + i] = M3[2 * C * C + r * C + i];
+    }
+    __syncthreads();
+    // dQ += (dP o D) K;  dK += (dP o D)^T Q
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[r * LC + i]; },
+                     [&](int i, int kk) { return Kn[i * dk + kk]; },
+                     [&](int r, int kk, float s) { dQ[r * dk + kk] += s; });
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sDP[i * LC + r]; },
+                     [&](int i, int kk) { return Qn[i * dk + kk]; },
+                     [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
+    __syncthreads();
+    // dGK = T^T dW (T = Linv diag(beta)); dK += Gamma dGK; d gamma += Gamma <dGK, K>;  dV = T^T dUnew
+    bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sLi[i * LC + r]; },
+                     [&](int i, int kk) { return dW[i * dk + kk]; },
+                     [&](int r, int kk, float s) {
+                         const float a = sb[r] * s;
+                         dK[r * dk + kk] += sG[r] * a;
+                         atomicAdd(&sk2[r], a * Kn[r * dk + kk]);
+                     });
+    bgemm<Tin, 4, 8>(len, dv, len, [&](int r, int i) { return sLi[i * LC + r]; },
+                     [&](int i, int n) { return dUn[i * dv + n]; },
+                     [&](int r, int n, float s) { st_out(dvout + (row + r) * dv + n, sb[r] * s); });
     __syncthreads();
     // dK += (dKK + dKK^T) K
     bgemm<Tin, 4, 8>(len, dk, len, [&](int r, int i) { return sY[r * LC + i] + sY[i * LC + r]; },
-                [&](int i, int kk) { return Kn[i * dk + kk]; },
-                [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
+                     [&](int i, int kk) { return Kn[i * dk + kk]; },
+                     [&](int r, int kk, float s) { dK[r * dk + kk] += s; });
     __syncthreads();
     if (threadIdx.x == 0) {
         float es = 0.f;
         for (int r = 0; r < len; ++r) {
-            sdg[r] -= se[r];
+            sdg[r] += sG[r] * sk2[r] - se[r];
             es += se[r];
         }
         sdg[len - 1] += es + expf(gC) * aux[2 * C];
@@ -768,11 +828,14 @@ static size_t smem_bbig(const Geo &g)
 {
     return sizeof(float) * ((g.dv < 128 ? g.dv : 128) * (g.dk + 1) + 4 * g.C + 4);
 }
+template <class Tin>
 static size_t smem_bchunk(const Geo &g)
 {
     const size_t LC = g.C + 1, LS = (g.dk > g.dv ? g.dk : g.dv) + 1;
-    return sizeof(float) * (7 * g.C * LC + g.C * LS + 8 * g.C);
+    const size_t stage = std::is_same<Tin, __nv_bfloat16>::value ? 0 : g.C * LS;
+    return sizeof(float) * (6 * g.C * LC + 5 * g.C + stage);
 }
+static size_t smem_bgrad(const Geo &g) { return sizeof(float) * (3 * (size_t)g.C * (g.C + 1) + 6 * g.C); }
 
 static int slice_width(const Geo &g) { return g.dv < 64 ? g.dv : 64; }
 
@@ -828,10 +891,12 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
-    if ((e = set_smem(k_bchunk<Tin>, smem_bchunk(g))) != cudaSuccess) return e;
+    if ((e = set_smem(k_bchunk<Tin>, smem_bchunk<Tin>(g))) != cudaSuccess) return e;
+    if (g.NC > 0) k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk<Tin>(g), st>>>(g, v, beta, dO, w);
+    if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    if ((e = set_smem(k_bgrad<Tin>, smem_bgrad(g))) != cudaSuccess) return e;
     if (g.NC > 0)
-        k_bchunk<Tin><<<dim3(g.NC, g.H), 512, smem_bchunk(g), st>>>(g, q, k, v, beta, dO, dq, dk,
-                                                                     dv, dbeta, dg, w);
+        k_bgrad<Tin><<<dim3(g.NC, g.H), 256, smem_bgrad(g), st>>>(g, q, k, dq, dk, dv, dbeta, dg, beta, w);
     return cudaPeekAtLastError();
 }
 

@@ -15,7 +15,8 @@ struct Ws {
     float *dSo, *dUn;          // backward: dS leaving the chunk, dUnew
     float *dQ, *dK, *dW;       // backward scratch [slots][C][dk]
     float *P;                  // [slots][C][C]   lower(Q K^T o D), diagonal kept
-    float *aux;                // backward [slots][2C + 4]: row sums and <dS_out, S_in>
+    float *aux;                // backward [slots][4C + 4]: row sums, <dS_out, S_in>, d gamma / d beta partials
+    float *M3;                 // backward [slots][3][C][C]: dP o D, (I + A)^-1, dKK
 };
 
 template <class Tin>

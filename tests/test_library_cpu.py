@@ -67,9 +67,9 @@ def test_workspace_size_and_validation(gdn):
 
 
 def test_plan_reports_path_and_kernel_count(gdn):
-    # fp32 runs the three general kernels, the backward five; packed input adds k_cstart
+    # fp32 runs the three general kernels, the backward six; packed input adds k_cstart
     assert gdn.dn_plan(_shape(gdn, dtype=0), False) == (gdn.DN_PATH_GENERAL, 3)
-    assert gdn.dn_plan(_shape(gdn, d=128), True) == (gdn.DN_PATH_GENERAL, 5)
+    assert gdn.dn_plan(_shape(gdn, d=128), True) == (gdn.DN_PATH_GENERAL, 6)
     assert gdn.dn_plan(_shape(gdn, B=1, dtype=0, cu=16, N=3), False) == (gdn.DN_PATH_GENERAL, 4)
     # bf16 d = 128 takes one of the tcgen05 kernels on an sm_103 device (one launch, plus
     # two for packed input); without such a device it falls to the general kernels
