@@ -12,6 +12,9 @@ What it follows:
     Table 1, rows "DeltaNet" (alpha = 1) and "Gated DeltaNet":
     S_t = S_{t-1}(alpha_t (I - beta_t k_t k_t^T)) + beta_t v_t k_t^T, stored
     transposed (d_k x d_v), read out as o_t = scale * q_t S_t;
+    with ``longhorn=True`` the step size is Longhorn's
+    beta_t / (1 + beta_t k_t^T k_t) in place of beta_t (same Table 1, row
+    "Longhorn", with its scalar beta);
   * backward — back-propagation through time of that loop, written by hand;
     the DeltaNet page ("Parallelizing Linear Transformers with the Delta Rule
     over Sequence Length", reply Q2 on chunk states) fixes only that the
@@ -61,9 +64,9 @@ def _load():
             I = ctypes.c_int
             D = ctypes.c_double
             lib.gdn_oracle_fwd.restype = I
-            lib.gdn_oracle_fwd.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, D, D, P, P, I]
+            lib.gdn_oracle_fwd.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, D, D, I, P, P, I]
             lib.gdn_oracle_bwd.restype = I
-            lib.gdn_oracle_bwd.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, D, D,
+            lib.gdn_oracle_bwd.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, I, D, D, I,
                                            P, P, P, P, P, P, P, P, I]
             _lib = lib
     return _lib
@@ -97,8 +100,8 @@ def _dims(q, v, cu_seqlens):
 
 
 def fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=1.0,
-        qk_l2norm=True, eps=EPS, nthreads=None):
-    """Token-by-token forward.  Arrays: q,k [NB,H,T,dk], v [NB,H,T,dv],
+        qk_l2norm=True, eps=EPS, nthreads=None, longhorn=False):
+    """Token-by-token forward (``longhorn``: Longhorn's step size).  Arrays: q,k [NB,H,T,dk], v [NB,H,T,dv],
     beta,g [NB,H,T], h0 [N,H,dk,dv] (N = NB, or the number of packed sequences).
     Returns (o [NB,H,T,dv], hT [N,H,dk,dv]) in float64."""
     q, k, v, beta, g, h0 = map(_f64, (q, k, v, beta, g, h0))
@@ -107,14 +110,15 @@ def fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=1.0,
     hT = np.zeros((n_seqs, H, dk, dv), np.float64)
     rc = _load().gdn_oracle_fwd(n_seqs, NB, H, Ttot, dk, dv, _ptr(offs), _ptr(q), _ptr(k),
                                 _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), int(bool(qk_l2norm)),
-                                float(scale), float(eps), _ptr(o), _ptr(hT), _threads(nthreads))
+                                float(scale), float(eps), int(bool(longhorn)), _ptr(o), _ptr(hT),
+                                _threads(nthreads))
     if rc != 0:
         raise RuntimeError("oracle forward failed with code %d" % rc)
     return o, hT
 
 
 def bwd(q, k, v, beta, g=None, h0=None, do=None, dhT=None, cu_seqlens=None, scale=1.0,
-        qk_l2norm=True, eps=EPS, nthreads=None):
+        qk_l2norm=True, eps=EPS, nthreads=None, longhorn=False):
     """Back-propagation through time of :func:`fwd` for the loss
     sum(o * do) + sum(hT * dhT).  Returns dict with dq, dk, dv, dbeta, dg (None when
     g is None) and dh0, all float64."""
@@ -128,7 +132,8 @@ def bwd(q, k, v, beta, g=None, h0=None, do=None, dhT=None, cu_seqlens=None, scal
                dh0=np.zeros((n_seqs, H, dk, dv), np.float64))
     rc = _load().gdn_oracle_bwd(n_seqs, NB, H, Ttot, dk, dv, _ptr(offs), _ptr(q), _ptr(k),
                                 _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), int(bool(qk_l2norm)),
-                                float(scale), float(eps), _ptr(do), _ptr(dhT), _ptr(out["dq"]),
+                                float(scale), float(eps), int(bool(longhorn)), _ptr(do), _ptr(dhT),
+                                _ptr(out["dq"]),
                                 _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dbeta"]),
                                 _ptr(out["dg"]), _ptr(out["dh0"]), _threads(nthreads))
     if rc != 0:

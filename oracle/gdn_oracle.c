@@ -26,6 +26,13 @@
  *   q and k are L2-normalised per token before use when qk_l2norm != 0:
  *       x_hat = x / sqrt(sum(x^2) + eps).
  *
+ *   Longhorn's step size (longhorn != 0; same rebuttal, Table 1, row
+ *   "Longhorn", scalar beta): the step uses
+ *       eps_t = beta_t / (1 + beta_t k_hat_t^T k_hat_t)
+ *   in place of beta_t, k_hat_t being the key the step uses (after the
+ *   normalisation, when it is on).  With alpha_t = exp(g_t) the step is then
+ *   the minimiser of ||S - alpha_t S_{t-1}||_F^2 + beta_t ||S k_t - v_t||^2.
+ *
  * Backward: back-propagation through time over the same loop, written by hand
  * (each line is the derivative of one forward line), with forward checkpoints
  * every CKPT tokens and the states of a segment recomputed before it is walked
@@ -49,7 +56,7 @@ typedef struct {
     int n_seqs, NB, H, Ttot, dk, dv;
     const long long *offs;
     const double *q, *k, *v, *beta, *g, *h0;
-    int qk_l2norm;
+    int qk_l2norm, longhorn;
     double scale, eps;
     /* forward outputs */
     double *o, *hT;
@@ -79,6 +86,15 @@ static void item_range(const job_t *J, int s, int h, long long *t0, long long *t
         *t1 = J->Ttot;
         *row = ((long long)s * J->H + h) * J->Ttot;
     }
+}
+
+/* the step size the update uses: beta, or Longhorn's beta / (1 + beta k^T k) */
+static double step_size(const job_t *J, double beta, const double *kh)
+{
+    if (!J->longhorn) return beta;
+    double kk = 0.0;
+    for (int i = 0; i < J->dk; ++i) kk += kh[i] * kh[i];
+    return beta / (1.0 + beta * kk);
 }
 
 static void l2norm(const double *x, int d, double eps, double *xh, double *rho_out)
@@ -127,7 +143,7 @@ static void fwd_item(job_t *J, int s, int h, double *M, double *kh, double *qh,
             memcpy(qh, qt, sizeof(double) * dk);
         }
         double alpha = J->g ? exp(J->g[row + t]) : 1.0;
-        step(M, kh, vt, J->beta[row + t], alpha, dk, dv, r, u);
+        step(M, kh, vt, step_size(J, J->beta[row + t], kh), alpha, dk, dv, r, u);
         double *ot = J->o + (row + t) * dv;
         for (int j = 0; j < dv; ++j) {
             double acc = 0.0;
@@ -179,7 +195,8 @@ static int bwd_item(job_t *J, int s, int h)
             if (J->qk_l2norm) l2norm(kt, dk, J->eps, kh, NULL);
             else memcpy(kh, kt, sizeof(double) * dk);
             double alpha = J->g ? exp(J->g[row + t]) : 1.0;
-            step(next, kh, J->v + (row + t) * dv, J->beta[row + t], alpha, dk, dv, r, u);
+            step(next, kh, J->v + (row + t) * dv, step_size(J, J->beta[row + t], kh), alpha, dk,
+                 dv, r, u);
         }
     }
 
@@ -197,7 +214,8 @@ static int bwd_item(job_t *J, int s, int h)
             if (J->qk_l2norm) l2norm(kt, dk, J->eps, kh, NULL);
             else memcpy(kh, kt, sizeof(double) * dk);
             double alpha = J->g ? exp(J->g[row + t]) : 1.0;
-            step(dst, kh, J->v + (row + t) * dv, J->beta[row + t], alpha, dk, dv, r, u);
+            step(dst, kh, J->v + (row + t) * dv, step_size(J, J->beta[row + t], kh), alpha, dk,
+                 dv, r, u);
         }
         for (long long t = tb - 1; t >= ta; --t) {
             const double *Sprev = seg + (size_t)(t - ta) * SZ;
@@ -214,7 +232,7 @@ static int bwd_item(job_t *J, int s, int h)
                 memcpy(kh, kt, sizeof(double) * dk);
                 memcpy(qh, qt, sizeof(double) * dk);
             }
-            double beta = J->beta[row + t];
+            double beta = step_size(J, J->beta[row + t], kh);
             double alpha = J->g ? exp(J->g[row + t]) : 1.0;
             /* recompute r and u of this token from the state before it */
             for (int j = 0; j < dv; ++j) {
@@ -266,6 +284,16 @@ static int bwd_item(job_t *J, int s, int h)
             }
             double *dvt = J->dv_out + (row + t) * dv;
             for (int j = 0; j < dv; ++j) dvt[j] = beta * du[j];
+            if (J->longhorn) {
+                /* beta = b / (1 + b kk), kk = k_hat^T k_hat: d/db = 1 / (1 + b kk)^2,
+                 * d/dkk = -b^2 / (1 + b kk)^2, and d kk / d k_hat = 2 k_hat */
+                double b = J->beta[row + t], kk = 0.0;
+                for (int i = 0; i < dk; ++i) kk += kh[i] * kh[i];
+                double den = 1.0 + b * kk;
+                double dkk = -dbeta * b * b / (den * den);
+                for (int i = 0; i < dk; ++i) dkh[i] += 2.0 * dkk * kh[i];
+                dbeta /= den * den;
+            }
             J->dbeta[row + t] = dbeta;
             if (J->dg) J->dg[row + t] = J->g ? alpha * dalpha : 0.0;
             /* through the normalisation x_hat = x * rho, rho = (|x|^2+eps)^-1/2 */
@@ -362,14 +390,14 @@ int gdn_oracle_fwd(int n_seqs, int NB, int H, int Ttot, int dk, int dv,
                    const long long *offs, const double *q, const double *k,
                    const double *v, const double *beta, const double *g,
                    const double *h0, int qk_l2norm, double scale, double eps,
-                   double *o, double *hT, int nthreads)
+                   int longhorn, double *o, double *hT, int nthreads)
 {
     if (check_dims(n_seqs, NB, H, Ttot, dk, dv, offs)) return 2;
     job_t J;
     memset(&J, 0, sizeof(J));
     J.n_seqs = n_seqs; J.NB = NB; J.H = H; J.Ttot = Ttot; J.dk = dk; J.dv = dv;
     J.offs = offs; J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0;
-    J.qk_l2norm = qk_l2norm; J.scale = scale; J.eps = eps;
+    J.qk_l2norm = qk_l2norm; J.scale = scale; J.eps = eps; J.longhorn = longhorn;
     J.o = o; J.hT = hT; J.nthreads = nthreads;
     return run(&J, 0);
 }
@@ -378,7 +406,7 @@ int gdn_oracle_bwd(int n_seqs, int NB, int H, int Ttot, int dk, int dv,
                    const long long *offs, const double *q, const double *k,
                    const double *v, const double *beta, const double *g,
                    const double *h0, int qk_l2norm, double scale, double eps,
-                   const double *dout, const double *dhT, double *dq, double *dk_out,
+                   int longhorn, const double *dout, const double *dhT, double *dq, double *dk_out,
                    double *dv_out, double *dbeta, double *dg, double *dh0, int nthreads)
 {
     if (check_dims(n_seqs, NB, H, Ttot, dk, dv, offs)) return 2;
@@ -386,7 +414,7 @@ int gdn_oracle_bwd(int n_seqs, int NB, int H, int Ttot, int dk, int dv,
     memset(&J, 0, sizeof(J));
     J.n_seqs = n_seqs; J.NB = NB; J.H = H; J.Ttot = Ttot; J.dk = dk; J.dv = dv;
     J.offs = offs; J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0;
-    J.qk_l2norm = qk_l2norm; J.scale = scale; J.eps = eps;
+    J.qk_l2norm = qk_l2norm; J.scale = scale; J.eps = eps; J.longhorn = longhorn;
     J.dout = dout; J.dhT = dhT; J.dq = dq; J.dk_out = dk_out; J.dv_out = dv_out;
     J.dbeta = dbeta; J.dg = dg; J.dh0 = dh0; J.nthreads = nthreads;
     return run(&J, 1);

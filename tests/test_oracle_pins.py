@@ -381,3 +381,95 @@ def test_threads_do_not_change_results():
     o1, h1 = oracle.fwd(q, k, v, beta, g, S0, nthreads=1)
     o2, h2 = oracle.fwd(q, k, v, beta, g, S0, nthreads=7)
     assert np.array_equal(o1, o2) and np.array_equal(h1, h2)
+
+
+# ---------------------------------------------------------------- [GDN-T1] row Longhorn
+@pytest.mark.parametrize("l2norm,gated", [(False, False), (False, True), (True, True)])
+def test_longhorn_steps_solve_the_regression_objective(l2norm, gated):
+    """[GDN-T1] row Longhorn: each step is the minimiser of
+    |S - a S_{t-1}|_F^2 + b |S k - v|^2 (a = 1 without the gate), i.e. the solution of the
+    normal equations S (I + b k k^T) = a S_{t-1} + b v k^T, solved here by numpy's dense
+    solver token after token (no closed form for the step size)."""
+    rng = RNG(50)
+    T, dk, dv = 7, 5, 4
+    q, k, v, beta, g, S0 = _rand_inputs(rng, 1, 2, T, dk, dv, gated=gated)
+    beta = beta * 3.0                       # step sizes where b |k|^2 is far from 0
+    o, hT = oracle.fwd(q, k, v, beta, g, S0, scale=0.8, qk_l2norm=l2norm, longhorn=True)
+    for h in range(2):
+        S = S0[0, h].T                      # pages' d_v x d_k orientation
+        for t in range(T):
+            kt, qt = k[0, h, t], q[0, h, t]
+            if l2norm:
+                kt = kt / np.sqrt((kt ** 2).sum() + oracle.EPS)
+                qt = qt / np.sqrt((qt ** 2).sum() + oracle.EPS)
+            a = np.exp(g[0, h, t]) if gated else 1.0
+            b = beta[0, h, t]
+            lhs = np.eye(dk) + b * np.outer(kt, kt)          # symmetric
+            S = np.linalg.solve(lhs, (a * S + b * np.outer(v[0, h, t], kt)).T).T
+            np.testing.assert_allclose(o[0, h, t], 0.8 * S @ qt, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(hT[0, h], S.T, rtol=1e-11, atol=1e-12)
+
+
+def test_longhorn_update_is_stationary_point_of_objective():
+    """The finite-difference gradient of |S - a S_{t-1}|^2 + b |S k - v|^2 vanishes at the
+    oracle's Longhorn state, and not at the plain delta-rule state for the same inputs."""
+    rng = RNG(51)
+    dk, dv = 4, 3
+    Sp = rng.standard_normal((dv, dk))
+    kv = rng.standard_normal(dk) * 1.5
+    vv = rng.standard_normal(dv)
+    a, b = 0.7, 0.9
+
+    def L(S):
+        return np.sum((S - a * Sp) ** 2) + b * np.sum((S @ kv - vv) ** 2)
+
+    args = (np.zeros((1, 1, 1, dk)), kv[None, None, None], vv[None, None, None],
+            np.array([[[b]]]), np.array([[[np.log(a)]]]), Sp.T[None, None].copy())
+    _, hl = oracle.fwd(*args, qk_l2norm=False, longhorn=True)
+    _, hd = oracle.fwd(*args, qk_l2norm=False)
+    assert np.abs(_fd_grad(L, hl[0, 0].T)).max() < 1e-7
+    assert np.abs(_fd_grad(L, hd[0, 0].T)).max() > 1e-2
+
+
+def test_longhorn_small_step_limit_and_retrieval():
+    """As b -> 0 the Longhorn step size b / (1 + b|k|^2) = b - b^2 |k|^2 + ..., so the step
+    agrees with the delta rule to first order in b; as b -> inf the stored value is read back exactly under the
+    written key (S_t k = v), which the delta rule does only for |k| = 1."""
+    rng = RNG(52)
+    dk, dv = 6, 3
+    q, k, v, _, _, S0 = _rand_inputs(rng, 1, 1, 1, dk, dv, gated=False)
+    k = k * 2.0
+    diff = []
+    for b in (1e-4, 1e-3):
+        beta = np.full((1, 1, 1), b)
+        _, hl = oracle.fwd(q, k, v, beta, None, S0, qk_l2norm=False, longhorn=True)
+        _, hd = oracle.fwd(q, k, v, beta, None, S0, qk_l2norm=False)
+        diff.append(np.abs(hl - hd).max())
+    # the two steps differ at second order in b: ten times b, a hundred times the gap
+    assert 0 < diff[0] < 1e-6 and abs(diff[1] / diff[0] / 100 - 1) < 0.05
+    _, hl = oracle.fwd(q, k, v, np.full((1, 1, 1), 1e12), None, S0, qk_l2norm=False, longhorn=True)
+    np.testing.assert_allclose(hl[0, 0].T @ k[0, 0, 0], v[0, 0, 0], rtol=1e-9, atol=1e-9)
+
+
+@pytest.mark.parametrize("gated,l2norm", [(True, False), (False, False), (True, True)])
+def test_longhorn_bptt_matches_finite_differences(gated, l2norm):
+    """Every gradient of the Longhorn loop, every coordinate, central differences in fp64:
+    the step size's dependence on beta and on the key is part of what is checked."""
+    rng = RNG(53)
+    q, k, v, beta, g, S0 = _rand_inputs(rng, 1, 1, 8, 3, 2, gated=gated)
+    beta = beta * 2.0
+    dO = rng.standard_normal((1, 1, 8, 2))
+    dST = rng.standard_normal((1, 1, 3, 2))
+    kw = dict(scale=1.1, qk_l2norm=l2norm, longhorn=True)
+    grads = oracle.bwd(q, k, v, beta, g, S0, dO, dST, **kw)
+    args = dict(q=q, k=k, v=v, beta=beta, g=g, S0=S0)
+    names = {"q": "dq", "k": "dk", "v": "dv", "beta": "dbeta", "g": "dg", "S0": "dh0"}
+    for name, gname in names.items():
+        if args[name] is None:
+            continue
+
+        def f(X, name=name):
+            a = dict(args); a[name] = X
+            return _loss(a["q"], a["k"], a["v"], a["beta"], a["g"], a["S0"], dO, dST, **kw)
+        fd = _fd_grad(f, args[name])
+        np.testing.assert_allclose(grads[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
