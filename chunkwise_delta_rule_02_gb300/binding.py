@@ -23,6 +23,7 @@ from ._build import LIB
 
 DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_WORKSPACE, DN_ERR_CUDA, DN_ERR_TIMEOUT = range(6)
 DN_F32, DN_BF16 = 0, 1
+DN_BETA_DELTA, DN_BETA_LONGHORN = 0, 1
 
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
@@ -34,7 +35,7 @@ class DnShape(ctypes.Structure):
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
                 ("num_seqs", ctypes.c_int32), ("qk_l2norm", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("eps", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("eps", ctypes.c_float), ("beta_mode", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -119,8 +120,10 @@ def _check(rc: int, where: str):
 
 
 def make_shape(q: torch.Tensor, v: torch.Tensor, chunk: int = 64, cu_seqlens=None,
-               scale: float = 1.0, qk_l2norm: bool = True, eps: float = 1e-6) -> DnShape:
-    """Shape record for q [B,H,T,dk], v [B,H,T,dv]; cu_seqlens a device int32 tensor."""
+               scale: float = 1.0, qk_l2norm: bool = True, eps: float = 1e-6,
+               longhorn: bool = False) -> DnShape:
+    """Shape record for q [B,H,T,dk], v [B,H,T,dv]; cu_seqlens a device int32 tensor;
+    longhorn: step size beta / (1 + beta k^T k) (DN_BETA_LONGHORN) instead of beta."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     if q.dtype == torch.float32:
@@ -129,7 +132,8 @@ def make_shape(q: torch.Tensor, v: torch.Tensor, chunk: int = 64, cu_seqlens=Non
         dt = DN_BF16
     else:
         raise TypeError("q must be float32 or bfloat16")
-    s = DnShape(B, H, T, dk, dv, chunk, dt, None, 0, int(bool(qk_l2norm)), float(scale), float(eps))
+    s = DnShape(B, H, T, dk, dv, chunk, dt, None, 0, int(bool(qk_l2norm)), float(scale), float(eps),
+                DN_BETA_LONGHORN if longhorn else DN_BETA_DELTA)
     if cu_seqlens is not None:
         s.cu_seqlens = _p(cu_seqlens)
         s.num_seqs = int(cu_seqlens.numel()) - 1
@@ -206,12 +210,13 @@ def gdn_decode_step(shape, q, k, v, beta, g, state_in, state_out, o, stream=None
 
 
 def decode_step(q, k, v, beta, g=None, state=None, out_state=None, scale=1.0, qk_l2norm=True,
-                eps=1e-6):
+                eps=1e-6, longhorn=False):
     """Allocate o (and the new state unless out_state is given; pass out_state=state for an
     in-place update) and run gdn_decode_step.  q, k [N,H,dk].  Returns (o, new_state)."""
     N, H, dk = q.shape
     dv = v.shape[-1]
-    shape = make_shape(q.view(N, H, 1, dk), v.view(N, H, 1, dv), 64, None, scale, qk_l2norm, eps)
+    shape = make_shape(q.view(N, H, 1, dk), v.view(N, H, 1, dv), 64, None, scale, qk_l2norm, eps,
+                       longhorn)
     o = torch.empty((N, H, dv), dtype=v.dtype, device=v.device)
     if out_state is None:
         out_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
@@ -235,9 +240,9 @@ def _nseq(q, cu_seqlens):
 
 
 def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0,
-            qk_l2norm=True, eps=1e-6, want_state=True, ws=None):
+            qk_l2norm=True, eps=1e-6, want_state=True, ws=None, longhorn=False):
     """Allocate o (and hT) and run gdn_chunk_fwd / dn_chunk_fwd.  Returns (o, hT)."""
-    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps)
+    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
     o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     N = _nseq(q, cu_seqlens)
     hT = torch.empty((N, q.shape[1], q.shape[-1], v.shape[-1]), dtype=torch.float32,
@@ -252,9 +257,9 @@ def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0
 
 
 def backward(q, k, v, beta, g, h0, dO, dhT, cu_seqlens=None, chunk=64, scale=1.0,
-             qk_l2norm=True, eps=1e-6, ws=None):
+             qk_l2norm=True, eps=1e-6, ws=None, longhorn=False):
     """Allocate the gradients and run gdn_chunk_bwd.  Returns a dict."""
-    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps)
+    shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
     out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                dbeta=torch.empty_like(beta),
                dg=torch.empty_like(g) if g is not None else None,

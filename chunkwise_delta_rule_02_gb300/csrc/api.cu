@@ -27,6 +27,7 @@ dn_status check_shape(const dn_shape *s, Geo *g)
     if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return DN_ERR_UNSUPPORTED;
     if (s->dk > kMaxD || s->dv > kMaxD) return DN_ERR_UNSUPPORTED;
     if (!(s->eps >= 0.f) || !(s->scale == s->scale)) return DN_ERR_INVALID_ARG;
+    if (s->beta_mode != DN_BETA_DELTA && s->beta_mode != DN_BETA_LONGHORN) return DN_ERR_INVALID_ARG;
     if (s->cu_seqlens) {
         if (s->B != 1 || s->num_seqs < 0) return DN_ERR_INVALID_ARG;
         if ((uintptr_t)s->cu_seqlens & 3u) return DN_ERR_INVALID_ARG;
@@ -41,6 +42,7 @@ dn_status check_shape(const dn_shape *s, Geo *g)
     x.N = x.varlen ? s->num_seqs : s->B;
     x.NC = x.varlen ? (s->T + x.C - 1) / x.C + x.N : x.B * ((s->T + x.C - 1) / x.C);
     x.l2norm = s->qk_l2norm != 0;
+    x.longhorn = s->beta_mode == DN_BETA_LONGHORN;
     x.scale = s->scale;
     x.eps = s->eps;
     x.cu = s->cu_seqlens;
@@ -60,7 +62,7 @@ int device_sms()
 
 struct Layout {
     size_t status, cstart, fast;
-    size_t Kn, Qn, W, U, Unew, gam, Sin, dSo, dUn, dQ, dK, dW, P, aux, M3;
+    size_t Kn, Qn, W, U, Unew, gam, eb, Sin, dSo, dUn, dQ, dK, dW, P, aux, M3;
     size_t total;
 };
 
@@ -90,6 +92,7 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast,
     L.U = take(slots * C * dv);
     L.Unew = take(slots * C * dv);
     L.gam = take(slots * C);
+    L.eb = take(slots * C);
     L.Sin = take(slots * dk * dv);
     L.P = take(slots * C * C);
     if (for_backward) {
@@ -111,7 +114,7 @@ gen::Ws general_ws(const Layout &L, char *base)
     gen::Ws w;
     auto F = [&](size_t o) { return o ? (float *)(base + o) : (float *)nullptr; };
     w.Kn = F(L.Kn); w.Qn = F(L.Qn); w.W = F(L.W); w.U = F(L.U); w.Unew = F(L.Unew);
-    w.gam = F(L.gam); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
+    w.gam = F(L.gam); w.eb = F(L.eb); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
     w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
     w.P = F(L.P); w.aux = F(L.aux); w.M3 = F(L.M3);
     return w;
@@ -322,6 +325,7 @@ dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, c
     dec::Args a;
     a.N = shape->B; a.H = shape->H; a.dk = shape->dk; a.dv = shape->dv;
     a.l2norm = shape->qk_l2norm != 0; a.scale = shape->scale; a.eps = shape->eps;
+    a.longhorn = shape->beta_mode == DN_BETA_LONGHORN;
     a.gate = g; a.state_in = state_in; a.state_out = state_out;
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;

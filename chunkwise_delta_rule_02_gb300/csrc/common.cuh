@@ -20,6 +20,7 @@ struct Geo {
     int NC;            // chunk slots per head (upper bound on chunks)
     int varlen;        // 1: packed, cu/cstart valid
     int l2norm;
+    int longhorn;      // step size beta / (1 + beta k^T k) instead of beta
     float scale, eps;
     const int32_t *cu;      // device [N+1] token offsets (packed)
     const int32_t *cstart;  // device [N+1] first chunk slot of each sequence (packed)

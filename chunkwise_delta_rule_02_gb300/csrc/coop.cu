@@ -138,6 +138,7 @@ struct Params {
     int H, T, N, items, Nc, Jmax_fixed;
     float scale, eps;
     int l2norm;
+    int longhorn;           // step size beta / (1 + beta k^T k) instead of beta
 };
 
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
@@ -602,6 +603,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
     float *s_beta = vb, *s_gl = vb + 64, *s_nk = vb + 128, *s_nq = vb + 192, *s_tc = vb + 256;
     float *s_qs = vb + 320, *s_ra = vb + 384, *s_cb = vb + 448, *s_f0 = vb + 512, *s_g = vb + 576;
     int *s_safe = (int *)(vb + 640);
+    float *s_kk = vb + 704;             // k_hat_r^T k_hat_r (Longhorn's step size)
     float *AX = (float *)(base + PP_AX);
     uint8_t *tl = base + PP_TL;
     const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
@@ -730,7 +732,12 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             for (int i = 0; i < 32; ++i) dg = (i == lane) ? __uint_as_float(v[i]) : dg;
             const int r = (q4 & 1) * 32 + lane;
             const float nrm = r < len ? (p.l2norm ? rsqrtf(dg + p.eps) : 1.f) : 0.f;
-            if (q4 < 2) s_nk[r] = nrm; else s_nq[r] = nrm;
+            if (q4 < 2) {
+                s_nk[r] = nrm;
+                s_kk[r] = dg * nrm * nrm;
+            } else {
+                s_nq[r] = nrm;
+            }
         }
         named_bar(bar_id, 128);
         const bool safe = *s_safe != 0;
@@ -738,9 +745,15 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         if (t < 64) {
             const float gl = s_gl[t];
             const float e = ex2f(gl);
-            s_tc[t] = s_beta[t] * e * s_nk[t];
+            // the step size: beta, or Longhorn's beta / (1 + beta k^T k)
+            float bt = s_beta[t];
+            if (p.longhorn) {
+                bt = bt / fmaf(bt, s_kk[t], 1.f);
+                s_beta[t] = bt;
+            }
+            s_tc[t] = bt * e * s_nk[t];
             s_qs[t] = e * s_nq[t];
-            s_ra[t] = s_beta[t] * s_nk[t] * e;
+            s_ra[t] = bt * s_nk[t] * e;
             s_cb[t] = safe ? s_nk[t] * ex2f(-gl) : 0.f;
             s_f0[t] = ex2f(glC - gl) * s_nk[t];
             if (t == 0) s_g[0] = ex2f(glC);
@@ -1116,7 +1129,7 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.ring = w + al(ctl_bytes) + (g.varlen ? al(sizeof(int32_t) * (size_t)(g.N + 1)) : 0);
     p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc;
     p.Jmax_fixed = g.varlen ? 0 : ((items + nc - 1) / nc) * ((g.T + C - 1) / C);
-    p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm;
+    p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm; p.longhorn = g.longhorn;
     cudaError_t e = cudaMemsetAsync(p.ctl, 0, ctl_bytes, st);
     if (e != cudaSuccess) return e;
     if (g.varlen) {

@@ -4,7 +4,8 @@
 // Per (sequence, head), with the state S stored d_k x d_v (key index outer) and
 // the token's normalised q, k:
 //     S' = alpha (I - beta k k^T) S + beta k v^T,   o = scale S'^T q
-// ("Gated DeltaNet", Table 1, row Gated DeltaNet; alpha = 1 is DeltaNet).
+// ("Gated DeltaNet", Table 1, row Gated DeltaNet; alpha = 1 is DeltaNet; with
+// Longhorn's step size beta / (1 + beta k^T k) in place of beta, row Longhorn).
 // Each column n of S evolves on its own:
 //     r_n = sum_i S[i][n] k_i,   u_n = beta (v_n - alpha r_n),
 //     S'[i][n] = alpha S[i][n] + k_i u_n,
@@ -28,6 +29,13 @@ constexpr int kGroups = 8;           // row groups: 256 threads
 constexpr int kRows = kMaxD / kGroups;   // rows per thread, 4-byte kernel
 constexpr int kRows4 = 128 / kGroups;    // rows per thread, 16-byte kernel (d_k <= 128)
 
+// the step size: beta, or Longhorn's beta / (1 + beta k^T k) ("Gated DeltaNet",
+// Table 1, row Longhorn), kk = k^T k of the key the update uses
+__device__ __forceinline__ float step_size(const Args &a, float b, float kk)
+{
+    return a.longhorn ? b / fmaf(b, kk, 1.f) : b;
+}
+
 template <class Tin>
 __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *__restrict__ q,
                                                           const Tin *__restrict__ k,
@@ -43,7 +51,7 @@ __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *_
     __shared__ float sk[kMaxD], sq[kMaxD];
     __shared__ float sr[kGroups][kCols], sp[kGroups][kCols];
     __shared__ float su[kCols];
-    __shared__ float sscal[2];   // k . q, alpha
+    __shared__ float sscal[3];   // k . q, alpha, k . k
 
     for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
         sk[i] = ld_in(k + item * a.dk + i);
@@ -74,6 +82,7 @@ __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *_
         if (col == 0) {
             sscal[0] = kq;
             sscal[1] = a.gate ? expf(a.gate[item]) : 1.f;
+            sscal[2] = kk * rk * rk;
         }
     }
     __syncthreads();
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *_
         }
         float u = 0.f;
         if (n < a.dv) {
-            const float b = ld_in(beta + item);
+            const float b = step_size(a, ld_in(beta + item), sscal[2]);
             u = b * (ld_in(v + item * a.dv + n) - alpha * rt);
             st_out(o + item * a.dv + n, a.scale * fmaf(alpha, pt, u * sscal[0]));
         }
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     __shared__ float sk[kMaxD], sq[kMaxD];
     __shared__ float4 sr[kGroups][32], sp[kGroups][32];
     __shared__ float4 su[32];
-    __shared__ float sscal[2];
+    __shared__ float sscal[3];
 
     for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
         sk[i] = ld_in(k + item * a.dk + i);
@@ -170,6 +179,7 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
         if (lane == 0) {
             sscal[0] = kq;
             sscal[1] = a.gate ? expf(a.gate[item]) : 1.f;
+            sscal[2] = kk * rk * rk;
         }
     }
     __syncthreads();
@@ -203,7 +213,8 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
             rt += reinterpret_cast<const float *>(&sr[g][L])[e];
             pt += reinterpret_cast<const float *>(&sp[g][L])[e];
         }
-        const float u = ld_in(beta + item) * (ld_in(v + item * a.dv + c) - alpha * rt);
+        const float b = step_size(a, ld_in(beta + item), sscal[2]);
+        const float u = b * (ld_in(v + item * a.dv + c) - alpha * rt);
         st_out(o + item * a.dv + c, a.scale * fmaf(alpha, pt, u * sscal[0]));
         reinterpret_cast<float *>(&su[L])[e] = u;
     }

@@ -9,6 +9,7 @@ namespace dec {
 struct Args {
     int N, H, dk, dv;          // sequences, heads, head dims (<= kMaxD)
     int l2norm;
+    int longhorn;              // step size beta / (1 + beta k^T k) instead of beta
     float scale, eps;
     const float *gate;         // [N][H] log-gate or null (alpha = 1)
     const float *state_in;     // [N][H][dk][dv] or null (zero state)

@@ -85,8 +85,8 @@ constexpr uint32_t AST = 68;            // row stride (floats) of the solve matr
 constexpr uint32_t OFF_AF = 180224;     // A fp32 [64][68]
 constexpr uint32_t OFF_XF = OFF_AF + 64 * AST * 4;  // X = (I + A)^-1 fp32 [64][68]
 constexpr uint32_t OFF_BG = OFF_XF + 64 * AST * 4;  // 2 stages x (beta[64], g[64]) fp32
-constexpr uint32_t OFF_VEC = OFF_BG + 2 * 128 * 4;  // per-chunk vectors, 8 x 64 floats
-constexpr uint32_t OFF_RING = OFF_VEC + 8 * 64 * 4; // 2 ring slots
+constexpr uint32_t OFF_VEC = OFF_BG + 2 * 128 * 4;  // per-chunk vectors, 9 x 64 floats
+constexpr uint32_t OFF_RING = OFF_VEC + 9 * 64 * 4; // 2 ring slots
 constexpr uint32_t OFF_BAR = OFF_RING + 2 * 320;
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
 constexpr uint32_t SMEM_USED = OFF_MISC + 64;
@@ -138,6 +138,7 @@ struct Params {
     int H, T, N;
     float scale, eps;
     int l2norm;
+    int longhorn;           // step size beta / (1 + beta k^T k) instead of beta
 };
 
 // shared-memory descriptor advanced by a byte offset (start address field, >> 4)
@@ -164,6 +165,7 @@ k_fast_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     float *s_qs = s_tc + 64;                    // exp(gamma_r) m_r G        (rows of Qt)
     float *s_ra = s_qs + 64;                    // beta_r n_r exp(gamma_r)   (rows of A, factored)
     float *s_cb = s_ra + 64;                    // n_i exp(-gamma_i)         (columns of A and P, factored)
+    float *s_kk = s_cb + 64;                    // k_hat_r^T k_hat_r         (Longhorn's step size)
     Ring *ring = (Ring *)(sm + OFF_RING);
     float *Af = (float *)(sm + OFF_AF);
     float *Xf = (float *)(sm + OFF_XF);
@@ -480,8 +482,10 @@ k_fast_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 sq += __shfl_xor_sync(0xffffffffu, sq, 1);
                 if (hh == 0) {
                     const bool ok = r < len;
-                    s_nk[r] = ok ? (p.l2norm ? rsqrtf(sk + p.eps) : 1.f) : 0.f;
+                    const float nk = ok ? (p.l2norm ? rsqrtf(sk + p.eps) : 1.f) : 0.f;
+                    s_nk[r] = nk;
                     s_nq[r] = ok ? (p.l2norm ? rsqrtf(sq + p.eps) : 1.f) : 0.f;
+                    s_kk[r] = sk * nk * nk;
                 }
             }
             named_bar(2, 128);
@@ -498,9 +502,15 @@ k_fast_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             if (t < 64) {
                 const float gl = s_gl[t];
                 const float e = ex2f(gl);
-                s_tc[t] = s_beta[t] * e * s_nk[t];
+                // the step size: beta, or Longhorn's beta / (1 + beta k^T k)
+                float bt = s_beta[t];
+                if (p.longhorn) {
+                    bt = bt / fmaf(bt, s_kk[t], 1.f);
+                    s_beta[t] = bt;
+                }
+                s_tc[t] = bt * e * s_nk[t];
                 s_qs[t] = e * s_nq[t] * Gn;
-                s_ra[t] = s_beta[t] * s_nk[t] * e;
+                s_ra[t] = bt * s_nk[t] * e;
                 s_cb[t] = safe ? s_nk[t] * ex2f(-gl) : 0.f;
                 ring[s].f[t] = ex2f(glC - gl) * s_nk[t] * fdiv;
                 if (t == 0) {
@@ -845,6 +855,7 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.cu = g.varlen ? g.cu : nullptr;
     p.order = nullptr;
     p.H = g.H; p.T = g.T; p.N = g.N; p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm;
+    p.longhorn = g.longhorn;
     if (g.varlen) {
         int32_t *order = (int32_t *)ws;
         k_order<<<(g.N + 127) / 128, 128, 0, st>>>(g.cu, g.N, order);

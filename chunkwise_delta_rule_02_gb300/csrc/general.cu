@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
     float *sQ = sK + C * LK;                        // [C][LK] normalised queries, then V [C][dv]
     float *sA = sQ + C * (LK > dv ? LK : dv);       // [C][LC]
     float *sT = sA + C * LC;                        // [C][LC]
-    float *sb = sT + C * LC;                        // [C] beta
+    float *sb = sT + C * LC;                        // [C] step sizes (beta, or Longhorn's)
     float *sg = sb + C;                             // [C] gamma
     float *sG = sg + C;                             // [C] exp(gamma)
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
@@ -237,6 +237,14 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
         sq = warp_sum(sq);
         float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
         float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
+        if (lane == 0) {
+            // the token's step size: beta, or Longhorn's beta / (1 + beta k^T k) with
+            // k^T k = |k|^2 rk^2 of the key the update uses
+            float bt = ld_in(beta + row + r);
+            if (g.longhorn) bt = bt / fmaf(bt, sk * rk * rk, 1.f);
+            sb[r] = bt;
+            w.eb[slot * C + r] = bt;
+        }
         for (int c = lane; c < dk; c += 32) {
             float x = ld_in(kr + c) * rk, y = ld_in(qr + c) * rq;
             sK[r * LK + c] = x;
@@ -258,13 +266,11 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
         if (lane < len) {
             sg[lane] = x0;
             sG[lane] = expf(x0);
-            sb[lane] = ld_in(beta + row + lane);
             w.gam[slot * C + lane] = x0;
         }
         if (lane + 32 < len) {
             sg[lane + 32] = x1;
             sG[lane + 32] = expf(x1);
-            sb[lane + 32] = ld_in(beta + row + lane + 32);
             w.gam[slot * C + lane + 32] = x1;
         }
     }
@@ -551,7 +557,6 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
 // 256-thread CTAs per SM.
 template <class Tin>
 __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict__ v,
-                                                const Tin *__restrict__ beta,
                                                 const Tin *__restrict__ dO, Ws w)
 {
     constexpr bool kStage = !std::is_same<Tin, __nv_bfloat16>::value;   // fp32: stage row operands
@@ -567,7 +572,7 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
     float *sLi = sDP + C * LC;      // (I + A)^-1
     float *sdT = sLi + C * LC;      // dT
     float *sY = sdT + C * LC;       // A, then dA, then dKK
-    float *sb = sY + C * LC;        // beta
+    float *sb = sY + C * LC;        // step sizes
     float *sg = sb + C;             // gamma
     float *sG = sg + C;             // exp(gamma)
     float *sdg = sG + C;            // d gamma (partial)
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
     const float sc = g.scale;
 
     for (int r = threadIdx.x; r < len; r += blockDim.x) {
-        sb[r] = ld_in(beta + row + r);
+        sb[r] = w.eb[slot * C + r];
         sg[r] = gam[r];
         sG[r] = expf(gam[r]);
         sdg[r] = sG[r] * aux[r];      // q-term of d gamma
@@ -702,8 +707,7 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
                                                Tin *__restrict__ dq, Tin *__restrict__ dkout,
                                                Tin *__restrict__ dvout,
                                                Tin *__restrict__ dbeta,
-                                               float *__restrict__ dg,
-                                               const Tin *__restrict__ beta, Ws w)
+                                               float *__restrict__ dg, Ws w)
 {
     const int j = blockIdx.x, h = blockIdx.y;
     int b, t0, len, seq, local;
@@ -713,7 +717,7 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
     float *sDP = sm;                // dP o D
     float *sLi = sDP + C * LC;      // (I + A)^-1
     float *sY = sLi + C * LC;       // dKK
-    float *sb = sY + C * LC;        // beta
+    float *sb = sY + C * LC;        // step sizes
     float *sG = sb + C;             // exp(gamma)
     float *sdg = sG + C;            // d gamma
     float *sdb = sdg + C;           // d beta
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
     const float gC = gam[len - 1];
 
     for (int r = threadIdx.x; r < len; r += blockDim.x) {
-        sb[r] = ld_in(beta + row + r);
+        sb[r] = w.eb[slot * C + r];
         sG[r] = expf(gam[r]);
         se[r] = expf(gC - gam[r]) * aux[C + r];
         sdg[r] = aux[2 * C + 4 + r];
@@ -802,8 +806,17 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
         sq = warp_sum(sq); sk = warp_sum(sk); pq = warp_sum(pq); pk = warp_sum(pk);
         float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
         float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
+        // sdb holds d/d(step size).  Longhorn's step e = b / (1 + b kap), kap = k^T k:
+        // de/db = (1 - e kap)^2 and de/dkap = -e^2, with d kap / dk = 2 k
+        float db = sdb[r], dkap = 0.f;
+        if (g.longhorn) {
+            const float kap = sk * rk * rk, e = sb[r], f = fmaf(-e, kap, 1.f);
+            dkap = -db * e * e;
+            db *= f * f;
+            pk = fmaf(2.f * dkap, kap, pk);
+        }
         for (int kk = lane; kk < dk; kk += 32) {
-            float a = dQ[r * dk + kk], c = dK[r * dk + kk];
+            float a = dQ[r * dk + kk], c = fmaf(2.f * dkap, Kn[r * dk + kk], dK[r * dk + kk]);
             if (g.l2norm) {
                 a = rq * (a - Qn[r * dk + kk] * pq);
                 c = rk * (c - Kn[r * dk + kk] * pk);
@@ -811,7 +824,7 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
             st_out(dq + (row + r) * dk + kk, a);
             st_out(dkout + (row + r) * dk + kk, c);
         }
-        if (lane == 0) st_out(dbeta + row + r, sdb[r]);
+        if (lane == 0) st_out(dbeta + row + r, db);
     }
 }
 
@@ -892,11 +905,11 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bchunk<Tin>, smem_bchunk<Tin>(g))) != cudaSuccess) return e;
-    if (g.NC > 0) k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk<Tin>(g), st>>>(g, v, beta, dO, w);
+    if (g.NC > 0) k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk<Tin>(g), st>>>(g, v, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bgrad<Tin>, smem_bgrad(g))) != cudaSuccess) return e;
     if (g.NC > 0)
-        k_bgrad<Tin><<<dim3(g.NC, g.H), 256, smem_bgrad(g), st>>>(g, q, k, dq, dk, dv, dbeta, dg, beta, w);
+        k_bgrad<Tin><<<dim3(g.NC, g.H), 256, smem_bgrad(g), st>>>(g, q, k, dq, dk, dv, dbeta, dg, w);
     return cudaPeekAtLastError();
 }
 

@@ -11,6 +11,7 @@ struct Ws {
     float *Kn, *Qn, *W;        // [slots][C][dk]  normalised K, Q; WY factor W
     float *U, *Unew;           // [slots][C][dv]
     float *gam;                // [slots][C]      within-chunk cumulative log-gate
+    float *eb;                 // [slots][C]      step size of each token (beta, or Longhorn's)
     float *Sin;                // [slots][dk][dv] state entering the chunk
     float *dSo, *dUn;          // backward: dS leaving the chunk, dUnew
     float *dQ, *dK, *dW;       // backward scratch [slots][C][dk]

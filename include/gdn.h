@@ -78,7 +78,19 @@ typedef struct {
     int32_t qk_l2norm;            /* 1: normalise q and k per token inside the kernels  */
     float scale;                  /* o = scale * S^T q                                  */
     float eps;                    /* normalisation epsilon (1e-6 is the default)        */
+    int32_t beta_mode;            /* dn_beta_mode: how beta becomes the step size       */
 } dn_shape;
+
+/* The step size each token's update uses ("Gated DeltaNet" rebuttal, Table 1):
+ *   DN_BETA_DELTA     beta_t as given (rows "DeltaNet" / "Gated DeltaNet");
+ *   DN_BETA_LONGHORN  beta_t / (1 + beta_t k_t^T k_t), k_t the key the update
+ *                     uses (after the normalisation when qk_l2norm = 1): row
+ *                     "Longhorn" with its scalar beta.  The update is then the
+ *                     minimiser of |S - alpha_t S_{t-1}|^2 + beta_t |S k_t - v_t|^2;
+ *                     gradients (gdn_chunk_bwd) are with respect to the raw beta
+ *                     and k through this map.
+ * Any other value: DN_ERR_INVALID_ARG. */
+typedef enum { DN_BETA_DELTA = 0, DN_BETA_LONGHORN = 1 } dn_beta_mode;
 
 /* Bytes of device workspace the calls below need for `shape` (0 on bad
  * arguments).  for_backward = 1 sizes it for gdn_chunk_bwd. */

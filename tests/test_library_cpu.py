@@ -46,8 +46,8 @@ def test_library_exports_every_declared_symbol(gdn):
         assert hasattr(lib, name), name
 
 
-def _shape(gdn, B=2, H=3, T=100, d=64, dtype=1, chunk=64, cu=None, N=0):
-    s = gdn.DnShape(B, H, T, d, d, chunk, dtype, cu, N, 1, 1.0, 1e-6)
+def _shape(gdn, B=2, H=3, T=100, d=64, dtype=1, chunk=64, cu=None, N=0, beta_mode=0):
+    s = gdn.DnShape(B, H, T, d, d, chunk, dtype, cu, N, 1, 1.0, 1e-6, beta_mode)
     return s
 
 
@@ -64,6 +64,19 @@ def test_workspace_size_and_validation(gdn):
         assert gdn.dn_uses_fast_path(b, False) == -1
     assert gdn.dn_workspace_size(_shape(gdn, B=2, cu=16, N=3), False) == 0   # packed needs B == 1
     assert gdn.dn_workspace_size(_shape(gdn, B=1, cu=16, N=3), False) > 0
+
+
+def test_beta_mode_is_validated(gdn):
+    """DN_BETA_DELTA and DN_BETA_LONGHORN are the two step-size modes; any other value
+    is rejected before any device work, and Longhorn's needs no extra workspace
+    beyond the per-token step sizes every general-path call records."""
+    for mode in (gdn.DN_BETA_DELTA, gdn.DN_BETA_LONGHORN):
+        for bwd in (False, True):
+            assert gdn.dn_workspace_size(_shape(gdn, beta_mode=mode), bwd) == \
+                gdn.dn_workspace_size(_shape(gdn), bwd)
+    for mode in (2, -1, 7):
+        assert gdn.dn_workspace_size(_shape(gdn, beta_mode=mode), False) == 0
+        assert gdn.dn_uses_fast_path(_shape(gdn, beta_mode=mode), False) == -1
 
 
 def test_plan_reports_path_and_kernel_count(gdn):
