@@ -52,3 +52,21 @@ def test_single_rank_defaults():
     import bench
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
     assert bench.whole_job_value(524288 // 16, 1, 1.0) == 32768 * 1000.0
+
+
+def test_cpu_baseline_counts_the_tokens_it_runs():
+    """The oracle leg gathers its items into one call; the tokens it reports are the
+    items' tokens divided by the heads (whole tokens), for fixed and packed input."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_delta_rule_02_gb300 import workloads as W
+    w = W.Workload("cb", 2, 3, 40, 8, "bf16", True, True, 1)
+    x = W.generate(w)
+    secs, tok = bench.oracle_sample_fwd(x, w, bench.sample_items(x, 4), 2)
+    assert secs > 0 and abs(tok - 40 * 4 / 3) < 1e-9
+    wv = W.Workload("cbv", 1, 2, 0, 8, "bf16", True, True, 2, varlen_total=1, varlen_n=1)
+    xv = W.generate(wv, lengths=[3, 0, 50])
+    secs, tok = bench.oracle_sample_fwd(xv, wv, bench.sample_items(xv, 100), 2)
+    assert secs > 0 and abs(tok - 53) < 1e-9
+    cb = bench.cpu_baseline(x, w)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
