@@ -288,11 +288,14 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     } else if (warp == 2) {
         // ---------------------------------------------------------------- packages (bulk copies)
         if (lane == 0) {
-            for (int j = 0; j < J; ++j) {
+            // two copies in flight: chunk j's copy is issued before chunk j - 1's has been
+            // waited for, and the producer's flag of chunk j is polled while that copy lands
+            int issued = 0, landed = 0;
+            bool ok = true;
+            for (int j = 0; j < J && ok; ++j) {
                 const int s = j & 1, slot = j % RING;
                 // wait for the producer's flag
                 const long long t0 = clock64();
-                bool ok = true;
                 unsigned ns = 32;
                 while (ld_acquire_gpu(&ready[slot]) != (uint32_t)(j + 1)) {
                     if (*abort_flag || clock64() - t0 > BUDGET) { ok = false; break; }
@@ -302,17 +305,26 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 if (!ok) { fail(); break; }
                 fence_async_global();
                 if (c == 0) CTR(j, 0);
-                if (j >= 2 && !wait(B_PEMPTY + s, (uint32_t)((j >> 1) - 1))) break;
+                if (j >= 2 && !(ok = wait(B_PEMPTY + s, (uint32_t)((j >> 1) - 1)))) break;
                 mbar_expect_tx(&bar[B_PFULL + s], PK_BYTES);
                 bulk_load(sm + CH_PK + s * PK_STRIDE, ring + (size_t)slot * PK_STRIDE, PK_BYTES,
                           &bar[B_PFULL + s]);
-                if (!wait(B_PFULL + s, (uint32_t)(j >> 1))) {
-                    mbar_wait(&bar[B_PFULL + s], (uint32_t)(j >> 1) & 1u, BUDGET, nullptr);
-                    break;
-                }
-                st_release_gpu(consumed, (uint32_t)(j + 1));   // the ring slot may be refilled
+                issued = j + 1;
                 if (c == 0) CTR(j, 1);
+                // chunk j - 1's copy has landed: its ring slot may be refilled
+                if (j >= 1) {
+                    if (!(ok = wait(B_PFULL + ((j - 1) & 1), (uint32_t)((j - 1) >> 1)))) break;
+                    landed = j;
+                    st_release_gpu(consumed, (uint32_t)landed);
+                }
             }
+            if (ok && issued == J && J > 0 && (ok = wait(B_PFULL + ((J - 1) & 1), (uint32_t)((J - 1) >> 1)))) {
+                landed = J;
+                st_release_gpu(consumed, (uint32_t)landed);
+            }
+            // on a failure, let the copies in flight land before shared memory goes away
+            for (int n = landed; n < issued; ++n)
+                mbar_wait(&bar[B_PFULL + (n & 1)], (uint32_t)(n >> 1) & 1u, BUDGET, nullptr);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
