@@ -141,13 +141,23 @@ def whole_job_value(tokens_per_rank: int, world: int, ms: float) -> float:
     return tokens_per_rank * world / (ms / 1000.0)
 
 
-def kernel_source_sha() -> str:
+# the translation unit and headers each profiled kernel is built from
+KERNEL_SOURCES = {
+    "k_coop_fwd": ["coop.cu", "fast.h", "prep_math.cuh", "sm100.cuh", "common.cuh"],
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources `kernel` is compiled from (all of csrc for an unlisted one)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunkwise_delta_rule_02_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(csrc))
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
+    with open(os.path.join(ROOT, "include", "gdn.h"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -160,7 +170,7 @@ def recorded_traffic(kernel: str, workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel + "@" + workload)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
