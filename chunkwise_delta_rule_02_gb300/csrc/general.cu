@@ -455,6 +455,254 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
     }
 }
 
+// ----------------------------------------------------------------------------- staged scans (bf16)
+// The two sequential scans for bf16 inputs with d_k, d_v <= 128: one CTA per
+// (sequence, head) walks the chunks in order, and every chunk's operands are first
+// copied (coalesced, rounded to bf16 once) into padded shared-memory tiles, so that
+// the warp-level tensor-core products read 32-bit operand pairs straight from shared
+// memory instead of gathering single elements from the fp32 workspace.
+
+// C = A B^T on the tensor cores for M % 16 == 0, N % 32 == 0, K % 16 == 0: A is
+// [M][lda] and Bt is [N][ldb], bf16, K contiguous (lda, ldb even; lda / 2 and
+// ldb / 2 = 4 mod 32 keeps the fragment loads free of bank conflicts).  St(m, n, v)
+// receives each result once.
+template <class FS>
+__device__ __forceinline__ void smma(int M, int N, int K, const __nv_bfloat16 *A, int lda,
+                                     const __nv_bfloat16 *Bt, int ldb, FS St)
+{
+    constexpr int NT = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int ntl = N / (8 * NT);
+    for (int tile = warp; tile < (M / 16) * ntl; tile += nw) {
+        const int m0 = (tile / ntl) * 16, n0 = (tile - (tile / ntl) * ntl) * 8 * NT;
+        float acc[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const uint32_t *a0p = reinterpret_cast<const uint32_t *>(A + (m0 + g) * lda) + t;
+        const uint32_t *a1p = reinterpret_cast<const uint32_t *>(A + (m0 + g + 8) * lda) + t;
+        for (int k0 = 0; k0 < K; k0 += 16) {
+            const int kw = k0 >> 1;
+            uint32_t a[4] = {a0p[kw], a1p[kw], a0p[kw + 4], a1p[kw + 4]};
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const uint32_t *bp = reinterpret_cast<const uint32_t *>(Bt + (n0 + 8 * j + g) * ldb) + t + kw;
+                uint32_t b[2] = {bp[0], bp[4]};
+                mma_bf16_16816(acc[j], a, b);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int m = m0 + g, n = n0 + 8 * j + 2 * t;
+            St(m, n, acc[j][0]);
+            St(m, n + 1, acc[j][1]);
+            St(m + 8, n, acc[j][2]);
+            St(m + 8, n + 1, acc[j][3]);
+        }
+    }
+}
+
+// padded row length (elements) for a K-long bf16 row: K + 8 with K % 64 == 0 gives
+// a row stride of 4 mod 32 words; other K % 16 == 0 round up to that pattern
+__host__ __device__ __forceinline__ int spad(int K) { return ((K + 63) / 64) * 64 + 8; }
+
+__host__ __device__ __forceinline__ bool staged_ok(const Geo &g)
+{
+    return g.dk <= 128 && g.dv <= 128 && g.dk % 16 == 0 && g.dv % 32 == 0;
+}
+
+// Copies the `rows` x `cols` fp32 row-major block at src (cols % 4 == 0, src 16-byte
+// aligned) through registers: every thread first issues its 16-byte loads for a batch,
+// then hands each value to put(r, c, v).  Rows at or past `live` read as zero.
+template <class FP>
+__device__ __forceinline__ void stage_f32(const float *__restrict__ src, int rows, int cols, int live, FP put)
+{
+    constexpr int VB = 8;
+    const int n4 = rows * cols / 4, c4 = cols / 4;
+    for (int base = threadIdx.x; base < n4; base += blockDim.x * VB) {
+        float4 v[VB];
+#pragma unroll
+        for (int u = 0; u < VB; ++u) {
+            const int e = base + u * blockDim.x;
+            v[u] = (e < n4 && e / c4 < live) ? __ldg(reinterpret_cast<const float4 *>(src) + e)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < VB; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < n4) {
+                const int r = e / c4, c = 4 * (e - r * c4);
+                put(r, c, v[u].x);
+                put(r, c + 1, v[u].y);
+                put(r, c + 2, v[u].z);
+                put(r, c + 3, v[u].w);
+            }
+        }
+    }
+}
+
+// forward recompute: S_in of every chunk, and Unew = U - W S_in, S <- Gamma_C S + K~^T Unew
+__global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict__ h0,
+                                                 float *__restrict__ hT, Ws w)
+{
+    const int s = blockIdx.x, h = blockIdx.y;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int L1 = spad(dk), L2 = spad(C);
+    int b, t0, L, j0, nch;
+    seq_of(g, s, b, t0, L, j0, nch);
+    extern __shared__ float sm[];
+    float *sS = sm;                                          // [dk][dv] fp32 state
+    float *sE = sS + dk * dv;                                // [C]
+    float *sU = sE + 64;                                     // [C][dv] U
+    __nv_bfloat16 *A1 = reinterpret_cast<__nv_bfloat16 *>(sU + C * dv);   // W [C][L1]
+    __nv_bfloat16 *B1 = A1 + C * L1;                         // S^T [dv][L1]
+    __nv_bfloat16 *A2 = B1 + dv * L1;                        // (diag(E) K)^T [dk][L2]
+    __nv_bfloat16 *B2 = A2 + dk * L2;                        // Unew^T [dv][L2]
+    const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
+    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+        const int kk = idx / dv, n = idx - kk * dv;
+        const float v = h0 ? h0[sidx + idx] : 0.f;
+        sS[idx] = v;
+        B1[n * L1 + kk] = __float2bfloat16_rn(v);
+    }
+    __syncthreads();
+    for (int c = 0; c < nch; ++c) {
+        const int len = min(C, L - c * C);
+        const size_t slot = (size_t)(j0 + c) * g.H + h;
+        const float *gam = w.gam + slot * C;
+        const float gC = gam[len - 1];
+        const float *W = w.W + slot * C * dk;
+        const float *Kn = w.Kn + slot * C * dk;
+        const float *U = w.U + slot * C * dv;
+        float *Un = w.Unew + slot * C * dv;
+        float *Sin = w.Sin + slot * dk * dv;
+        for (int r = threadIdx.x; r < C; r += blockDim.x) sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) Sin[idx] = sS[idx];
+        __syncthreads();
+        stage_f32(W, C, dk, len, [&](int r, int kk, float v) { A1[r * L1 + kk] = __float2bfloat16_rn(v); });
+        stage_f32(Kn, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + r] = __float2bfloat16_rn(sE[r] * v); });
+        stage_f32(U, C, dv, len, [&](int r, int n, float v) { sU[r * dv + n] = v; });
+        __syncthreads();
+        // Unew[r][n] = U[r][n] - sum_kk W[r][kk] S[kk][n]
+        smma(C, dv, dk, A1, L1, B1, L1, [&](int r, int n, float acc) {
+            const float u = r < len ? sU[r * dv + n] - acc : 0.f;
+            if (r < len) Un[r * dv + n] = u;
+            B2[n * L2 + r] = __float2bfloat16_rn(u);
+        });
+        __syncthreads();
+        // S[kk][n] <- Gamma_C S[kk][n] + sum_r E_r K[r][kk] Unew[r][n]
+        const float GC = expf(gC);
+        smma(dk, dv, C, A2, L2, B2, L2, [&](int kk, int n, float acc) {
+            const float v = fmaf(GC, sS[kk * dv + n], acc);
+            sS[kk * dv + n] = v;
+            B1[n * L1 + kk] = __float2bfloat16_rn(v);
+        });
+        __syncthreads();
+    }
+    if (hT)
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) hT[sidx + idx] = sS[idx];
+}
+
+// backward scan: dS_out of every chunk, and
+//   dUnew = P^T dO + K~ dS,   dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
+__global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__restrict__ dO,
+                                                  const float *__restrict__ dhT,
+                                                  float *__restrict__ dh0, Ws w)
+{
+    const int s = blockIdx.x, h = blockIdx.y;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int L1 = spad(C + dk), L2 = spad(2 * C);
+    int b, t0, L, j0, nch;
+    seq_of(g, s, b, t0, L, j0, nch);
+    extern __shared__ float sm[];
+    float *sdS = sm;                                         // [dk][dv] fp32
+    float *sE = sdS + dk * dv;                               // [C] exp(gamma_C - gamma_r)
+    float *sG = sE + 64;                                     // [C] exp(gamma_r)
+    __nv_bfloat16 *A1 = reinterpret_cast<__nv_bfloat16 *>(sG + 64);   // [P^T | diag(E) K] [C][L1]
+    __nv_bfloat16 *B1 = A1 + C * L1;                         // [dO^T | dS^T] [dv][L1]
+    __nv_bfloat16 *A2 = B1 + dv * L1;                        // [diag(G) Q | -W]^T [dk][L2]
+    __nv_bfloat16 *B2 = A2 + dk * L2;                        // [dO^T | dUnew^T] [dv][L2]
+    const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
+    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+        const int kk = idx / dv, n = idx - kk * dv;
+        const float v = dhT ? dhT[sidx + idx] : 0.f;
+        sdS[idx] = v;
+        B1[n * L1 + C + kk] = __float2bfloat16_rn(v);
+    }
+    __syncthreads();
+    for (int c = nch - 1; c >= 0; --c) {
+        const int len = min(C, L - c * C);
+        const size_t slot = (size_t)(j0 + c) * g.H + h;
+        const size_t row = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
+        const float *gam = w.gam + slot * C;
+        const float gC = gam[len - 1];
+        const float *Qn = w.Qn + slot * C * dk;
+        const float *Kn = w.Kn + slot * C * dk;
+        const float *W = w.W + slot * C * dk;
+        const float *Pg = w.P + slot * C * C;
+        float *dUg = w.dUn + slot * C * dv;
+        float *dSo = w.dSo + slot * dk * dv;
+        for (int r = threadIdx.x; r < C; r += blockDim.x) {
+            sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
+            sG[r] = r < len ? expf(gam[r]) : 0.f;
+        }
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) dSo[idx] = sdS[idx];
+        __syncthreads();
+        // P[x][i] -> A1[i][x]; columns i >= len of P are not written by the preparation,
+        // but they only reach rows i >= len of dUnew, which are dropped below
+        stage_f32(Pg, C, C, len, [&](int x, int i, float v) { A1[i * L1 + x] = __float2bfloat16_rn(v); });
+        stage_f32(Kn, C, dk, len, [&](int r, int kk, float v) { A1[r * L1 + C + kk] = __float2bfloat16_rn(sE[r] * v); });
+        stage_f32(Qn, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + r] = __float2bfloat16_rn(sG[r] * v); });
+        stage_f32(W, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + C + r] = __float2bfloat16_rn(-v); });
+        {
+            // scale dO -> both B tiles, 8 bf16 per 16-byte load
+            const int n8 = C * dv / 8, c8 = dv / 8;
+            for (int base = threadIdx.x; base < n8; base += blockDim.x * 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = base + u * blockDim.x;
+                    v[u] = (e < n8 && e / c8 < len) ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = base + u * blockDim.x;
+                    if (e >= n8) continue;
+                    const int r = e / c8, n = 8 * (e - r * c8);
+                    const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(g.scale * __uint_as_float(wv[q] << 16));
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
+                        B1[(n + 2 * q) * L1 + r] = lo;
+                        B1[(n + 2 * q + 1) * L1 + r] = hi;
+                        B2[(n + 2 * q) * L2 + r] = lo;
+                        B2[(n + 2 * q + 1) * L2 + r] = hi;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // dUnew[i][n] = sum_x P[x][i] dO[x][n] + E_i sum_kk K[i][kk] dS[kk][n]
+        smma(C, dv, C + dk, A1, L1, B1, L1, [&](int i, int n, float u) {
+            if (i < len) dUg[i * dv + n] = u;
+            B2[n * L2 + C + i] = __float2bfloat16_rn(i < len ? u : 0.f);
+        });
+        __syncthreads();
+        // dS[kk][n] <- Gamma_C dS[kk][n] + sum_x G_x Q[x][kk] dO[x][n] - sum_x W[x][kk] dUnew[x][n]
+        const float GC = expf(gC);
+        smma(dk, dv, 2 * C, A2, L2, B2, L2, [&](int kk, int n, float acc) {
+            const float v = fmaf(GC, sdS[kk * dv + n], acc);
+            sdS[kk * dv + n] = v;
+            B1[n * L1 + C + kk] = __float2bfloat16_rn(v);
+        });
+        __syncthreads();
+    }
+    if (dh0)
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) dh0[sidx + idx] = sdS[idx];
+}
+
 // ----------------------------------------------------------------------------- backward: state products
 // Per chunk: Y = scale dO S_in^T (dQ = diag(Gamma) Y), dW = -dUnew S_in^T and
 // Kt = Unew dS_out^T (dK = diag(exp(gamma_C - gamma)) Kt); plus the row sums
@@ -852,6 +1100,23 @@ static size_t smem_bgrad(const Geo &g) { return sizeof(float) * (3 * (size_t)g.C
 
 static int slice_width(const Geo &g) { return g.dv < 64 ? g.dv : 64; }
 
+static size_t smem_scan_st(const Geo &g)
+{
+    const size_t L1 = spad(g.dk), L2 = spad(g.C);
+    return sizeof(float) * ((size_t)g.dk * g.dv + 64 + (size_t)g.C * g.dv) +
+           2 * ((g.C + g.dv) * L1 + (g.dk + g.dv) * L2);
+}
+static size_t smem_bscan_st(const Geo &g)
+{
+    const size_t L1 = spad(g.C + g.dk), L2 = spad(2 * g.C);
+    return sizeof(float) * ((size_t)g.dk * g.dv + 128) + 2 * ((g.C + g.dv) * L1 + (g.dk + g.dv) * L2);
+}
+template <class Tin>
+static bool use_staged(const Geo &g, const void *dO = nullptr)
+{
+    return std::is_same<Tin, __nv_bfloat16>::value && staged_ok(g) && ((uintptr_t)dO & 15u) == 0;
+}
+
 template <class K>
 static cudaError_t set_smem(K kernel, size_t bytes)
 {
@@ -868,6 +1133,11 @@ static cudaError_t forward_states(const Geo &g, const Tin *q, const Tin *k, cons
     if ((e = set_smem(k_prep<Tin>, smem_prep(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_prep<Tin><<<dim3(g.NC, g.H), 256, smem_prep(g), st>>>(g, q, k, v, beta, gate, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    if (use_staged<Tin>(g)) {
+        if ((e = set_smem(k_scan_st, smem_scan_st(g))) != cudaSuccess) return e;
+        if (g.N > 0) k_scan_st<<<dim3(g.N, g.H), 256, smem_scan_st(g), st>>>(g, h0, hT, w);
+        return cudaPeekAtLastError();
+    }
     const int BV = slice_width(g);
     if ((e = set_smem(k_scan<Tin>, smem_scan(g, BV))) != cudaSuccess) return e;
     if (g.N > 0)
@@ -895,11 +1165,19 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
 {
     cudaError_t e = forward_states(g, q, k, v, beta, gate, h0, nullptr, w, st);
     if (e != cudaSuccess) return e;
-    const int BV = slice_width(g);
-    if ((e = set_smem(k_bscan<Tin>, smem_bscan(g, BV))) != cudaSuccess) return e;
-    if (g.N > 0)
-        k_bscan<Tin><<<dim3(g.N, g.H, (g.dv + BV - 1) / BV), 256, smem_bscan(g, BV), st>>>(
-            g, dO, dhT, dh0, w, BV);
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (use_staged<Tin>(g, dO)) {
+            if ((e = set_smem(k_bscan_st, smem_bscan_st(g))) != cudaSuccess) return e;
+            if (g.N > 0) k_bscan_st<<<dim3(g.N, g.H), 256, smem_bscan_st(g), st>>>(g, dO, dhT, dh0, w);
+        }
+    }
+    if (!use_staged<Tin>(g, dO)) {
+        const int BV = slice_width(g);
+        if ((e = set_smem(k_bscan<Tin>, smem_bscan(g, BV))) != cudaSuccess) return e;
+        if (g.N > 0)
+            k_bscan<Tin><<<dim3(g.N, g.H, (g.dv + BV - 1) / BV), 256, smem_bscan(g, BV), st>>>(
+                g, dO, dhT, dh0, w, BV);
+    }
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
