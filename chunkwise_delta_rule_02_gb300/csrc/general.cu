@@ -457,89 +457,140 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
 
 // ----------------------------------------------------------------------------- staged scans (bf16)
 // The two sequential scans for bf16 inputs with d_k, d_v <= 128: one CTA per
-// (sequence, head) walks the chunks in order, and every chunk's operands are first
-// copied (coalesced, rounded to bf16 once) into padded shared-memory tiles, so that
-// the warp-level tensor-core products read 32-bit operand pairs straight from shared
-// memory instead of gathering single elements from the fp32 workspace.
+// (sequence, head) walks the chunks in order.  Each chunk's operands are first
+// copied into shared memory in their natural row-major layout (16-byte loads issued
+// in batches, rounded to bf16 once, rows padded by 8 elements so that 8 consecutive
+// rows fall in different bank groups), and the warp-level tensor-core products take
+// their fragments with ldmatrix (transposing on load where the reduction runs down
+// the rows).
 
-// C = A B^T on the tensor cores for M % 16 == 0, N % 32 == 0, K % 16 == 0: A is
-// [M][lda] and Bt is [N][ldb], bf16, K contiguous (lda, ldb even; lda / 2 and
-// ldb / 2 = 4 mod 32 keeps the fragment loads free of bank conflicts).  St(m, n, v)
-// receives each result once.
-template <class FS>
-__device__ __forceinline__ void smma(int M, int N, int K, const __nv_bfloat16 *A, int lda,
-                                     const __nv_bfloat16 *Bt, int ldb, FS St)
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const __nv_bfloat16 *p, bool trans)
 {
-    constexpr int NT = 4;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int ntl = N / (8 * NT);
-    for (int tile = warp; tile < (M / 16) * ntl; tile += nw) {
-        const int m0 = (tile / ntl) * 16, n0 = (tile - (tile / ntl) * ntl) * 8 * NT;
-        float acc[NT][4];
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    if (trans)
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+    else
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+// acc (the warp's 32 x 32 tile at m0, n0: two 16-row halves of four 16 x 8
+// accumulators) += A B over k in [0, K), K % 16 == 0.  A(m, k) is stored at
+// A[m * lda + k] (AT false) or A[k * lda + m] (AT true); B(k, n) at B[n * ldb + k]
+// (BT false) or B[k * ldb + n] (BT true).  lda, ldb % 8 == 0; m0, n0 % 32 == 0.
+template <bool AT, bool BT>
+__device__ __forceinline__ void tile_mma(float (&acc)[2][4][4], const __nv_bfloat16 *A, int lda,
+                                         const __nv_bfloat16 *B, int ldb, int m0, int n0, int K)
+{
+    const int lane = threadIdx.x & 31, mi = lane >> 3, r = lane & 7;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        uint32_t a[2][4], b[2][4];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        const uint32_t *a0p = reinterpret_cast<const uint32_t *>(A + (m0 + g) * lda) + t;
-        const uint32_t *a1p = reinterpret_cast<const uint32_t *>(A + (m0 + g + 8) * lda) + t;
-        for (int k0 = 0; k0 < K; k0 += 16) {
-            const int kw = k0 >> 1;
-            uint32_t a[4] = {a0p[kw], a1p[kw], a0p[kw + 4], a1p[kw + 4]};
+        for (int h = 0; h < 2; ++h) {
+            const int mh = m0 + 16 * h;
+            if (AT) ldsm4(a[h], A + (k0 + (mi >> 1) * 8 + r) * lda + mh + (mi & 1) * 8, true);
+            else ldsm4(a[h], A + (mh + (mi & 1) * 8 + r) * lda + k0 + (mi >> 1) * 8, false);
+        }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const uint32_t *bp = reinterpret_cast<const uint32_t *>(Bt + (n0 + 8 * j + g) * ldb) + t + kw;
-                uint32_t b[2] = {bp[0], bp[4]};
-                mma_bf16_16816(acc[j], a, b);
+        for (int jp = 0; jp < 2; ++jp) {
+            const int nt = 2 * jp + (mi >> 1);
+            if (BT) ldsm4(b[jp], B + (k0 + (mi & 1) * 8 + r) * ldb + n0 + 8 * nt, true);
+            else ldsm4(b[jp], B + (n0 + 8 * nt + r) * ldb + k0 + (mi & 1) * 8, false);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t bb[2] = {b[j >> 1][2 * (j & 1)], b[j >> 1][2 * (j & 1) + 1]};
+                mma_bf16_16816(acc[h][j], a[h], bb);
             }
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int m = m0 + g, n = n0 + 8 * j + 2 * t;
-            St(m, n, acc[j][0]);
-            St(m, n + 1, acc[j][1]);
-            St(m + 8, n, acc[j][2]);
-            St(m + 8, n + 1, acc[j][3]);
-        }
     }
 }
 
-// padded row length (elements) for a K-long bf16 row: K + 8 with K % 64 == 0 gives
-// a row stride of 4 mod 32 words; other K % 16 == 0 round up to that pattern
-__host__ __device__ __forceinline__ int spad(int K) { return ((K + 63) / 64) * 64 + 8; }
-
-__host__ __device__ __forceinline__ bool staged_ok(const Geo &g)
+// Runs Body(m0, n0, acc) for every 32 x 32 tile of an M x N product (M, N % 32 == 0),
+// the tiles dealt round-robin to the warps, with acc zeroed; then St(m, n, v0, v1)
+// for each pair of adjacent results (n even).  ntl_log2 = log2(N / 32).
+template <class Body, class FS>
+__device__ __forceinline__ void tiles(int M, int ntl_log2, Body body, FS St)
 {
-    return g.dk <= 128 && g.dv <= 128 && g.dk % 16 == 0 && g.dv % 32 == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int ntiles = (M / 32) << ntl_log2;
+    for (int tile = warp; tile < ntiles; tile += nw) {
+        const int m0 = (tile >> ntl_log2) * 32, n0 = (tile & ((1 << ntl_log2) - 1)) * 32;
+        float acc[2][4][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[h][j][0] = acc[h][j][1] = acc[h][j][2] = acc[h][j][3] = 0.f;
+        body(m0, n0, acc);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + 8 * j + 2 * t;
+                St(m0 + 16 * h + g, n, acc[h][j][0], acc[h][j][1]);
+                St(m0 + 16 * h + g + 8, n, acc[h][j][2], acc[h][j][3]);
+            }
+    }
 }
 
-// Copies the `rows` x `cols` fp32 row-major block at src (cols % 4 == 0, src 16-byte
+__device__ __forceinline__ int ilog2(int x) { return 31 - __clz(x); }
+
+__host__ __device__ __forceinline__ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// head dims of 32, 64 or 128 and chunks of 32 or 64: every tile is a whole number of
+// 32 x 32 warp tiles and every index split is a shift
+__host__ __device__ __forceinline__ bool staged_ok(const Geo &g)
+{
+    return pow2(g.dk) && pow2(g.dv) && g.dk >= 32 && g.dv >= 32 && g.dk <= 128 && g.dv <= 128 && g.C >= 32;
+}
+
+// Copies the rows x cols fp32 row-major block at src (cols % 4 == 0, src 16-byte
 // aligned) through registers: every thread first issues its 16-byte loads for a batch,
-// then hands each value to put(r, c, v).  Rows at or past `live` read as zero.
+// then hands each group of four to put(r, c, v).  Rows at or past `live` read as zero.
 template <class FP>
 __device__ __forceinline__ void stage_f32(const float *__restrict__ src, int rows, int cols, int live, FP put)
 {
     constexpr int VB = 8;
-    const int n4 = rows * cols / 4, c4 = cols / 4;
+    const int lc4 = ilog2(cols) - 2, n4 = (rows * cols) >> 2;   // cols: a power of two >= 4
     for (int base = threadIdx.x; base < n4; base += blockDim.x * VB) {
         float4 v[VB];
 #pragma unroll
         for (int u = 0; u < VB; ++u) {
             const int e = base + u * blockDim.x;
-            v[u] = (e < n4 && e / c4 < live) ? __ldg(reinterpret_cast<const float4 *>(src) + e)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = (e < n4 && (e >> lc4) < live) ? __ldg(reinterpret_cast<const float4 *>(src) + e)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < VB; ++u) {
             const int e = base + u * blockDim.x;
-            if (e < n4) {
-                const int r = e / c4, c = 4 * (e - r * c4);
-                put(r, c, v[u].x);
-                put(r, c + 1, v[u].y);
-                put(r, c + 2, v[u].z);
-                put(r, c + 3, v[u].w);
-            }
+            if (e < n4) put(e >> lc4, (e & ((1 << lc4) - 1)) << 2, v[u]);
         }
     }
 }
+
+// four values, scaled, as bf16 at dst (8-byte aligned)
+__device__ __forceinline__ void put_bf4(__nv_bfloat16 *dst, float4 v, float s)
+{
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(bf16x2(s * v.x, s * v.y), bf16x2(s * v.z, s * v.w));
+}
+
+__device__ __forceinline__ void put_bf2(__nv_bfloat16 *dst, float lo, float hi)
+{
+    *reinterpret_cast<uint32_t *>(dst) = bf16x2(lo, hi);
+}
+
+// brings [p, p + bytes) into L2 ahead of use (p 16-byte aligned, bytes % 16 == 0)
+__device__ __forceinline__ void l2_prefetch(const void *p, size_t bytes)
+{
+    if (bytes > 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)bytes) : "memory");
+}
+
+// row strides (elements) of the staged tiles
+__host__ __device__ __forceinline__ int spad(int cols) { return cols + 8; }
 
 // forward recompute: S_in of every chunk, and Unew = U - W S_in, S <- Gamma_C S + K~^T Unew
 __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict__ h0,
@@ -547,60 +598,82 @@ __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict_
 {
     const int s = blockIdx.x, h = blockIdx.y;
     const int C = g.C, dk = g.dk, dv = g.dv;
-    const int L1 = spad(dk), L2 = spad(C);
+    const int LS = dv + 8, LK = spad(dk), LV = spad(dv), ldv = ilog2(dv);
     int b, t0, L, j0, nch;
     seq_of(g, s, b, t0, L, j0, nch);
     extern __shared__ float sm[];
-    float *sS = sm;                                          // [dk][dv] fp32 state
-    float *sE = sS + dk * dv;                                // [C]
+    float *sS = sm;                                          // [dk][LS] fp32 state
+    float *sE = sS + dk * LS;                                // [C] exp(gamma_C - gamma_r)
     float *sU = sE + 64;                                     // [C][dv] U
-    __nv_bfloat16 *A1 = reinterpret_cast<__nv_bfloat16 *>(sU + C * dv);   // W [C][L1]
-    __nv_bfloat16 *B1 = A1 + C * L1;                         // S^T [dv][L1]
-    __nv_bfloat16 *A2 = B1 + dv * L1;                        // (diag(E) K)^T [dk][L2]
-    __nv_bfloat16 *B2 = A2 + dk * L2;                        // Unew^T [dv][L2]
+    __nv_bfloat16 *Wt = reinterpret_cast<__nv_bfloat16 *>(sU + C * dv);   // W [C][LK]
+    __nv_bfloat16 *Sb = Wt + C * LK;                         // S [dk][LV]
+    __nv_bfloat16 *EK = Sb + dk * LV;                        // diag(E) K [C][LK]
+    __nv_bfloat16 *Ub = EK + C * LK;                         // Unew [C][LV]
     const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
-    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
-        const int kk = idx / dv, n = idx - kk * dv;
-        const float v = h0 ? h0[sidx + idx] : 0.f;
-        sS[idx] = v;
-        B1[n * L1 + kk] = __float2bfloat16_rn(v);
+    for (int idx = threadIdx.x; idx < dk * dv / 2; idx += blockDim.x) {
+        const int kk = (2 * idx) >> ldv, n = (2 * idx) & (dv - 1);
+        const float v0 = h0 ? h0[sidx + 2 * idx] : 0.f, v1 = h0 ? h0[sidx + 2 * idx + 1] : 0.f;
+        *reinterpret_cast<float2 *>(sS + kk * LS + n) = make_float2(v0, v1);
+        put_bf2(Sb + kk * LV + n, v0, v1);
     }
     __syncthreads();
+    auto prefetch = [&](int c) {
+        // the chunk's workspace rows, while the chunk before it is computed
+        if (threadIdx.x == 0 && c >= 0 && c < nch) {
+            const size_t sl = (size_t)(j0 + c) * g.H + h;
+            l2_prefetch(w.W + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.Kn + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.U + sl * C * dv, sizeof(float) * C * dv);
+            l2_prefetch(w.gam + sl * C, sizeof(float) * C);
+        }
+    };
+    prefetch(0);
     for (int c = 0; c < nch; ++c) {
+        prefetch(c + 1);
         const int len = min(C, L - c * C);
         const size_t slot = (size_t)(j0 + c) * g.H + h;
         const float *gam = w.gam + slot * C;
         const float gC = gam[len - 1];
-        const float *W = w.W + slot * C * dk;
-        const float *Kn = w.Kn + slot * C * dk;
-        const float *U = w.U + slot * C * dv;
         float *Un = w.Unew + slot * C * dv;
         float *Sin = w.Sin + slot * dk * dv;
         for (int r = threadIdx.x; r < C; r += blockDim.x) sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
-        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) Sin[idx] = sS[idx];
+        for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+            const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+            reinterpret_cast<float4 *>(Sin)[idx] = *reinterpret_cast<const float4 *>(sS + kk * LS + n);
+        }
         __syncthreads();
-        stage_f32(W, C, dk, len, [&](int r, int kk, float v) { A1[r * L1 + kk] = __float2bfloat16_rn(v); });
-        stage_f32(Kn, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + r] = __float2bfloat16_rn(sE[r] * v); });
-        stage_f32(U, C, dv, len, [&](int r, int n, float v) { sU[r * dv + n] = v; });
+        stage_f32(w.W + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Wt + r * LK + kk, v, 1.f); });
+        stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
+        stage_f32(w.U + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) {
+            *reinterpret_cast<float4 *>(sU + r * dv + n) = v;
+        });
         __syncthreads();
         // Unew[r][n] = U[r][n] - sum_kk W[r][kk] S[kk][n]
-        smma(C, dv, dk, A1, L1, B1, L1, [&](int r, int n, float acc) {
-            const float u = r < len ? sU[r * dv + n] - acc : 0.f;
-            if (r < len) Un[r * dv + n] = u;
-            B2[n * L2 + r] = __float2bfloat16_rn(u);
-        });
+        tiles(C, ldv - 5, [&](int m0, int n0, float (&acc)[2][4][4]) { tile_mma<false, true>(acc, Wt, LK, Sb, LV, m0, n0, dk); },
+              [&](int r, int n, float a0, float a1) {
+                  const bool live = r < len;
+                  const float u0 = live ? sU[r * dv + n] - a0 : 0.f, u1 = live ? sU[r * dv + n + 1] - a1 : 0.f;
+                  if (live) *reinterpret_cast<float2 *>(Un + r * dv + n) = make_float2(u0, u1);
+                  put_bf2(Ub + r * LV + n, u0, u1);
+              });
         __syncthreads();
         // S[kk][n] <- Gamma_C S[kk][n] + sum_r E_r K[r][kk] Unew[r][n]
         const float GC = expf(gC);
-        smma(dk, dv, C, A2, L2, B2, L2, [&](int kk, int n, float acc) {
-            const float v = fmaf(GC, sS[kk * dv + n], acc);
-            sS[kk * dv + n] = v;
-            B1[n * L1 + kk] = __float2bfloat16_rn(v);
-        });
+        tiles(dk, ldv - 5, [&](int m0, int n0, float (&acc)[2][4][4]) { tile_mma<true, true>(acc, EK, LK, Ub, LV, m0, n0, C); },
+              [&](int kk, int n, float a0, float a1) {
+                  float2 *sp = reinterpret_cast<float2 *>(sS + kk * LS + n);
+                  const float2 o = *sp;
+                  const float v0 = fmaf(GC, o.x, a0), v1 = fmaf(GC, o.y, a1);
+                  *sp = make_float2(v0, v1);
+                  put_bf2(Sb + kk * LV + n, v0, v1);
+              });
         __syncthreads();
     }
     if (hT)
-        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) hT[sidx + idx] = sS[idx];
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+            const int kk = idx >> ldv, n = idx & (dv - 1);
+            hT[sidx + idx] = sS[kk * LS + n];
+        }
 }
 
 // backward scan: dS_out of every chunk, and
@@ -611,96 +684,125 @@ __global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__
 {
     const int s = blockIdx.x, h = blockIdx.y;
     const int C = g.C, dk = g.dk, dv = g.dv;
-    const int L1 = spad(C + dk), L2 = spad(2 * C);
+    const int LS = dv + 8, LC = spad(C), LK = spad(dk), LV = spad(dv), ldv = ilog2(dv);
     int b, t0, L, j0, nch;
     seq_of(g, s, b, t0, L, j0, nch);
     extern __shared__ float sm[];
-    float *sdS = sm;                                         // [dk][dv] fp32
-    float *sE = sdS + dk * dv;                               // [C] exp(gamma_C - gamma_r)
+    float *sdS = sm;                                         // [dk][LS] fp32
+    float *sE = sdS + dk * LS;                               // [C] exp(gamma_C - gamma_r)
     float *sG = sE + 64;                                     // [C] exp(gamma_r)
-    __nv_bfloat16 *A1 = reinterpret_cast<__nv_bfloat16 *>(sG + 64);   // [P^T | diag(E) K] [C][L1]
-    __nv_bfloat16 *B1 = A1 + C * L1;                         // [dO^T | dS^T] [dv][L1]
-    __nv_bfloat16 *A2 = B1 + dv * L1;                        // [diag(G) Q | -W]^T [dk][L2]
-    __nv_bfloat16 *B2 = A2 + dk * L2;                        // [dO^T | dUnew^T] [dv][L2]
+    __nv_bfloat16 *Ps = reinterpret_cast<__nv_bfloat16 *>(sG + 64);   // P [C][LC]
+    __nv_bfloat16 *EK = Ps + C * LC;                         // diag(E) K [C][LK]
+    __nv_bfloat16 *GQ = EK + C * LK;                         // diag(G) Q [C][LK]
+    __nv_bfloat16 *Wn = GQ + C * LK;                         // -W [C][LK]
+    __nv_bfloat16 *dOb = Wn + C * LK;                        // scale dO [C][LV]
+    __nv_bfloat16 *dUb = dOb + C * LV;                       // dUnew [C][LV]
+    __nv_bfloat16 *dSb = dUb + C * LV;                       // dS [dk][LV]
     const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
-    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
-        const int kk = idx / dv, n = idx - kk * dv;
-        const float v = dhT ? dhT[sidx + idx] : 0.f;
-        sdS[idx] = v;
-        B1[n * L1 + C + kk] = __float2bfloat16_rn(v);
+    for (int idx = threadIdx.x; idx < dk * dv / 2; idx += blockDim.x) {
+        const int kk = (2 * idx) >> ldv, n = (2 * idx) & (dv - 1);
+        const float v0 = dhT ? dhT[sidx + 2 * idx] : 0.f, v1 = dhT ? dhT[sidx + 2 * idx + 1] : 0.f;
+        *reinterpret_cast<float2 *>(sdS + kk * LS + n) = make_float2(v0, v1);
+        put_bf2(dSb + kk * LV + n, v0, v1);
     }
     __syncthreads();
+    auto prefetch = [&](int c) {
+        // the chunk's workspace rows and dO rows, while the chunk after it is computed
+        if (threadIdx.x == 0 && c >= 0 && c < nch) {
+            const size_t sl = (size_t)(j0 + c) * g.H + h;
+            const int ln = min(C, L - c * C);
+            l2_prefetch(w.P + sl * C * C, sizeof(float) * C * C);
+            l2_prefetch(w.Kn + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.Qn + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.W + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.gam + sl * C, sizeof(float) * C);
+            l2_prefetch(dO + (((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C) * dv, sizeof(__nv_bfloat16) * ln * dv);
+        }
+    };
+    prefetch(nch - 1);
     for (int c = nch - 1; c >= 0; --c) {
+        prefetch(c - 1);
         const int len = min(C, L - c * C);
         const size_t slot = (size_t)(j0 + c) * g.H + h;
         const size_t row = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
         const float *gam = w.gam + slot * C;
         const float gC = gam[len - 1];
-        const float *Qn = w.Qn + slot * C * dk;
-        const float *Kn = w.Kn + slot * C * dk;
-        const float *W = w.W + slot * C * dk;
-        const float *Pg = w.P + slot * C * C;
         float *dUg = w.dUn + slot * C * dv;
         float *dSo = w.dSo + slot * dk * dv;
         for (int r = threadIdx.x; r < C; r += blockDim.x) {
             sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
             sG[r] = r < len ? expf(gam[r]) : 0.f;
         }
-        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) dSo[idx] = sdS[idx];
+        for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+            const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+            reinterpret_cast<float4 *>(dSo)[idx] = *reinterpret_cast<const float4 *>(sdS + kk * LS + n);
+        }
         __syncthreads();
-        // P[x][i] -> A1[i][x]; columns i >= len of P are not written by the preparation,
-        // but they only reach rows i >= len of dUnew, which are dropped below
-        stage_f32(Pg, C, C, len, [&](int x, int i, float v) { A1[i * L1 + x] = __float2bfloat16_rn(v); });
-        stage_f32(Kn, C, dk, len, [&](int r, int kk, float v) { A1[r * L1 + C + kk] = __float2bfloat16_rn(sE[r] * v); });
-        stage_f32(Qn, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + r] = __float2bfloat16_rn(sG[r] * v); });
-        stage_f32(W, C, dk, len, [&](int r, int kk, float v) { A2[kk * L2 + C + r] = __float2bfloat16_rn(-v); });
+        // P's columns i >= len are not written by the preparation; they only reach rows
+        // i >= len of dUnew, which are dropped below
+        stage_f32(w.P + slot * C * C, C, C, len, [&](int x, int i, float4 v) { put_bf4(Ps + x * LC + i, v, 1.f); });
+        stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
+        stage_f32(w.Qn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(GQ + r * LK + kk, v, sG[r]); });
+        stage_f32(w.W + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Wn + r * LK + kk, v, -1.f); });
         {
-            // scale dO -> both B tiles, 8 bf16 per 16-byte load
-            const int n8 = C * dv / 8, c8 = dv / 8;
+            // scale dO, 8 bf16 per 16-byte load
+            const int n8 = (C * dv) >> 3, lc8 = ldv - 3;
             for (int base = threadIdx.x; base < n8; base += blockDim.x * 4) {
                 uint4 v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int e = base + u * blockDim.x;
-                    v[u] = (e < n8 && e / c8 < len) ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e)
+                    v[u] = (e < n8 && (e >> lc8) < len) ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e)
                                                     : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int e = base + u * blockDim.x;
                     if (e >= n8) continue;
-                    const int r = e / c8, n = 8 * (e - r * c8);
+                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
                     const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    uint32_t o[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(g.scale * __uint_as_float(wv[q] << 16));
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
-                        B1[(n + 2 * q) * L1 + r] = lo;
-                        B1[(n + 2 * q + 1) * L1 + r] = hi;
-                        B2[(n + 2 * q) * L2 + r] = lo;
-                        B2[(n + 2 * q + 1) * L2 + r] = hi;
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        o[q] = bf16x2(g.scale * __uint_as_float(wv[q] << 16), g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
+                    *reinterpret_cast<uint4 *>(dOb + r * LV + n) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
         }
         __syncthreads();
         // dUnew[i][n] = sum_x P[x][i] dO[x][n] + E_i sum_kk K[i][kk] dS[kk][n]
-        smma(C, dv, C + dk, A1, L1, B1, L1, [&](int i, int n, float u) {
-            if (i < len) dUg[i * dv + n] = u;
-            B2[n * L2 + C + i] = __float2bfloat16_rn(i < len ? u : 0.f);
-        });
+        tiles(C, ldv - 5,
+              [&](int m0, int n0, float (&acc)[2][4][4]) {
+                  tile_mma<true, true>(acc, Ps, LC, dOb, LV, m0, n0, C);
+                  tile_mma<false, true>(acc, EK, LK, dSb, LV, m0, n0, dk);
+              },
+              [&](int i, int n, float u0, float u1) {
+                  const bool live = i < len;
+                  if (live) *reinterpret_cast<float2 *>(dUg + i * dv + n) = make_float2(u0, u1);
+                  put_bf2(dUb + i * LV + n, live ? u0 : 0.f, live ? u1 : 0.f);
+              });
         __syncthreads();
         // dS[kk][n] <- Gamma_C dS[kk][n] + sum_x G_x Q[x][kk] dO[x][n] - sum_x W[x][kk] dUnew[x][n]
         const float GC = expf(gC);
-        smma(dk, dv, 2 * C, A2, L2, B2, L2, [&](int kk, int n, float acc) {
-            const float v = fmaf(GC, sdS[kk * dv + n], acc);
-            sdS[kk * dv + n] = v;
-            B1[n * L1 + C + kk] = __float2bfloat16_rn(v);
-        });
+        tiles(dk, ldv - 5,
+              [&](int m0, int n0, float (&acc)[2][4][4]) {
+                  tile_mma<true, true>(acc, GQ, LK, dOb, LV, m0, n0, C);
+                  tile_mma<true, true>(acc, Wn, LK, dUb, LV, m0, n0, C);
+              },
+              [&](int kk, int n, float a0, float a1) {
+                  float2 *sp = reinterpret_cast<float2 *>(sdS + kk * LS + n);
+                  const float2 o = *sp;
+                  const float v0 = fmaf(GC, o.x, a0), v1 = fmaf(GC, o.y, a1);
+                  *sp = make_float2(v0, v1);
+                  put_bf2(dSb + kk * LV + n, v0, v1);
+              });
         __syncthreads();
     }
     if (dh0)
-        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) dh0[sidx + idx] = sdS[idx];
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+            const int kk = idx >> ldv, n = idx & (dv - 1);
+            dh0[sidx + idx] = sdS[kk * LS + n];
+        }
 }
 
 // ----------------------------------------------------------------------------- backward: state products
@@ -1102,14 +1204,15 @@ static int slice_width(const Geo &g) { return g.dv < 64 ? g.dv : 64; }
 
 static size_t smem_scan_st(const Geo &g)
 {
-    const size_t L1 = spad(g.dk), L2 = spad(g.C);
-    return sizeof(float) * ((size_t)g.dk * g.dv + 64 + (size_t)g.C * g.dv) +
-           2 * ((g.C + g.dv) * L1 + (g.dk + g.dv) * L2);
+    const size_t LS = g.dv + 8, LK = spad(g.dk), LV = spad(g.dv);
+    return sizeof(float) * ((size_t)g.dk * LS + 64 + (size_t)g.C * g.dv) +
+           2 * (2 * g.C * LK + (size_t)(g.dk + g.C) * LV);
 }
 static size_t smem_bscan_st(const Geo &g)
 {
-    const size_t L1 = spad(g.C + g.dk), L2 = spad(2 * g.C);
-    return sizeof(float) * ((size_t)g.dk * g.dv + 128) + 2 * ((g.C + g.dv) * L1 + (g.dk + g.dv) * L2);
+    const size_t LS = g.dv + 8, LC = spad(g.C), LK = spad(g.dk), LV = spad(g.dv);
+    return sizeof(float) * ((size_t)g.dk * LS + 128) +
+           2 * (g.C * LC + 3 * g.C * LK + (size_t)(2 * g.C + g.dk) * LV);
 }
 template <class Tin>
 static bool use_staged(const Geo &g, const void *dO = nullptr)
