@@ -897,6 +897,155 @@ __global__ void __launch_bounds__(512) k_bbig(Geo g, const Tin *__restrict__ dO,
     if (threadIdx.x == 0) aux[2 * C] = sred[0];
 }
 
+// The same three state products for bf16 inputs on the staged layout (the shapes of
+// staged_ok): dO, dUnew, Unew and both states rounded to bf16 into row-major tiles,
+// Q and K kept in fp32 for the row sums, <dS_out, S_in> accumulated in fp32 while
+// the states are loaded.  512 threads; the 3 (C / 32)(d_k / 32) warp tiles of the
+// three products are dealt round-robin to the warps.
+__global__ void __launch_bounds__(512) k_bbig_st(Geo g, const __nv_bfloat16 *__restrict__ dO, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int LV = spad(dv), LQ = dk + 4, ldv = ilog2(dv), ldk = ilog2(dk);
+    extern __shared__ float sm[];
+    float *sE = sm;                 // [C] exp(gamma_C - gamma_r)
+    float *sG = sE + 64;            // [C] exp(gamma_r)
+    float *sqt = sG + 64;           // [C] <Q_r, Y_r>
+    float *set = sqt + 64;          // [C] <Kt_r, K_r>
+    float *sred = set + 64;         // [4] <dS_out, S_in>
+    float *Qs = sred + 4;           // [C][LQ] fp32
+    float *Ks = Qs + C * LQ;        // [C][LQ] fp32
+    __nv_bfloat16 *dOs = reinterpret_cast<__nv_bfloat16 *>(Ks + C * LQ);   // scale dO [C][LV]
+    __nv_bfloat16 *dUs = dOs + C * LV;                       // dUnew [C][LV]
+    __nv_bfloat16 *Us = dUs + C * LV;                        // Unew [C][LV]
+    __nv_bfloat16 *Ss = Us + C * LV;                         // S_in [dk][LV]
+    __nv_bfloat16 *dSs = Ss + dk * LV;                       // dS_out [dk][LV]
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const float *gam = w.gam + slot * C;
+    const float gC = gam[len - 1], sc = g.scale;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int r = threadIdx.x; r < C; r += blockDim.x) {
+        sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
+        sG[r] = r < len ? expf(gam[r]) : 0.f;
+        sqt[r] = 0.f;
+        set[r] = 0.f;
+    }
+    if (threadIdx.x == 0) sred[0] = 0.f;
+    stage_f32(w.Qn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Qs + r * LQ + kk) = v; });
+    stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Ks + r * LQ + kk) = v; });
+    stage_f32(w.dUn + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) { put_bf4(dUs + r * LV + n, v, 1.f); });
+    stage_f32(w.Unew + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) { put_bf4(Us + r * LV + n, v, 1.f); });
+    {
+        // both states, and <dS_out, S_in> in fp32 on the way
+        const float4 *S4 = reinterpret_cast<const float4 *>(w.Sin + slot * dk * dv);
+        const float4 *D4 = reinterpret_cast<const float4 *>(w.dSo + slot * dk * dv);
+        const int n4 = (dk * dv) >> 2, lc4 = ldv - 2;
+        float p = 0.f;
+        for (int base = threadIdx.x; base < n4; base += blockDim.x * 4) {
+            float4 a[4], d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * blockDim.x;
+                a[u] = e < n4 ? __ldg(S4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                d[u] = e < n4 ? __ldg(D4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = base + u * blockDim.x;
+                if (e >= n4) continue;
+                p = fmaf(a[u].x, d[u].x, fmaf(a[u].y, d[u].y, fmaf(a[u].z, d[u].z, fmaf(a[u].w, d[u].w, p))));
+                const int kk = e >> lc4, n = (e & ((1 << lc4) - 1)) << 2;
+                put_bf4(Ss + kk * LV + n, a[u], 1.f);
+                put_bf4(dSs + kk * LV + n, d[u], 1.f);
+            }
+        }
+        p = warp_sum(p);
+        __syncthreads();   // sred cleared
+        if (lane == 0) atomicAdd(sred, p);
+    }
+    {
+        // scale dO, 8 bf16 per 16-byte load
+        const int n8 = (C * dv) >> 3, lc8 = ldv - 3;
+        for (int base = threadIdx.x; base < n8; base += blockDim.x * 2) {
+            uint4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = base + u * blockDim.x;
+                v[u] = (e < n8 && (e >> lc8) < len) ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = base + u * blockDim.x;
+                if (e >= n8) continue;
+                const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
+                const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    o[q] = bf16x2(sc * __uint_as_float(wv[q] << 16), sc * __uint_as_float(wv[q] & 0xFFFF0000u));
+                *reinterpret_cast<uint4 *>(dOs + r * LV + n) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+    __syncthreads();
+    float *dQ = w.dQ + slot * C * dk;
+    float *dK = w.dK + slot * C * dk;
+    float *dW = w.dW + slot * C * dk;
+    const int gq = lane >> 2, t = lane & 3;
+    const int ltn = ldk - 5, per = (C / 32) << ltn;   // warp tiles per product
+    for (int tile = warp; tile < 3 * per; tile += nw) {
+        const int prod = tile / per, tl = tile - prod * per;
+        const int m0 = (tl >> ltn) * 32, n0 = (tl & ((1 << ltn) - 1)) * 32;
+        float acc[2][4][4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[hh][jj][0] = acc[hh][jj][1] = acc[hh][jj][2] = acc[hh][jj][3] = 0.f;
+        // Y = dO S_in^T, Z = dUnew S_in^T, X = Unew dS_out^T (rows r, columns kk, sum over n)
+        const __nv_bfloat16 *A = prod == 0 ? dOs : (prod == 1 ? dUs : Us);
+        const __nv_bfloat16 *B = prod == 2 ? dSs : Ss;
+        tile_mma<false, false>(acc, A, LV, B, LV, m0, n0, dv);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = m0 + 16 * hh + gq + 8 * half;
+                const bool live = r < len;
+                float rs = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int kk = n0 + 8 * jj + 2 * t;
+                    const float v0 = acc[hh][jj][2 * half], v1 = acc[hh][jj][2 * half + 1];
+                    if (prod == 0) {
+                        if (live) *reinterpret_cast<float2 *>(dQ + r * dk + kk) = make_float2(sG[r] * v0, sG[r] * v1);
+                        rs = fmaf(Qs[r * LQ + kk], v0, fmaf(Qs[r * LQ + kk + 1], v1, rs));
+                    } else if (prod == 1) {
+                        if (live) *reinterpret_cast<float2 *>(dW + r * dk + kk) = make_float2(-v0, -v1);
+                    } else {
+                        if (live) *reinterpret_cast<float2 *>(dK + r * dk + kk) = make_float2(sE[r] * v0, sE[r] * v1);
+                        rs = fmaf(Ks[r * LQ + kk], v0, fmaf(Ks[r * LQ + kk + 1], v1, rs));
+                    }
+                }
+                if (prod != 1) {
+                    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+                    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+                    if (t == 0 && live) atomicAdd(prod == 0 ? &sqt[r] : &set[r], rs);
+                }
+            }
+    }
+    __syncthreads();
+    float *aux = w.aux + slot * (4 * C + 4);
+    for (int r = threadIdx.x; r < len; r += blockDim.x) {
+        aux[r] = sqt[r];
+        aux[C + r] = set[r];
+    }
+    if (threadIdx.x == 0) aux[2 * C] = sred[0];
+}
+
 // ----------------------------------------------------------------------------- backward per chunk
 // Two kernels per chunk.  k_bchunk: K K^T, dP, the solve (I + A)^-1 and its
 // adjoint, dT, and the gate / beta terms that need the C x C matrices; it hands
@@ -1208,6 +1357,11 @@ static size_t smem_scan_st(const Geo &g)
     return sizeof(float) * ((size_t)g.dk * LS + 64 + (size_t)g.C * g.dv) +
            2 * (2 * g.C * LK + (size_t)(g.dk + g.C) * LV);
 }
+static size_t smem_bbig_st(const Geo &g)
+{
+    const size_t LV = spad(g.dv), LQ = g.dk + 4;
+    return sizeof(float) * (4 * 64 + 4 + 2 * (size_t)g.C * LQ) + 2 * (3 * g.C + 2 * (size_t)g.dk) * LV;
+}
 static size_t smem_bscan_st(const Geo &g)
 {
     const size_t LS = g.dv + 8, LC = spad(g.C), LK = spad(g.dk), LV = spad(g.dv);
@@ -1282,8 +1436,16 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
                 g, dO, dhT, dh0, w, BV);
     }
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
-    if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
-    if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (use_staged<Tin>(g, dO)) {
+            if ((e = set_smem(k_bbig_st, smem_bbig_st(g))) != cudaSuccess) return e;
+            if (g.NC > 0) k_bbig_st<<<dim3(g.NC, g.H), 512, smem_bbig_st(g), st>>>(g, dO, w);
+        }
+    }
+    if (!use_staged<Tin>(g, dO)) {
+        if ((e = set_smem(k_bbig<Tin>, smem_bbig(g))) != cudaSuccess) return e;
+        if (g.NC > 0) k_bbig<Tin><<<dim3(g.NC, g.H), 512, smem_bbig(g), st>>>(g, dO, w);
+    }
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if ((e = set_smem(k_bchunk<Tin>, smem_bchunk<Tin>(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk<Tin>(g), st>>>(g, v, dO, w);
