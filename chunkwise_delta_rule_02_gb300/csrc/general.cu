@@ -1327,6 +1327,229 @@ __global__ void __launch_bounds__(256, 3) k_bgrad(Geo g, const Tin *__restrict__
     }
 }
 
+// k_bgrad for bf16 inputs on the staged layout (the shapes of staged_ok): K, Q, dW,
+// dUnew and the three C x C matrices from k_bchunk rounded to bf16 into row-major
+// tiles (entries past the chunk masked to zero), the products on ldmatrix fragments.
+// Warp w owns one 32 x 32 tile of dQ and dK (and of dV) and chains the products
+// through its registers; the normalisation chain rule then runs per row as in k_bgrad.
+__global__ void __launch_bounds__(256, 2) k_bgrad_st(Geo g, const __nv_bfloat16 *__restrict__ q,
+                                                    const __nv_bfloat16 *__restrict__ k,
+                                                    __nv_bfloat16 *__restrict__ dq,
+                                                    __nv_bfloat16 *__restrict__ dkout,
+                                                    __nv_bfloat16 *__restrict__ dvout,
+                                                    __nv_bfloat16 *__restrict__ dbeta,
+                                                    float *__restrict__ dg, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int LK = spad(dk), LV = spad(dv), LC = spad(C);
+    extern __shared__ float sm[];
+    float *sb = sm;                 // [C] step sizes
+    float *sG = sb + 64;            // [C] exp(gamma)
+    float *sdg = sG + 64;           // [C] d gamma
+    float *sdb = sdg + 64;          // [C] d beta
+    float *se = sdb + 64;           // [C] e_r (K~ gate term)
+    float *sk2 = se + 64;           // [C] <dGK_r, K_r>
+    __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(sk2 + 64);   // K [C][LK]
+    __nv_bfloat16 *Qb = Kb + C * LK;                         // Q [C][LK]
+    __nv_bfloat16 *dWb = Qb + C * LK;                        // dW [C][LK]
+    __nv_bfloat16 *dUb = dWb + C * LK;                       // dUnew [C][LV] (first the fp32 dKK)
+    const int dub = C * LV > 2 * C * C ? C * LV : 2 * C * C; // elements: room for either
+    __nv_bfloat16 *DPb = dUb + dub;                          // dP o D [C][LC]
+    __nv_bfloat16 *Lib = DPb + C * LC;                       // (I + A)^-1 [C][LC]
+    __nv_bfloat16 *YYb = Lib + C * LC;                       // dKK + dKK^T [C][LC]
+    float *Yf = reinterpret_cast<float *>(dUb);              // dKK fp32 [C][C], before dUnew is staged
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const float *Qn = w.Qn + slot * C * dk;
+    const float *Kn = w.Kn + slot * C * dk;
+    const float *aux = w.aux + slot * (4 * C + 4);
+    const float *M3 = w.M3 + slot * 3 * C * C;
+    float *dQ = w.dQ + slot * C * dk;
+    float *dK = w.dK + slot * C * dk;
+    const float *gam = w.gam + slot * C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const float gC = gam[len - 1];
+    const int lC = ilog2(C);
+
+    for (int r = threadIdx.x; r < C; r += blockDim.x) {
+        const bool live = r < len;
+        sb[r] = live ? w.eb[slot * C + r] : 0.f;
+        sG[r] = live ? expf(gam[r]) : 0.f;
+        se[r] = live ? expf(gC - gam[r]) * aux[C + r] : 0.f;
+        sdg[r] = live ? aux[2 * C + 4 + r] : 0.f;
+        sdb[r] = live ? aux[3 * C + 4 + r] : 0.f;
+        sk2[r] = 0.f;
+    }
+    stage_f32(Kn, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Kb + r * LK + kk, v, 1.f); });
+    stage_f32(Qn, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Qb + r * LK + kk, v, 1.f); });
+    stage_f32(w.dW + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(dWb + r * LK + kk, v, 1.f); });
+    // the C x C matrices, entries with r or i past the chunk set to zero
+    auto mask4 = [&](int i, float4 v) {
+        return make_float4(i < len ? v.x : 0.f, i + 1 < len ? v.y : 0.f, i + 2 < len ? v.z : 0.f, i + 3 < len ? v.w : 0.f);
+    };
+    stage_f32(M3, C, C, len, [&](int r, int i, float4 v) { put_bf4(DPb + r * LC + i, mask4(i, v), 1.f); });
+    stage_f32(M3 + C * C, C, C, len, [&](int r, int i, float4 v) { put_bf4(Lib + r * LC + i, mask4(i, v), 1.f); });
+    stage_f32(M3 + 2 * C * C, C, C, len, [&](int r, int i, float4 v) {
+        *reinterpret_cast<float4 *>(Yf + r * C + i) = mask4(i, v);
+    });
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < C * C / 2; idx += blockDim.x) {
+        const int r = (2 * idx) >> lC, i = (2 * idx) & (C - 1);
+        put_bf2(YYb + r * LC + i, Yf[r * C + i] + Yf[i * C + r], Yf[r * C + i + 1] + Yf[(i + 1) * C + r]);
+    }
+    __syncthreads();
+    stage_f32(w.dUn + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) { put_bf4(dUb + r * LV + n, v, 1.f); });
+    __syncthreads();
+
+    const int gq = lane >> 2, t = lane & 3;
+    auto zero = [&](float (&a)[2][4][4]) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) a[hh][jj][0] = a[hh][jj][1] = a[hh][jj][2] = a[hh][jj][3] = 0.f;
+    };
+    // (row, column) of element e (0..3) of accumulator [hh][jj] in the tile at (m0, n0)
+    auto rc = [&](int m0, int n0, int hh, int jj, int e, int &r, int &c) {
+        r = m0 + 16 * hh + gq + 8 * (e >> 1);
+        c = n0 + 8 * jj + 2 * t + (e & 1);
+    };
+    const int ltk = ilog2(dk) - 5, ntk = (C / 32) << ltk;
+    if (warp < ntk) {
+        const int m0 = (warp >> ltk) * 32, n0 = (warp & ((1 << ltk) - 1)) * 32;
+        float acc[2][4][4];
+        // dQ += (dP o D) K
+        zero(acc);
+        tile_mma<false, true>(acc, DPb, LC, Kb, LK, m0, n0, C);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int r, c;
+                    rc(m0, n0, hh, jj, e, r, c);
+                    if (r < len) {
+                        float2 *p = reinterpret_cast<float2 *>(dQ + r * dk + c);
+                        const float2 o = *p;
+                        *p = make_float2(o.x + acc[hh][jj][e], o.y + acc[hh][jj][e + 1]);
+                    }
+                }
+        // dGK = T^T dW (T = Linv diag(beta)): d gamma gets G_r <beta_r dGK_r, K_r>, and
+        // dK starts from G_r beta_r dGK
+        zero(acc);
+        tile_mma<true, true>(acc, Lib, LC, dWb, LK, m0, n0, C);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = m0 + 16 * hh + gq + 8 * half;
+                float rs = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int c = n0 + 8 * jj + 2 * t;
+                    float &a0 = acc[hh][jj][2 * half], &a1 = acc[hh][jj][2 * half + 1];
+                    a0 *= sb[r];
+                    a1 *= sb[r];
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(Kb + r * LK + c);
+                    rs = fmaf(a0, __uint_as_float(kw << 16), fmaf(a1, __uint_as_float(kw & 0xFFFF0000u), rs));
+                    a0 *= sG[r];
+                    a1 *= sG[r];
+                }
+                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+                if (t == 0 && r < len) atomicAdd(&sk2[r], rs);
+            }
+        // dK += (dP o D)^T Q + (dKK + dKK^T) K, on top of G beta dGK
+        tile_mma<true, true>(acc, DPb, LC, Qb, LK, m0, n0, C);
+        tile_mma<false, true>(acc, YYb, LC, Kb, LK, m0, n0, C);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int r, c;
+                    rc(m0, n0, hh, jj, e, r, c);
+                    if (r < len) {
+                        float2 *p = reinterpret_cast<float2 *>(dK + r * dk + c);
+                        const float2 o = *p;
+                        *p = make_float2(o.x + acc[hh][jj][e], o.y + acc[hh][jj][e + 1]);
+                    }
+                }
+    }
+    const int ltv = ilog2(dv) - 5, ntv = (C / 32) << ltv;
+    for (int tile = warp; tile < ntv; tile += nw) {
+        // dV = T^T dUnew
+        const int m0 = (tile >> ltv) * 32, n0 = (tile & ((1 << ltv) - 1)) * 32;
+        float acc[2][4][4];
+        zero(acc);
+        tile_mma<true, true>(acc, Lib, LC, dUb, LV, m0, n0, C);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, c;
+                    rc(m0, n0, hh, jj, e, r, c);
+                    if (r < len) st_out(dvout + (row + r) * dv + c, sb[r] * acc[hh][jj][e]);
+                }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float es = 0.f;
+        for (int r = 0; r < len; ++r) {
+            sdg[r] += sG[r] * sk2[r] - se[r];
+            es += se[r];
+        }
+        sdg[len - 1] += es + expf(gC) * aux[2 * C];
+        // d g = reverse cumulative sum of d gamma within the chunk
+        float acc = 0.f;
+        for (int r = len - 1; r >= 0; --r) {
+            acc += sdg[r];
+            if (dg) dg[row + r] = acc;
+        }
+    }
+    // the normalisation chain rule for dq, dk
+    for (int r = warp; r < len; r += nw) {
+        const __nv_bfloat16 *qr = q + (row + r) * dk;
+        const __nv_bfloat16 *kr = k + (row + r) * dk;
+        float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
+        for (int kk = lane; kk < dk; kk += 32) {
+            float x = ld_in(qr + kk), y = ld_in(kr + kk);
+            sq = fmaf(x, x, sq);
+            sk = fmaf(y, y, sk);
+            pq = fmaf(Qn[r * dk + kk], dQ[r * dk + kk], pq);
+            pk = fmaf(Kn[r * dk + kk], dK[r * dk + kk], pk);
+        }
+        sq = warp_sum(sq); sk = warp_sum(sk); pq = warp_sum(pq); pk = warp_sum(pk);
+        float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
+        float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
+        // sdb holds d/d(step size).  Longhorn's step e = b / (1 + b kap), kap = k^T k:
+        // de/db = (1 - e kap)^2 and de/dkap = -e^2, with d kap / dk = 2 k
+        float db = sdb[r], dkap = 0.f;
+        if (g.longhorn) {
+            const float kap = sk * rk * rk, e = sb[r], f = fmaf(-e, kap, 1.f);
+            dkap = -db * e * e;
+            db *= f * f;
+            pk = fmaf(2.f * dkap, kap, pk);
+        }
+        for (int kk = lane; kk < dk; kk += 32) {
+            float a = dQ[r * dk + kk], c = fmaf(2.f * dkap, Kn[r * dk + kk], dK[r * dk + kk]);
+            if (g.l2norm) {
+                a = rq * (a - Qn[r * dk + kk] * pq);
+                c = rk * (c - Kn[r * dk + kk] * pk);
+            }
+            st_out(dq + (row + r) * dk + kk, a);
+            st_out(dkout + (row + r) * dk + kk, c);
+        }
+        if (lane == 0) st_out(dbeta + row + r, db);
+    }
+}
+
 // ----------------------------------------------------------------------------- host launchers
 static size_t smem_prep(const Geo &g)
 {
@@ -1361,6 +1584,12 @@ static size_t smem_bbig_st(const Geo &g)
 {
     const size_t LV = spad(g.dv), LQ = g.dk + 4;
     return sizeof(float) * (4 * 64 + 4 + 2 * (size_t)g.C * LQ) + 2 * (3 * g.C + 2 * (size_t)g.dk) * LV;
+}
+static size_t smem_bgrad_st(const Geo &g)
+{
+    const size_t LK = spad(g.dk), LV = spad(g.dv), LC = spad(g.C);
+    const size_t dub = (size_t)g.C * LV * 2 > (size_t)g.C * g.C * 4 ? (size_t)g.C * LV * 2 : (size_t)g.C * g.C * 4;
+    return sizeof(float) * 6 * 64 + 2 * (3 * (size_t)g.C * LK + 3 * (size_t)g.C * LC) + dub;
 }
 static size_t smem_bscan_st(const Geo &g)
 {
@@ -1450,6 +1679,14 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     if ((e = set_smem(k_bchunk<Tin>, smem_bchunk<Tin>(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_bchunk<Tin><<<dim3(g.NC, g.H), 256, smem_bchunk<Tin>(g), st>>>(g, v, dO, w);
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (use_staged<Tin>(g, dO)) {
+            if ((e = set_smem(k_bgrad_st, smem_bgrad_st(g))) != cudaSuccess) return e;
+            if (g.NC > 0)
+                k_bgrad_st<<<dim3(g.NC, g.H), 256, smem_bgrad_st(g), st>>>(g, q, k, dq, dk, dv, dbeta, dg, w);
+            return cudaPeekAtLastError();
+        }
+    }
     if ((e = set_smem(k_bgrad<Tin>, smem_bgrad(g))) != cudaSuccess) return e;
     if (g.NC > 0)
         k_bgrad<Tin><<<dim3(g.NC, g.H), 256, smem_bgrad(g), st>>>(g, q, k, dq, dk, dv, dbeta, dg, w);
