@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "general.h"
+#include "prep_math.cuh"
 
 namespace gdn {
 namespace gen {
@@ -286,7 +287,27 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
                 [&](int kk, int n) { return sK[n * LK + kk]; },
                 [&](int m, int n, float s) { Pg[m * C + n] = (n <= m) ? s * expf(sg[m] - sg[n]) : 0.f; });
     __syncthreads();
-    unit_lower_solve(sA, sT, sb, len, LC);   // T = (I + A)^-1 diag(beta)
+    // T = (I + A)^-1 diag(beta)
+    bool solved = false;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (C == 64) {
+            // blocked solve (16 x 16 diagonal blocks by substitution, the rest on the
+            // tensor cores in tf32) over the full 64 x 64, so A is zero outside the chunk
+            for (int idx = threadIdx.x; idx < 64 * 64; idx += blockDim.x) {
+                const int r = idx >> 6, c = idx & 63;
+                if (r >= len || c >= len) sA[r * 65 + c] = 0.f;
+            }
+            __syncthreads();
+            if (warp < 4) prep::solve_unit_lower_64<65>(sA, sT, lane, warp, 1);
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < 64 * 64; idx += blockDim.x) {
+                const int r = idx >> 6, c = idx & 63;
+                sT[r * 65 + c] = (c <= r && c < len) ? sT[r * 65 + c] * sb[c] : 0.f;
+            }
+            solved = true;
+        }
+    }
+    if (!solved) unit_lower_solve(sA, sT, sb, len, LC);
     for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
         int r = idx / dv, c = idx - r * dv;
         sQ[r * dv + c] = ld_in(v + (row + r) * dv + c);
