@@ -1153,7 +1153,25 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
         sY[r * LC + i] = (i < r) ? sb[r] * sKK[r * LC + i] * expf(sg[r] - sg[i]) : 0.f;
     }
     __syncthreads();
-    unit_lower_solve(sY, sLi, nullptr, len, LC);
+    bool solved = false;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (C == 64) {
+            // blocked solve over the full 64 x 64 (A zero outside the chunk), as in k_prep
+            for (int idx = threadIdx.x; idx < 64 * 64; idx += blockDim.x) {
+                const int r = idx >> 6, c = idx & 63;
+                if (r >= len || c >= len) sY[r * 65 + c] = 0.f;
+            }
+            __syncthreads();
+            if (warp < 4) prep::solve_unit_lower_64<65>(sY, sLi, lane, warp, 1);
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < 64 * 64; idx += blockDim.x) {
+                const int r = idx >> 6, c = idx & 63;
+                if (c > r) sLi[r * 65 + c] = 0.f;
+            }
+            solved = true;
+        }
+    }
+    if (!solved) unit_lower_solve(sY, sLi, nullptr, len, LC);
     if (kStage) {
         for (int idx = threadIdx.x; idx < len * dv; idx += blockDim.x) {
             int r = idx / dv, c = idx - r * dv;
