@@ -559,6 +559,14 @@ __device__ __forceinline__ void tiles(int M, int ntl_log2, Body body, FS St)
 
 __device__ __forceinline__ int ilog2(int x) { return 31 - __clz(x); }
 
+// floats of padding after k_bchunk's last C x C buffer so that its last two buffers
+// can hold two staged bf16 tiles of C rows of max(dk, dv) + 8 elements
+__host__ __device__ __forceinline__ int bchunk_pad(int C, int dk, int dv)
+{
+    const int need = C * ((dk > dv ? dk : dv) + 8), have = 2 * C * (C + 1);
+    return need > have ? ((need - have + 3) & ~3) : 0;
+}
+
 __host__ __device__ __forceinline__ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // head dims of 32, 64 or 128 and chunks of 32 or 64: every tile is a whole number of
@@ -1089,10 +1097,14 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
     float *sKK = sm;                // K K^T
     float *sdP = sKK + C * LC;      // lower(dO Unew^T)
     float *sDP = sdP + C * LC;      // dP o D, later X = Linv^T dT diag(beta)
-    float *sLi = sDP + C * LC;      // (I + A)^-1
-    float *sdT = sLi + C * LC;      // dT
-    float *sY = sdT + C * LC;       // A, then dA, then dKK
-    float *sb = sY + C * LC;        // step sizes
+    float *sdT = sDP + C * LC;      // dT
+    float *sLi = sdT + C * LC;      // (I + A)^-1
+    float *sY = sLi + C * LC;       // A, then dA, then dKK
+    // bf16 path: before the solve, sLi, sY and a pad hold two staged operand tiles
+    __nv_bfloat16 *Ta = reinterpret_cast<__nv_bfloat16 *>(sLi);
+    const int LT = spad(dk > dv ? dk : dv);
+    __nv_bfloat16 *Tb = Ta + C * LT;
+    float *sb = sY + C * LC + bchunk_pad(C, dk, dv);   // step sizes
     float *sg = sb + C;             // gamma
     float *sG = sg + C;             // exp(gamma)
     float *sdg = sG + C;            // d gamma (partial)
@@ -1127,6 +1139,100 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
     __syncthreads();
     auto Dm = [&](int r, int i) { return i <= r ? expf(sg[r] - sg[i]) : 0.f; };
     auto Kt = [&](int kk, int i) { return kStage ? sS[i * LS + kk] : Kn[i * dk + kk]; };
+    bool staged = false;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        staged = staged_ok(g) && (((uintptr_t)dO | (uintptr_t)v) & 15u) == 0;
+        if (staged) {
+            // the four C x C products on staged bf16 tiles, two tiles at a time
+            const int ltc = ilog2(C) - 5, nt = 1 << (2 * ltc);   // warp tiles per C x C product
+            auto each = [&](int nprod, auto prod) {
+                for (int tile = warp; tile < nprod * nt; tile += nw) {
+                    const int p = tile >> (2 * ltc), tl = tile & (nt - 1);
+                    const int m0 = (tl >> ltc) * 32, n0 = (tl & ((1 << ltc) - 1)) * 32;
+                    float acc[2][4][4];
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) acc[hh][jj][0] = acc[hh][jj][1] = acc[hh][jj][2] = acc[hh][jj][3] = 0.f;
+                    prod(p, m0, n0, acc);
+                }
+            };
+            // element (r, i) of accumulator [hh][jj][e] in the tile at (m0, n0)
+            auto at = [&](int m0, int n0, int hh, int jj, int e, int &r, int &i) {
+                r = m0 + 16 * hh + (lane >> 2) + 8 * (e >> 1);
+                i = n0 + 8 * jj + 2 * (lane & 3) + (e & 1);
+            };
+            // K K^T and dT = dW (diag(Gamma) K)^T
+            const int LKt = spad(dk), LVt = spad(dv);
+            stage_f32(Kn, C, dk, len, [&](int r, int kk, float4 x) { put_bf4(Ta + r * LKt + kk, x, 1.f); });
+            stage_f32(dW, C, dk, len, [&](int r, int kk, float4 x) { put_bf4(Tb + r * LKt + kk, x, 1.f); });
+            __syncthreads();
+            each(2, [&](int p, int m0, int n0, float (&acc)[2][4][4]) {
+                tile_mma<false, false>(acc, p ? Tb : Ta, LKt, Ta, LKt, m0, n0, dk);
+                for (int hh = 0; hh < 2; ++hh)
+                    for (int jj = 0; jj < 4; ++jj)
+                        for (int e = 0; e < 4; ++e) {
+                            int r, i;
+                            at(m0, n0, hh, jj, e, r, i);
+                            if (p == 0) sKK[r * LC + i] = acc[hh][jj][e];
+                            else sdT[r * LC + i] = i < len ? sG[i] * acc[hh][jj][e] : 0.f;
+                        }
+            });
+            __syncthreads();
+            // dP = lower(scale dO Unew^T)
+            {
+                const int n8 = (C * dv) >> 3, lc8 = ilog2(dv) - 3;
+                for (int e = threadIdx.x; e < n8; e += blockDim.x) {
+                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
+                    uint4 x = r < len ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o[q] = bf16x2(sc * __uint_as_float(wv[q] << 16), sc * __uint_as_float(wv[q] & 0xFFFF0000u));
+                    *reinterpret_cast<uint4 *>(Ta + r * LVt + n) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            stage_f32(Un, C, dv, len, [&](int r, int n, float4 x) { put_bf4(Tb + r * LVt + n, x, 1.f); });
+            __syncthreads();
+            each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
+                tile_mma<false, false>(acc, Ta, LVt, Tb, LVt, m0, n0, dv);
+                for (int hh = 0; hh < 2; ++hh)
+                    for (int jj = 0; jj < 4; ++jj)
+                        for (int e = 0; e < 4; ++e) {
+                            int r, i;
+                            at(m0, n0, hh, jj, e, r, i);
+                            const bool keep = i <= r && r < len;
+                            sdP[r * LC + i] = keep ? acc[hh][jj][e] : 0.f;
+                            sDP[r * LC + i] = keep ? acc[hh][jj][e] * expf(sg[r] - sg[i]) : 0.f;
+                        }
+            });
+            __syncthreads();
+            // dT += dUnew V^T
+            stage_f32(dUn, C, dv, len, [&](int r, int n, float4 x) { put_bf4(Ta + r * LVt + n, x, 1.f); });
+            {
+                const int n8 = (C * dv) >> 3, lc8 = ilog2(dv) - 3;
+                for (int e = threadIdx.x; e < n8; e += blockDim.x) {
+                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
+                    *reinterpret_cast<uint4 *>(Tb + r * LVt + n) =
+                        r < len ? __ldg(reinterpret_cast<const uint4 *>(v + row * dv) + e) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            __syncthreads();
+            each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
+                tile_mma<false, false>(acc, Ta, LVt, Tb, LVt, m0, n0, dv);
+                for (int hh = 0; hh < 2; ++hh)
+                    for (int jj = 0; jj < 4; ++jj)
+                        for (int e = 0; e < 4; ++e) {
+                            int r, i;
+                            at(m0, n0, hh, jj, e, r, i);
+                            if (i < len) sdT[r * LC + i] += acc[hh][jj][e];
+                        }
+            });
+            __syncthreads();
+        }
+    }
+    if (!staged) {
     // K K^T and the first half of dT = dW (diag(Gamma) K)^T + dUnew V^T
     bgemm<Tin, 4, 4>(len, len, dk, [&](int r, int kk) { return Kn[r * dk + kk]; }, Kt,
                      [&](int r, int i, float s) { sKK[r * LC + i] = s; });
@@ -1148,6 +1254,7 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
                          sdP[r * LC + i] = (i <= r) ? s : 0.f;
                          sDP[r * LC + i] = (i <= r) ? s * expf(sg[r] - sg[i]) : 0.f;
                      });
+    }
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
         sY[r * LC + i] = (i < r) ? sb[r] * sKK[r * LC + i] * expf(sg[r] - sg[i]) : 0.f;
@@ -1178,15 +1285,17 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             sS[r * LS + c] = ld_in(v + (row + r) * dv + c);
         }
     }
+    (void)staged;
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
         M3[r * C + i] = sDP[r * LC + i];
     }
     __syncthreads();
-    // dT += dUnew V^T
-    bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
-                     [&](int n, int i) { return kStage ? sS[i * LS + n] : ld_in(v + (row + i) * dv + n); },
-                     [&](int r, int i, float s) { sdT[r * LC + i] += s; });
+    // dT += dUnew V^T (the staged path did it before the solve)
+    if (!staged)
+        bgemm<Tin, 4, 4>(len, len, dv, [&](int r, int n) { return dUn[r * dv + n]; },
+                         [&](int n, int i) { return kStage ? sS[i * LS + n] : ld_in(v + (row + i) * dv + n); },
+                         [&](int r, int i, float s) { sdT[r * LC + i] += s; });
     __syncthreads();
     // d beta through T = Linv diag(beta)
     for (int i = threadIdx.x; i < len; i += blockDim.x) {
@@ -1607,7 +1716,7 @@ static size_t smem_bchunk(const Geo &g)
 {
     const size_t LC = g.C + 1, LS = (g.dk > g.dv ? g.dk : g.dv) + 1;
     const size_t stage = std::is_same<Tin, __nv_bfloat16>::value ? 0 : g.C * LS;
-    return sizeof(float) * (6 * g.C * LC + 5 * g.C + stage);
+    return sizeof(float) * (6 * g.C * LC + bchunk_pad(g.C, g.dk, g.dv) + 5 * g.C + stage);
 }
 static size_t smem_bgrad(const Geo &g) { return sizeof(float) * (3 * (size_t)g.C * (g.C + 1) + 6 * g.C); }
 
