@@ -1169,8 +1169,11 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             __syncthreads();
             each(2, [&](int p, int m0, int n0, float (&acc)[2][4][4]) {
                 tile_mma<false, false>(acc, p ? Tb : Ta, LKt, Ta, LKt, m0, n0, dk);
+#pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             int r, i;
                             at(m0, n0, hh, jj, e, r, i);
@@ -1197,8 +1200,11 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             __syncthreads();
             each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
                 tile_mma<false, false>(acc, Ta, LVt, Tb, LVt, m0, n0, dv);
+#pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             int r, i;
                             at(m0, n0, hh, jj, e, r, i);
@@ -1221,8 +1227,11 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             __syncthreads();
             each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
                 tile_mma<false, false>(acc, Ta, LVt, Tb, LVt, m0, n0, dv);
+#pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             int r, i;
                             at(m0, n0, hh, jj, e, r, i);
@@ -1698,6 +1707,179 @@ __global__ void __launch_bounds__(256, 2) k_bgrad_st(Geo g, const __nv_bfloat16 
     }
 }
 
+// k_prep for bf16 inputs on the staged layout (the shapes of staged_ok, 16-byte
+// aligned v): the normalised K and Q rounded to bf16 into row-major tiles as the norms
+// are taken, V copied as it is, and the four products (A, P, W, U) on ldmatrix
+// fragments; T and T diag(Gamma) are staged the same way after the solve.
+__global__ void __launch_bounds__(256) k_prep_st(Geo g, const __nv_bfloat16 *__restrict__ q,
+                                                 const __nv_bfloat16 *__restrict__ k,
+                                                 const __nv_bfloat16 *__restrict__ v,
+                                                 const __nv_bfloat16 *__restrict__ beta,
+                                                 const float *__restrict__ gate, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv, LC = C + 1;
+    const int LK = spad(dk), LV = spad(dv), LT = spad(C);
+    extern __shared__ float sm[];
+    float *sA = sm;                                 // [C][LC] A, for the solve
+    float *sT = sA + C * LC;                        // [C][LC] (I + A)^-1, or T
+    float *sb = sT + C * LC;                        // [C] step sizes (beta, or Longhorn's)
+    float *sg = sb + 64;                            // [C] gamma
+    float *sG = sg + 64;                            // [C] exp(gamma)
+    __nv_bfloat16 *Kb = reinterpret_cast<__nv_bfloat16 *>(sG + 64);   // normalised K [C][LK]
+    __nv_bfloat16 *Qb = Kb + C * LK;                // normalised Q [C][LK]
+    __nv_bfloat16 *Vb = Qb + C * LK;                // V [C][LV]
+    __nv_bfloat16 *Tb = Vb + C * LV;                // T [C][LT]
+    __nv_bfloat16 *TGb = Tb + C * LT;               // T diag(Gamma) [C][LT]
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+
+    for (int r = warp; r < C; r += nw) {
+        if (r >= len) {
+            for (int c = lane; c < dk; c += 32) {
+                Kb[r * LK + c] = __float2bfloat16_rn(0.f);
+                Qb[r * LK + c] = __float2bfloat16_rn(0.f);
+            }
+            if (lane == 0) sb[r] = 0.f;
+            continue;
+        }
+        const __nv_bfloat16 *kr = k + (row + r) * dk;
+        const __nv_bfloat16 *qr = q + (row + r) * dk;
+        float sk = 0.f, sq = 0.f;
+        for (int c = lane; c < dk; c += 32) {
+            float x = ld_in(kr + c), y = ld_in(qr + c);
+            sk = fmaf(x, x, sk);
+            sq = fmaf(y, y, sq);
+        }
+        sk = warp_sum(sk);
+        sq = warp_sum(sq);
+        float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
+        float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
+        if (lane == 0) {
+            // the token's step size: beta, or Longhorn's beta / (1 + beta k^T k) with
+            // k^T k = |k|^2 rk^2 of the key the update uses
+            float bt = ld_in(beta + row + r);
+            if (g.longhorn) bt = bt / fmaf(bt, sk * rk * rk, 1.f);
+            sb[r] = bt;
+            w.eb[slot * C + r] = bt;
+        }
+        for (int c = lane; c < dk; c += 32) {
+            float x = ld_in(kr + c) * rk, y = ld_in(qr + c) * rq;
+            Kb[r * LK + c] = __float2bfloat16_rn(x);
+            Qb[r * LK + c] = __float2bfloat16_rn(y);
+            w.Kn[slot * C * dk + r * dk + c] = x;
+            w.Qn[slot * C * dk + r * dk + c] = y;
+        }
+    }
+    if (warp == 0) {
+        // within-chunk cumulative log-gate, two rows per lane (C <= 64)
+        float x0 = (gate && lane < len) ? gate[row + lane] : 0.f;
+        float x1 = (gate && lane + 32 < len) ? gate[row + lane + 32] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+            if (lane >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        sg[lane] = x0;
+        sG[lane] = lane < len ? expf(x0) : 0.f;
+        sg[lane + 32] = x1;
+        sG[lane + 32] = lane + 32 < len ? expf(x1) : 0.f;
+        if (lane < len) w.gam[slot * C + lane] = x0;
+        if (lane + 32 < len) w.gam[slot * C + lane + 32] = x1;
+    }
+    {
+        // V, 8 bf16 per 16-byte load (rows past the chunk zero)
+        const int n8 = (C * dv) >> 3, lc8 = ilog2(dv) - 3;
+        for (int e = threadIdx.x; e < n8; e += blockDim.x) {
+            const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
+            *reinterpret_cast<uint4 *>(Vb + r * LV + n) =
+                r < len ? __ldg(reinterpret_cast<const uint4 *>(v + row * dv) + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __syncthreads();
+    const int ltc = ilog2(C) - 5, nt = 1 << (2 * ltc);   // warp tiles of a C x C product
+    auto at = [&](int m0, int n0, int hh, int jj, int e, int &r, int &c) {
+        r = m0 + 16 * hh + (lane >> 2) + 8 * (e >> 1);
+        c = n0 + 8 * jj + 2 * (lane & 3) + (e & 1);
+    };
+    auto zero = [&](float (&a)[2][4][4]) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) a[hh][jj][0] = a[hh][jj][1] = a[hh][jj][2] = a[hh][jj][3] = 0.f;
+    };
+    // A = strict_lower(diag(beta) (K K^T o D)),  P = lower(Q K^T o D)
+    float *Pg = w.P + slot * C * C;
+    for (int tile = warp; tile < 2 * nt; tile += nw) {
+        const int p = tile >> (2 * ltc), tl = tile & (nt - 1);
+        const int m0 = (tl >> ltc) * 32, n0 = (tl & ((1 << ltc) - 1)) * 32;
+        float acc[2][4][4];
+        zero(acc);
+        tile_mma<false, false>(acc, p ? Qb : Kb, LK, Kb, LK, m0, n0, dk);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int r, i;
+                    at(m0, n0, hh, jj, e, r, i);
+                    const bool live = r < len && i < len;
+                    if (p == 0) sA[r * LC + i] = (live && i < r) ? sb[r] * acc[hh][jj][e] * expf(sg[r] - sg[i]) : 0.f;
+                    else Pg[r * C + i] = (live && i <= r) ? acc[hh][jj][e] * expf(sg[r] - sg[i]) : 0.f;
+                }
+    }
+    __syncthreads();
+    // T = (I + A)^-1 diag(beta)
+    if (C == 64) {
+        if (warp < 4) prep::solve_unit_lower_64<65>(sA, sT, lane, warp, 1);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+            const int r = idx >> 6, i = idx & 63;
+            const float t = (i <= r && r < len) ? sT[r * LC + i] * sb[i] : 0.f;
+            Tb[r * LT + i] = __float2bfloat16_rn(t);
+            TGb[r * LT + i] = __float2bfloat16_rn(t * sG[i]);
+        }
+    } else {
+        unit_lower_solve(sA, sT, sb, len, LC);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+            const int r = idx >> (ltc + 5), i = idx & (C - 1);
+            const float t = (i <= r && r < len) ? sT[r * LC + i] : 0.f;
+            Tb[r * LT + i] = __float2bfloat16_rn(t);
+            TGb[r * LT + i] = __float2bfloat16_rn(t * sG[i]);
+        }
+    }
+    __syncthreads();
+    // W = T diag(Gamma) K,  U = T V
+    const int ltk = ilog2(dk) - 5, ltv = ilog2(dv) - 5;
+    const int ntw = (C / 32) << ltk, ntu = (C / 32) << ltv;
+    for (int tile = warp; tile < ntw + ntu; tile += nw) {
+        const bool isw = tile < ntw;
+        const int tl = isw ? tile : tile - ntw, lt = isw ? ltk : ltv, D = isw ? dk : dv;
+        const int m0 = (tl >> lt) * 32, n0 = (tl & ((1 << lt) - 1)) * 32;
+        float acc[2][4][4];
+        zero(acc);
+        if (isw) tile_mma<false, true>(acc, TGb, LT, Kb, LK, m0, n0, C);
+        else tile_mma<false, true>(acc, Tb, LT, Vb, LV, m0, n0, C);
+        float *dst = (isw ? w.W + slot * C * dk : w.U + slot * C * dv);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    int r, c;
+                    at(m0, n0, hh, jj, e, r, c);
+                    if (r < len) *reinterpret_cast<float2 *>(dst + r * D + c) = make_float2(acc[hh][jj][e], acc[hh][jj][e + 1]);
+                }
+    }
+}
+
 // ----------------------------------------------------------------------------- host launchers
 static size_t smem_prep(const Geo &g)
 {
@@ -1739,6 +1921,11 @@ static size_t smem_bgrad_st(const Geo &g)
     const size_t dub = (size_t)g.C * LV * 2 > (size_t)g.C * g.C * 4 ? (size_t)g.C * LV * 2 : (size_t)g.C * g.C * 4;
     return sizeof(float) * 6 * 64 + 2 * (3 * (size_t)g.C * LK + 3 * (size_t)g.C * LC) + dub;
 }
+static size_t smem_prep_st(const Geo &g)
+{
+    const size_t LC = g.C + 1, LK = spad(g.dk), LV = spad(g.dv), LT = spad(g.C);
+    return sizeof(float) * (2 * g.C * LC + 3 * 64) + 2 * (size_t)g.C * (2 * LK + LV + 2 * LT);
+}
 static size_t smem_bscan_st(const Geo &g)
 {
     const size_t LS = g.dv + 8, LC = spad(g.C), LK = spad(g.dk), LV = spad(g.dv);
@@ -1764,8 +1951,18 @@ static cudaError_t forward_states(const Geo &g, const Tin *q, const Tin *k, cons
                                   const Ws &w, cudaStream_t st)
 {
     cudaError_t e;
-    if ((e = set_smem(k_prep<Tin>, smem_prep(g))) != cudaSuccess) return e;
-    if (g.NC > 0) k_prep<Tin><<<dim3(g.NC, g.H), 256, smem_prep(g), st>>>(g, q, k, v, beta, gate, w);
+    bool prepped = false;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (use_staged<Tin>(g, v)) {
+            if ((e = set_smem(k_prep_st, smem_prep_st(g))) != cudaSuccess) return e;
+            if (g.NC > 0) k_prep_st<<<dim3(g.NC, g.H), 256, smem_prep_st(g), st>>>(g, q, k, v, beta, gate, w);
+            prepped = true;
+        }
+    }
+    if (!prepped) {
+        if ((e = set_smem(k_prep<Tin>, smem_prep(g))) != cudaSuccess) return e;
+        if (g.NC > 0) k_prep<Tin><<<dim3(g.NC, g.H), 256, smem_prep(g), st>>>(g, q, k, v, beta, gate, w);
+    }
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if (use_staged<Tin>(g)) {
         if ((e = set_smem(k_scan_st, smem_scan_st(g))) != cudaSuccess) return e;
