@@ -529,6 +529,35 @@ __device__ __forceinline__ void tile_mma(float (&acc)[2][4][4], const __nv_bfloa
     }
 }
 
+// acc (32 x 32 tile at m0, n0) += A B over k in [0, K), K % 8 == 0, on the tensor
+// cores in tf32 (operands rounded to 10-bit mantissas, fp32 accumulation), from fp32
+// accessors A(m, k), B(k, n).
+template <class FA, class FB>
+__device__ __forceinline__ void tile_tf32(float (&acc)[2][4][4], FA A, FB B, int m0, int n0, int K)
+{
+    const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t a[2][4], b[4][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = m0 + 16 * h + gq;
+            a[h][0] = prep::tf32(A(m, k0 + t));
+            a[h][1] = prep::tf32(A(m + 8, k0 + t));
+            a[h][2] = prep::tf32(A(m, k0 + t + 4));
+            a[h][3] = prep::tf32(A(m + 8, k0 + t + 4));
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            b[jj][0] = prep::tf32(B(k0 + t, n0 + 8 * jj + gq));
+            b[jj][1] = prep::tf32(B(k0 + t + 4, n0 + 8 * jj + gq));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) prep::mma_tf32_16x8x8(acc[h][jj], a[h], b[jj]);
+    }
+}
+
 // Runs Body(m0, n0, acc) for every 32 x 32 tile of an M x N product (M, N % 32 == 0),
 // the tiles dealt round-robin to the warps, with acc zeroed; then St(m, n, v0, v1)
 // for each pair of adjacent results (n even).  ntl_log2 = log2(N / 32).
@@ -1306,6 +1335,90 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
                          [&](int n, int i) { return kStage ? sS[i * LS + n] : ld_in(v + (row + i) * dv + n); },
                          [&](int r, int i, float s) { sdT[r * LC + i] += s; });
     __syncthreads();
+    if (staged && solved) {
+        // the same tail on the full 64 x 64 (everything outside the chunk is zero):
+        // d beta through T, X = Linv^T (dT diag(beta)) and dA = strict_lower(-X Linv^T)
+        // on the tensor cores in tf32, then one elementwise pass for the gate and beta
+        // sums and dKK
+        for (int i = threadIdx.x; i < len; i += blockDim.x) {
+            float a = 0.f;
+            for (int r = i; r < len; ++r) a = fmaf(sLi[r * LC + i], sdT[r * LC + i], a);
+            sdb[i] += a;
+        }
+        auto tiles64 = [&](auto A, auto B, auto St) {
+            // four 32 x 32 tiles, warps 0..3
+            if (warp < 4) {
+                const int m0 = (warp >> 1) * 32, n0 = (warp & 1) * 32;
+                float acc[2][4][4];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) acc[hh][jj][0] = acc[hh][jj][1] = acc[hh][jj][2] = acc[hh][jj][3] = 0.f;
+                tile_tf32(acc, A, B, m0, n0, 64);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            St(m0 + 16 * hh + (lane >> 2) + 8 * (e >> 1), n0 + 8 * jj + 2 * (lane & 3) + (e & 1),
+                               acc[hh][jj][e]);
+            }
+        };
+        tiles64([&](int a, int r) { return sLi[r * LC + a]; },
+                [&](int r, int bb) { return bb < len ? sdT[r * LC + bb] * sb[bb] : 0.f; },
+                [&](int a, int bb, float x) { sDP[a * LC + bb] = x; });
+        __syncthreads();
+        tiles64([&](int a, int c) { return sDP[a * LC + c]; }, [&](int c, int bb) { return sLi[bb * LC + c]; },
+                [&](int a, int bb, float x) { sY[a * LC + bb] = (bb < a) ? -x : 0.f; });
+        __syncthreads();
+        // F = dA o KK o D (beta sums) into sDP, E = beta_r F + dP o P (gate sums) into sdT,
+        // and sY <- dKK = dA o beta_r o D
+        for (int idx = threadIdx.x; idx < len * 64; idx += blockDim.x) {
+            const int r = idx >> 6, i = idx & 63;
+            float f = 0.f, e = 0.f, y = 0.f;
+            if (i < len) {
+                const float d = i <= r ? expf(sg[r] - sg[i]) : 0.f, dA = sY[r * LC + i];
+                f = dA * sKK[r * LC + i] * d;
+                e = fmaf(sb[r], f, i <= r ? sdP[r * LC + i] * Pg[r * C + i] : 0.f);
+                y = dA * sb[r] * d;
+            }
+            sDP[r * LC + i] = f;
+            sdT[r * LC + i] = e;
+            sY[r * LC + i] = y;
+        }
+        __syncthreads();
+        for (int r = warp; r < len; r += nw) {
+            float db = 0.f, rs = 0.f;
+            for (int i = lane; i < len; i += 32) {
+                db += sDP[r * LC + i];
+                rs += sdT[r * LC + i];
+            }
+            db = warp_sum(db);
+            rs = warp_sum(rs);
+            if (lane == 0) {
+                sdb[r] += db;
+                sdg[r] += rs;
+            }
+        }
+        for (int i = warp; i < len; i += nw) {
+            float cs = 0.f;
+            for (int r = lane; r < len; r += 32) cs += sdT[r * LC + i];
+            cs = warp_sum(cs);
+            if (lane == 0) atomicAdd(&sdg[i], -cs);
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
+            int r = idx / len, i = idx - r * len;
+            M3[C * C + r * C + i] = sLi[r * LC + i];
+            M3[2 * C * C + r * C + i] = sY[r * LC + i];
+        }
+        for (int r = threadIdx.x; r < len; r += blockDim.x) {
+            aux[2 * C + 4 + r] = sdg[r];
+            aux[3 * C + 4 + r] = sdb[r];
+        }
+        return;
+    }
     // d beta through T = Linv diag(beta)
     for (int i = threadIdx.x; i < len; i += blockDim.x) {
         float a = 0.f;
