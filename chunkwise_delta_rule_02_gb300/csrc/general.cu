@@ -1783,40 +1783,64 @@ __global__ void __launch_bounds__(256, 2) k_bgrad_st(Geo g, const __nv_bfloat16 
             if (dg) dg[row + r] = acc;
         }
     }
-    // the normalisation chain rule for dq, dk
-    for (int r = warp; r < len; r += nw) {
-        const __nv_bfloat16 *qr = q + (row + r) * dk;
-        const __nv_bfloat16 *kr = k + (row + r) * dk;
-        float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
-        for (int kk = lane; kk < dk; kk += 32) {
-            float x = ld_in(qr + kk), y = ld_in(kr + kk);
-            sq = fmaf(x, x, sq);
-            sk = fmaf(y, y, sk);
-            pq = fmaf(Qn[r * dk + kk], dQ[r * dk + kk], pq);
-            pk = fmaf(Kn[r * dk + kk], dK[r * dk + kk], pk);
-        }
-        sq = warp_sum(sq); sk = warp_sum(sk); pq = warp_sum(pq); pk = warp_sum(pk);
-        float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
-        float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
-        // sdb holds d/d(step size).  Longhorn's step e = b / (1 + b kap), kap = k^T k:
-        // de/db = (1 - e kap)^2 and de/dkap = -e^2, with d kap / dk = 2 k
-        float db = sdb[r], dkap = 0.f;
-        if (g.longhorn) {
-            const float kap = sk * rk * rk, e = sb[r], f = fmaf(-e, kap, 1.f);
-            dkap = -db * e * e;
-            db *= f * f;
-            pk = fmaf(2.f * dkap, kap, pk);
-        }
-        for (int kk = lane; kk < dk; kk += 32) {
-            float a = dQ[r * dk + kk], c = fmaf(2.f * dkap, Kn[r * dk + kk], dK[r * dk + kk]);
-            if (g.l2norm) {
-                a = rq * (a - Qn[r * dk + kk] * pq);
-                c = rk * (c - Kn[r * dk + kk] * pk);
+    // the normalisation chain rule for dq, dk: two rows per warp at a time, every
+    // load of a row issued before any of it is used (d_k <= 128: at most 4 per lane)
+    const int ne = dk >> 5;
+    for (int r0 = 2 * warp; r0 < len; r0 += 2 * nw) {
+        float xq[2][4], xk[2][4], Qv[2][4], Kv[2][4], a[2][4], c[2][4];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = r0 + rr;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kk = lane + 32 * e;
+                const bool on = r < len && e < ne;
+                xq[rr][e] = on ? ld_in(q + (row + r) * dk + kk) : 0.f;
+                xk[rr][e] = on ? ld_in(k + (row + r) * dk + kk) : 0.f;
+                Qv[rr][e] = on ? Qn[r * dk + kk] : 0.f;
+                Kv[rr][e] = on ? Kn[r * dk + kk] : 0.f;
+                a[rr][e] = on ? dQ[r * dk + kk] : 0.f;
+                c[rr][e] = on ? dK[r * dk + kk] : 0.f;
             }
-            st_out(dq + (row + r) * dk + kk, a);
-            st_out(dkout + (row + r) * dk + kk, c);
         }
-        if (lane == 0) st_out(dbeta + row + r, db);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = r0 + rr;
+            if (r >= len) break;
+            float sq = 0.f, sk = 0.f, pq = 0.f, pk = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sq = fmaf(xq[rr][e], xq[rr][e], sq);
+                sk = fmaf(xk[rr][e], xk[rr][e], sk);
+                pq = fmaf(Qv[rr][e], a[rr][e], pq);
+                pk = fmaf(Kv[rr][e], c[rr][e], pk);
+            }
+            sq = warp_sum(sq); sk = warp_sum(sk); pq = warp_sum(pq); pk = warp_sum(pk);
+            const float rq = g.l2norm ? rsqrtf(sq + g.eps) : 1.f;
+            const float rk = g.l2norm ? rsqrtf(sk + g.eps) : 1.f;
+            // sdb holds d/d(step size).  Longhorn's step e = b / (1 + b kap), kap = k^T k:
+            // de/db = (1 - e kap)^2 and de/dkap = -e^2, with d kap / dk = 2 k
+            float db = sdb[r], dkap = 0.f;
+            if (g.longhorn) {
+                const float kap = sk * rk * rk, ee = sb[r], f = fmaf(-ee, kap, 1.f);
+                dkap = -db * ee * ee;
+                db *= f * f;
+                pk = fmaf(2.f * dkap, kap, pk);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (e >= ne) break;
+                const int kk = lane + 32 * e;
+                float av = a[rr][e], cv = fmaf(2.f * dkap, Kv[rr][e], c[rr][e]);
+                if (g.l2norm) {
+                    av = rq * (av - Qv[rr][e] * pq);
+                    cv = rk * (cv - Kv[rr][e] * pk);
+                }
+                st_out(dq + (row + r) * dk + kk, av);
+                st_out(dkout + (row + r) * dk + kk, cv);
+            }
+            if (lane == 0) st_out(dbeta + row + r, db);
+        }
     }
 }
 
