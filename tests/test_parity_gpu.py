@@ -237,6 +237,31 @@ def test_head_dim_256_forward_and_backward(dtype, T, dk, dv, chunk):
         _assert_close(n, got[n], ref[n], TOL[dtype])
 
 
+@pytest.mark.parametrize("T,dk,dv,chunk", [(130, 64, 128, 32), (97, 128, 64, 64), (70, 32, 32, 32),
+                                          (64, 128, 32, 64), (33, 64, 64, 32)])
+def test_staged_bf16_shapes_forward_and_backward(T, dk, dv, chunk):
+    """The staged bf16 kernels (power-of-two head dims 32-128, chunks of 32 or 64):
+    d_k != d_v both ways, chunk 32 (column solve) and 64 (blocked solve), ragged tails."""
+    from chunkwise_delta_rule_02_gb300 import workloads
+    w = workloads.Workload("stg", 2, 2, T, max(dk, dv), "bf16", True, True, seed=3 * T + dk + dv,
+                           chunk=chunk, backward=True)
+    x = workloads.generate(w)
+    for key in ("q", "k"):
+        x[key] = x[key][..., :dk].contiguous()
+    for key in ("v", "do"):
+        x[key] = x[key][..., :dv].contiguous()
+    for key in ("h0", "dhT"):
+        x[key] = x[key][:, :, :dk, :dv].contiguous()
+    o, hT = _run_fwd(x, chunk=chunk)
+    ro, rh = oracle_fwd(x)
+    _assert_close("o", o, ro, TOL["bf16"])
+    _assert_close("hT", hT, rh, TOL["bf16"])
+    got = _run_bwd(x, chunk=chunk)
+    ref = oracle_bwd(x)
+    for n in GRADS:
+        _assert_close(n, got[n], ref[n], TOL["bf16"])
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_backward_varlen_small(dtype):
     from chunkwise_delta_rule_02_gb300 import workloads
