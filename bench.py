@@ -473,10 +473,15 @@ def main():
     kname = {binding.DN_PATH_COOP: "k_coop_fwd", binding.DN_PATH_FUSED: "k_fast_fwd"}.get(path, "general_fwd")
     if w.backward:
         launches_per_step += binding.dn_plan(shape, True)[1]
+    if w.backward:
+        # the timed region is the whole step: the forward plus the backward's kernels
+        kdesc = "whole forward+backward step (%d kernels)" % launches_per_step
+    else:
+        kdesc = kname if fast else "whole step (general kernels)"
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / pk["hbm_gbs"], "traffic": recorded_traffic(kname, w.name),
-            "kernel": kname if fast else "whole step (general kernels)",
-            "algorithmic_bytes_per_launch": abytes, "peak_source": src}
+            "frac": achieved / pk["hbm_gbs"],
+            "traffic": None if w.backward else recorded_traffic(kname, w.name),
+            "kernel": kdesc, "algorithmic_bytes_per_launch": abytes, "peak_source": src}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -485,7 +490,9 @@ def main():
                        "pass": "forward+backward" if w.backward else "forward",
                        "path": {binding.DN_PATH_COOP: "cooperative tcgen05 kernel",
                                 binding.DN_PATH_FUSED: "fused tcgen05 kernel per (sequence, head)"}.get(
-                                    path, "general fp32 kernels"),
+                                    path, "general fp32 kernels")
+                               + ("; backward: recompute, reverse scan and per-chunk kernels"
+                                  " (staged bf16 tensor-core products)" if w.backward else ""),
                        "l2": "no flush: inputs %.2f GB per step > 129 MB L2" % (abytes / 1e9),
                        "parallelism": "replicas over ranks" if world > 1 else "single GPU"},
             "roofline": roof, "clocks": clocks, "e2e": e2e,
