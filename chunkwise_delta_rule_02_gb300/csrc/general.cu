@@ -1,5 +1,5 @@
-// General chunk kernels: fp32 arithmetic on the CUDA cores, any head dim up to
-// 128, chunk 16/32/64, float32 or bfloat16 inputs, gated or not, packed or not.
+// General chunk kernels: any head dim up to 256, chunk 16/32/64, float32 or
+// bfloat16 inputs, gated or not, packed or not.
 //
 // These kernels carry the fp32 workload (whose 1e-4 tolerance tensor-core
 // operands cannot meet), every shape the tcgen05 kernels do not take, and the
@@ -27,6 +27,14 @@
 // L1) or without bank conflicts (from shared memory).  Operands that would be
 // read across rows instead are first staged in shared memory with an odd row
 // stride.
+//
+// For bf16 inputs with power-of-two head dims 32..128 and chunks of 32 or 64
+// the staged kernels (k_prep_st, k_scan_st, k_bscan_st, k_bbig_st, k_bgrad_st
+// and the staged branch of k_bchunk) replace these: each chunk's operands are
+// loaded once with batched 16-byte loads, rounded to bf16 into row-major
+// shared-memory tiles with rows padded by 8 elements, and multiplied on the
+// tensor cores with ldmatrix fragments and 32 x 32 warp tiles (tile_mma).  The
+// fp32 path keeps the kernels above.
 #include <type_traits>
 
 #include "common.cuh"
@@ -1323,7 +1331,6 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             sS[r * LS + c] = ld_in(v + (row + r) * dv + c);
         }
     }
-    (void)staged;
     for (int idx = threadIdx.x; idx < len * len; idx += blockDim.x) {
         int r = idx / len, i = idx - r * len;
         M3[r * C + i] = sDP[r * LC + i];
