@@ -27,7 +27,7 @@ namespace {
 constexpr int kCols = 32;            // d_v columns per CTA (one warp's width)
 constexpr int kGroups = 8;           // row groups: 256 threads
 constexpr int kRows = kMaxD / kGroups;   // rows per thread, 4-byte kernel
-constexpr int kRows4 = 128 / kGroups;    // rows per thread, 16-byte kernel (d_k <= 128)
+constexpr int kGroups4 = 16;             // row groups of the 16-byte kernel: 512 threads
 
 // the step size: beta, or Longhorn's beta / (1 + beta k^T k) ("Gated DeltaNet",
 // Table 1, row Longhorn), kk = k^T k of the key the update uses
@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(kCols * kGroups) k_decode(Args a, const Tin *_
 
 // The same step with 16-byte state accesses: one CTA per (sequence, head), lane
 // l of every warp owns columns 4l .. 4l + 3, so a warp moves one 512-byte state
-// row per instruction (needs d_v % 4 == 0 and 16-byte aligned states).
-template <class Tin>
-__global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__ q,
+// row per instruction (needs d_v % 4 == 0 and 16-byte aligned states).  NG warps
+// take interleaved rows (128 / NG rows per thread): 16 warps keep two CTAs and
+// 32 warps per SM, with all their state loads in flight.
+template <class Tin, int NG>
+__global__ void __launch_bounds__(32 * NG) k_decode4(Args a, const Tin *__restrict__ q,
                                                  const Tin *__restrict__ k,
                                                  const Tin *__restrict__ v,
                                                  const Tin *__restrict__ beta,
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     const bool live = n4 < a.dv;
     const size_t item = (size_t)seq * a.H + h;
     __shared__ float sk[kMaxD], sq[kMaxD];
-    __shared__ float4 sr[kGroups][32], sp[kGroups][32];
+    __shared__ float4 sr[NG][32], sp[NG][32];
     __shared__ float4 su[32];
     __shared__ float sscal[3];
 
@@ -187,11 +189,12 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     const float4 *Sin = a.state_in ? reinterpret_cast<const float4 *>(a.state_in + item * a.dk * a.dv) : nullptr;
     float4 *Sout = reinterpret_cast<float4 *>(a.state_out + item * a.dk * a.dv);
     const int dv4 = a.dv >> 2;
-    float4 s[kRows4];
+    constexpr int NR = 128 / NG;   // rows per thread (d_k <= 128)
+    float4 s[NR];
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f), p = r;
 #pragma unroll
-    for (int j = 0; j < kRows4; ++j) {
-        const int i = rg + kGroups * j;
+    for (int j = 0; j < NR; ++j) {
+        const int i = rg + NG * j;
         s[j] = (live && i < a.dk && Sin) ? Sin[(size_t)i * dv4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < a.dk) {
             const float ki = sk[i], qi = sq[i];
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
         const int c = threadIdx.x, L = c >> 2, e = c & 3;
         float rt = 0.f, pt = 0.f;
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) {
+        for (int g = 0; g < NG; ++g) {
             rt += reinterpret_cast<const float *>(&sr[g][L])[e];
             pt += reinterpret_cast<const float *>(&sp[g][L])[e];
         }
@@ -222,8 +225,8 @@ __global__ void __launch_bounds__(256) k_decode4(Args a, const Tin *__restrict__
     if (live) {
         const float4 u = su[lane];
 #pragma unroll
-        for (int j = 0; j < kRows4; ++j) {
-            const int i = rg + kGroups * j;
+        for (int j = 0; j < NR; ++j) {
+            const int i = rg + NG * j;
             if (i < a.dk) {
                 const float ki = sk[i];
                 Sout[(size_t)i * dv4 + lane] = make_float4(fmaf(alpha, s[j].x, ki * u.x), fmaf(alpha, s[j].y, ki * u.y),
@@ -243,7 +246,7 @@ cudaError_t step(const Args &a, const Tin *q, const Tin *k, const Tin *v, const 
     const bool aligned = ((uintptr_t)a.state_out & 15u) == 0 && ((uintptr_t)a.state_in & 15u) == 0;
     if (a.dv % 4 == 0 && a.dv <= 128 && a.dk <= 128 && aligned) {
         if (a.N > 0x7fffffff || a.H > 65535) return cudaErrorInvalidValue;
-        k_decode4<Tin><<<dim3((unsigned)a.N, a.H), kCols * kGroups, 0, st>>>(a, q, k, v, beta, o);
+        k_decode4<Tin, kGroups4><<<dim3((unsigned)a.N, a.H), 32 * kGroups4, 0, st>>>(a, q, k, v, beta, o);
         return cudaPeekAtLastError();
     }
     const int nsl = (a.dv + kCols - 1) / kCols;
