@@ -29,8 +29,8 @@
 // stride.
 //
 // For bf16 inputs with power-of-two head dims 32..128 and chunks of 32 or 64
-// the staged kernels (k_prep_st, k_scan_st, k_bscan_st, k_bbig_st, k_bgrad_st
-// and the staged branch of k_bchunk) replace these: each chunk's operands are
+// the staged kernels (k_prep_st, k_scan_st, k_out_st, k_bscan_st, k_bbig_st,
+// k_bgrad_st and the staged branch of k_bchunk) replace these: each chunk's operands are
 // loaded once with batched 16-byte loads, rounded to bf16 into row-major
 // shared-memory tiles with rows padded by 8 elements, and multiplied on the
 // tensor cores with ldmatrix fragments and 32 x 32 warp tiles (tile_mma).  The
@@ -2024,6 +2024,57 @@ __global__ void __launch_bounds__(256) k_prep_st(Geo g, const __nv_bfloat16 *__r
     }
 }
 
+// k_out for bf16 inputs on the staged layout (the shapes of staged_ok):
+// O = diag(Gamma) Q S_in + P Unew from bf16 tiles (Q and P row-major, S_in and Unew
+// read down their rows with ldmatrix.trans), one 32 x 32 output tile per warp.
+__global__ void __launch_bounds__(256) k_out_st(Geo g, __nv_bfloat16 *__restrict__ o, Ws w)
+{
+    const int j = blockIdx.x, h = blockIdx.y;
+    int b, t0, len, seq, local;
+    if (!chunk_of(g, j, b, t0, len, seq, local)) return;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int LK = spad(dk), LV = spad(dv), LC = spad(C);
+    extern __shared__ float sm[];
+    float *sG = sm;                                                       // [C] exp(gamma)
+    __nv_bfloat16 *Qb = reinterpret_cast<__nv_bfloat16 *>(sG + 64);       // diag(Gamma) Q [C][LK]
+    __nv_bfloat16 *Sb = Qb + C * LK;                                      // S_in [dk][LV]
+    __nv_bfloat16 *Pb = Sb + dk * LV;                                     // P [C][LC]
+    __nv_bfloat16 *Ub = Pb + C * LC;                                      // Unew [C][LV]
+    const size_t row = ((size_t)b * g.H + h) * g.T + t0;
+    const size_t slot = (size_t)j * g.H + h;
+    const float *gam = w.gam + slot * C;
+    for (int r = threadIdx.x; r < C; r += blockDim.x) sG[r] = r < len ? expf(gam[r]) : 0.f;
+    __syncthreads();
+    stage_f32(w.Qn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 x) { put_bf4(Qb + r * LK + kk, x, sG[r]); });
+    stage_f32(w.Sin + slot * dk * dv, dk, dv, dk, [&](int kk, int n, float4 x) { put_bf4(Sb + kk * LV + n, x, 1.f); });
+    // P's entries outside the chunk are zero (written so by k_prep_st)
+    stage_f32(w.P + slot * C * C, C, C, len, [&](int r, int i, float4 x) { put_bf4(Pb + r * LC + i, x, 1.f); });
+    stage_f32(w.Unew + slot * C * dv, C, dv, len, [&](int r, int n, float4 x) { put_bf4(Ub + r * LV + n, x, 1.f); });
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int ltv = ilog2(dv) - 5, nt = (C / 32) << ltv;
+    const float sc = g.scale;
+    for (int tile = warp; tile < nt; tile += nw) {
+        const int m0 = (tile >> ltv) * 32, n0 = (tile & ((1 << ltv) - 1)) * 32;
+        float acc[2][4][4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) acc[hh][jj][0] = acc[hh][jj][1] = acc[hh][jj][2] = acc[hh][jj][3] = 0.f;
+        tile_mma<false, true>(acc, Qb, LK, Sb, LV, m0, n0, dk);
+        tile_mma<false, true>(acc, Pb, LC, Ub, LV, m0, n0, C);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = m0 + 16 * hh + (lane >> 2) + 8 * (e >> 1), n = n0 + 8 * jj + 2 * (lane & 3) + (e & 1);
+                    if (r < len) st_out(o + (row + r) * dv + n, sc * acc[hh][jj][e]);
+                }
+    }
+}
+
 // ----------------------------------------------------------------------------- host launchers
 static size_t smem_prep(const Geo &g)
 {
@@ -2069,6 +2120,11 @@ static size_t smem_prep_st(const Geo &g)
 {
     const size_t LC = g.C + 1, LK = spad(g.dk), LV = spad(g.dv), LT = spad(g.C);
     return sizeof(float) * (2 * g.C * LC + 3 * 64) + 2 * (size_t)g.C * (2 * LK + LV + 2 * LT);
+}
+static size_t smem_out_st(const Geo &g)
+{
+    const size_t LK = spad(g.dk), LV = spad(g.dv), LC = spad(g.C);
+    return sizeof(float) * 64 + 2 * ((size_t)g.C * LK + (size_t)g.dk * LV + (size_t)g.C * LC + (size_t)g.C * LV);
 }
 static size_t smem_bscan_st(const Geo &g)
 {
@@ -2127,6 +2183,13 @@ cudaError_t fwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
 {
     cudaError_t e = forward_states(g, q, k, v, beta, gate, h0, hT, w, st);
     if (e != cudaSuccess) return e;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (use_staged<Tin>(g, v)) {
+            if ((e = set_smem(k_out_st, smem_out_st(g))) != cudaSuccess) return e;
+            if (g.NC > 0) k_out_st<<<dim3(g.NC, g.H), 256, smem_out_st(g), st>>>(g, o, w);
+            return cudaPeekAtLastError();
+        }
+    }
     if ((e = set_smem(k_out<Tin>, smem_out(g))) != cudaSuccess) return e;
     if (g.NC > 0) k_out<Tin><<<dim3(g.NC, g.H), 256, smem_out(g), st>>>(g, o, w);
     return cudaPeekAtLastError();
