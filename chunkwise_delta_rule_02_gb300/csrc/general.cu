@@ -993,6 +993,16 @@ __global__ void __launch_bounds__(512) k_bbig_st(Geo g, const __nv_bfloat16 *__r
     const float *gam = w.gam + slot * C;
     const float gC = gam[len - 1], sc = g.scale;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) {
+        // every row this CTA reads, into L2 before the staging loads below
+        l2_prefetch(w.Qn + slot * C * dk, sizeof(float) * C * dk);
+        l2_prefetch(w.Kn + slot * C * dk, sizeof(float) * C * dk);
+        l2_prefetch(w.dUn + slot * C * dv, sizeof(float) * C * dv);
+        l2_prefetch(w.Unew + slot * C * dv, sizeof(float) * C * dv);
+        l2_prefetch(w.Sin + slot * dk * dv, sizeof(float) * dk * dv);
+        l2_prefetch(w.dSo + slot * dk * dv, sizeof(float) * dk * dv);
+        l2_prefetch(dO + row * dv, sizeof(__nv_bfloat16) * len * dv);
+    }
     for (int r = threadIdx.x; r < C; r += blockDim.x) {
         sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
         sG[r] = r < len ? expf(gam[r]) : 0.f;
@@ -1179,6 +1189,16 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
     bool staged = false;
     if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
         staged = staged_ok(g) && (((uintptr_t)dO | (uintptr_t)v) & 15u) == 0;
+        if (staged && threadIdx.x == 0) {
+            // every row this CTA reads, into L2 before the staging loads below
+            l2_prefetch(Kn, sizeof(float) * C * dk);
+            l2_prefetch(dW, sizeof(float) * C * dk);
+            l2_prefetch(Un, sizeof(float) * C * dv);
+            l2_prefetch(dUn, sizeof(float) * C * dv);
+            l2_prefetch(Pg, sizeof(float) * C * C);
+            l2_prefetch(dO + row * dv, sizeof(__nv_bfloat16) * len * dv);
+            l2_prefetch(v + row * dv, sizeof(__nv_bfloat16) * len * dv);
+        }
         if (staged) {
             // the four C x C products on staged bf16 tiles, two tiles at a time
             const int ltc = ilog2(C) - 5, nt = 1 << (2 * ltc);   // warp tiles per C x C product
@@ -1648,6 +1668,16 @@ __global__ void __launch_bounds__(256, 2) k_bgrad_st(Geo g, const __nv_bfloat16 
     float *dK = w.dK + slot * C * dk;
     const float *gam = w.gam + slot * C;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) {
+        // every workspace row this CTA reads, into L2 before the staging loads below
+        l2_prefetch(Kn, sizeof(float) * C * dk);
+        l2_prefetch(Qn, sizeof(float) * C * dk);
+        l2_prefetch(w.dW + slot * C * dk, sizeof(float) * C * dk);
+        l2_prefetch(M3, sizeof(float) * 3 * C * C);
+        l2_prefetch(w.dUn + slot * C * dv, sizeof(float) * C * dv);
+        l2_prefetch(dQ, sizeof(float) * C * dk);
+        l2_prefetch(dK, sizeof(float) * C * dk);
+    }
     const float gC = gam[len - 1];
     const int lC = ilog2(C);
 
