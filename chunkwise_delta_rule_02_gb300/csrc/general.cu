@@ -1910,6 +1910,12 @@ __global__ void __launch_bounds__(256) k_prep_st(Geo g, const __nv_bfloat16 *__r
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) {
+        // the chunk's q, k, v rows into L2 before the per-row loads below
+        l2_prefetch(q + row * dk, sizeof(__nv_bfloat16) * len * dk);
+        l2_prefetch(k + row * dk, sizeof(__nv_bfloat16) * len * dk);
+        l2_prefetch(v + row * dv, sizeof(__nv_bfloat16) * len * dv);
+    }
 
     for (int r = warp; r < C; r += nw) {
         if (r >= len) {
