@@ -107,6 +107,34 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi)
     return r;
 }
 
+// brings [p, p + bytes) into L2 ahead of use (p 16-byte aligned, bytes % 16 == 0)
+__device__ __forceinline__ void l2_prefetch(const void *p, size_t bytes)
+{
+    if (bytes > 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)bytes) : "memory");
+}
+
+// For e in [0, n): put(e, get(e)), every thread issuing eight loads before it stores any,
+// so that their latencies overlap (get reads global memory, put writes shared memory).
+template <class FG, class FP>
+__device__ __forceinline__ void batched_copy(int n, FG get, FP put)
+{
+    constexpr int VB = 8;
+    for (int base = threadIdx.x; base < n; base += blockDim.x * VB) {
+        float x[VB];
+#pragma unroll
+        for (int u = 0; u < VB; ++u) {
+            const int e = base + u * blockDim.x;
+            x[u] = e < n ? get(e) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < VB; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < n) put(e, x[u]);
+        }
+    }
+}
+
 // D += A B for one 16 x 8 x 16 tile: A row-major, B column-major, bf16 in, fp32 accumulate
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
 {
@@ -341,18 +369,48 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
     int b, t0, L, j0, nch;
     seq_of(g, s, b, t0, L, j0, nch);
     extern __shared__ float sm[];
+    const int LK = dk + 1;
     float *sS = sm;               // [dk][BV]
     float *sU = sS + dk * BV;     // [C][BV]
     float *sE = sU + C * BV;      // [C] exp(gamma_C - gamma_r)
+    float *sW = sE + C;           // [C][LK] W of the chunk
+    float *sK = sW + C * LK;      // [C][LK] K of the chunk
     const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
     for (int idx = threadIdx.x; idx < dk * nb; idx += blockDim.x) {
         int kk = idx / nb, n = idx - kk * nb;
         sS[kk * BV + n] = h0 ? h0[sidx + (size_t)kk * dv + n0 + n] : 0.f;
     }
+    // W and K of a chunk are copied into shared memory first (all loads of a thread in
+    // flight together), the next chunk's rows prefetched into L2 meanwhile
+    auto stage_rows = [&](const float *src, float *dst, int len) {
+        constexpr int VB = 8;
+        for (int base = threadIdx.x; base < len * dk; base += blockDim.x * VB) {
+            float x[VB];
+#pragma unroll
+            for (int u = 0; u < VB; ++u) {
+                const int e = base + u * blockDim.x;
+                x[u] = e < len * dk ? src[e] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < VB; ++u) {
+                const int e = base + u * blockDim.x;
+                if (e < len * dk) {
+                    const int r = e / dk;
+                    dst[r * LK + e - r * dk] = x[u];
+                }
+            }
+        }
+    };
     __syncthreads();
     for (int c = 0; c < nch; ++c) {
         const int len = min(C, L - c * C);
         const size_t slot = (size_t)(j0 + c) * g.H + h;
+        if (threadIdx.x == 0 && c + 1 < nch) {
+            const size_t sl = slot + g.H;
+            l2_prefetch(w.W + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.Kn + sl * C * dk, sizeof(float) * C * dk);
+            l2_prefetch(w.U + sl * C * dv, sizeof(float) * C * dv);
+        }
         const float *gam = w.gam + slot * C;
         const float gC = gam[len - 1];
         for (int r = threadIdx.x; r < len; r += blockDim.x) sE[r] = expf(gC - gam[r]);
@@ -360,20 +418,27 @@ __global__ void __launch_bounds__(256) k_scan(Geo g, const float *__restrict__ h
             int kk = idx / nb, n = idx - kk * nb;
             w.Sin[slot * dk * dv + (size_t)kk * dv + n0 + n] = sS[kk * BV + n];
         }
-        const float *W = w.W + slot * C * dk;
-        const float *U = w.U + slot * C * dv;
+        stage_rows(w.W + slot * C * dk, sW, len);
+        stage_rows(w.Kn + slot * C * dk, sK, len);
+        batched_copy(len * nb, [&](int idx) {
+            const int r = idx / nb;
+            return w.U[slot * C * dv + (size_t)r * dv + n0 + idx - r * nb];
+        }, [&](int idx, float val) {
+            const int r = idx / nb;
+            sU[r * BV + idx - r * nb] = val;
+        });
+        __syncthreads();
         float *Un = w.Unew + slot * C * dv;
-        bgemm<Tin, 4, 4>(len, nb, dk, [&](int r, int kk) { return W[r * dk + kk]; },
+        bgemm<Tin, 4, 4>(len, nb, dk, [&](int r, int kk) { return sW[r * LK + kk]; },
                     [&](int kk, int n) { return sS[kk * BV + n]; },
                     [&](int r, int n, float acc) {
-                        float u = U[r * dv + n0 + n] - acc;
+                        float u = sU[r * BV + n] - acc;
                         sU[r * BV + n] = u;
                         Un[r * dv + n0 + n] = u;
                     });
         __syncthreads();
-        const float *Kn = w.Kn + slot * C * dk;
         const float GC = expf(gC);
-        bgemm<Tin, 8, 4>(dk, nb, len, [&](int kk, int r) { return sE[r] * Kn[r * dk + kk]; },
+        bgemm<Tin, 8, 4>(dk, nb, len, [&](int kk, int r) { return sE[r] * sK[r * LK + kk]; },
                     [&](int r, int n) { return sU[r * BV + n]; },
                     [&](int kk, int n, float acc) { sS[kk * BV + n] = fmaf(GC, sS[kk * BV + n], acc); });
         __syncthreads();
@@ -395,7 +460,12 @@ __global__ void __launch_bounds__(256) k_out(Geo g, Tout *__restrict__ o, Ws w)
     if (!chunk_of(g, j, b, t0, len, seq, local)) return;
     const int C = g.C, dk = g.dk, dv = g.dv;
     extern __shared__ float sm[];
+    // the operands in shared memory: A = [diag(Gamma) Q | P] rows, B = [S_in ; Unew]
+    // one 64-column slice of d_v at a time
+    const int KA = dk + len, LA = dk + C + 1, BV = 64, LB = BV + 1;
     float *sG = sm;            // [C] exp(gamma)
+    float *sA = sG + C;        // [C][LA]
+    float *sB = sA + C * LA;   // [dk + C][LB]
     const size_t row = ((size_t)b * g.H + h) * g.T + t0;
     const size_t slot = (size_t)j * g.H + h;
     const float *gam = w.gam + slot * C;
@@ -405,11 +475,29 @@ __global__ void __launch_bounds__(256) k_out(Geo g, Tout *__restrict__ o, Ws w)
     const float *Pg = w.P + slot * C * C;
     for (int r = threadIdx.x; r < len; r += blockDim.x) sG[r] = expf(gam[r]);
     __syncthreads();
+    batched_copy(len * KA, [&](int idx) {
+        const int r = idx / KA, x = idx - r * KA;
+        return x < dk ? sG[r] * Qn[r * dk + x] : Pg[r * C + (x - dk)];
+    }, [&](int idx, float val) {
+        const int r = idx / KA;
+        sA[r * LA + idx - r * KA] = val;
+    });
     const float sc = g.scale;
-    rgemm<4, 8>(len, dv, dk + len,
-                [&](int r, int x) { return x < dk ? sG[r] * Qn[r * dk + x] : Pg[r * C + (x - dk)]; },
-                [&](int x, int n) { return x < dk ? Sin[(size_t)x * dv + n] : Un[(x - dk) * dv + n]; },
-                [&](int r, int n, float acc) { st_out(o + (row + r) * dv + n, sc * acc); });
+    for (int n0 = 0; n0 < dv; n0 += BV) {
+        const int nb = min(BV, dv - n0);
+        __syncthreads();
+        batched_copy(KA * nb, [&](int idx) {
+            const int x = idx / nb, n = idx - x * nb;
+            return x < dk ? Sin[(size_t)x * dv + n0 + n] : Un[(x - dk) * dv + n0 + n];
+        }, [&](int idx, float val) {
+            const int x = idx / nb;
+            sB[x * LB + idx - x * nb] = val;
+        });
+        __syncthreads();
+        rgemm<4, 8>(len, nb, KA, [&](int r, int x) { return sA[r * LA + x]; },
+                    [&](int x, int n) { return sB[x * LB + n]; },
+                    [&](int r, int n, float acc) { st_out(o + (row + r) * dv + n0 + n, sc * acc); });
+    }
 }
 
 // ----------------------------------------------------------------------------- backward scan
@@ -648,12 +736,6 @@ __device__ __forceinline__ void put_bf2(__nv_bfloat16 *dst, float lo, float hi)
     *reinterpret_cast<uint32_t *>(dst) = bf16x2(lo, hi);
 }
 
-// brings [p, p + bytes) into L2 ahead of use (p 16-byte aligned, bytes % 16 == 0)
-__device__ __forceinline__ void l2_prefetch(const void *p, size_t bytes)
-{
-    if (bytes > 0)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)bytes) : "memory");
-}
 
 // row strides (elements) of the staged tiles
 __host__ __device__ __forceinline__ int spad(int cols) { return cols + 8; }
@@ -2117,8 +2199,14 @@ static size_t smem_prep(const Geo &g)
     const size_t LK = g.dk + 1, LC = g.C + 1;
     return sizeof(float) * (g.C * LK + g.C * (LK > (size_t)g.dv ? LK : g.dv) + 2 * g.C * LC + 3 * g.C);
 }
-static size_t smem_scan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + g.C * BV + g.C); }
-static size_t smem_out(const Geo &g) { return sizeof(float) * g.C; }
+static size_t smem_scan(const Geo &g, int BV)
+{
+    return sizeof(float) * (g.dk * BV + g.C * BV + g.C + 2 * (size_t)g.C * (g.dk + 1));
+}
+static size_t smem_out(const Geo &g)
+{
+    return sizeof(float) * (g.C + (size_t)g.C * (g.dk + g.C + 1) + (size_t)(g.dk + g.C) * 65);
+}
 static size_t smem_bscan(const Geo &g, int BV) { return sizeof(float) * (g.dk * BV + 2 * g.C * BV + 2 * g.C); }
 static size_t smem_bbig(const Geo &g)
 {
