@@ -736,6 +736,31 @@ __device__ __forceinline__ void put_bf2(__nv_bfloat16 *dst, float lo, float hi)
     *reinterpret_cast<uint32_t *>(dst) = bf16x2(lo, hi);
 }
 
+// The same copy split in two, for a block of at most NB x blockDim.x pieces of 16 bytes:
+// reg_load issues every load into registers, reg_put hands them to put(r, c, v), so
+// that the loads of several blocks are in flight together.
+template <int NB>
+__device__ __forceinline__ void reg_load(float4 (&v)[NB], const float *__restrict__ src, int rows, int cols, int live)
+{
+    const int lc4 = ilog2(cols) - 2, n4 = (rows * cols) >> 2;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        v[u] = (e < n4 && (e >> lc4) < live) ? __ldg(reinterpret_cast<const float4 *>(src) + e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+template <int NB, class FP>
+__device__ __forceinline__ void reg_put(const float4 (&v)[NB], int rows, int cols, FP put)
+{
+    const int lc4 = ilog2(cols) - 2, n4 = (rows * cols) >> 2;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        if (e < n4) put(e >> lc4, (e & ((1 << lc4) - 1)) << 2, v[u]);
+    }
+}
+
 
 // row strides (elements) of the staged tiles
 __host__ __device__ __forceinline__ int spad(int cols) { return cols + 8; }
@@ -765,8 +790,10 @@ __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict_
         put_bf2(Sb + kk * LV + n, v0, v1);
     }
     __syncthreads();
+    // chunk c's W, K, U rows and log-gates: into L2 two chunks ahead; at the top of the
+    // chunk, every load of its operands is issued at once into registers, then the
+    // registers go to shared memory once the previous chunk's state has been written out
     auto prefetch = [&](int c) {
-        // the chunk's workspace rows, while the chunk before it is computed
         if (threadIdx.x == 0 && c >= 0 && c < nch) {
             const size_t sl = (size_t)(j0 + c) * g.H + h;
             l2_prefetch(w.W + sl * C * dk, sizeof(float) * C * dk);
@@ -775,27 +802,38 @@ __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict_
             l2_prefetch(w.gam + sl * C, sizeof(float) * C);
         }
     };
+    constexpr int NB = 8;   // C * d / 4 <= 8 * 256 pieces
+    float4 rW[NB], rK[NB], rU[NB];
+    float rg = 0.f, rgC = 0.f;   // gam[threadIdx.x] and gam[len - 1] of the chunk
+    auto issue = [&](int c) {
+        const int ln = min(C, L - c * C);
+        const size_t sl = (size_t)(j0 + c) * g.H + h;
+        reg_load(rW, w.W + sl * C * dk, C, dk, ln);
+        reg_load(rK, w.Kn + sl * C * dk, C, dk, ln);
+        reg_load(rU, w.U + sl * C * dv, C, dv, ln);
+        rg = (int)threadIdx.x < ln ? __ldg(w.gam + sl * C + threadIdx.x) : 0.f;
+        rgC = __ldg(w.gam + sl * C + ln - 1);
+    };
     prefetch(0);
+    prefetch(1);
     for (int c = 0; c < nch; ++c) {
-        prefetch(c + 1);
+        issue(c);
         const int len = min(C, L - c * C);
         const size_t slot = (size_t)(j0 + c) * g.H + h;
-        const float *gam = w.gam + slot * C;
-        const float gC = gam[len - 1];
+        const float gC = rgC;
         float *Un = w.Unew + slot * C * dv;
         float *Sin = w.Sin + slot * dk * dv;
-        for (int r = threadIdx.x; r < C; r += blockDim.x) sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
+        if ((int)threadIdx.x < C) sE[threadIdx.x] = (int)threadIdx.x < len ? expf(gC - rg) : 0.f;
         for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
             const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
             reinterpret_cast<float4 *>(Sin)[idx] = *reinterpret_cast<const float4 *>(sS + kk * LS + n);
         }
         __syncthreads();
-        stage_f32(w.W + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Wt + r * LK + kk, v, 1.f); });
-        stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
-        stage_f32(w.U + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) {
-            *reinterpret_cast<float4 *>(sU + r * dv + n) = v;
-        });
+        reg_put(rW, C, dk, [&](int r, int kk, float4 v) { put_bf4(Wt + r * LK + kk, v, 1.f); });
+        reg_put(rK, C, dk, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
+        reg_put(rU, C, dv, [&](int r, int n, float4 v) { *reinterpret_cast<float4 *>(sU + r * dv + n) = v; });
         __syncthreads();
+        prefetch(c + 2);
         // Unew[r][n] = U[r][n] - sum_kk W[r][kk] S[kk][n]
         tiles(C, ldv - 5, [&](int m0, int n0, float (&acc)[2][4][4]) { tile_mma<false, true>(acc, Wt, LK, Sb, LV, m0, n0, dk); },
               [&](int r, int n, float a0, float a1) {
@@ -854,8 +892,10 @@ __global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__
         put_bf2(dSb + kk * LV + n, v0, v1);
     }
     __syncthreads();
+    // chunk c's P, K, Q, W, dO rows and log-gates: into L2 two chunks ahead; at the top
+    // of the chunk, every load of its operands is issued at once into registers, then the
+    // registers go to shared memory once the previous chunk's dS has been written out
     auto prefetch = [&](int c) {
-        // the chunk's workspace rows and dO rows, while the chunk after it is computed
         if (threadIdx.x == 0 && c >= 0 && c < nch) {
             const size_t sl = (size_t)(j0 + c) * g.H + h;
             const int ln = min(C, L - c * C);
@@ -867,19 +907,41 @@ __global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__
             l2_prefetch(dO + (((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C) * dv, sizeof(__nv_bfloat16) * ln * dv);
         }
     };
+    constexpr int NB = 8, NBP = 4;   // C * d / 4 <= 8 * 256 and C * C / 4, C * d / 8 <= 4 * 256 pieces
+    float4 rP[NBP], rK[NB], rQ[NB], rW[NB];
+    uint4 rO[NBP];
+    float rg = 0.f, rgC = 0.f;   // gam[threadIdx.x] and gam[len - 1] of the chunk
+    const int n8 = (C * dv) >> 3, lc8 = ldv - 3;
+    auto issue = [&](int c) {
+        const int ln = min(C, L - c * C);
+        const size_t sl = (size_t)(j0 + c) * g.H + h;
+        const size_t rw = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
+        reg_load(rP, w.P + sl * C * C, C, C, ln);
+        reg_load(rK, w.Kn + sl * C * dk, C, dk, ln);
+        reg_load(rQ, w.Qn + sl * C * dk, C, dk, ln);
+        reg_load(rW, w.W + sl * C * dk, C, dk, ln);
+#pragma unroll
+        for (int u = 0; u < NBP; ++u) {
+            const int e = threadIdx.x + u * blockDim.x;
+            rO[u] = (e < n8 && (e >> lc8) < ln) ? __ldg(reinterpret_cast<const uint4 *>(dO + rw * dv) + e)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+        }
+        rg = (int)threadIdx.x < ln ? __ldg(w.gam + sl * C + threadIdx.x) : 0.f;
+        rgC = __ldg(w.gam + sl * C + ln - 1);
+    };
     prefetch(nch - 1);
+    prefetch(nch - 2);
     for (int c = nch - 1; c >= 0; --c) {
-        prefetch(c - 1);
+        issue(c);
         const int len = min(C, L - c * C);
         const size_t slot = (size_t)(j0 + c) * g.H + h;
-        const size_t row = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
-        const float *gam = w.gam + slot * C;
-        const float gC = gam[len - 1];
+        const float gC = rgC;
         float *dUg = w.dUn + slot * C * dv;
         float *dSo = w.dSo + slot * dk * dv;
-        for (int r = threadIdx.x; r < C; r += blockDim.x) {
-            sE[r] = r < len ? expf(gC - gam[r]) : 0.f;
-            sG[r] = r < len ? expf(gam[r]) : 0.f;
+        if ((int)threadIdx.x < C) {
+            const bool live = (int)threadIdx.x < len;
+            sE[threadIdx.x] = live ? expf(gC - rg) : 0.f;
+            sG[threadIdx.x] = live ? expf(rg) : 0.f;
         }
         for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
             const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
@@ -888,36 +950,25 @@ __global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__
         __syncthreads();
         // P's columns i >= len are not written by the preparation; they only reach rows
         // i >= len of dUnew, which are dropped below
-        stage_f32(w.P + slot * C * C, C, C, len, [&](int x, int i, float4 v) { put_bf4(Ps + x * LC + i, v, 1.f); });
-        stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
-        stage_f32(w.Qn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(GQ + r * LK + kk, v, sG[r]); });
-        stage_f32(w.W + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Wn + r * LK + kk, v, -1.f); });
-        {
-            // scale dO, 8 bf16 per 16-byte load
-            const int n8 = (C * dv) >> 3, lc8 = ldv - 3;
-            for (int base = threadIdx.x; base < n8; base += blockDim.x * 4) {
-                uint4 v[4];
+        reg_put(rP, C, C, [&](int x, int i, float4 v) { put_bf4(Ps + x * LC + i, v, 1.f); });
+        reg_put(rK, C, dk, [&](int r, int kk, float4 v) { put_bf4(EK + r * LK + kk, v, sE[r]); });
+        reg_put(rQ, C, dk, [&](int r, int kk, float4 v) { put_bf4(GQ + r * LK + kk, v, sG[r]); });
+        reg_put(rW, C, dk, [&](int r, int kk, float4 v) { put_bf4(Wn + r * LK + kk, v, -1.f); });
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = base + u * blockDim.x;
-                    v[u] = (e < n8 && (e >> lc8) < len) ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e)
-                                                    : make_uint4(0u, 0u, 0u, 0u);
-                }
+        for (int u = 0; u < NBP; ++u) {
+            // scale dO, 8 bf16 per piece
+            const int e = threadIdx.x + u * blockDim.x;
+            if (e >= n8) continue;
+            const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
+            const uint32_t wv[4] = {rO[u].x, rO[u].y, rO[u].z, rO[u].w};
+            uint32_t o[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = base + u * blockDim.x;
-                    if (e >= n8) continue;
-                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
-                    const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                    uint32_t o[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        o[q] = bf16x2(g.scale * __uint_as_float(wv[q] << 16), g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
-                    *reinterpret_cast<uint4 *>(dOb + r * LV + n) = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            }
+            for (int q = 0; q < 4; ++q)
+                o[q] = bf16x2(g.scale * __uint_as_float(wv[q] << 16), g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
+            *reinterpret_cast<uint4 *>(dOb + r * LV + n) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         __syncthreads();
+        prefetch(c - 2);
         // dUnew[i][n] = sum_x P[x][i] dO[x][n] + E_i sum_kk K[i][kk] dS[kk][n]
         tiles(C, ldv - 5,
               [&](int m0, int n0, float (&acc)[2][4][4]) {
