@@ -750,6 +750,29 @@ __device__ __forceinline__ void reg_load(float4 (&v)[NB], const float *__restric
                                              : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
+// rows x cols bf16 row-major (cols a power of two >= 8), eight elements per piece
+template <int NB>
+__device__ __forceinline__ void reg_load_bf(uint4 (&v)[NB], const __nv_bfloat16 *__restrict__ src, int rows, int cols,
+                                            int live)
+{
+    const int lc8 = ilog2(cols) - 3, n8 = (rows * cols) >> 3;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        v[u] = (e < n8 && (e >> lc8) < live) ? __ldg(reinterpret_cast<const uint4 *>(src) + e)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+template <int NB, class FP>
+__device__ __forceinline__ void reg_put_bf(const uint4 (&v)[NB], int rows, int cols, FP put)
+{
+    const int lc8 = ilog2(cols) - 3, n8 = (rows * cols) >> 3;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+        const int e = threadIdx.x + u * blockDim.x;
+        if (e < n8) put(e >> lc8, (e & ((1 << lc8) - 1)) << 3, v[u]);
+    }
+}
 template <int NB, class FP>
 __device__ __forceinline__ void reg_put(const float4 (&v)[NB], int rows, int cols, FP put)
 {
@@ -1143,10 +1166,18 @@ __global__ void __launch_bounds__(512) k_bbig_st(Geo g, const __nv_bfloat16 *__r
         set[r] = 0.f;
     }
     if (threadIdx.x == 0) sred[0] = 0.f;
-    stage_f32(w.Qn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Qs + r * LQ + kk) = v; });
-    stage_f32(w.Kn + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Ks + r * LQ + kk) = v; });
-    stage_f32(w.dUn + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) { put_bf4(dUs + r * LV + n, v, 1.f); });
-    stage_f32(w.Unew + slot * C * dv, C, dv, len, [&](int r, int n, float4 v) { put_bf4(Us + r * LV + n, v, 1.f); });
+    {
+        // the four row blocks in one batch of loads (512 threads: C d / 4 <= 4 x 512 pieces)
+        float4 rq[4], rk[4], rdu[4], ru[4];
+        reg_load(rq, w.Qn + slot * C * dk, C, dk, len);
+        reg_load(rk, w.Kn + slot * C * dk, C, dk, len);
+        reg_load(rdu, w.dUn + slot * C * dv, C, dv, len);
+        reg_load(ru, w.Unew + slot * C * dv, C, dv, len);
+        reg_put(rq, C, dk, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Qs + r * LQ + kk) = v; });
+        reg_put(rk, C, dk, [&](int r, int kk, float4 v) { *reinterpret_cast<float4 *>(Ks + r * LQ + kk) = v; });
+        reg_put(rdu, C, dv, [&](int r, int n, float4 v) { put_bf4(dUs + r * LV + n, v, 1.f); });
+        reg_put(ru, C, dv, [&](int r, int n, float4 v) { put_bf4(Us + r * LV + n, v, 1.f); });
+    }
     {
         // both states, and <dS_out, S_in> in fp32 on the way
         const float4 *S4 = reinterpret_cast<const float4 *>(w.Sin + slot * dk * dv);
@@ -1354,8 +1385,14 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             };
             // K K^T and dT = dW (diag(Gamma) K)^T
             const int LKt = spad(dk), LVt = spad(dv);
-            stage_f32(Kn, C, dk, len, [&](int r, int kk, float4 x) { put_bf4(Ta + r * LKt + kk, x, 1.f); });
-            stage_f32(dW, C, dk, len, [&](int r, int kk, float4 x) { put_bf4(Tb + r * LKt + kk, x, 1.f); });
+            {
+                // K and dW in one batch of loads (C d / 4 <= 8 x 256 pieces)
+                float4 ra[8], rb[8];
+                reg_load(ra, Kn, C, dk, len);
+                reg_load(rb, dW, C, dk, len);
+                reg_put(ra, C, dk, [&](int r, int kk, float4 x) { put_bf4(Ta + r * LKt + kk, x, 1.f); });
+                reg_put(rb, C, dk, [&](int r, int kk, float4 x) { put_bf4(Tb + r * LKt + kk, x, 1.f); });
+            }
             __syncthreads();
             each(2, [&](int p, int m0, int n0, float (&acc)[2][4][4]) {
                 tile_mma<false, false>(acc, p ? Tb : Ta, LKt, Ta, LKt, m0, n0, dk);
@@ -1372,21 +1409,23 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
                         }
             });
             __syncthreads();
-            // dP = lower(scale dO Unew^T)
+            // dP = lower(scale dO Unew^T); scale dO and Unew in one batch of loads
+            // (C d / 8 <= 4 x 256 and C d / 4 <= 8 x 256 pieces)
             {
-                const int n8 = (C * dv) >> 3, lc8 = ilog2(dv) - 3;
-                for (int e = threadIdx.x; e < n8; e += blockDim.x) {
-                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
-                    uint4 x = r < len ? __ldg(reinterpret_cast<const uint4 *>(dO + row * dv) + e) : make_uint4(0u, 0u, 0u, 0u);
+                uint4 ro[4];
+                float4 ru[8];
+                reg_load_bf(ro, dO + row * dv, C, dv, len);
+                reg_load(ru, Un, C, dv, len);
+                reg_put_bf(ro, C, dv, [&](int r, int n, uint4 x) {
                     const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
                     uint32_t o[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         o[q] = bf16x2(sc * __uint_as_float(wv[q] << 16), sc * __uint_as_float(wv[q] & 0xFFFF0000u));
                     *reinterpret_cast<uint4 *>(Ta + r * LVt + n) = make_uint4(o[0], o[1], o[2], o[3]);
-                }
+                });
+                reg_put(ru, C, dv, [&](int r, int n, float4 x) { put_bf4(Tb + r * LVt + n, x, 1.f); });
             }
-            stage_f32(Un, C, dv, len, [&](int r, int n, float4 x) { put_bf4(Tb + r * LVt + n, x, 1.f); });
             __syncthreads();
             each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
                 tile_mma<false, false>(acc, Ta, LVt, Tb, LVt, m0, n0, dv);
@@ -1405,14 +1444,14 @@ __global__ void __launch_bounds__(256, 2) k_bchunk(Geo g, const Tin *__restrict_
             });
             __syncthreads();
             // dT += dUnew V^T
-            stage_f32(dUn, C, dv, len, [&](int r, int n, float4 x) { put_bf4(Ta + r * LVt + n, x, 1.f); });
             {
-                const int n8 = (C * dv) >> 3, lc8 = ilog2(dv) - 3;
-                for (int e = threadIdx.x; e < n8; e += blockDim.x) {
-                    const int r = e >> lc8, n = (e & ((1 << lc8) - 1)) << 3;
-                    *reinterpret_cast<uint4 *>(Tb + r * LVt + n) =
-                        r < len ? __ldg(reinterpret_cast<const uint4 *>(v + row * dv) + e) : make_uint4(0u, 0u, 0u, 0u);
-                }
+                // dUnew and V in one batch of loads
+                float4 ru[8];
+                uint4 rv[4];
+                reg_load(ru, dUn, C, dv, len);
+                reg_load_bf(rv, v + row * dv, C, dv, len);
+                reg_put(ru, C, dv, [&](int r, int n, float4 x) { put_bf4(Ta + r * LVt + n, x, 1.f); });
+                reg_put_bf(rv, C, dv, [&](int r, int n, uint4 x) { *reinterpret_cast<uint4 *>(Tb + r * LVt + n) = x; });
             }
             __syncthreads();
             each(1, [&](int, int m0, int n0, float (&acc)[2][4][4]) {
@@ -1823,18 +1862,28 @@ __global__ void __launch_bounds__(256, 2) k_bgrad_st(Geo g, const __nv_bfloat16 
         sdb[r] = live ? aux[3 * C + 4 + r] : 0.f;
         sk2[r] = 0.f;
     }
-    stage_f32(Kn, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Kb + r * LK + kk, v, 1.f); });
-    stage_f32(Qn, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(Qb + r * LK + kk, v, 1.f); });
-    stage_f32(w.dW + slot * C * dk, C, dk, len, [&](int r, int kk, float4 v) { put_bf4(dWb + r * LK + kk, v, 1.f); });
     // the C x C matrices, entries with r or i past the chunk set to zero
     auto mask4 = [&](int i, float4 v) {
         return make_float4(i < len ? v.x : 0.f, i + 1 < len ? v.y : 0.f, i + 2 < len ? v.z : 0.f, i + 3 < len ? v.w : 0.f);
     };
-    stage_f32(M3, C, C, len, [&](int r, int i, float4 v) { put_bf4(DPb + r * LC + i, mask4(i, v), 1.f); });
-    stage_f32(M3 + C * C, C, C, len, [&](int r, int i, float4 v) { put_bf4(Lib + r * LC + i, mask4(i, v), 1.f); });
-    stage_f32(M3 + 2 * C * C, C, C, len, [&](int r, int i, float4 v) {
-        *reinterpret_cast<float4 *>(Yf + r * C + i) = mask4(i, v);
-    });
+    {
+        // K and Q in one batch of loads, then dW with the three C x C matrices
+        // (C d / 4 <= 8 x 256 and C C / 4 <= 4 x 256 pieces)
+        float4 ra[8], rb[8];
+        reg_load(ra, Kn, C, dk, len);
+        reg_load(rb, Qn, C, dk, len);
+        reg_put(ra, C, dk, [&](int r, int kk, float4 v) { put_bf4(Kb + r * LK + kk, v, 1.f); });
+        reg_put(rb, C, dk, [&](int r, int kk, float4 v) { put_bf4(Qb + r * LK + kk, v, 1.f); });
+        float4 rc[8], r0[4], r1[4], r2[4];
+        reg_load(rc, w.dW + slot * C * dk, C, dk, len);
+        reg_load(r0, M3, C, C, len);
+        reg_load(r1, M3 + C * C, C, C, len);
+        reg_load(r2, M3 + 2 * C * C, C, C, len);
+        reg_put(rc, C, dk, [&](int r, int kk, float4 v) { put_bf4(dWb + r * LK + kk, v, 1.f); });
+        reg_put(r0, C, C, [&](int r, int i, float4 v) { put_bf4(DPb + r * LC + i, mask4(i, v), 1.f); });
+        reg_put(r1, C, C, [&](int r, int i, float4 v) { put_bf4(Lib + r * LC + i, mask4(i, v), 1.f); });
+        reg_put(r2, C, C, [&](int r, int i, float4 v) { *reinterpret_cast<float4 *>(Yf + r * C + i) = mask4(i, v); });
+    }
     __syncthreads();
     for (int idx = threadIdx.x; idx < C * C / 2; idx += blockDim.x) {
         const int r = (2 * idx) >> lC, i = (2 * idx) & (C - 1);
