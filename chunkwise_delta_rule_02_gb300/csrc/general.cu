@@ -789,7 +789,7 @@ __device__ __forceinline__ void reg_put(const float4 (&v)[NB], int rows, int col
 __host__ __device__ __forceinline__ int spad(int cols) { return cols + 8; }
 
 // forward recompute: S_in of every chunk, and Unew = U - W S_in, S <- Gamma_C S + K~^T Unew
-__global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict__ h0,
+__global__ void __launch_bounds__(512) k_scan_st(Geo g, const float *__restrict__ h0,
                                                  float *__restrict__ hT, Ws w)
 {
     const int s = blockIdx.x, h = blockIdx.y;
@@ -825,7 +825,7 @@ __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict_
             l2_prefetch(w.gam + sl * C, sizeof(float) * C);
         }
     };
-    constexpr int NB = 8;   // C * d / 4 <= 8 * 256 pieces
+    constexpr int NB = 4;   // C * d / 4 <= 4 * 512 pieces
     float4 rW[NB], rK[NB], rU[NB];
     float rg = 0.f, rgC = 0.f;   // gam[threadIdx.x] and gam[len - 1] of the chunk
     auto issue = [&](int c) {
@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(256) k_scan_st(Geo g, const float *__restrict_
 
 // backward scan: dS_out of every chunk, and
 //   dUnew = P^T dO + K~ dS,   dS <- Gamma_C dS + (Gamma Q)^T dO - W^T dUnew
-__global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__restrict__ dO,
+__global__ void __launch_bounds__(512) k_bscan_st(Geo g, const __nv_bfloat16 *__restrict__ dO,
                                                   const float *__restrict__ dhT,
                                                   float *__restrict__ dh0, Ws w)
 {
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(256) k_bscan_st(Geo g, const __nv_bfloat16 *__
             l2_prefetch(dO + (((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C) * dv, sizeof(__nv_bfloat16) * ln * dv);
         }
     };
-    constexpr int NB = 8, NBP = 4;   // C * d / 4 <= 8 * 256 and C * C / 4, C * d / 8 <= 4 * 256 pieces
+    constexpr int NB = 4, NBP = 2;   // C * d / 4 <= 4 * 512 and C * C / 4, C * d / 8 <= 2 * 512 pieces
     float4 rP[NBP], rK[NB], rQ[NB], rW[NB];
     uint4 rO[NBP];
     float rg = 0.f, rgC = 0.f;   // gam[threadIdx.x] and gam[len - 1] of the chunk
@@ -2390,7 +2390,7 @@ static cudaError_t forward_states(const Geo &g, const Tin *q, const Tin *k, cons
     if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
     if (use_staged<Tin>(g)) {
         if ((e = set_smem(k_scan_st, smem_scan_st(g))) != cudaSuccess) return e;
-        if (g.N > 0) k_scan_st<<<dim3(g.N, g.H), 256, smem_scan_st(g), st>>>(g, h0, hT, w);
+        if (g.N > 0) k_scan_st<<<dim3(g.N, g.H), 512, smem_scan_st(g), st>>>(g, h0, hT, w);
         return cudaPeekAtLastError();
     }
     const int BV = slice_width(g);
@@ -2430,7 +2430,7 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
         if (use_staged<Tin>(g, dO)) {
             if ((e = set_smem(k_bscan_st, smem_bscan_st(g))) != cudaSuccess) return e;
-            if (g.N > 0) k_bscan_st<<<dim3(g.N, g.H), 256, smem_bscan_st(g), st>>>(g, dO, dhT, dh0, w);
+            if (g.N > 0) k_bscan_st<<<dim3(g.N, g.H), 512, smem_bscan_st(g), st>>>(g, dO, dhT, dh0, w);
         }
     }
     if (!use_staged<Tin>(g, dO)) {
