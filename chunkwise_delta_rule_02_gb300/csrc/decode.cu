@@ -152,6 +152,22 @@ __global__ void __launch_bounds__(32 * NG) k_decode4(Args a, const Tin *__restri
     __shared__ float4 su[32];
     __shared__ float sscal[3];
 
+    // the state's loads go out first: they do not depend on the token, and their
+    // latency then covers the normalisation of q and k below
+    const float4 *Sin = a.state_in ? reinterpret_cast<const float4 *>(a.state_in + item * a.dk * a.dv) : nullptr;
+    float4 *Sout = reinterpret_cast<float4 *>(a.state_out + item * a.dk * a.dv);
+    const int dv4 = a.dv >> 2;
+    constexpr int NR = 128 / NG;   // rows per thread (d_k <= 128)
+    float4 s[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int i = rg + NG * j;
+        s[j] = (live && i < a.dk && Sin) ? Sin[(size_t)i * dv4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // so do this thread's v and beta (thread c < d_v owns column c below)
+    const float vc = (int)threadIdx.x < a.dv ? ld_in(v + item * a.dv + threadIdx.x) : 0.f;
+    const float braw = ld_in(beta + item);
+
     for (int i = threadIdx.x; i < a.dk; i += blockDim.x) {
         sk[i] = ld_in(k + item * a.dk + i);
         sq[i] = ld_in(q + item * a.dk + i);
@@ -186,16 +202,10 @@ __global__ void __launch_bounds__(32 * NG) k_decode4(Args a, const Tin *__restri
     }
     __syncthreads();
     const float alpha = sscal[1];
-    const float4 *Sin = a.state_in ? reinterpret_cast<const float4 *>(a.state_in + item * a.dk * a.dv) : nullptr;
-    float4 *Sout = reinterpret_cast<float4 *>(a.state_out + item * a.dk * a.dv);
-    const int dv4 = a.dv >> 2;
-    constexpr int NR = 128 / NG;   // rows per thread (d_k <= 128)
-    float4 s[NR];
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f), p = r;
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
         const int i = rg + NG * j;
-        s[j] = (live && i < a.dk && Sin) ? Sin[(size_t)i * dv4 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
         if (i < a.dk) {
             const float ki = sk[i], qi = sq[i];
             r.x = fmaf(s[j].x, ki, r.x); r.y = fmaf(s[j].y, ki, r.y);
@@ -216,8 +226,8 @@ __global__ void __launch_bounds__(32 * NG) k_decode4(Args a, const Tin *__restri
             rt += reinterpret_cast<const float *>(&sr[g][L])[e];
             pt += reinterpret_cast<const float *>(&sp[g][L])[e];
         }
-        const float b = step_size(a, ld_in(beta + item), sscal[2]);
-        const float u = b * (ld_in(v + item * a.dv + c) - alpha * rt);
+        const float b = step_size(a, braw, sscal[2]);
+        const float u = b * (vc - alpha * rt);
         st_out(o + item * a.dv + c, a.scale * fmaf(alpha, pt, u * sscal[0]));
         reinterpret_cast<float *>(&su[L])[e] = u;
     }
