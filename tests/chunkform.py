@@ -73,6 +73,45 @@ def fwd_seq(q, k, v, beta, g, h0, C, scale=1.0, l2norm=True, eps=1e-6):
     return O, S
 
 
+def fwd_seq_substituted(q, k, v, beta, g, h0, C, scale=1.0, l2norm=True, eps=1e-6):
+    """fwd_seq with the state substituted into the next chunk's Unew:
+
+        Unew_{j+1} = U_{j+1} - Gamma_c(j) W_{j+1} S_j + N_{j+1} Unew_j,
+        N_{j+1}    = -W_{j+1} (diag(exp(gamma_c - gamma)) K)_j^T,
+
+    which follows from S_{j+1} = Gamma_c(j) S_j + K~_j^T Unew_j.  Unew then depends
+    on the previous chunk's Unew through one C x C product, and on a state one chunk
+    older, so a kernel can keep the state update off its critical cycle.  The first
+    chunk of a sequence uses Unew_0 = U_0 - W_0 S_0."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    if l2norm:
+        q, _ = l2n(q, eps)
+        k, _ = l2n(k, eps)
+    S = np.zeros((dk, dv)) if h0 is None else h0.copy()   # S_j, the state entering chunk j
+    O = np.zeros((L, dv))
+    prev = None   # (Gamma_c, K~, Unew, S) of chunk j - 1
+    for c0 in range(0, L, C):
+        c1 = min(L, c0 + C)
+        Q, K, V, b = q[c0:c1], k[c0:c1], v[c0:c1], beta[c0:c1]
+        gg = None if g is None else g[c0:c1]
+        gam, Gam, D, KK, A, Linv, Tm, eC = _chunk_consts(K, b, gg)
+        W = Tm @ (Gam[:, None] * K)
+        U = Tm @ V
+        if prev is None:
+            Unew = U - W @ S
+        else:
+            GC_p, Kt_p, Unew_p, S_p = prev
+            N = -W @ Kt_p.T
+            Unew = U - GC_p * (W @ S_p) + N @ Unew_p
+        M = np.tril(Q @ K.T * D)
+        O[c0:c1] = scale * (Gam[:, None] * (Q @ S) + M @ Unew)
+        Kt = eC[:, None] * K
+        prev = (Gam[-1], Kt, Unew, S)
+        S = Gam[-1] * S + Kt.T @ Unew
+    return O, S
+
+
 def bwd_seq(q, k, v, beta, g, h0, dO, dST, C, scale=1.0, l2norm=True, eps=1e-6):
     """Reverse-mode gradients of (O, S_final) for one (sequence, head)."""
     L, dk = k.shape

@@ -281,6 +281,22 @@ def test_chunk_form_equals_recurrence(C):
         np.testing.assert_allclose(S, hT[0, 0], rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("C", [1, 5, 16, 64])
+def test_substituted_chain_equals_recurrence(C):
+    """The chain with the state substituted into the next chunk's Unew (one C x C
+    product on the critical cycle, the state one chunk behind) reproduces the token
+    recurrence: gated and not, with an initial state, ragged tail included."""
+    rng = RNG(40 + C)
+    L, dk, dv = 150, 8, 6
+    q, k, v, beta, g, S0 = _rand_inputs(rng, 1, 1, L, dk, dv)
+    for gg in (g, None):
+        o, hT = oracle.fwd(q, k, v, beta, gg, S0, scale=0.7)
+        O, S = chunkform.fwd_seq_substituted(q[0, 0], k[0, 0], v[0, 0], beta[0, 0],
+                                             None if gg is None else gg[0, 0], S0[0, 0], C, scale=0.7)
+        np.testing.assert_allclose(O, o[0, 0], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(S, hT[0, 0], rtol=1e-9, atol=1e-11)
+
+
 @pytest.mark.parametrize("C", [1, 5, 64])
 def test_chunk_backward_equals_bptt(C):
     rng = RNG(30 + C)
