@@ -81,8 +81,13 @@ def fwd_seq_substituted(q, k, v, beta, g, h0, C, scale=1.0, l2norm=True, eps=1e-
 
     which follows from S_{j+1} = Gamma_c(j) S_j + K~_j^T Unew_j.  Unew then depends
     on the previous chunk's Unew through one C x C product, and on a state one chunk
-    older, so a kernel can keep the state update off its critical cycle.  The first
-    chunk of a sequence uses Unew_0 = U_0 - W_0 S_0."""
+    older, so a kernel can keep the state update off its critical cycle.  The output
+    takes the older state the same way, with R_{j+1} = Qt_{j+1} K~_j^T
+    (Qt = diag(Gamma) Q):
+
+        O_{j+1} = scale * (Gamma_c(j) Qt_{j+1} S_j + R_{j+1} Unew_j + M_{j+1} Unew_{j+1}).
+
+    The first chunk of a sequence uses Unew_0 = U_0 - W_0 S_0 and O_0 as in fwd_seq."""
     L, dk = k.shape
     dv = v.shape[1]
     if l2norm:
@@ -105,7 +110,12 @@ def fwd_seq_substituted(q, k, v, beta, g, h0, C, scale=1.0, l2norm=True, eps=1e-
             N = -W @ Kt_p.T
             Unew = U - GC_p * (W @ S_p) + N @ Unew_p
         M = np.tril(Q @ K.T * D)
-        O[c0:c1] = scale * (Gam[:, None] * (Q @ S) + M @ Unew)
+        Qt = Gam[:, None] * Q
+        if prev is None:
+            O[c0:c1] = scale * (Qt @ S + M @ Unew)
+        else:
+            R = Qt @ Kt_p.T
+            O[c0:c1] = scale * (GC_p * (Qt @ S_p) + R @ Unew_p + M @ Unew)
         Kt = eC[:, None] * K
         prev = (Gam[-1], Kt, Unew, S)
         S = Gam[-1] * S + Kt.T @ Unew

@@ -283,9 +283,9 @@ def test_chunk_form_equals_recurrence(C):
 
 @pytest.mark.parametrize("C", [1, 5, 16, 64])
 def test_substituted_chain_equals_recurrence(C):
-    """The chain with the state substituted into the next chunk's Unew (one C x C
-    product on the critical cycle, the state one chunk behind) reproduces the token
-    recurrence: gated and not, with an initial state, ragged tail included."""
+    """The chain with the state substituted into the next chunk's Unew and output (one
+    C x C product on the critical cycle, the state one chunk behind) reproduces the
+    token recurrence: gated and not, with an initial state, ragged tail included."""
     rng = RNG(40 + C)
     L, dk, dv = 150, 8, 6
     q, k, v, beta, g, S0 = _rand_inputs(rng, 1, 1, L, dk, dv)
