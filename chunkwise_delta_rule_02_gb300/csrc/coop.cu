@@ -951,8 +951,8 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         named_bar(bar_id, 128);
         if (c == 0 && t == 0) CTR(j, 23);
         if (t == 64) {
-            // publish -W; the ready flag goes up at the top of the next round, once
-            // every copy of the package has landed
+            // publish -W; the ready flag goes up at the top of the pipeline's next
+            // task, once every copy of the package has landed
             if (!*abort_flag) {
                 bulk_store(dst + PK_WQ, tl, 8192);
                 bulk_store(dst + PK_WQ + 16384, tl + 16384, 8192);
