@@ -275,6 +275,73 @@ def run_reference(args, w, x):
 
 
 DECODE_WORKLOAD = "gdn_decode_bf16_n256h16d128"
+DECODE_SHAPE = (256, 16, 128)   # sequences, heads, head dim
+
+
+def decode_inputs():
+    """The decode workload's seeded inputs on the host: q, k, v [N,H,d] bf16, beta [N,H]
+    bf16, log-gate g [N,H] fp32 and the fp32 state [N,H,d,d]."""
+    import torch
+    N, H, d = DECODE_SHAPE
+    gen = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(N, H, d, generator=gen).to(torch.bfloat16) for _ in range(3))
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).to(torch.bfloat16)
+    g = -torch.nn.functional.softplus(torch.randn(N, H, generator=gen)) / 16
+    S = 0.02 * torch.randn(N, H, d, d, generator=gen)
+    return q, k, v, beta, g, S
+
+
+def oracle_decode_step(inputs, nthreads):
+    """One decode step of every (sequence, head) by the fp64 oracle (its token loop on
+    sequences of length 1, from the given state); returns the seconds it took."""
+    import oracle
+    f = lambda t: t.double().numpy()
+    q, k, v, beta, g, S = (f(t) for t in inputs)
+    args = (q[:, :, None], k[:, :, None], v[:, :, None], beta[:, :, None], g[:, :, None], S)
+    t0 = time.perf_counter()
+    oracle.fwd(*args, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def decode_cpu_baseline(inputs):
+    """The oracle's decode step on all of the workload's items, repeated until the
+    passes add up to about 10 s of host-thread time."""
+    nthreads = os.cpu_count() or 1
+    N, H, _ = DECODE_SHAPE
+    secs, passes = 0.0, 0
+    while passes < 64 and (passes == 0 or secs * nthreads < CPU_BASELINE_MIN_CPU_SECONDS):
+        secs += oracle_decode_step(inputs, nthreads)
+        passes += 1
+    return {"value": N * passes / secs, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": "fp64 oracle decode step of all %d sequences x %d heads over %d host threads, "
+                      "%d pass(es)" % (N, H, nthreads, passes),
+            "seconds": secs}
+
+
+def run_reference_decode(args):
+    """The reference arm on the decode workload: the oracle's decode step on the host,
+    rank 0 only."""
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return
+    inputs = decode_inputs()
+    nthreads = os.cpu_count() or 1
+    N, H, d = DECODE_SHAPE
+    for _ in range(min(max(args.warmup, 0), 1)):
+        oracle_decode_step(inputs, nthreads)
+    times = [oracle_decode_step(inputs, nthreads) for _ in range(args.steps)]
+    ms = 1000.0 * sum(times) / len(times)
+    value = N / (ms / 1000.0)
+    line = {"metric": "recurrent decode step tokens/s on 1 GB300; % of HBM roofline",
+            "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": DECODE_WORKLOAD, "N": N, "H": H, "d": d},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                             "sample": "per step: fp64 oracle decode step of all %d sequences x %d heads"
+                                       % (N, H)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
 
 
 def run_decode(args):
@@ -285,12 +352,9 @@ def run_decode(args):
     import chunkwise_delta_rule_02_gb300 as gdn
     from chunkwise_delta_rule_02_gb300 import binding
     rank, world, local = dist_env()
-    N, H, d = 256, 16, 128
-    gen = torch.Generator().manual_seed(5)
-    q, k, v = (torch.randn(N, H, d, generator=gen).to(torch.bfloat16) for _ in range(3))
-    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).to(torch.bfloat16)
-    g = -torch.nn.functional.softplus(torch.randn(N, H, generator=gen)) / 16
-    S = 0.02 * torch.randn(N, H, d, d, generator=gen)
+    N, H, d = DECODE_SHAPE
+    host_inputs = decode_inputs()
+    q, k, v, beta, g, S = (t.clone() for t in host_inputs)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pg = None
@@ -341,6 +405,8 @@ def run_decode(args):
                              "frac": achieved / pk["hbm_gbs"], "traffic": None, "kernel": "k_decode",
                              "algorithmic_bytes_per_launch": nbytes, "peak_source": src},
                 "clocks": clocks, "e2e": None, "gpu_launches": args.steps}
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = decode_cpu_baseline(host_inputs)
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
@@ -356,8 +422,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
-    if args.workload == DECODE_WORKLOAD and args.impl == "ours":
-        run_decode(args)
+    if args.workload == DECODE_WORKLOAD:
+        if args.impl == "ours":
+            run_decode(args)
+        else:
+            run_reference_decode(args)
         return
     import torch
     from chunkwise_delta_rule_02_gb300 import workloads

@@ -70,3 +70,47 @@ def test_cpu_baseline_counts_the_tokens_it_runs():
     assert secs > 0 and abs(tok - 53) < 1e-9
     cb = bench.cpu_baseline(x, w)
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+
+
+def _reference_line(*extra):
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *extra],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+REFERENCE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                  "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "impl", "config",
+                  "cpu_baseline", "e2e"}
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle timed on the host) on the default
+    forward workload: one JSON line with the contract's keys, no device needed."""
+    line = _reference_line("--steps", "1", "--warmup", "0")
+    assert REFERENCE_KEYS <= set(line)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["workload"] == "gdn_fwd_bf16_b4h16t8192d128_h0"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_on_the_decode_workload():
+    line = _reference_line("--workload", "gdn_decode_bf16_n256h16d128", "--steps", "2", "--warmup", "1")
+    assert REFERENCE_KEYS <= set(line)
+    assert line["config"]["workload"] == "gdn_decode_bf16_n256h16d128"
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+
+
+def test_decode_inputs_are_seeded():
+    sys.path.insert(0, ROOT)
+    import bench
+    a, b = bench.decode_inputs(), bench.decode_inputs()
+    for x, y in zip(a, b):
+        assert x.shape == y.shape and bool((x == y).all())
+    N, H, d = bench.DECODE_SHAPE
+    assert a[5].shape == (N, H, d, d) and a[0].shape == (N, H, d)
