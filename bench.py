@@ -44,6 +44,70 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def chunk_lengths(w, x):
+    """Lengths of every chunk of one head: the chunks of each sequence, the last one
+    possibly partial (chunks never cross a sequence)."""
+    C = w.chunk
+    if x["cu_seqlens"] is not None:
+        cu = [int(t) for t in x["cu_seqlens"].tolist()]
+        lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    else:
+        lens = [x["q"].shape[2]] * x["q"].shape[0]
+    out = []
+    for L in lens:
+        out += [C] * (L // C) + ([L % C] if L % C else [])
+    return out
+
+
+def chunk_flops_fwd(c: int, dk: int, dv: int) -> int:
+    """Counted FLOPs of the forward's dense contractions on one chunk of c rows, as
+    dense rectangles: K K^T, Q K^T, T (diag(Gamma) K) (2 c^2 dk each), T V, P Unew
+    (2 c^2 dv each), W S, Q S, K~^T Unew (2 c dk dv each), plus the unit-lower-
+    triangular inverse (about c^3 / 3 multiply-adds)."""
+    return 2 * (3 * c * c * dk + 2 * c * c * dv + 3 * c * dk * dv) + (2 * c ** 3) // 3
+
+
+def chunk_flops_bwd(c: int, dk: int, dv: int) -> int:
+    """Counted FLOPs of the backward's dense contractions on one chunk, as the
+    backward kernels run them (recompute included):
+      recompute   K K^T, Q K^T, T (Gamma K)  [c^2 dk];  T V  [c^2 dv];  W S, K~^T Unew  [c dk dv];
+                  the inverse (c^3 / 3 multiply-adds)
+      dS scan     P^T dO  [c^2 dv];  K~ dS, (Gamma Q)^T dO, W^T dUnew  [c dk dv]
+      states      dO S_in^T, dUnew S_in^T, Unew dS_out^T  [c dk dv]
+      c x c part  K K^T, dW (Gamma K)^T  [c^2 dk];  dUnew V^T, dO Unew^T  [c^2 dv];
+                  the inverse's adjoint, two c x c x c products
+      c x d part  (dP o D) K, (dP o D)^T Q, T^T dW, (dKK + dKK^T) K  [c^2 dk];  T^T dUnew  [c^2 dv]"""
+    return 2 * (9 * c * c * dk + 5 * c * c * dv + 8 * c * dk * dv + 2 * c ** 3) + (2 * c ** 3) // 3
+
+
+def algorithmic_flops(w, x, backward=False) -> int:
+    """Counted FLOPs of one forward (or backward) call over every (sequence, head)."""
+    dk, dv = x["q"].shape[-1], x["v"].shape[-1]
+    f = chunk_flops_bwd if backward else chunk_flops_fwd
+    return x["q"].shape[1] * sum(f(c, dk, dv) for c in chunk_lengths(w, x))
+
+
+def roofline(abytes: int, flops: int, ms: float, pk: dict, src: str, sustained: bool) -> dict:
+    """The slower of the two bounds (compulsory bytes at the measured HBM copy rate,
+    counted FLOPs at the measured dense bf16 rate) and the fraction of it reached:
+    frac = roofline time / measured time = achieved / peak of the binding bound."""
+    tf_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    tflops = pk.get(tf_key) or FALLBACK_PEAKS[tf_key]
+    t_hbm = abytes / (pk["hbm_gbs"] * 1e9)
+    t_flop = flops / (tflops * 1e12)
+    secs = ms / 1000.0
+    if t_hbm >= t_flop:
+        r = {"bound": "hbm", "achieved": abytes / secs / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / secs / 1e12, "peak": tflops, "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r.update({"hbm_time_us": t_hbm * 1e6, "tensor_time_us": t_flop * 1e6,
+              "hbm_frac": t_hbm / secs, "tensor_frac": t_flop / secs,
+              "algorithmic_bytes_per_launch": int(abytes), "flops_per_launch": int(flops),
+              "peak_source": src + (" (HBM copy; bf16 %s)" % ("sustained" if sustained else "burst"))})
+    return r
+
+
 def algorithmic_bytes(w, x) -> int:
     """Compulsory HBM bytes of one forward: read q, k, v, beta (input dtype), g (fp32),
     h0 (fp32 state); write o (input dtype) and the final state (fp32)."""
@@ -68,6 +132,67 @@ def algorithmic_bytes_bwd(w, x) -> int:
     per = (4 * d * es + es) + (3 * d * es + es) + (8 if x["g"] is not None else 0)
     nstate = x["h0"].numel() * 4 if x["h0"] is not None else 0
     return int(tokheads * per + 3 * nstate)
+
+
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries) every millisecond on a host thread, each sample time-stamped, so that
+    even a timed region of a few milliseconds holds samples."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.ok = False
+        self._stop = False
+        self._thread = None
+        try:
+            import ctypes
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            self.get_reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = (float(mx.value) if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0
+                            else None)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        import ctypes
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            a = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+            b = self.get_reasons(self.h, ctypes.byref(rs))
+            if a == 0:
+                self.samples.append((time.perf_counter(), float(mhz.value), int(rs.value) if b == 0 else 0))
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            import threading
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop = True
+            self._thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and the reasons seen in the samples taken in [t0, t1]."""
+        sel = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not sel:
+            return None
+        reasons = sorted({n for _, _, r in sel for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for _, m, _ in sel), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sel)}
 
 
 class ClockSampler:
@@ -117,6 +242,51 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+SOAK_SECONDS = 0.6   # untimed steps after the timed region, so nvidia-smi's 200 ms samples see load
+
+
+def run_timed(step, steps: int, stream, barrier, index: int):
+    """Time exactly `steps` calls of step() with CUDA events on `stream`, bracketed by
+    barrier() (a synchronize) on both sides.  NVML samples the SM clock every
+    millisecond from just before to just after the timed region; afterwards untimed
+    steps keep the GPU loaded for SOAK_SECONDS while nvidia-smi samples too.
+    Returns (per-step milliseconds, clocks record)."""
+    import torch
+    nv = NvmlSampler(index)
+    smi = ClockSampler(index)
+    nv.start()
+    smi.start()
+    time.sleep(0.02)
+    barrier()
+    t0 = time.perf_counter()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    barrier()
+    t1 = time.perf_counter()
+    soak_end = t1 + SOAK_SECONDS
+    n_soak = 0
+    while time.perf_counter() < soak_end:
+        step()
+        n_soak += 1
+        if n_soak % 8 == 0:
+            torch.cuda.synchronize()
+    barrier()
+    t2 = time.perf_counter()
+    nv.stop()
+    under_load = smi.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    timed = nv.summary(t0, t1)
+    clocks = dict(timed) if timed else (dict(under_load) if under_load else {})
+    clocks["source"] = "nvml, 1 ms, timed region" if timed else "nvidia-smi, 200 ms"
+    clocks["timed_region_s"] = t1 - t0
+    clocks["soak"] = {"steps": n_soak, "seconds": t2 - t1,
+                      "nvml": nv.summary(t1, t2), "nvidia_smi": under_load}
+    return per, clocks
 
 
 def dist_env():
@@ -175,11 +345,12 @@ def recorded_traffic(kernel: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
-def oracle_sample_fwd(x, w, items, nthreads):
-    """Run the fp64 oracle forward on `items` (sequence, head) pairs of x in one call,
-    the items side by side so that every host thread has work; returns (seconds, tokens)
-    where tokens counts whole tokens (all heads of a position).  Only the oracle call is
-    timed, not the gathering of the items."""
+def oracle_sample_fwd(x, w, items, nthreads, backward=False):
+    """Run the fp64 oracle forward (with backward=True: its backward, which runs the
+    forward too) on `items` (sequence, head) pairs of x in one call, the items side by
+    side so that every host thread has work; returns (seconds, tokens) where tokens
+    counts whole tokens (all heads of a position).  Only the oracle call is timed, not
+    the gathering of the items."""
     import numpy as np
     import torch
     import oracle
@@ -194,13 +365,20 @@ def oracle_sample_fwd(x, w, items, nthreads):
         h0 = None if x["h0"] is None else torch.stack([x["h0"][s, h] for s, h in items])[:, None]
         args = [f(cat(x[n])) for n in ("q", "k", "v", "beta", "g")]
         t0 = time.perf_counter()
-        oracle.fwd(*args, f(h0), cu_seqlens=offs, nthreads=nthreads)
+        if backward:
+            dhT = None if x.get("dhT") is None else torch.stack([x["dhT"][s, h] for s, h in items])[:, None]
+            oracle.bwd(*args, f(h0), f(cat(x["do"])), f(dhT), cu_seqlens=offs, nthreads=nthreads)
+        else:
+            oracle.fwd(*args, f(h0), cu_seqlens=offs, nthreads=nthreads)
         secs = time.perf_counter() - t0
         return secs, float(offs[-1]) / H
     st = lambda t: None if t is None else torch.stack([t[b, h] for b, h in items])[None]
     args = [f(st(x[n])) for n in ("q", "k", "v", "beta", "g", "h0")]
     t0 = time.perf_counter()
-    oracle.fwd(*args, nthreads=nthreads)
+    if backward:
+        oracle.bwd(*args, f(st(x["do"])), f(st(x["dhT"])), nthreads=nthreads)
+    else:
+        oracle.fwd(*args, nthreads=nthreads)
     secs = time.perf_counter() - t0
     return secs, float(x["q"].shape[2]) * len(items) / H
 
@@ -218,29 +396,64 @@ def sample_items(x, n_items):
 
 CPU_BASELINE_MIN_CPU_SECONDS = 10.0   # host threads x wall seconds
 CPU_BASELINE_MAX_PASSES = 8
+SINGLE_CORE_MIN_SECONDS = 2.0
+
+
+def host_cpu() -> dict:
+    """Architecture and model name of the host CPU (lscpu, else /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    return {"arch": platform.machine(), "model": model, "logical_cpus": os.cpu_count()}
 
 
 def cpu_baseline(x, w, budget_items=256):
-    """The oracle, as it stands, on up to `budget_items` (sequence, head) items of the
+    """The oracle, as it stands (its backward, which includes the forward, on a
+    forward+backward workload), on up to `budget_items` (sequence, head) items of the
     workload (all of them for the bench workloads), repeated until the passes add up to
-    about 10 s of host-thread time."""
+    about 10 s of host-thread time; plus the same oracle on one host thread, on one
+    item, repeated for about 2 s."""
     nthreads = os.cpu_count() or 1
     items = sample_items(x, budget_items)
     secs, tok, passes = 0.0, 0.0, 0
     while passes < CPU_BASELINE_MAX_PASSES and (passes == 0 or
                                                 secs * min(nthreads, len(items)) < CPU_BASELINE_MIN_CPU_SECONDS):
-        s, t = oracle_sample_fwd(x, w, items, nthreads)
+        s, t = oracle_sample_fwd(x, w, items, nthreads, backward=w.backward)
         secs += s
         tok += t
         passes += 1
     cores = min(nthreads, len(items))
+    s1, t1, p1 = 0.0, 0.0, 0
+    while p1 == 0 or s1 < SINGLE_CORE_MIN_SECONDS:
+        s, t = oracle_sample_fwd(x, w, items[:1], 1, backward=w.backward)
+        s1 += s
+        t1 += t
+        p1 += 1
+    what = "backward (with its forward)" if w.backward else "forward"
     return {"value": tok / secs, "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
-            "sample": "fp64 oracle forward on %d of the workload's %d (sequence, head) items, whole "
+            "sample": "fp64 oracle %s on %d of the workload's %d (sequence, head) items, whole "
                       "sequences, in one call over %d host threads, %d pass(es); tokens counted as "
-                      "whole tokens (items / heads)" % (len(items), len(sample_items(x, 1 << 30)),
+                      "whole tokens (items / heads)" % (what, len(items), len(sample_items(x, 1 << 30)),
                                                         cores, passes),
-            "seconds": secs}
+            "seconds": secs,
+            "single_core": {"value": t1 / s1, "unit": "tokens/s", "cores": 1, "seconds": s1,
+                            "sample": "the same oracle %s on 1 (sequence, head) item, %d pass(es)"
+                                      % (what, p1)},
+            "host": host_cpu()}
 
 
 def run_reference(args, w, x):
@@ -378,18 +591,8 @@ def run_decode(args):
     for _ in range(max(3, args.warmup)):
         step()
     barrier()
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
-    barrier()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    barrier()
-    clocks = clk.stop()
-    ms = max_over_ranks(sum(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)) / args.steps, pg, dev)
+    per, clocks = run_timed(step, args.steps, stream, barrier, local)
+    ms = max_over_ranks(sum(per) / len(per), pg, dev)
     if rank == 0:
         pk, src = peaks()
         nbytes = N * H * (2 * d * d * 4 + 4 * d * 2 + 2 + 4)
@@ -483,18 +686,7 @@ def main():
     if binding.dn_device_status(ws, stream) != binding.DN_OK:
         raise RuntimeError("device status error after warm-up")
 
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
-    barrier()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    barrier()
-    clocks = clk.stop()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    per, clocks = run_timed(step, args.steps, stream, barrier, local)
     ms = max_over_ranks(sum(per) / len(per), pg, dev)
     tokens = w.tokens
     value = whole_job_value(tokens, world, ms)
@@ -537,7 +729,7 @@ def main():
 
     pk, src = peaks()
     abytes = algorithmic_bytes(w, x) + (algorithmic_bytes_bwd(w, x) if w.backward else 0)
-    achieved = abytes / (ms / 1000.0) / 1e9
+    flops = algorithmic_flops(w, x) + (algorithmic_flops(w, x, backward=True) if w.backward else 0)
     path, launches_per_step = binding.dn_plan(shape, False)
     kname = {binding.DN_PATH_COOP: "k_coop_fwd", binding.DN_PATH_FUSED: "k_fast_fwd"}.get(path, "general_fwd")
     if w.backward:
@@ -547,10 +739,11 @@ def main():
         kdesc = "whole forward+backward step (%d kernels)" % launches_per_step
     else:
         kdesc = kname if fast else "whole step (general kernels)"
-    roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / pk["hbm_gbs"],
-            "traffic": None if w.backward else recorded_traffic(kname, w.name),
-            "kernel": kdesc, "algorithmic_bytes_per_launch": abytes, "peak_source": src}
+    # a single forward kernel is timed back to back on its own (burst tensor peak); the
+    # forward+backward step is a sequence of kernels (sustained tensor peak)
+    roof = roofline(abytes, flops, ms, pk, src, sustained=w.backward)
+    roof["traffic"] = None if w.backward else recorded_traffic(kname, w.name)
+    roof["kernel"] = kdesc
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

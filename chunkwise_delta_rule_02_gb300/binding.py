@@ -7,8 +7,12 @@ call returns an error status, these functions raise.
 
 The names match the C ABI: dn_workspace_size, dn_chunk_fwd, gdn_chunk_fwd,
 gdn_chunk_bwd, dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status,
-dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc, gdn_decode_step.  ``forward`` / ``backward`` additionally allocate outputs
-and the workspace with torch (device memory only).
+dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc, dn_noalloc_status,
+gdn_decode_step, dn_state_affine.  ``forward`` / ``backward`` additionally
+allocate outputs and the workspace with torch (device memory only) and, unless
+told not to, read the device status word after the call (which synchronises the
+stream) so that a bounded wait that ran out, malformed packed offsets or a
+log-gate outside its domain raise instead of returning invalid results.
 """
 from __future__ import annotations
 
@@ -21,13 +25,15 @@ import torch
 
 from ._build import LIB
 
-DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_WORKSPACE, DN_ERR_CUDA, DN_ERR_TIMEOUT = range(6)
+(DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_WORKSPACE, DN_ERR_CUDA, DN_ERR_TIMEOUT,
+ DN_ERR_DOMAIN) = range(7)
 DN_F32, DN_BF16 = 0, 1
 DN_BETA_DELTA, DN_BETA_LONGHORN = 0, 1
 
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
-           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_plan", "gdn_decode_step"]
+           "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_noalloc_status", "dn_plan",
+           "gdn_decode_step"]
 
 
 class DnShape(ctypes.Structure):
@@ -85,6 +91,8 @@ def lib():
             L.gdn_decode_step.restype = I
             L.dn_device_status.argtypes = [P, P]
             L.dn_device_status.restype = I
+            L.dn_noalloc_status.argtypes = [P]
+            L.dn_noalloc_status.restype = I
             L.dn_status_str.argtypes = [I]
             L.dn_status_str.restype = ctypes.c_char_p
             _lib = L
@@ -228,6 +236,11 @@ def dn_device_status(ws, stream=None) -> int:
     return int(lib().dn_device_status(_p(ws), _stream(stream)))
 
 
+def dn_noalloc_status(stream=None) -> int:
+    """Status word of the most recent gdn_chunk_fwd_noalloc call (syncs the stream)."""
+    return int(lib().dn_noalloc_status(_stream(stream)))
+
+
 def alloc_workspace(shape: DnShape, for_backward: bool, device) -> torch.Tensor:
     n = dn_workspace_size(shape, for_backward)
     if n == 0:
@@ -240,8 +253,11 @@ def _nseq(q, cu_seqlens):
 
 
 def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0,
-            qk_l2norm=True, eps=1e-6, want_state=True, ws=None, longhorn=False):
-    """Allocate o (and hT) and run gdn_chunk_fwd / dn_chunk_fwd.  Returns (o, hT)."""
+            qk_l2norm=True, eps=1e-6, want_state=True, ws=None, longhorn=False,
+            check_status=True):
+    """Allocate o (and hT) and run gdn_chunk_fwd / dn_chunk_fwd.  Returns (o, hT).
+    check_status: read the device status word afterwards (synchronises the stream)
+    and raise GdnError if the kernels flagged anything."""
     shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
     o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     N = _nseq(q, cu_seqlens)
@@ -253,12 +269,15 @@ def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0
         dn_chunk_fwd(shape, q, k, v, beta, h0, o, hT, ws)
     else:
         gdn_chunk_fwd(shape, q, k, v, beta, g, h0, o, hT, ws)
+    if check_status:
+        _check(dn_device_status(ws), "gdn_chunk_fwd (device status)")
     return o, hT
 
 
 def backward(q, k, v, beta, g, h0, dO, dhT, cu_seqlens=None, chunk=64, scale=1.0,
-             qk_l2norm=True, eps=1e-6, ws=None, longhorn=False):
-    """Allocate the gradients and run gdn_chunk_bwd.  Returns a dict."""
+             qk_l2norm=True, eps=1e-6, ws=None, longhorn=False, check_status=True):
+    """Allocate the gradients and run gdn_chunk_bwd.  Returns a dict.  check_status
+    as in forward."""
     shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
     out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                dbeta=torch.empty_like(beta),
@@ -269,4 +288,6 @@ def backward(q, k, v, beta, g, h0, dO, dhT, cu_seqlens=None, chunk=64, scale=1.0
         ws = alloc_workspace(shape, True, q.device)
     gdn_chunk_bwd(shape, q, k, v, beta, g, h0, dO, dhT, out["dq"], out["dk"], out["dv"],
                   out["dbeta"], out["dg"], out["dh0"], ws)
+    if check_status:
+        _check(dn_device_status(ws), "gdn_chunk_bwd (device status)")
     return out

@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -154,19 +156,22 @@ bool use_coop()
     return coop::available();
 }
 
-bool fast_ok(const dn_shape *s, const Geo &g, int for_backward)
+// honour_env = false ignores GDN_FORCE_GENERAL (the allocation-free entry point
+// serves the fused-kernel shapes whatever the environment says).
+bool fast_ok(const dn_shape *s, const Geo &g, int for_backward, bool honour_env = true)
 {
-    return !for_backward && !force_general() && fast::supports(g, s->dtype);
+    return !for_backward && !(honour_env && force_general()) && fast::supports(g, s->dtype);
 }
 
 dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size_t ws_bytes,
-                     cudaStream_t st, Layout &L, bool &fast, bool with_ring)
+                     cudaStream_t st, Layout &L, bool &fast, bool with_ring, bool honour_env = true)
 {
-    fast = fast_ok(s, g, for_backward);
+    fast = fast_ok(s, g, for_backward, honour_env);
     L = make_layout(g, s, for_backward, fast, with_ring);
     if (!ws || !is_aligned16(ws)) return DN_ERR_WORKSPACE;
     if (ws_bytes < L.total) return DN_ERR_WORKSPACE;
     char *base = (char *)ws;
+    g.status = (uint32_t *)(base + L.status);
     if (cudaMemsetAsync(base + L.status, 0, sizeof(uint32_t), st) != cudaSuccess) return DN_ERR_CUDA;
     if (g.varlen) {
         g.cstart = (const int32_t *)(base + L.cstart);
@@ -179,7 +184,8 @@ dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size
 
 dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *v,
                    const void *beta, const float *gate, const float *h0, void *o, float *hT,
-                   void *ws, size_t ws_bytes, void *stream, bool allow_coop = true)
+                   void *ws, size_t ws_bytes, void *stream, bool allow_coop = true,
+                   bool honour_env = true)
 {
     Geo g;
     dn_status rc = check_shape(s, &g);
@@ -193,7 +199,7 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
     Layout L;
     bool fast;
     const bool coop_run = allow_coop && use_coop();
-    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast, coop_run)) != DN_OK) return rc;
+    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast, coop_run, honour_env)) != DN_OK) return rc;
     char *base = (char *)ws;
     cudaError_t e;
     if (fast && coop_run) {
@@ -216,6 +222,21 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
                                         gate, h0, (__nv_bfloat16 *)o, hT, w, st);
     }
     return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+// Synchronises `st`, then reads the status word at device address `word_dev`,
+// clears it if it is set, and maps its bits to a status code (a timeout first,
+// then malformed packed offsets, then a log-gate outside its domain).
+dn_status read_status_word(void *word_dev, cudaStream_t st)
+{
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DN_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, word_dev, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DN_ERR_CUDA;
+    if (word == 0) return DN_OK;
+    if (cudaMemset(word_dev, 0, sizeof(word)) != cudaSuccess) return DN_ERR_CUDA;
+    if (word & kStatusTimeout) return DN_ERR_TIMEOUT;
+    if (word & kStatusBadOffsets) return DN_ERR_INVALID_ARG;
+    return DN_ERR_DOMAIN;
 }
 
 }  // namespace
@@ -408,21 +429,51 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices];
+struct NoAllocEntry {
+    CUcontext ctx;   // context the address belongs to
+    void *ptr;       // device address of g_noalloc_scratch in it
+};
+NoAllocEntry g_noalloc[kMaxDevices];
 
-// Device address of the array on the current device, looked up once per device
-// (with that device current) and cached.  Returns null on failure.
+// The calling thread's current CUDA context (null if none), through the driver
+// entry point the runtime hands out, so that the library links only cudart.
+CUcontext current_context()
+{
+    typedef CUresult (*GetCurrent)(CUcontext *);
+    static GetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (GetCurrent)p;
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of the array on the current device.  It is looked up with
+// cudaGetSymbolAddress, with that device current, on the first call on each
+// device, and again whenever the device's context has changed since (after
+// cudaDeviceReset the module is loaded anew and the array can move).  Returns
+// null on failure.
 void *noalloc_scratch()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoAllocEntry &e = g_noalloc[dev];
+    if (!e.ptr || !ctx || e.ctx != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        g_noalloc_ptr[dev] = ptr;
+        e.ptr = ptr;
+        e.ctx = current_context();   // current now, if it was not before the lookup
     }
-    return g_noalloc_ptr[dev];
+    return e.ptr;
 }
 }  // namespace
 
@@ -433,25 +484,26 @@ dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void
     Geo geo;
     dn_status rc = check_shape(shape, &geo);
     if (rc != DN_OK) return rc;
-    if (!fast_ok(shape, geo, 0)) return DN_ERR_UNSUPPORTED;
+    if (!fast_ok(shape, geo, 0, false)) return DN_ERR_UNSUPPORTED;
     if (make_layout(geo, shape, 0, true, false).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
     void *ws = noalloc_scratch();
     if (!ws) return DN_ERR_CUDA;
     // the one-CTA-per-item fused kernel: its scratch fits the static array
-    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, kNoAllocScratchBytes, stream, false);
+    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, kNoAllocScratchBytes, stream, false, false);
+}
+
+dn_status dn_noalloc_status(void *stream)
+{
+    void *ws = noalloc_scratch();
+    if (!ws) return DN_ERR_CUDA;
+    // the status word is the first word of the static array (the workspace layout's header)
+    return read_status_word(ws, (cudaStream_t)stream);
 }
 
 dn_status dn_device_status(void *ws, void *stream)
 {
     if (!ws) return DN_ERR_WORKSPACE;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return DN_ERR_CUDA;
-    uint32_t word = 0;
-    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DN_ERR_CUDA;
-    if (word == 0) return DN_OK;
-    if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return DN_ERR_CUDA;
-    if (word & kStatusTimeout) return DN_ERR_TIMEOUT;
-    return DN_ERR_INVALID_ARG;
+    return read_status_word(ws, (cudaStream_t)stream);
 }
 
 const char *dn_status_str(dn_status s)
@@ -463,6 +515,7 @@ const char *dn_status_str(dn_status s)
     case DN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case DN_ERR_CUDA: return "CUDA error";
     case DN_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case DN_ERR_DOMAIN: return "an input value outside its documented domain (log-gate g > 0)";
     }
     return "unknown status";
 }

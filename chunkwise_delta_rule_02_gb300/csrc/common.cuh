@@ -24,6 +24,7 @@ struct Geo {
     float scale, eps;
     const int32_t *cu;      // device [N+1] token offsets (packed)
     const int32_t *cstart;  // device [N+1] first chunk slot of each sequence (packed)
+    uint32_t *status;       // device status word of the call (see kStatus*)
 };
 
 // Chunk slot j -> (batch row b, first token t0 on that row's time axis, rows).
@@ -76,8 +77,10 @@ __device__ __forceinline__ float ld_in(const __nv_bfloat16 *p) { return __bfloat
 __device__ __forceinline__ void st_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
-// Device status word (first word of every workspace).
-enum : uint32_t { kStatusOk = 0, kStatusTimeout = 1u, kStatusBadOffsets = 2u };
+// Device status word (first word of every workspace).  kStatusPositiveGate: a
+// log-gate g > 0 was read (alpha > 1, outside the documented domain: the chunk
+// form's decay ratios exp(gamma_r - gamma_i) are then growth factors).
+enum : uint32_t { kStatusOk = 0, kStatusTimeout = 1u, kStatusBadOffsets = 2u, kStatusPositiveGate = 4u };
 
 __device__ __forceinline__ void raise_status(uint32_t *status, uint32_t bit)
 {

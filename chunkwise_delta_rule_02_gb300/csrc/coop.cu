@@ -700,6 +700,8 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             if (p.gate) {
                 g0 = lane < len ? p.gate[row0 + lane] : 0.f;
                 g1 = lane + 32 < len ? p.gate[row0 + lane + 32] : 0.f;
+                if (__any_sync(0xffffffffu, g0 > 0.f || g1 > 0.f) && lane == 0)
+                    raise_status(p.status, kStatusPositiveGate);
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {

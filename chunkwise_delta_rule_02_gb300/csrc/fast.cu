@@ -267,6 +267,8 @@ k_fast_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 bg[r] = r < len ? __bfloat162float(p.beta[row + r]) : 0.f;
                 bg[64 + r] = (r < len && p.gate) ? p.gate[row + r] : 0.f;
             }
+            if (__any_sync(0xffffffffu, bg[64 + lane] > 0.f || bg[96 + lane] > 0.f) && lane == 0)
+                raise_status(p.status, kStatusPositiveGate);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_FULL + s]);
             issued = n + 1;

@@ -294,6 +294,8 @@ __global__ void __launch_bounds__(256) k_prep(Geo g, const Tin *__restrict__ q,
         // within-chunk cumulative log-gate, two rows per lane (C <= 64)
         float x0 = (gate && lane < len) ? gate[row + lane] : 0.f;
         float x1 = (gate && lane + 32 < len) ? gate[row + lane + 32] : 0.f;
+        if (__any_sync(0xffffffffu, x0 > 0.f || x1 > 0.f) && lane == 0)
+            raise_status(g.status, kStatusPositiveGate);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
@@ -2140,6 +2142,8 @@ __global__ void __launch_bounds__(256) k_prep_st(Geo g, const __nv_bfloat16 *__r
         // within-chunk cumulative log-gate, two rows per lane (C <= 64)
         float x0 = (gate && lane < len) ? gate[row + lane] : 0.f;
         float x1 = (gate && lane + 32 < len) ? gate[row + lane + 32] : 0.f;
+        if (__any_sync(0xffffffffu, x0 > 0.f || x1 > 0.f) && lane == 0)
+            raise_status(g.status, kStatusPositiveGate);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);

@@ -45,7 +45,10 @@
  * Argument errors are found on the host before anything is launched.  Launch
  * errors return DN_ERR_CUDA.  Every device-side wait in the kernels is
  * bounded; a wait that runs out records DN_ERR_TIMEOUT in the workspace's
- * status word, which dn_device_status reads back.
+ * status word, which dn_device_status reads back.  The same word records what
+ * only the device can see in the inputs: malformed packed offsets
+ * (DN_ERR_INVALID_ARG) and a log-gate g > 0 (DN_ERR_DOMAIN).  Each call clears
+ * the word when it starts, so it describes the most recent call on it.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
@@ -63,7 +66,8 @@ typedef enum {
     DN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. dk > 256)     */
     DN_ERR_WORKSPACE = 3,     /* ws == NULL or ws_bytes < dn_workspace_size     */
     DN_ERR_CUDA = 4,          /* a CUDA call or kernel launch failed            */
-    DN_ERR_TIMEOUT = 5        /* a bounded device wait ran out (see above)      */
+    DN_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (see above)      */
+    DN_ERR_DOMAIN = 6         /* an input outside its domain: log-gate g > 0    */
 } dn_status;
 
 typedef enum { DN_F32 = 0, DN_BF16 = 1 } dn_dtype;
@@ -108,7 +112,14 @@ dn_status dn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, cons
 
 /* Gated DeltaNet forward (Table 1 row "Gated DeltaNet"): as dn_chunk_fwd plus
  *   g [B,H,T] float32 log-gate, alpha = exp(g); g must be <= 0 (alpha <= 1).
- *   g == NULL is the same as g = 0 (alpha = 1).                               */
+ *   g == NULL is the same as g = 0 (alpha = 1).
+ * A gate alpha in (0, 1] is a decay; the chunk form relies on it, through the
+ * ratios exp(gamma_r - gamma_i) <= 1 inside a chunk and the state's pending
+ * decay factor.  A value g > 0 is not rejected (the device would have to read g
+ * before the launch) but flagged: the kernels set the status word and
+ * dn_device_status returns DN_ERR_DOMAIN.  The result is still computed; it
+ * follows the recurrence only while exp(sum of g over a chunk) and the growth
+ * of the state stay inside float32 range.                                      */
 dn_status gdn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, const void *v,
                         const void *beta, const float *g, const float *h0, void *o,
                         float *hT, void *ws, size_t ws_bytes, void *stream);
@@ -176,16 +187,33 @@ dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k
  * otherwise DN_ERR_UNSUPPORTED), and at most about 32,000 packed sequences
  * (larger returns DN_ERR_WORKSPACE).  The first call on each device looks up
  * the array's device address with that device current; make that first call
- * before any stream capture.  All calls share the one array, so calls whose
- * work overlaps on the GPU race on it: serialise them (one stream, or events).
- * Arguments, layouts and the other errors are those of gdn_chunk_fwd. */
+ * before any stream capture.  The address is looked up again when the
+ * device's context has changed (for example after cudaDeviceReset).  All calls
+ * share the one array, so calls whose work overlaps on the GPU race on it:
+ * serialise them (one stream, or events).  GDN_FORCE_GENERAL does not apply
+ * here.  Arguments, layouts and host-side errors are those of gdn_chunk_fwd;
+ * what the device finds (a bounded wait that ran out, malformed packed offsets,
+ * a log-gate g > 0) goes to the array's status word, read by
+ * dn_noalloc_status. */
 dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void *k,
                                 const void *v, const void *beta, const float *g,
                                 const float *h0, void *o, float *hT, void *stream);
 
-/* Synchronises `stream`, then reads and clears the status word that bounded
- * device waits write into `ws` (DN_OK or DN_ERR_TIMEOUT). */
+/* Synchronises `stream`, then reads and clears the status word in `ws` that
+ * the last call using `ws` wrote: DN_OK, DN_ERR_TIMEOUT (a bounded device wait
+ * ran out; the outputs are not valid), DN_ERR_INVALID_ARG (malformed packed
+ * offsets; those sequences were treated as empty) or DN_ERR_DOMAIN (a log-gate
+ * g > 0 was read), in that order of precedence. */
 dn_status dn_device_status(void *ws, void *stream);
+
+/* The same for gdn_chunk_fwd_noalloc, whose status word lies in the library's
+ * static scratch array on the current device rather than in a workspace:
+ * synchronises `stream`, then reads, clears and maps that word as
+ * dn_device_status does.  Allocates nothing.  As the array is shared, the word
+ * describes the most recent gdn_chunk_fwd_noalloc call on this device; read it
+ * before the next one starts.  Returns DN_ERR_CUDA if the array's address
+ * cannot be looked up. */
+dn_status dn_noalloc_status(void *stream);
 
 /* Static description of a status code. */
 const char *dn_status_str(dn_status s);

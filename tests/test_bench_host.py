@@ -114,3 +114,111 @@ def test_decode_inputs_are_seeded():
         assert x.shape == y.shape and bool((x == y).all())
     N, H, d = bench.DECODE_SHAPE
     assert a[5].shape == (N, H, d, d) and a[0].shape == (N, H, d)
+
+
+# ----------------------------------------------------------------------------- FLOP counts
+class _Counted:
+    """Wraps numpy so that every matrix product of the chunk form adds its
+    2 m n k FLOPs to a counter (an independent tally of what the formulas claim)."""
+
+    def __init__(self):
+        import numpy as np
+
+        self.n = 0
+        outer = self
+
+        class Arr(np.ndarray):
+            def __matmul__(self, other):
+                return outer._mm(np.asarray(self), np.asarray(other))
+
+            def __rmatmul__(self, other):
+                return outer._mm(np.asarray(other), np.asarray(self))
+
+        self.Arr = Arr
+
+    def _mm(self, a, b):
+        import numpy as np
+        self.n += 2 * a.shape[0] * a.shape[1] * b.shape[1]
+        return np.matmul(a, b).view(self.Arr)
+
+    def wrap(self, x):
+        import numpy as np
+        return np.asarray(x, dtype=np.float64).view(self.Arr)
+
+
+def _chunkform():
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import chunkform
+    return chunkform
+
+
+def test_forward_flop_formula_counts_the_chunk_form_products():
+    """bench.algorithmic_flops (forward) = the products the chunk form multiplies, per
+    chunk (ragged tails included), times the heads, plus the solve's c^3 / 3 multiply-adds."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_delta_rule_02_gb300 import workloads as W
+    cf = _chunkform()
+    for C, T, dk, dv in ((64, 70, 8, 6), (16, 37, 4, 12)):
+        w = W.Workload("fl", 2, 3, T, dk, "f32", True, False, 1, chunk=C)
+        x = W.generate(w)
+        x["v"] = x["v"][..., :1].expand(*x["v"].shape[:-1], dv).contiguous()
+        cnt = _Counted()
+        rng = np.random.default_rng(0)
+        for _ in range(2 * 3):   # every (batch row, head)
+            cf.fwd_seq(cnt.wrap(rng.normal(size=(T, dk))), cnt.wrap(rng.normal(size=(T, dk))),
+                       cnt.wrap(rng.normal(size=(T, dv))), rng.random(T), -rng.random(T) / 16, None, C)
+        solve = 3 * sum((2 * c ** 3) // 3 for c in bench.chunk_lengths(w, x))   # heads x chunks
+        assert bench.algorithmic_flops(w, x) == cnt.n + solve
+
+
+def test_backward_flop_formula_counts_the_backward_products():
+    """bench.algorithmic_flops (backward) against the products of the chunk-form
+    backward, less those it computes twice where the kernels compute them once: its
+    second pass recomputes T (Gamma K), T V and W S_in, it forms Q S_in for the gate
+    term (the kernels reuse dO S_in^T), and it applies dKK and dKK^T to K separately
+    (the kernels add them first)."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_delta_rule_02_gb300 import workloads as W
+    cf = _chunkform()
+    C, T, dk, dv = 16, 37, 4, 6
+    w = W.Workload("flb", 1, 1, T, dk, "f32", True, False, 1, chunk=C)
+    x = W.generate(w)
+    x["v"] = x["v"][..., :1].expand(*x["v"].shape[:-1], dv).contiguous()
+    cnt = _Counted()
+    rng = np.random.default_rng(1)
+    cf.bwd_seq(cnt.wrap(rng.normal(size=(T, dk))), cnt.wrap(rng.normal(size=(T, dk))),
+               cnt.wrap(rng.normal(size=(T, dv))), rng.random(T), -rng.random(T) / 16, None,
+               cnt.wrap(rng.normal(size=(T, dv))), None, C)
+    lens = bench.chunk_lengths(w, x)
+    twice = sum(2 * (2 * c * c * dk + c * c * dv + 2 * c * dk * dv) for c in lens)
+    solve = sum((2 * c ** 3) // 3 for c in lens)
+    assert bench.algorithmic_flops(w, x, backward=True) == cnt.n - twice + solve
+
+
+def test_roofline_takes_the_slower_bound():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0, "bf16_tflops_sustained": 50.0}
+    r = bench.roofline(1e9, 1e13, 1000.0, pk, "test", sustained=False)   # 1 ms of HBM, 100 ms of FLOPs
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.1) < 1e-12 and r["unit"] == "TFLOP/s"
+    r = bench.roofline(1e9, 1e13, 1000.0, pk, "test", sustained=True)
+    assert abs(r["frac"] - 0.2) < 1e-12 and r["peak"] == 50.0
+    r = bench.roofline(1e11, 1e12, 1000.0, pk, "test", sustained=False)  # 100 ms of HBM, 10 ms of FLOPs
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.1) < 1e-12 and r["unit"] == "GB/s"
+
+
+def test_forward_counts_of_the_headline_workload():
+    """B4 H16 T8192 d128, C = 64: 1.83e5 FLOP and 1030 B per token-head (plus the
+    states), so the forward is bound by HBM at the measured peaks."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunkwise_delta_rule_02_gb300 import workloads as W
+    w = W.WORKLOADS["gdn_fwd_bf16_b4h16t8192d128_h0"]
+    x = W.generate(w, T=128)   # two chunks per item: the count per token does not depend on T
+    th = 4 * 16 * 128
+    assert bench.algorithmic_flops(w, x) == th * (6 * 128 * 128 + 10 * 64 * 128) + 4 * 16 * 2 * (2 * 64 ** 3 // 3)
+    assert bench.algorithmic_bytes(w, x) == th * 1030 + 2 * 4 * 16 * 128 * 128 * 4

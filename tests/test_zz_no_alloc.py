@@ -69,6 +69,45 @@ def test_noalloc_matches_workspace_entry_point(lengths):
         assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
 
 
+def _noalloc_call(lib, shape, d, o, hT, g=None):
+    return lib.gdn_chunk_fwd_noalloc(ctypes.byref(shape), d["q"].data_ptr(), d["k"].data_ptr(),
+                                     d["v"].data_ptr(), d["beta"].data_ptr(),
+                                     None if g is None else g.data_ptr(), None, o.data_ptr(),
+                                     hT.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_status_word_is_readable():
+    """What the device finds during an allocation-free call (here malformed packed
+    offsets, then a log-gate above zero) reaches the caller through
+    dn_noalloc_status, which needs no workspace pointer; reading clears it."""
+    from chunkwise_delta_rule_02_gb300 import binding
+    lib = binding.lib()
+    d = _inputs([10, 5, 5], seed=32)
+    o = torch.zeros_like(d["v"])
+    hT = torch.zeros((3, d["q"].shape[1], 128, 128), device=DEV)
+    bad = torch.tensor([0, 10, 5, 20], dtype=torch.int32, device=DEV)   # not monotone
+    shape = binding.make_shape(d["q"], d["v"], cu_seqlens=bad)
+    assert _noalloc_call(lib, shape, d, o, hT, d["g"]) == binding.DN_OK
+    assert binding.dn_noalloc_status() == binding.DN_ERR_INVALID_ARG
+    assert binding.dn_noalloc_status() == binding.DN_OK
+    shape = binding.make_shape(d["q"], d["v"], cu_seqlens=d["cu_seqlens"])
+    assert _noalloc_call(lib, shape, d, o, hT, d["g"].abs()) == binding.DN_OK
+    assert binding.dn_noalloc_status() == binding.DN_ERR_DOMAIN
+    assert _noalloc_call(lib, shape, d, o, hT, d["g"]) == binding.DN_OK
+    assert binding.dn_noalloc_status() == binding.DN_OK
+
+
+def test_noalloc_ignores_the_general_path_override(monkeypatch):
+    """GDN_FORCE_GENERAL sends the workspace entry points to the general kernels;
+    the allocation-free one has no workspace for them and keeps the fused kernel."""
+    monkeypatch.setenv("GDN_FORCE_GENERAL", "1")
+    d = _inputs(None, seed=33)
+    ro, rh = _reference(d)
+    for o, hT in _noalloc(d):
+        assert rel(o, ro) <= TOL["bf16"], rel(o, ro)
+        assert rel(hT, rh) <= TOL["bf16"], rel(hT, rh)
+
+
 def test_noalloc_rejects_what_it_cannot_serve():
     from chunkwise_delta_rule_02_gb300 import binding
     lib = binding.lib()
