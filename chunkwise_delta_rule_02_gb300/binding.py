@@ -33,7 +33,7 @@ DN_BETA_DELTA, DN_BETA_LONGHORN = 0, 1
 EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
            "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_noalloc_status", "dn_plan",
-           "gdn_decode_step"]
+           "gdn_decode_step", "dn_state_affine"]
 
 
 class DnShape(ctypes.Structure):
@@ -93,6 +93,8 @@ def lib():
             L.dn_device_status.restype = I
             L.dn_noalloc_status.argtypes = [P]
             L.dn_noalloc_status.restype = I
+            L.dn_state_affine.argtypes = [P, P, P, P, I, I, I, P]
+            L.dn_state_affine.restype = I
             L.dn_status_str.argtypes = [I]
             L.dn_status_str.restype = ctypes.c_char_p
             _lib = L
@@ -230,6 +232,18 @@ def decode_step(q, k, v, beta, g=None, state=None, out_state=None, scale=1.0, qk
         out_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     gdn_decode_step(shape, q, k, v, beta, g, state, out_state, o)
     return o, out_state
+
+
+def dn_state_affine(A, S, B, out, stream=None):
+    """out_i = A_i S_i + B_i over the leading dimensions: A [..., dk, dk], S, B, out
+    [..., dk, dv], float32 device tensors (B may be None)."""
+    dk, dv = S.shape[-2], S.shape[-1]
+    count = S.numel() // (dk * dv) if S.numel() else 0
+    for t in (A, S, B, out):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise TypeError("dn_state_affine takes contiguous float32 tensors")
+    rc = lib().dn_state_affine(_p(A), _p(S), _p(B), _p(out), count, dk, dv, _stream(stream))
+    _check(rc, "dn_state_affine")
 
 
 def dn_device_status(ws, stream=None) -> int:

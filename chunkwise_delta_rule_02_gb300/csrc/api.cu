@@ -8,6 +8,7 @@
 
 #include <mutex>
 
+#include "affine.h"
 #include "common.cuh"
 #include "decode.h"
 #include "fast.h"
@@ -358,6 +359,25 @@ dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, c
                                      (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta,
                                      (__nv_bfloat16 *)o, st);
     return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+dn_status dn_state_affine(const float *A, const float *S, const float *B, float *out, int count,
+                          int dk, int dv, void *stream)
+{
+    if (count < 0 || dk < 1 || dv < 1 || dk > kMaxD || dv > kMaxD) return DN_ERR_INVALID_ARG;
+    if (count == 0) return DN_OK;
+    if (count > 65535) return DN_ERR_UNSUPPORTED;
+    if (!A || !S || !out) return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {A, S, B, out};
+    for (const void *p : ptrs)
+        if (p && ((uintptr_t)p & 3u)) return DN_ERR_INVALID_ARG;
+    // out may not overlap A or S (other CTAs still read them while it is written)
+    const uintptr_t o0 = (uintptr_t)out, o1 = o0 + (size_t)count * dk * dv * sizeof(float);
+    const uintptr_t a0 = (uintptr_t)A, a1 = a0 + (size_t)count * dk * dk * sizeof(float);
+    const uintptr_t s0 = (uintptr_t)S, s1 = s0 + (size_t)count * dk * dv * sizeof(float);
+    if ((o0 < a1 && a0 < o1) || (o0 < s1 && s0 < o1)) return DN_ERR_INVALID_ARG;
+    return aff::state_affine(A, S, B, out, count, dk, dv, (cudaStream_t)stream) == cudaSuccess ? DN_OK
+                                                                                             : DN_ERR_CUDA;
 }
 
 size_t dn_host_arena_size(const dn_shape *s, int gated, int with_h0)

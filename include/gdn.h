@@ -157,6 +157,23 @@ dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, c
                           const void *beta, const float *g, const float *state_in,
                           float *state_out, void *o, void *stream);
 
+/* Batched affine map of states: out_i = A_i S_i + B_i for i < count, fp32.
+ * The recurrence is linear in the state ("Gated DeltaNet" rebuttal, Table 1,
+ * row "Gated DeltaNet": S_t = S_{t-1} alpha_t (I - beta_t k_t k_t^T) + ...),
+ * so the state leaving a span of tokens is A S + B, with A the product of the
+ * span's transitions (the final state of a forward call with v = 0 and
+ * h0 = I) and B the span's own final state from a zero state (a forward call
+ * with h0 = NULL).  Composing these maps over consecutive spans in order gives
+ * every span its entering state: the exchange step of a forward split along the
+ * sequence (each GPU, or each pass, owning a span).
+ *   A   [count][dk][dk], S, B, out [count][dk][dv], all device float32,
+ *       row-major, 4-byte aligned; B may be NULL (zero); out must not overlap A
+ *       or S (DN_ERR_INVALID_ARG), it may be B.
+ * count <= 65535 (DN_ERR_UNSUPPORTED above), dk, dv in 1..256.  Asynchronous
+ * on `stream`; allocates nothing.                                               */
+dn_status dn_state_affine(const float *A, const float *S, const float *B, float *out, int count,
+                          int dk, int dv, void *stream);
+
 /* Bytes of the device staging arena gdn_chunk_fwd_host needs (0 on bad args). */
 size_t dn_host_arena_size(const dn_shape *shape, int gated, int with_h0);
 

@@ -137,3 +137,21 @@ def test_workloads_are_seeded_and_shaped():
     full = W.generate(W.WORKLOADS["gdn_fwd_bf16_varlen_h32_n8_t65536"])
     assert full["q"].shape == (1, 32, 65536, 128)
     assert full["cu_seqlens"].tolist()[-1] == 65536
+
+
+def test_state_affine_checks_its_arguments_on_the_host(gdn):
+    """dn_state_affine rejects bad sizes, misaligned pointers and an output that
+    overlaps A or S before launching anything (no device is touched here)."""
+    lib = gdn.lib()
+    base = 1 << 20
+    ok_ptrs = (base, base + 0x100000, base + 0x200000, base + 0x300000)
+    assert lib.dn_state_affine(*ok_ptrs[:4], 0, 16, 16, None) == gdn.DN_OK          # nothing to do
+    assert lib.dn_state_affine(*ok_ptrs[:4], -1, 16, 16, None) == gdn.DN_ERR_INVALID_ARG
+    assert lib.dn_state_affine(*ok_ptrs[:4], 2, 300, 16, None) == gdn.DN_ERR_INVALID_ARG
+    assert lib.dn_state_affine(*ok_ptrs[:4], 70000, 16, 16, None) == gdn.DN_ERR_UNSUPPORTED
+    assert lib.dn_state_affine(base + 2, *ok_ptrs[1:4], 2, 16, 16, None) == gdn.DN_ERR_INVALID_ARG
+    # out overlapping S, then A
+    assert lib.dn_state_affine(base, base + 0x100000, None, base + 0x100000 + 64, 2, 16, 16,
+                               None) == gdn.DN_ERR_INVALID_ARG
+    assert lib.dn_state_affine(base, base + 0x100000, None, base + 1024, 2, 16, 16,
+                               None) == gdn.DN_ERR_INVALID_ARG
