@@ -28,6 +28,7 @@
 // reports a timeout through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "fast.h"
 #include "prep_math.cuh"
@@ -64,13 +65,19 @@ constexpr int NTHREADS = 512;
 constexpr int RING = 9;   // deeper rings spill packages from L2 to HBM (10 slots: +78 MB per launch)
 // control block, in 32-bit words: line 0 holds the task counter [0] and Jmax [1];
 // then one 128-byte line per chain CTA for its consumed count and one for its
-// RING ready flags, so that pollers and the task counter do not share lines
+// RING ready flags, so that pollers and the task counter do not share lines; the
+// last line holds the launch-wide abort word (set by the first CTA whose bounded
+// wait runs out, polled by every cross-CTA wait so that the launch winds down)
 constexpr int CTL_LINE = 32;
 static_assert(RING <= CTL_LINE, "ready flags of one chain CTA fit one line");
-__host__ __device__ constexpr size_t ctl_words(int nc) { return (size_t)CTL_LINE * (1 + 2 * (size_t)nc); }
+__host__ __device__ constexpr size_t ctl_words(int nc) { return (size_t)CTL_LINE * (2 + 2 * (size_t)nc); }
 __device__ __forceinline__ uint32_t *consumed_word(uint32_t *ctl, int c) { return ctl + CTL_LINE * (1 + c); }
 __device__ __forceinline__ uint32_t *ready_words(uint32_t *ctl, int nc, int c) { return ctl + CTL_LINE * (1 + nc + c); }
+__device__ __forceinline__ uint32_t *abort_word(uint32_t *ctl, int nc) { return ctl + CTL_LINE * (1 + 2 * nc); }
 constexpr long long BUDGET = 4000000000LL;                 // clock cycles (about 2 s)
+// With the test hook GDN_DEBUG_WITHHOLD_TASK set, the cross-CTA flag waits give up
+// after this many cycles (about 1 ms) instead of BUDGET.
+constexpr long long HOOK_FLAG_BUDGET = 2000000LL;
 constexpr float RENORM_BELOW = 9.313225746154785e-10f;      // 2^-30
 
 // package (ring slot in global memory and its copy in a chain CTA's shared memory)
@@ -139,6 +146,8 @@ struct Params {
     float scale, eps;
     int l2norm;
     int longhorn;           // step size beta / (1 + beta k^T k) instead of beta
+    int withhold;           // test hook: this task's package is never published (-1: none)
+    long long flag_budget;  // cycles a cross-CTA flag wait may take before it gives up
 };
 
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
@@ -220,6 +229,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint32_t *consumed = consumed_word(p.ctl, c);
     uint32_t *ready = ready_words(p.ctl, p.Nc, c);
+    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc);
     const uint8_t *ring = p.ring + (size_t)c * RING * PK_STRIDE;
 
     if (tid == 0) {
@@ -250,6 +260,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
         if (!*abort_flag) {
             *abort_flag = 1;
             raise_status(p.status, kStatusTimeout);
+            atomicExch((uint32_t *)gabort, 1u);
         }
     };
     auto wait = [&](int b, uint32_t k) -> bool {
@@ -278,12 +289,12 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 tma_load_2d(sm + CH_V + 8192, tm_v, &bar[B_VFULL], 64, row);
                 jv = j;
             }
-            if (*abort_flag) {
-                // let copies in flight land before shared memory goes away
-                for (int jj = (jk > 0 ? jk - 1 : 0); jj <= jk; ++jj)
-                    mbar_wait(&bar[B_KFULL + (jj & 1)], (uint32_t)(jj >> 1) & 1u, BUDGET, nullptr);
-                if (jv >= 0) mbar_wait(&bar[B_VFULL], (uint32_t)jv & 1u, BUDGET, nullptr);
-            }
+            // the last copies issued into each buffer have landed before shared memory
+            // goes away (on the normal path they have long since been consumed and
+            // these waits return at once; after an abort nothing else waits for them)
+            for (int jj = (jk > 0 ? jk - 1 : 0); jj <= jk; ++jj)
+                mbar_wait(&bar[B_KFULL + (jj & 1)], (uint32_t)(jj >> 1) & 1u, BUDGET, nullptr);
+            if (jv >= 0) mbar_wait(&bar[B_VFULL], (uint32_t)jv & 1u, BUDGET, nullptr);
         }
     } else if (warp == 2) {
         // ---------------------------------------------------------------- packages (bulk copies)
@@ -298,7 +309,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 const long long t0 = clock64();
                 unsigned ns = 32;
                 while (ld_acquire_gpu(&ready[slot]) != (uint32_t)(j + 1)) {
-                    if (*abort_flag || clock64() - t0 > BUDGET) { ok = false; break; }
+                    if (*abort_flag || *gabort || clock64() - t0 > p.flag_budget) { ok = false; break; }
                     __nanosleep(ns);
                     ns = ns < 256 ? 2 * ns : ns;
                 }
@@ -620,10 +631,12 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
     uint8_t *tl = base + PP_TL;
     const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
     const long long ntasks = (long long)p.Nc * Jmax;
+    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc);
     auto fail = [&]() {
         if (!*abort_flag) {
             *abort_flag = 1;
             raise_status(p.status, kStatusTimeout);
+            atomicExch((uint32_t *)gabort, 1u);
         }
     };
     auto wait = [&](int b, uint32_t k) -> bool {
@@ -642,6 +655,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         return false;
     };
     uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
+    uint32_t tma_phase = 0;   // (t == 0) barrier phase of the K, Q copy last issued
     bool tma_pending = false, mma_issued = false;
     uint32_t *pend_ready = nullptr;     // (t == 64) flag of a package still being written
     uint32_t pend_val = 0;
@@ -656,7 +670,8 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         }
         if (t == 0) {
             const int tk = (int)atomicAdd(&p.ctl[0], 1u);
-            *task_word = *abort_flag ? 0x7fffffff : tk;   // one decision for the whole pipeline
+            // one decision for the whole pipeline
+            *task_word = (*abort_flag || *gabort) ? 0x7fffffff : tk;
         }
         named_bar(bar_id, 128);
         const int task = *task_word;
@@ -666,6 +681,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         Item I;
         int n;
         if (!locate(c, j, I, n)) continue;
+        if (task == p.withhold) continue;   // test hook: the chain CTA's wait for it must run out
         if (c == 0 && t == 0) CTR(j, 12);
         const int len = min(C, I.L - n * C);
         const long long row0 = I.rowbase + (long long)n * C;
@@ -678,7 +694,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             const long long t0 = clock64();
             unsigned ns = 64;
             while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
-                if (clock64() - t0 > BUDGET) { fail(); break; }
+                if (*gabort || clock64() - t0 > p.flag_budget) { fail(); break; }
                 __nanosleep(ns);
                 ns = ns < 256 ? 2 * ns : ns;   // a freed slot is seen within ~0.3 us
             }
@@ -689,6 +705,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 tma_load_2d(tl + 8192, tm_q, &bar[P_FULL], 0, (int)row0);
                 tma_load_2d(tl + 24576, tm_q, &bar[P_FULL], 64, (int)row0);
                 tma_pending = true;
+                tma_phase = k_task;
                 if (c == 0) CTR(j, 13);
             }
         }
@@ -978,7 +995,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
     }
     if (t == 0) {
         // nothing of this pipeline may still be in flight when the block exits
-        if (tma_pending) mbar_wait(&bar[P_FULL], k_task & 1u, BUDGET, nullptr);
+        if (tma_pending) mbar_wait(&bar[P_FULL], tma_phase & 1u, BUDGET, nullptr);
         if (mma_issued) {
             mma_commit(&bar[P_DONE]);
             mbar_wait(&bar[P_DONE], 0, BUDGET, nullptr);
@@ -1144,6 +1161,18 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc;
     p.Jmax_fixed = g.varlen ? 0 : ((items + nc - 1) / nc) * ((g.T + C - 1) / C);
     p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm; p.longhorn = g.longhorn;
+    // Test hook (failure detection): GDN_DEBUG_WITHHOLD_TASK=n makes the preparation
+    // CTAs skip task n (chunk n / Nc of chain CTA n % Nc), so that chain CTA's bounded
+    // wait for the package runs out; every cross-CTA flag wait then gives up after
+    // about 1 ms, the launch winds down and the status word reports the timeout.
+    p.withhold = -1;
+    p.flag_budget = BUDGET;
+    if (const char *e = getenv("GDN_DEBUG_WITHHOLD_TASK")) {
+        if (e[0]) {
+            p.withhold = atoi(e);
+            p.flag_budget = HOOK_FLAG_BUDGET;
+        }
+    }
     cudaError_t e = cudaMemsetAsync(p.ctl, 0, ctl_bytes, st);
     if (e != cudaSuccess) return e;
     if (g.varlen) {
