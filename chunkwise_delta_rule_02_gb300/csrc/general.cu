@@ -585,13 +585,15 @@ __global__ void __launch_bounds__(256) k_bscan(Geo g, const Tin *__restrict__ dO
 
 __device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const __nv_bfloat16 *p, bool trans)
 {
+    // the "memory" clobber: the statement reads shared memory through an address held
+    // in a register, so the compiler must not move shared-memory stores across it
     const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
     if (trans)
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
     else
         asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
 }
 
 // acc (the warp's 32 x 32 tile at m0, n0: two 16-row halves of four 16 x 8
