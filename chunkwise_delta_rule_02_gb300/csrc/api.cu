@@ -115,6 +115,7 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast,
 gen::Ws general_ws(const Layout &L, char *base)
 {
     gen::Ws w;
+    memset(&w, 0, sizeof(w));
     auto F = [&](size_t o) { return o ? (float *)(base + o) : (float *)nullptr; };
     w.Kn = F(L.Kn); w.Qn = F(L.Qn); w.W = F(L.W); w.U = F(L.U); w.Unew = F(L.Unew);
     w.gam = F(L.gam); w.eb = F(L.eb); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
@@ -270,7 +271,10 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
     int path, n;
     if (for_backward) {
         path = DN_PATH_GENERAL;
-        n = 6 + offsets;                    // k_prep, k_scan, k_bscan, k_bbig, k_bchunk, k_bgrad
+        // k_prep, k_scan, k_bscan, then k_bwd_tc (tcgen05) or k_bbig, k_bchunk, k_bgrad;
+        // the pointer alignment the tcgen05 kernel also needs is not known here
+        const void *aligned = (const void *)(uintptr_t)256;
+        n = (gen::bwd_uses_tc(g, shape->dtype, aligned, aligned, aligned, aligned) ? 4 : 6) + offsets;
     } else if (!fast_ok(shape, g, 0)) {
         path = DN_PATH_GENERAL;
         n = 3 + offsets;                    // k_prep, k_scan, k_out

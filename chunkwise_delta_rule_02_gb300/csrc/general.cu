@@ -39,6 +39,10 @@
 
 #include "common.cuh"
 #include "general.h"
+
+#include <stdlib.h>
+
+#include "bwd_tc.h"
 #include "prep_math.cuh"
 
 namespace gdn {
@@ -629,34 +633,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[2][4][4], const __nv_bfloa
     }
 }
 
-// acc (32 x 32 tile at m0, n0) += A B over k in [0, K), K % 8 == 0, on the tensor
-// cores in tf32 (operands rounded to 10-bit mantissas, fp32 accumulation), from fp32
-// accessors A(m, k), B(k, n).
-template <class FA, class FB>
-__device__ __forceinline__ void tile_tf32(float (&acc)[2][4][4], FA A, FB B, int m0, int n0, int K)
-{
-    const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
-    for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t a[2][4], b[4][2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int m = m0 + 16 * h + gq;
-            a[h][0] = prep::tf32(A(m, k0 + t));
-            a[h][1] = prep::tf32(A(m + 8, k0 + t));
-            a[h][2] = prep::tf32(A(m, k0 + t + 4));
-            a[h][3] = prep::tf32(A(m + 8, k0 + t + 4));
-        }
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            b[jj][0] = prep::tf32(B(k0 + t, n0 + 8 * jj + gq));
-            b[jj][1] = prep::tf32(B(k0 + t + 4, n0 + 8 * jj + gq));
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) prep::mma_tf32_16x8x8(acc[h][jj], a[h], b[jj]);
-    }
-}
+using prep::tile_tf32;
 
 // Runs Body(m0, n0, acc) for every 32 x 32 tile of an M x N product (M, N % 32 == 0),
 // the tiles dealt round-robin to the warps, with acc zeroed; then St(m, n, v0, v1)
@@ -850,10 +827,19 @@ __global__ void __launch_bounds__(512) k_scan_st(Geo g, const float *__restrict_
         const float gC = rgC;
         float *Un = w.Unew + slot * C * dv;
         float *Sin = w.Sin + slot * dk * dv;
+        __nv_bfloat16 *Unb = w.Un_b ? w.Un_b + slot * C * dv : nullptr;
         if ((int)threadIdx.x < C) sE[threadIdx.x] = (int)threadIdx.x < len ? expf(gC - rg) : 0.f;
-        for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
-            const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
-            reinterpret_cast<float4 *>(Sin)[idx] = *reinterpret_cast<const float4 *>(sS + kk * LS + n);
+        if (w.Sin_b) {
+            __nv_bfloat16 *Sb16 = w.Sin_b + slot * dk * dv;
+            for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+                const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+                put_bf4(Sb16 + 4 * idx, *reinterpret_cast<const float4 *>(sS + kk * LS + n), 1.f);
+            }
+        } else {
+            for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+                const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+                reinterpret_cast<float4 *>(Sin)[idx] = *reinterpret_cast<const float4 *>(sS + kk * LS + n);
+            }
         }
         __syncthreads();
         reg_put(rW, C, dk, [&](int r, int kk, float4 v) { put_bf4(Wt + r * LK + kk, v, 1.f); });
@@ -866,7 +852,8 @@ __global__ void __launch_bounds__(512) k_scan_st(Geo g, const float *__restrict_
               [&](int r, int n, float a0, float a1) {
                   const bool live = r < len;
                   const float u0 = live ? sU[r * dv + n] - a0 : 0.f, u1 = live ? sU[r * dv + n + 1] - a1 : 0.f;
-                  if (live) *reinterpret_cast<float2 *>(Un + r * dv + n) = make_float2(u0, u1);
+                  if (Unb) put_bf2(Unb + r * dv + n, u0, u1);
+                  else if (live) *reinterpret_cast<float2 *>(Un + r * dv + n) = make_float2(u0, u1);
                   put_bf2(Ub + r * LV + n, u0, u1);
               });
         __syncthreads();
@@ -965,14 +952,23 @@ __global__ void __launch_bounds__(512) k_bscan_st(Geo g, const __nv_bfloat16 *__
         const float gC = rgC;
         float *dUg = w.dUn + slot * C * dv;
         float *dSo = w.dSo + slot * dk * dv;
+        __nv_bfloat16 *dUb16 = w.dUn_b ? w.dUn_b + slot * C * dv : nullptr;
         if ((int)threadIdx.x < C) {
             const bool live = (int)threadIdx.x < len;
             sE[threadIdx.x] = live ? expf(gC - rg) : 0.f;
             sG[threadIdx.x] = live ? expf(rg) : 0.f;
         }
-        for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
-            const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
-            reinterpret_cast<float4 *>(dSo)[idx] = *reinterpret_cast<const float4 *>(sdS + kk * LS + n);
+        if (w.dSo_b) {
+            __nv_bfloat16 *dS16 = w.dSo_b + slot * dk * dv;
+            for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+                const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+                put_bf4(dS16 + 4 * idx, *reinterpret_cast<const float4 *>(sdS + kk * LS + n), 1.f);
+            }
+        } else {
+            for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+                const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+                reinterpret_cast<float4 *>(dSo)[idx] = *reinterpret_cast<const float4 *>(sdS + kk * LS + n);
+            }
         }
         __syncthreads();
         // P's columns i >= len are not written by the preparation; they only reach rows
@@ -1004,7 +1000,8 @@ __global__ void __launch_bounds__(512) k_bscan_st(Geo g, const __nv_bfloat16 *__
               },
               [&](int i, int n, float u0, float u1) {
                   const bool live = i < len;
-                  if (live) *reinterpret_cast<float2 *>(dUg + i * dv + n) = make_float2(u0, u1);
+                  if (dUb16) put_bf2(dUb16 + i * dv + n, live ? u0 : 0.f, live ? u1 : 0.f);
+                  else if (live) *reinterpret_cast<float2 *>(dUg + i * dv + n) = make_float2(u0, u1);
                   put_bf2(dUb + i * LV + n, live ? u0 : 0.f, live ? u1 : 0.f);
               });
         __syncthreads();
@@ -2425,13 +2422,45 @@ cudaError_t fwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
     return cudaPeekAtLastError();
 }
 
+// GDN_BWD_STAGED=1 keeps the staged warp-level per-chunk kernels for shapes the
+// tcgen05 per-chunk backward takes (used by the tests to compare the two).
+static bool force_staged_bwd()
+{
+    const char *e = getenv("GDN_BWD_STAGED");
+    return e && e[0] && e[0] != '0';
+}
+
+bool bwd_uses_tc(const Geo &g, int dtype, const void *q, const void *k, const void *v, const void *dO)
+{
+    return dtype == DN_BF16 && staged_ok(g) && btc::supports(g, dtype) && !force_staged_bwd() &&
+           ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)dO) & 15u) == 0);
+}
+
 template <class Tin>
 cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,
                 const float *gate, const float *h0, const Tin *dO, const float *dhT, Tin *dq,
                 Tin *dk, Tin *dv, Tin *dbeta, float *dg, float *dh0, const Ws &w,
                 cudaStream_t st)
 {
-    cudaError_t e = forward_states(g, q, k, v, beta, gate, h0, nullptr, w, st);
+    cudaError_t e;
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (bwd_uses_tc(g, DN_BF16, q, k, v, dO)) {
+            // recompute and the two staged scans, writing bf16 states and Unew / dUnew
+            // (over the fp32 arrays they replace), then the tcgen05 per-chunk gradients
+            Ws w2 = w;
+            w2.Sin_b = reinterpret_cast<__nv_bfloat16 *>(w.Sin);
+            w2.dSo_b = reinterpret_cast<__nv_bfloat16 *>(w.dSo);
+            w2.Un_b = reinterpret_cast<__nv_bfloat16 *>(w.Unew);
+            w2.dUn_b = reinterpret_cast<__nv_bfloat16 *>(w.dUn);
+            if ((e = forward_states(g, q, k, v, beta, gate, h0, nullptr, w2, st)) != cudaSuccess) return e;
+            if ((e = set_smem(k_bscan_st, smem_bscan_st(g))) != cudaSuccess) return e;
+            if (g.N > 0) k_bscan_st<<<dim3(g.N, g.H), 512, smem_bscan_st(g), st>>>(g, dO, dhT, dh0, w2);
+            if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+            return btc::grads(g, q, k, v, beta, gate, dO, w2.Sin_b, w2.dSo_b, w2.Un_b, w2.dUn_b, dq, dk, dv,
+                              dbeta, dg, st);
+        }
+    }
+    e = forward_states(g, q, k, v, beta, gate, h0, nullptr, w, st);
     if (e != cudaSuccess) return e;
     if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
         if (use_staged<Tin>(g, dO)) {

@@ -18,12 +18,20 @@ struct Ws {
     float *P;                  // [slots][C][C]   lower(Q K^T o D), diagonal kept
     float *aux;                // backward [slots][4C + 4]: row sums, <dS_out, S_in>, d gamma / d beta partials
     float *M3;                 // backward [slots][3][C][C]: dP o D, (I + A)^-1, dKK
+    // bf16 copies for the tcgen05 per-chunk backward (null otherwise): when set, the
+    // staged scans write these instead of Sin / Unew (forward scan) and dSo / dUn
+    // (backward scan), with the rows past a chunk's end as zeros
+    __nv_bfloat16 *Sin_b, *dSo_b;   // [slots][dk][dv]
+    __nv_bfloat16 *Un_b, *dUn_b;    // [slots][C][dv]
 };
 
 template <class Tin>
 cudaError_t fwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,
                 const float *gate, const float *h0, Tin *o, float *hT, const Ws &w,
                 cudaStream_t st);
+
+// Whether gdn_chunk_bwd takes the tcgen05 per-chunk backward for this call.
+bool bwd_uses_tc(const Geo &g, int dtype, const void *q, const void *k, const void *v, const void *dO);
 
 template <class Tin>
 cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,

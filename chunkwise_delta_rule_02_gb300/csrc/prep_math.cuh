@@ -44,6 +44,35 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// acc (32 x 32 tile at m0, n0) += A B over k in [0, K), K % 8 == 0, on the tensor
+// cores in tf32 (operands rounded to 10-bit mantissas, fp32 accumulation), from fp32
+// accessors A(m, k), B(k, n).
+template <class FA, class FB>
+__device__ __forceinline__ void tile_tf32(float (&acc)[2][4][4], FA A, FB B, int m0, int n0, int K)
+{
+    const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t a[2][4], b[4][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int m = m0 + 16 * h + gq;
+            a[h][0] = tf32(A(m, k0 + t));
+            a[h][1] = tf32(A(m + 8, k0 + t));
+            a[h][2] = tf32(A(m, k0 + t + 4));
+            a[h][3] = tf32(A(m + 8, k0 + t + 4));
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            b[jj][0] = tf32(B(k0 + t, n0 + 8 * jj + gq));
+            b[jj][1] = tf32(B(k0 + t + 4, n0 + 8 * jj + gq));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) mma_tf32_16x8x8(acc[h][jj], a[h], b[jj]);
+    }
+}
+
 // X = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row stride
 // AST floats), called by the 128 threads of one warpgroup (warp q4 = 0..3 in the
 // group, lane = lane id).  Diagonal 16 x 16 blocks by substitution (warp w:
@@ -143,9 +172,16 @@ __device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, 
         }
         __syncwarp();   // every lane has read A_ii before its block is overwritten
         if (lane < 16) {
-            float4 *dst = reinterpret_cast<float4 *>(AX + (base + c) * AST + base);
+            if constexpr (AST % 4 == 0) {
+                float4 *dst = reinterpret_cast<float4 *>(AX + (base + c) * AST + base);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            } else {
+                static_assert(AST % 2 == 0, "rows must stay 8-byte aligned");
+                float2 *dst = reinterpret_cast<float2 *>(AX + (base + c) * AST + base);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[q] = make_float2(x[2 * q], x[2 * q + 1]);
+            }
         }
     }
     sm100::named_bar(bar_id, 128);
