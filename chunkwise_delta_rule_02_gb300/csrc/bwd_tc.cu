@@ -64,6 +64,8 @@ namespace {
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int NTHREADS = 512;
+constexpr int NCOMPUTE = NTHREADS - 32;    // warps 0..14 compute; warp 15 issues the copies
+constexpr int NCWARPS = NCOMPUTE / 32;
 constexpr long long BUDGET = 4000000000LL;   // clock cycles (about 2 s) for any one wait
 
 // shared memory (bytes from a 1024-aligned base).  Tiles are bf16 with the 128-byte
@@ -80,7 +82,8 @@ constexpr uint32_t SM_XTRA = SM_BAR + 1024;   // two fp32 C x C buffers of their
 constexpr int AST = 66;                    // row stride (floats) of the fp32 C x C buffers: rows
                                            // 8-byte aligned, a column touches 16 banks
 constexpr uint32_t FBYTES = 64 * AST * 4;  // one fp32 C x C buffer
-constexpr uint32_t SM_END = SM_XTRA + FBYTES;
+constexpr uint32_t SM_OUT = SM_XTRA + 17408;   // dq, dk tiles (bf16, 16 KB each) for the tensor stores
+constexpr uint32_t SM_END = SM_OUT + 32768;
 constexpr uint32_t SMEM_BYTES = SM_END + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t UOD_HALF = 24576;
@@ -90,7 +93,9 @@ constexpr uint32_t F_AX = SM_S;                // fp32 [64][AST]: A, then the pa
 constexpr uint32_t F_KD = SM_S + FBYTES;       // K^K^T o D (strict lower), then dKK
 constexpr uint32_t F_G = SM_S + 2 * FBYTES;    // P, then dP o P, then E
 static_assert(SM_S + 3 * FBYTES <= SM_VEC, "fp32 buffers over S_in, dS_out");
-constexpr uint32_t F_TMP = SM_XTRA;            // Linv o dT
+constexpr uint32_t F_TMP = SM_XTRA;            // Linv o dT, then the dv tile
+static_assert(FBYTES <= 17408 && SM_XTRA % 1024 == 0, "dv tile over the Linv o dT buffer");
+constexpr uint32_t T_DQ = SM_OUT, T_DK = SM_OUT + 16384, T_DV = SM_XTRA;   // [64 rows][128] bf16, two 8 KB halves
 constexpr uint32_t T_Z = SM_UOD;           // Z rows (over Unew): half h at h * UOD_HALF
 constexpr uint32_t T_DP = SM_UOD + 8192;   // (dP o D) n_i [r][i] (over dO, half 0)
 constexpr uint32_t T_DP2 = SM_UOD + UOD_HALF + 8192;   // (dP o D) m_r [r][i] (over dO, half 1)
@@ -119,7 +124,7 @@ constexpr uint32_t TM_X = 256;    // X (lanes 0..63) until the end
 constexpr uint32_t TM_DP = 384;   // dO Unew^T (64 columns) -> T^T dUnew accumulator (128)
 constexpr uint32_t TM_ADJ = 384;  // X2 (64 columns), dA' = X2 Linv^T (64 columns), after dO Unew^T is read
 
-enum { B_TMA = 0, B_M1, B_M4, B_M5, B_X2, B_DA, B_M6, B_KQFREE, B_DRAIN, NBAR };
+enum { B_TMA = 0, B_M1, B_M4, B_M5, B_X2, B_DA, B_M6, B_KQFREE, B_SDSFREE, B_DRAIN, NBAR };
 
 constexpr uint32_t ID_128_128 = idesc(1, 128, 128, false, false);
 constexpr uint32_t ID_128_64 = idesc(1, 128, 64, false, false);
@@ -190,6 +195,17 @@ __device__ __forceinline__ void put_row16(uint8_t *half, int row, int c0, const 
     }
 }
 
+// N consecutive floats of an fp32 C x C buffer row (rows only 8-byte aligned) into registers
+template <int N>
+__device__ __forceinline__ void rowN(const float *v, float (&x)[N])
+{
+#pragma unroll
+    for (int q = 0; q < N / 2; ++q) {
+        const float2 t = reinterpret_cast<const float2 *>(v)[q];
+        x[2 * q] = t.x; x[2 * q + 1] = t.y;
+    }
+}
+
 __device__ __forceinline__ float warp_sum32(float v)
 {
 #pragma unroll
@@ -205,7 +221,8 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
          const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_ds,
          const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_du,
-         const Params p)
+         const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+         const __grid_constant__ CUtensorMap tm_dv, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -319,29 +336,61 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             tma_prefetch_2d(&tm_ds, x, slot * D); tma_prefetch_2d(&tm_ds, x, slot * D + 64);
         }
     };
-    // Thread 0 issues the MMAs; the copies are issued by a lane of the last warp, which
-    // has no epilogue work where they are issued (a thread can stall on issuing copies
-    // while earlier ones are in flight, and would hold up its warp and every barrier).
-    // A task's copies go out in three parts, each as soon as the previous task no
-    // longer needs the space: the states, then Unew, dO, dUnew and V, then K and Q.
-    const bool producer = tid == NTHREADS - 32;
-    bool mma_issued = false, tma_pending = false;
-    int issued_parts = 0;   // (producer) parts of the next task's copies issued
+    // Warp 15 (one lane) issues every copy and takes no part in the compute barriers: a
+    // thread can stall on issuing copies while earlier ones are in flight.  A task's
+    // copies go out in three parts, each as soon as the previous task no longer needs
+    // the space (mbarriers): the states once its F / E pass has read the fp32 buffers
+    // over them, then Unew, dO, dUnew and V once its last products have completed, then
+    // K and Q once its last epilogue has read its K rows.  Thread 0 issues the MMAs.
+    // A staged output tile (rows of the chunk, two 64-column halves) to global memory:
+    // the tensor store by thread 0 for a whole chunk, else the chunk's rows by the compute
+    // threads with plain 16-byte stores, consecutive threads along a row.
+    auto store_tile = [&](const CUtensorMap *map, uint32_t tile, __nv_bfloat16 *out, long long row, int len) {
+        if (len == C) {
+            if (tid == 0) {
+                tma_store_2d(map, sm + tile, 0, (int)row);
+                tma_store_2d(map, sm + tile + 8192, 64, (int)row);
+                bulk_commit();
+            }
+        } else {
+            for (int e = tid; e < len * 16; e += NCOMPUTE) {
+                const int r = e >> 4, c16 = e & 15, hh = c16 >> 3;
+                const uint4 v = *reinterpret_cast<const uint4 *>(sm + tile + hh * 8192 + sw128(r, (c16 & 7) * 16));
+                reinterpret_cast<uint4 *>(out + (row + r) * D)[c16] = v;
+            }
+        }
+    };
+    bool mma_issued = false;
     uint32_t it = 0;   // tasks run by this CTA (barrier phases)
+    if (warp == NCWARPS) {
+        if (lane == 0) {
+            uint32_t n = 0;   // tasks whose copies have been issued (one B_TMA phase each)
+            int tt = next_valid(blockIdx.x);
+            while (tt < p.ntasks) {
+                if (n > 0 && !mbar_wait(&bar[B_SDSFREE], (n - 1) & 1u, BUDGET, s_abort)) break;
+                issue_sds(tt);
+                bool ok = n == 0 || mbar_wait(&bar[B_M6], (n - 1) & 1u, BUDGET, s_abort);
+                issue_uodv(tt);   // issued either way, so that the phase the first part opened completes
+                ok = ok && (n == 0 || mbar_wait(&bar[B_KQFREE], (n - 1) & 1u, BUDGET, s_abort));
+                issue_kq(tt);
+                ++n;
+                const int tn = next_valid(tt + gridDim.x);
+                // the task after into L2 once this task's copies have landed (its compute starts)
+                ok = ok && mbar_wait(&bar[B_TMA], (n - 1) & 1u, BUDGET, s_abort);
+                if (ok && tn < p.ntasks) prefetch_l2(tn);
+                if (!ok) break;
+                tt = tn;
+            }
+            // every copy issued has landed before the block exits
+            if (n > 0) mbar_wait(&bar[B_TMA], (n - 1) & 1u, BUDGET, nullptr);
+        }
+    } else {
     int t = next_valid(blockIdx.x);
-    if (producer && t < p.ntasks) {
-        issue_sds(t);
-        issue_uodv(t);
-        issue_kq(t);
-        tma_pending = true;
-    }
     while (t < p.ntasks) {
         int j, h, b, t0, len;
         task_of(t, j, h, b, t0, len);
         const long long row = ((long long)b * g.H + h) * g.T + t0;   // first token of the chunk
         const int tnext = next_valid(t + gridDim.x);
-        if (producer && tnext < p.ntasks) prefetch_l2(tnext);   // into L2 while this task runs
-        issued_parts = 0;
         BTR(it, 0);
         // beta, g of the chunk; gamma by a warp scan, in log2 units
         if (warp == 0) {
@@ -370,10 +419,12 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if (lane == 0) *s_safe = mx < 100.f;
         }
-        if (wait(B_TMA, it)) tma_pending = false;
+        wait(B_TMA, it);
+        // the previous task's tensor stores have read their staged tiles (long since)
+        if (tid == 0) bulk_wait_read();
         if (len < C) {
             // rows past the chunk's end are zero in every token tile
-            for (int e = tid; e < (C - len) * 6 * 2 * 8; e += NTHREADS) {
+            for (int e = tid; e < (C - len) * 6 * 2 * 8; e += NCOMPUTE) {
                 const int r = len + e / 96, rest = e % 96, tile = rest / 16, piece = rest % 16;
                 const int hh = piece >> 3, c16 = piece & 7;
                 uint32_t base;
@@ -389,7 +440,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             }
             fence_async_smem();
         }
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         if (*s_abort) break;
         BTR(it, 1);
         const float gC = V(V_GAM)[len - 1];
@@ -422,7 +473,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             // two rows per warp step, 16-byte pieces over the lanes
             float acc = 0.f;
             const int hh = (lane >> 3) & 1, c16 = lane & 7;
-            for (int kk = 2 * warp + (lane >> 4); kk < D; kk += 32) {
+            for (int kk = 2 * warp + (lane >> 4); kk < D; kk += 2 * NCWARPS) {
                 const uint32_t off = hh * 16384 + sw128(kk, c16 * 16);
                 const uint4 a = *reinterpret_cast<const uint4 *>(sm + SM_S + off);
                 const uint4 d = *reinterpret_cast<const uint4 *>(sm + SM_DS + off);
@@ -448,27 +499,28 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             const int r = (q4 & 1) * 32 + lane;
             const float nrm = r < len ? (g.l2norm ? rsqrtf(dg + g.eps) : 1.f) : 0.f;
             if (q4 < 2) {
+                // the key row's norm, k^T k after it, the step size, Gamma n
+                const float kap = dg * nrm * nrm;
+                float bt = V(V_BETA)[r];
+                if (g.longhorn) bt = bt / fmaf(bt, kap, 1.f);
                 V(V_N)[r] = nrm;
-                V(V_KAP)[r] = dg * nrm * nrm;
+                V(V_KAP)[r] = kap;
+                V(V_B)[r] = bt;
+                V(V_GN)[r] = V(V_G)[r] * nrm;
             } else {
                 V(V_M)[r] = nrm;
             }
         }
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         float sds = 0.f;   // <dS_out, S_in>
-        for (int w = 0; w < 16; ++w) sds += red[RED_SDS + w];
-        if (tid < 64) {
-            float bt = V(V_BETA)[tid];
-            if (g.longhorn) bt = bt / fmaf(bt, V(V_KAP)[tid], 1.f);
-            V(V_B)[tid] = bt;
-            V(V_GN)[tid] = V(V_G)[tid] * V(V_N)[tid];
-        }
-        __syncthreads();
+        for (int w = 0; w < NCWARPS; ++w) sds += red[RED_SDS + w];
         BTR(it, 3);
         // ------------------------------------------------------------------ first epilogues
         const float *gam = V(V_GAM);
         const bool safe = *s_safe != 0;
-        // D_ri = exp(gamma_r - gamma_i) for i <= r
+        // D_ri = exp(gamma_r - gamma_i) for i <= r: exp(gamma_r) exp(-gamma_i) while both stay
+        // in range.  (Each loop below computes into registers and stores after the loop, so
+        // that its reads of the vectors need not wait for stores through other pointers.)
         auto Dri = [&](int r, int i) { return safe ? V(V_G)[r] * V(V_GI)[i] : ex2f(gam[r] - gam[i]); };
         if (q4 < 2) {
             const int r = q4 * 32 + lane;   // chunk row (lanes 0..63)
@@ -481,9 +533,13 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int i = 32 * cg + e;
-                    const float kd = (i < r && r < len) ? nr * V(V_N)[i] * v[e] * Dri(r, i) : 0.f;
-                    fKD[r * AST + i] = kd;
-                    fAX[r * AST + i] = br * kd;
+                    v[e] = (i < r && r < len) ? nr * V(V_N)[i] * v[e] * Dri(r, i) : 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int i = 32 * cg + e;
+                    *reinterpret_cast<float2 *>(fKD + r * AST + i) = make_float2(v[e], v[e + 1]);
+                    *reinterpret_cast<float2 *>(fAX + r * AST + i) = make_float2(br * v[e], br * v[e + 1]);
                 }
             }
         } else {
@@ -497,23 +553,28 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int i = 32 * cg + e;
-                    fG[r * AST + i] = (i <= r && r < len) ? mr * V(V_N)[i] * v[e] * Dri(r, i) : 0.f;
+                    v[e] = (i <= r && r < len) ? mr * V(V_N)[i] * v[e] * Dri(r, i) : 0.f;
                 }
-            } else {
-                // Z = dUnew S_in^T into the Z tile (bf16 rows), one 64-column half per warp group
-                const int hh = cg - 2;
-                float v[32];
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    tld32(tmem + lrow + TM_YZ + 64 * hh + 32 * part, v);
-                    tmem_ld_wait();
-                    put_row32(sm + T_Z + hh * UOD_HALF, r, 32 * part, v);
+                for (int e = 0; e < 32; e += 2)
+                    *reinterpret_cast<float2 *>(fG + r * AST + 32 * cg + e) = make_float2(v[e], v[e + 1]);
+            } else if (warp < NCWARPS) {
+                // Z = dUnew S_in^T into the Z tile (bf16 rows): warps 10 and 14 one 64-column
+                // half each of lanes 64..95, warp 11 both halves of lanes 96..127
+                float v[32];
+                for (int hh = (q4 == 3 ? 0 : cg - 2); hh <= (q4 == 3 ? 1 : cg - 2); ++hh) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        tld32(tmem + lrow + TM_YZ + 64 * hh + 32 * part, v);
+                        tmem_ld_wait();
+                        put_row32(sm + T_Z + hh * UOD_HALF, r, 32 * part, v);
+                    }
                 }
             }
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         if (tid == 0) {
             // ---------------------------------------------------------- dT parts: Z K^T | dUnew V^T
             tc_fence_after();
@@ -540,9 +601,16 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 const bool keep = i <= r && r < len;
                 const float dp = keep ? sc * v[e] : 0.f;
                 const float dpd = keep ? dp * Dri(r, i) : 0.f;
-                fG[r * AST + i] *= dp;        // dP o P
+                v[e] = dp;
                 dp1[e] = dpd * V(V_N)[i];
                 dp2[e] = dpd * mr;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                // dP o P over P's row
+                float2 *pp = reinterpret_cast<float2 *>(fG + r * AST + 32 * cg + e);
+                const float2 pv = *pp;
+                *pp = make_float2(pv.x * v[e], pv.y * v[e + 1]);
             }
             put_row32(sm + T_DP, r, 32 * cg, dp1);
             put_row32(sm + T_DP2, r, 32 * cg, dp2);
@@ -551,7 +619,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             solve_unit_lower_64_packed<AST>(fAX, lane, (q4 - 2) + 2 * cg, 1);
         }
         fence_async_smem();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         wait(B_M4, it);
         tc_fence_after();
         BTR(it, 5);
@@ -569,8 +637,11 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 const int i = 32 * cg + e;
                 const float dt = (r < len && i < len) ? uv[e] - V(V_GN)[i] * wv[e] : 0.f;
                 tb[e] = dt * V(V_B)[i];
-                fTMP[r * AST + i] = i <= r ? fAX[i * AST + r] * dt : 0.f;   // Linv[r][i] dT[r][i]
+                wv[e] = i <= r ? fAX[i * AST + r] * dt : 0.f;   // Linv[r][i] dT[r][i]
             }
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+                *reinterpret_cast<float2 *>(fTMP + r * AST + 32 * cg + e) = make_float2(wv[e], wv[e + 1]);
             put_row32(sm + T_ADJ, r, 32 * cg, tb);
         } else if (q4 >= 2 && cg < 2) {
             // Linv [r][i] (r >= i) into its bf16 tile; Linv[r][i] = AX[i][r]
@@ -585,7 +656,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         if (tid == 0) {
             // ---------------------------------------------------------- dQ2 = (dP o D) diag(n) K,
             // X2 = Linv^T (dT diag b)
@@ -600,7 +671,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             mma_commit(&bar[B_X2]);
         }
         BTR(it, 6);
-        for (int i = warp; i < C; i += 16) {
+        for (int i = warp; i < C; i += NCWARPS) {
             // d b through T = Linv diag(b): column sums of Linv o dT
             float a = fTMP[lane * AST + i] + fTMP[(lane + 32) * AST + i];
             a = warp_sum32(a);
@@ -618,7 +689,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         if (tid == 0) {
             tc_fence_after();
             for (int k = 0; k < 4; ++k)
@@ -649,21 +720,13 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             red[cg * 64 + r] = pq;
             named_bar(2, 256);
             pq = red[r] + red[64 + r] + red[128 + r] + red[192 + r];
-            if (r < len) {
-                uint32_t w[16];
+            // dq row r, columns [32 cg, 32 cg + 32), into its staged tile
+            if (g.l2norm) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float a0 = y[2 * e], a1 = y[2 * e + 1];
-                    if (g.l2norm) {
-                        a0 = mr * (a0 - qx[2 * e] * mr * pq);
-                        a1 = mr * (a1 - qx[2 * e + 1] * mr * pq);
-                    }
-                    w[e] = pack_bf16(a0, a1);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.dq + (row + r) * D + 32 * cg);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                for (int e = 0; e < 32; ++e) y[e] = mr * (y[e] - qx[e] * mr * pq);
             }
+            put_row32(sm + T_DQ + (cg >> 1) * 8192, r, 32 * (cg & 1), y);
+            fence_async_smem();
         }
         wait(B_DA, it);
         tc_fence_after();
@@ -676,31 +739,39 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             tld16(tmem + lrow + TM_ADJ + 64 + 16 * cg, x);
             tmem_ld_wait();
             const float ba = V(V_B)[a];
+            float kdI[16], gI[16];
+            rowN(fKD + a * AST + 16 * cg, kdI);
+            rowN(fG + a * AST + 16 * cg, gI);
             float db = 0.f, rs = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int bb = 16 * cg + e;
                 const float dA = (bb < a && a < len) ? -x[e] : 0.f;
-                const float kd = fKD[a * AST + bb];
-                const float f = dA * kd;
-                const float ev = fmaf(ba, f, fG[a * AST + bb]);
+                const float f = dA * kdI[e];
+                const float ev = fmaf(ba, f, gI[e]);
                 db += f;
                 rs += ev;
-                fG[a * AST + bb] = ev;
-                fKD[a * AST + bb] = dA * ba * Dri(a, bb);
+                gI[e] = ev;
+                kdI[e] = dA * ba * Dri(a, bb);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                *reinterpret_cast<float2 *>(fG + a * AST + 16 * cg + e) = make_float2(gI[e], gI[e + 1]);
+                *reinterpret_cast<float2 *>(fKD + a * AST + 16 * cg + e) = make_float2(kdI[e], kdI[e + 1]);
             }
             // a region of their own: the dq epilogue's partials may still be being read
             red[RED_FE + cg * 64 + a] = db;
             red[RED_FE + 256 + cg * 64 + a] = rs;
         }
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
+        store_tile(&tm_dq, T_DQ, p.dq, row, len);
         if (tid < 64) {
             const float *rf = red + RED_FE;
             V(V_DB)[tid] += rf[tid] + rf[64 + tid] + rf[128 + tid] + rf[192 + tid];
             V(V_DG)[tid] += rf[256 + tid] + rf[320 + tid] + rf[384 + tid] + rf[448 + tid];
         }
-        for (int i = warp; i < C; i += 16) {
+        for (int i = warp; i < C; i += NCWARPS) {
             float cs = fG[lane * AST + i] + fG[(lane + 32) * AST + i];
             cs = warp_sum32(cs);
             if (lane == 0) V(V_CS)[i] = cs;
@@ -718,15 +789,10 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         BTR(it, 9);
         if (tid < 64) V(V_DG)[tid] -= V(V_CS)[tid];
-        // the next task's states: the fp32 buffers over them are no longer read
-        if (producer && tnext < p.ntasks && !*s_abort) {
-            issue_sds(tnext);
-            tma_pending = true;
-            issued_parts = 1;
-        }
+        if (tid == 0) mbar_arrive(&bar[B_SDSFREE]);   // the fp32 buffers over the states are no longer read
         if (tid == 0) {
             // ---------------------------------------------------------- dK, T^T dW, T^T dUnew
             tc_fence_after();
@@ -745,11 +811,6 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         }
         wait(B_M6, it);
         tc_fence_after();
-        // the next task's Unew, dO, dUnew, V: the last products have read those regions
-        if (producer && issued_parts == 1) {
-            issue_uodv(tnext);
-            issued_parts = 2;
-        }
         BTR(it, 10);
         // ------------------------------------------------------------------ dk, dv, d beta, dg
         if (q4 < 2) {
@@ -762,6 +823,7 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_KQFREE]);   // this task's K rows have been read
             tmem_ld_wait();
+            BTR(it, 13);
             const float bi = V(V_B)[i], gi = V(V_G)[i], ei = V(V_E)[i], ni = V(V_N)[i];
             float k2 = 0.f, pk = 0.f, kxs = 0.f;
 #pragma unroll
@@ -780,7 +842,9 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             float dvv[32];
             tld32(tmem + lrow + TM_DP + 32 * cg, dvv);
             tmem_ld_wait();
+            BTR(it, 14);
             named_bar(2, 256);
+            BTR(it, 15);
             k2 = red[i] + red[64 + i] + red[128 + i] + red[192 + i];
             pk = red[256 + i] + red[320 + i] + red[384 + i] + red[448 + i];
             if (cg == 0) V(V_K2)[i] = k2;
@@ -791,37 +855,23 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 dkap = -db * bi * bi;
                 pk = fmaf(2.f * dkap, kap, pk);
             }
-            if (i < len) {
-                uint32_t wk[16], wv[16];
+            // dk and dv rows i, columns [32 cg, 32 cg + 32), into their staged tiles
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float c0 = fmaf(2.f * dkap, kx[2 * e] * ni, ka[2 * e]);
-                    float c1 = fmaf(2.f * dkap, kx[2 * e + 1] * ni, ka[2 * e + 1]);
-                    if (g.l2norm) {
-                        c0 = ni * (c0 - kx[2 * e] * ni * pk);
-                        c1 = ni * (c1 - kx[2 * e + 1] * ni * pk);
-                    }
-                    wk[e] = pack_bf16(c0, c1);
-                    wv[e] = pack_bf16(bi * dvv[2 * e], bi * dvv[2 * e + 1]);
-                }
-                uint4 *dkp = reinterpret_cast<uint4 *>(p.dk + (row + i) * D + 32 * cg);
-                uint4 *dvp = reinterpret_cast<uint4 *>(p.dv + (row + i) * D + 32 * cg);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    dkp[q] = make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
-                    dvp[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-                }
+            for (int e = 0; e < 32; ++e) {
+                float c = fmaf(2.f * dkap, kx[e] * ni, ka[e]);
+                if (g.l2norm) c = ni * (c - kx[e] * ni * pk);
+                ka[e] = c;
+                dvv[e] *= bi;
             }
-        }
-        if (producer && issued_parts == 2) {
-            // the next task's K, Q once every epilogue warp has read this task's K rows
-            wait(B_KQFREE, it);
-            issue_kq(tnext);
-            issued_parts = 3;
+            put_row32(sm + T_DK + (cg >> 1) * 8192, i, 32 * (cg & 1), ka);
+            put_row32(sm + T_DV + (cg >> 1) * 8192, i, 32 * (cg & 1), dvv);
+            fence_async_smem();
         }
         tc_fence_before();
-        __syncthreads();
+        named_bar(3, NCOMPUTE);
         BTR(it, 11);
+        store_tile(&tm_dk, T_DK, p.dk, row, len);
+        store_tile(&tm_dv, T_DV, p.dv, row, len);
         if (warp == 0) {
             // d gamma, its reverse cumulative sum within the chunk (dg), and d beta
             const int r0 = lane, r1 = lane + 32;
@@ -866,22 +916,17 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                 p.dbeta[row + r] = __float2bfloat16_rn(db);
             }
         }
-        __syncthreads();   // the vectors are rewritten by the next task
+        named_bar(3, NCOMPUTE);   // the vectors are rewritten by the next task
         BTR(it, 12);
         ++it;
         t = tnext;
-        if (*s_abort) {
-            // complete the phase the next task's first copies opened, so the drain can wait for it
-            if (producer && t < p.ntasks) {
-                if (issued_parts == 1) issue_uodv(t);
-                if (issued_parts >= 1 && issued_parts < 3) issue_kq(t);
-            }
-            break;
-        }
+        if (*s_abort) break;
     }
-    // drain: nothing of this CTA may still be in flight when it exits
-    if (producer && tma_pending) mbar_wait(&bar[B_TMA], it & 1u, BUDGET, nullptr);
+    }   // compute warps
+    // drain: nothing of this CTA may still be in flight when it exits (the producer waited
+    // for its copies above)
     if (tid == 0) {
+        bulk_wait_all();   // the tensor stores of the last task
         if (mma_issued) {
             mma_commit(&bar[B_DRAIN]);
             mbar_wait(&bar[B_DRAIN], 0, BUDGET, nullptr);
@@ -941,10 +986,11 @@ cudaError_t grads(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k, 
     if (ntasks == 0 || g.T == 0) return cudaSuccess;
     const long long rows = (long long)g.B * g.H * g.T;
     const long long slots = (long long)g.NC * g.H;
-    CUtensorMap mq, mk, mv, mo, ms, mds, mu, mdu;
+    CUtensorMap mq, mk, mv, mo, ms, mds, mu, mdu, mgq, mgk, mgv;
     if (!make_map(&mq, q, rows) || !make_map(&mk, k, rows) || !make_map(&mv, v, rows) ||
         !make_map(&mo, dO, rows) || !make_map(&ms, Sin, slots * D) || !make_map(&mds, dSo, slots * D) ||
-        !make_map(&mu, Un, slots * C) || !make_map(&mdu, dUn, slots * C))
+        !make_map(&mu, Un, slots * C) || !make_map(&mdu, dUn, slots * C) || !make_map(&mgq, dq, rows) ||
+        !make_map(&mgk, dk, rows) || !make_map(&mgv, dv, rows))
         return cudaErrorInvalidValue;
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)) !=
@@ -957,7 +1003,7 @@ cudaError_t grads(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k, 
     p.g = g; p.beta = beta; p.gate = gate; p.dq = dq; p.dk = dk; p.dv = dv; p.dbeta = dbeta; p.dg = dg;
     p.ntasks = ntasks;
     const int grid = ntasks < sms ? ntasks : sms;
-    k_bwd_tc<<<grid, NTHREADS, SMEM_BYTES, st>>>(mq, mk, mv, mo, ms, mds, mu, mdu, p);
+    k_bwd_tc<<<grid, NTHREADS, SMEM_BYTES, st>>>(mq, mk, mv, mo, ms, mds, mu, mdu, mgq, mgk, mgv, p);
     return cudaPeekAtLastError();
 }
 
