@@ -3,8 +3,10 @@
 One step = one pass of the hot path over one batch of synthetic input resident in
 HBM: the Gated DeltaNet forward (L2 norm, gate cumsum, Gram + UT solve, W/U, state
 scan, output, final state) on the workload B4 H16 T8192 d128 bf16 with an initial
-state, chunk 64 — or, with --workload, another of the five workloads (the
-forward+backward one runs the forward and the backward per step).
+state, chunk 64 — or, with --workload, another workload of
+chunkwise_delta_rule_02_gb300.workloads (the forward+backward one runs the
+forward and the backward per step; two forward workloads take chunk 32, one of
+them head dim 256).
 
 Prints ONE JSON line (rank 0).  Under torchrun each rank runs its own replica of
 the workload on its own GPU (the path shards over sequences and heads with no

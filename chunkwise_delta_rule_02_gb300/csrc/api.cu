@@ -69,21 +69,21 @@ struct Layout {
     size_t total;
 };
 
-// with_ring: the fused forward will be the cooperative kernel (its package ring
-// lives in the workspace); otherwise the one-CTA-per-item fused kernel.
-Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, bool fast, bool with_ring)
+// Which forward kernel a call takes.
+enum class Fwd { General, Coop, PerItem };
+
+// kind: the fused forward the call takes (its scratch follows the header); the
+// cooperative kernel's package ring lives in the workspace.
+Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, Fwd kind)
 {
     Layout L;
     memset(&L, 0, sizeof(L));
     size_t off = 0;
     L.status = off; off += 256;
     L.cstart = off; off += align256(sizeof(int32_t) * (size_t)(g.N + 1));
-    if (fast && !for_backward) {
-        // room for either fused forward: the cooperative one (ring of packages) or,
-        // where a cooperative launch is not available, the one-CTA-per-item kernel
-        const size_t a = fast::workspace_bytes(g);
-        const size_t b = with_ring ? coop::workspace_bytes(g, device_sms()) : 0;
-        L.fast = off; off += align256(a > b ? a : b);
+    if (kind != Fwd::General && !for_backward) {
+        const size_t a = kind == Fwd::Coop ? coop::workspace_bytes(g, device_sms()) : fast::workspace_bytes(g);
+        L.fast = off; off += align256(a);
         L.total = off;
         return L;
     }
@@ -158,18 +158,25 @@ bool use_coop()
     return coop::available();
 }
 
-// honour_env = false ignores GDN_FORCE_GENERAL (the allocation-free entry point
-// serves the fused-kernel shapes whatever the environment says).
-bool fast_ok(const dn_shape *s, const Geo &g, int for_backward, bool honour_env = true)
+// The forward a call takes: the cooperative kernel (bf16, d_k = d_v = 128 with
+// C = 64 or 32, d_k = d_v = 256 with C = 32) where the device runs it and
+// allow_coop holds, else the one-CTA-per-item fused kernel (bf16, d 128, C 64),
+// else the general kernels.  honour_env = false ignores GDN_FORCE_GENERAL (the
+// allocation-free entry point serves the fused-kernel shapes whatever the
+// environment says).
+Fwd fwd_kind(const dn_shape *s, const Geo &g, int for_backward, bool allow_coop, bool honour_env = true)
 {
-    return !for_backward && !(honour_env && force_general()) && fast::supports(g, s->dtype);
+    if (for_backward || (honour_env && force_general())) return Fwd::General;
+    if (allow_coop && use_coop() && coop::supports(g, s->dtype)) return Fwd::Coop;
+    if (fast::supports(g, s->dtype)) return Fwd::PerItem;
+    return Fwd::General;
 }
 
 dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size_t ws_bytes,
-                     cudaStream_t st, Layout &L, bool &fast, bool with_ring, bool honour_env = true)
+                     cudaStream_t st, Layout &L, Fwd &kind, bool allow_coop, bool honour_env = true)
 {
-    fast = fast_ok(s, g, for_backward, honour_env);
-    L = make_layout(g, s, for_backward, fast, with_ring);
+    kind = fwd_kind(s, g, for_backward, allow_coop, honour_env);
+    L = make_layout(g, s, for_backward, kind);
     if (!ws || !is_aligned16(ws)) return DN_ERR_WORKSPACE;
     if (ws_bytes < L.total) return DN_ERR_WORKSPACE;
     char *base = (char *)ws;
@@ -199,17 +206,16 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
         if (p && !is_aligned16(p)) return DN_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
-    bool fast;
-    const bool coop_run = allow_coop && use_coop();
-    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, fast, coop_run, honour_env)) != DN_OK) return rc;
+    Fwd kind;
+    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, kind, allow_coop, honour_env)) != DN_OK) return rc;
     char *base = (char *)ws;
     cudaError_t e;
-    if (fast && coop_run) {
+    if (kind == Fwd::Coop) {
         e = coop::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                       (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
                       (__nv_bfloat16 *)o, hT, base + L.fast, ws_bytes - L.fast,
                       (uint32_t *)(base + L.status), st);
-    } else if (fast) {
+    } else if (kind == Fwd::PerItem) {
         e = fast::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                       (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
                       (__nv_bfloat16 *)o, hT, base + L.fast, (uint32_t *)(base + L.status), st);
@@ -252,15 +258,14 @@ size_t dn_workspace_size(const dn_shape *shape, int for_backward)
 {
     Geo g;
     if (check_shape(shape, &g) != DN_OK) return 0;
-    bool fast = fast_ok(shape, g, for_backward);
-    return make_layout(g, shape, for_backward, fast, fast && !for_backward && use_coop()).total;
+    return make_layout(g, shape, for_backward, fwd_kind(shape, g, for_backward, true)).total;
 }
 
 int dn_uses_fast_path(const dn_shape *shape, int for_backward)
 {
     Geo g;
     if (check_shape(shape, &g) != DN_OK) return -1;
-    return fast_ok(shape, g, for_backward) ? 1 : 0;
+    return fwd_kind(shape, g, for_backward, true) != Fwd::General ? 1 : 0;
 }
 
 int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
@@ -275,10 +280,10 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
         // the pointer alignment the tcgen05 kernel also needs is not known here
         const void *aligned = (const void *)(uintptr_t)256;
         n = (gen::bwd_uses_tc(g, shape->dtype, aligned, aligned, aligned, aligned) ? 4 : 6) + offsets;
-    } else if (!fast_ok(shape, g, 0)) {
+    } else if (fwd_kind(shape, g, 0, true) == Fwd::General) {
         path = DN_PATH_GENERAL;
         n = 3 + offsets;                    // k_prep, k_scan, k_out
-    } else if (use_coop()) {
+    } else if (fwd_kind(shape, g, 0, true) == Fwd::Coop) {
         path = DN_PATH_COOP;
         n = 1 + 2 * offsets;                // k_coop_fwd (+ k_cstart, k_plan)
     } else {
@@ -319,8 +324,8 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
         if (p && !is_aligned16(p)) return DN_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
-    bool fast;
-    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, fast, false)) != DN_OK) return rc;
+    Fwd kind;
+    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, kind, false)) != DN_OK) return rc;
     gen::Ws w = general_ws(L, (char *)ws);
     cudaError_t e;
     if (shape->dtype == DN_F32)
@@ -508,8 +513,8 @@ dn_status gdn_chunk_fwd_noalloc(const dn_shape *shape, const void *q, const void
     Geo geo;
     dn_status rc = check_shape(shape, &geo);
     if (rc != DN_OK) return rc;
-    if (!fast_ok(shape, geo, 0, false)) return DN_ERR_UNSUPPORTED;
-    if (make_layout(geo, shape, 0, true, false).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
+    if (fwd_kind(shape, geo, 0, false, false) != Fwd::PerItem) return DN_ERR_UNSUPPORTED;
+    if (make_layout(geo, shape, 0, Fwd::PerItem).total > kNoAllocScratchBytes) return DN_ERR_WORKSPACE;
     void *ws = noalloc_scratch();
     if (!ws) return DN_ERR_CUDA;
     // the one-CTA-per-item fused kernel: its scratch fits the static array

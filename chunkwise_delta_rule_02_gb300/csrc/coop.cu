@@ -1,18 +1,21 @@
 // Cooperative persistent forward of the (gated) delta rule for bf16 inputs with
-// d_k = d_v = 128 and chunk C = 64: one launch whose CTAs take one of two roles.
+// d_k = d_v, one launch whose CTAs take one of two roles.  Instances: chunk C = 64
+// with d = 128, and C = 32 with d = 128 or 256 (at d = 256 and C = 64 one chunk's
+// operand tiles do not fit a CTA's shared memory).
 //
-//   preparation CTAs (two independent pipelines each): for a chunk, compute
+//   preparation CTAs (four independent pipelines each): for a chunk, compute
 //     everything that does not depend on the state -- norms, gates, the Gram and
 //     Q K^T masks, the UT transform T = (I + A)^-1 diag(beta), T' = T diag(exp(gamma) n),
 //     -W = -T' K, Qt = diag(exp(gamma) m) Q, P = lower(Q K^T o D) with the norms --
-//     and publish them as one 50 KB package into an L2-resident ring slot of the
-//     chain CTA that owns the chunk;
-//   chain CTAs (one per SM, persistent over their (sequence, head) items): keep
-//     the state in TMEM and run, per chunk, only
-//       U^T            = V^T T^T                       (4 tcgen05 MMAs)
-//       [Unew^T | O^T] += S^T [-W | Qt]^T              (8, shared-memory operands, N = 128)
-//       S_hat^T        += (f o Unew)^T K               (4)
-//       O^T            += Unew^T P^T                   (4)
+//     and publish them as one package into an L2-resident ring slot of the chain
+//     CTAs that own the chunk;
+//   chain CTAs (one per SM, persistent over their (sequence, head) items; at
+//     d_v = 256 two of them per item, each owning 128 of its d_v columns and
+//     reading the same packages): keep the state in TMEM and run, per chunk, only
+//       U^T            = V^T T^T                       (tcgen05 MMAs, K = C)
+//       [Unew^T | O^T] += S^T [-W | Qt]^T              (shared-memory operands, N = 2C, K = d_k)
+//       S_hat^T        += (f o Unew)^T K               (N = d_k, K = C)
+//       O^T            += Unew^T P^T                   (N = C, K = C)
 //     with bf16 copies of S (the A operand above), Unew and f o Unew written to
 //     shared memory by the warpgroups that read the accumulators.
 //
@@ -23,8 +26,8 @@
 // The launch is cooperative, so every CTA is resident and the producer /
 // consumer flags in the workspace cannot deadlock on scheduling.  Tasks are
 // handed out in order (chunk index major), a preparation pipeline waits for its
-// ring slot to be consumed (RING slots per chain CTA), and a chain CTA waits for
-// its next package; every such wait, like every mbarrier wait, is bounded and
+// ring slot to be consumed (RING slots per ring), and a chain CTA waits for its
+// next package; every such wait, like every mbarrier wait, is bounded and
 // reports a timeout through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -59,64 +62,105 @@ using namespace prep;
 
 namespace {
 
-constexpr int C = 64;
-constexpr int D = 128;
 constexpr int NTHREADS = 512;
-constexpr int RING = 9;   // deeper rings spill packages from L2 to HBM (10 slots: +78 MB per launch)
+constexpr int PIPES = 4;   // preparation pipelines per CTA (four warps each)
 // control block, in 32-bit words: line 0 holds the task counter [0] and Jmax [1];
-// then one 128-byte line per chain CTA for its consumed count and one for its
-// RING ready flags, so that pollers and the task counter do not share lines; the
-// last line holds the launch-wide abort word (set by the first CTA whose bounded
-// wait runs out, polled by every cross-CTA wait so that the launch winds down)
+// then one 128-byte line per chain CTA for its consumed count and one per ring
+// (chain group) for its RING ready flags, so that pollers and the task counter do
+// not share lines; the last line holds the launch-wide abort word (set by the
+// first CTA whose bounded wait runs out, polled by every cross-CTA wait so that
+// the launch winds down)
 constexpr int CTL_LINE = 32;
-static_assert(RING <= CTL_LINE, "ready flags of one chain CTA fit one line");
-__host__ __device__ constexpr size_t ctl_words(int nc) { return (size_t)CTL_LINE * (2 + 2 * (size_t)nc); }
+__host__ __device__ constexpr size_t ctl_words(int nc, int ng) { return (size_t)CTL_LINE * (2 + (size_t)nc + (size_t)ng); }
 __device__ __forceinline__ uint32_t *consumed_word(uint32_t *ctl, int c) { return ctl + CTL_LINE * (1 + c); }
-__device__ __forceinline__ uint32_t *ready_words(uint32_t *ctl, int nc, int c) { return ctl + CTL_LINE * (1 + nc + c); }
-__device__ __forceinline__ uint32_t *abort_word(uint32_t *ctl, int nc) { return ctl + CTL_LINE * (1 + 2 * nc); }
+__device__ __forceinline__ uint32_t *ready_words(uint32_t *ctl, int nc, int grp) { return ctl + CTL_LINE * (1 + nc + grp); }
+__device__ __forceinline__ uint32_t *abort_word(uint32_t *ctl, int nc, int ng) { return ctl + CTL_LINE * (1 + nc + ng); }
 constexpr long long BUDGET = 4000000000LL;                 // clock cycles (about 2 s)
 // With the test hook GDN_DEBUG_WITHHOLD_TASK set, the cross-CTA flag waits give up
 // after this many cycles (about 1 ms) instead of BUDGET.
 constexpr long long HOOK_FLAG_BUDGET = 2000000LL;
 constexpr float RENORM_BELOW = 9.313225746154785e-10f;      // 2^-30
 
-// package (ring slot in global memory and its copy in a chain CTA's shared memory)
-constexpr uint32_t PK_WQ = 0;          // 32 KB: per 64-column half [-W rows | Qt rows], bf16, 128B swizzle
-constexpr uint32_t PK_T = 32768;       // 8 KB : T bf16 [r][i]
-constexpr uint32_t PK_P = 40960;       // 8 KB : P bf16 [r][i]
-constexpr uint32_t PK_VEC = 49152;     // f0[64] = exp(gamma_C - gamma_r) n_r, then exp(gamma_C)
-constexpr uint32_t PK_BYTES = 50176;
-constexpr uint32_t PK_STRIDE = 51200;
+__host__ __device__ constexpr uint32_t round1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+__host__ __device__ constexpr uint32_t umax(uint32_t a, uint32_t b) { return a > b ? a : b; }
 
-// chain CTA shared memory
-constexpr uint32_t CH_K = 0;                        // 2 x 16 KB K tiles
-constexpr uint32_t CH_V = 32768;                    // 16 KB V tile
-constexpr uint32_t CH_PK = 49152;                   // 2 package slots
-constexpr uint32_t CH_SB = CH_PK + 2 * PK_STRIDE;   // S^T bf16 [dv][dk], two 64-column halves (32 KB)
-constexpr uint32_t CH_U1 = CH_SB + 32768;           // Unew^T bf16 [dv][token] (16 KB)
-constexpr uint32_t CH_U2 = CH_U1 + 16384;           // (f o Unew)^T bf16 (16 KB)
-constexpr uint32_t CH_BAR = CH_U2 + 16384;
-constexpr uint32_t CH_END = CH_BAR + 32 * 8 + 64;
+// Layout of one instance: chunk C_, head dims d_k = d_v = DK_.  Every bf16 operand
+// tile is stored in 64-column panels of 128-byte rows with the 128-byte swizzle; a
+// row of C elements (C = 32) fills the first half of its 128 bytes.
+template <int C_, int DK_>
+struct Cfg {
+    static constexpr int C = C_;
+    static constexpr int DK = DK_;
+    static constexpr int DV = DK_;
+    static constexpr int NV = DV / 128;        // chain CTAs per (sequence, head)
+    static constexpr int NQ = DK / 64;         // 64-column panels of a d_k-wide tile
+    static constexpr int KW = C / 32;          // warps over a chunk's rows
+    static constexpr uint32_t PANEL = (uint32_t)C * 128;   // one panel of a chunk's rows
+    // package ring depth: about 450 KB per ring (deeper rings spill packages from
+    // L2 to HBM: 10 slots of the C = 64 package added 78 MB of DRAM traffic per launch)
+    static constexpr int RING = C == 64 ? 9 : (DK == 128 ? 18 : 20);
 
-// preparation CTA shared memory, per pipeline (four pipelines of four warps)
-constexpr int PIPES = 4;
-constexpr uint32_t AST = 72;                        // row stride (floats) of the solve buffer
-constexpr uint32_t PP_TL = 0;                       // 32 KB: per 64-column half [K rows | Q rows];
-                                                    //   K becomes -W, Q becomes Qt and then T (half 0) | P (half 1)
-constexpr uint32_t PP_AX = 32768;                   // fp32 [64][72]: A below the diagonal, X^T on and
-                                                    //   above it; then T' (bf16, first 8 KB)
-constexpr uint32_t PP_VEC = PP_AX + 64 * AST * 4;   // vectors, 12 x 64 floats
-constexpr uint32_t PP_BAR = PP_VEC + 12 * 256;      // barriers + task word
-constexpr uint32_t PP_STRIDE = 55296;               // 54 KB, a multiple of 1 KB (128-byte swizzle)
-static_assert(PP_BAR + 64 <= PP_STRIDE, "pipeline layout");
-static_assert(PP_STRIDE % 1024 == 0 && PP_AX % 1024 == 0, "swizzled operands need 1 KB alignment");
-constexpr uint32_t SMEM_USED = (CH_END > PIPES * PP_STRIDE ? CH_END : PIPES * PP_STRIDE);
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory");
+    // package (ring slot in global memory and its copy in a chain CTA's shared memory)
+    static constexpr uint32_t WQ_PANEL = 2 * PANEL;        // per panel [-W rows | Qt rows]
+    static constexpr uint32_t PK_WQ = 0;
+    static constexpr uint32_t PK_T = NQ * WQ_PANEL;        // T bf16 [r][i]
+    static constexpr uint32_t PK_P = PK_T + PANEL;         // P bf16 [r][i]
+    static constexpr uint32_t PK_VEC = PK_P + PANEL;       // f0[64] = exp(gamma_C - gamma_r) n_r, then exp(gamma_C)
+    static constexpr uint32_t VEC_BYTES = 272;
+    static constexpr uint32_t PK_BYTES = PK_VEC + VEC_BYTES;
+    static constexpr uint32_t PK_STRIDE = round1k(PK_BYTES);
 
-// chain TMEM columns
-constexpr uint32_t TM_S = 0;        // S_hat^T fp32 (lane = dv, column = dk)
-constexpr uint32_t TM_XO = 128;     // 2 x 128: [X (64) | O (64)] per chunk parity
+    // chain CTA shared memory
+    static constexpr uint32_t KTILE = NQ * PANEL;
+    static constexpr uint32_t CH_K = 0;                          // 2 K tiles [token][d_k]
+    static constexpr uint32_t CH_V = 2 * KTILE;                  // V tile [token][128 d_v]
+    static constexpr uint32_t CH_PK = CH_V + 2 * PANEL;          // 2 package slots
+    static constexpr uint32_t CH_SB = CH_PK + 2 * PK_STRIDE;     // S^T bf16 [dv][dk], NQ panels of 128 rows
+    static constexpr uint32_t CH_U1 = CH_SB + NQ * 16384;        // Unew^T bf16 [dv][token] (16 KB)
+    static constexpr uint32_t CH_U2 = CH_U1 + 16384;             // (f o Unew)^T bf16 (16 KB)
+    static constexpr uint32_t CH_BAR = CH_U2 + 16384;
+    static constexpr uint32_t CH_END = CH_BAR + 32 * 8 + 64;
+
+    // preparation pipeline shared memory
+    static constexpr uint32_t AST = C == 64 ? 72 : 40;           // row stride (floats) of the solve buffer
+    static constexpr uint32_t PP_TL = 0;        // per panel [K rows | Q rows]; K becomes -W, Q becomes Qt
+                                                //   and then T (panel 0) | P (panel 1)
+    static constexpr uint32_t PP_AX = NQ * WQ_PANEL;             // fp32 [C][AST]: A below the diagonal, X^T on
+                                                                 //   and above it; then T' (bf16)
+    // The M = 128 products read 128 A rows where C = 32 fills fewer: T' K reads
+    // 16 KB from PP_AX, the Gram 8 KB past the last [K | Q] panel.  Both windows
+    // end before the vectors and barriers and hold only the solve buffer, which
+    // nothing writes while those products run; their result rows are never read.
+    static constexpr uint32_t PP_VEC = PP_AX + umax((uint32_t)C * AST * 4, 16384);   // vectors, 12 x 64 floats
+    static constexpr uint32_t PP_BAR = PP_VEC + 12 * 256;        // barriers + task word
+    static constexpr uint32_t PP_STRIDE = round1k(PP_BAR + 64);
+    static constexpr uint32_t SMEM_USED = umax(CH_END, PIPES * PP_STRIDE);
+    static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+
+    // chain TMEM columns: S_hat^T fp32 (lane = dv, column = dk), then per chunk
+    // parity [X (C) | O (C)]
+    static constexpr uint32_t TM_S = 0;
+    static constexpr uint32_t TM_XO = DK;
+    static constexpr uint32_t XO_STRIDE = 2 * C;
+
+    static constexpr uint32_t ID_U = idesc(1, 128, C, true, false);         // V^T T^T
+    static constexpr uint32_t ID_XO = idesc(1, 128, 2 * C, false, false);   // S^T [-W | Qt]^T; [K;Q][K;Q]^T
+    static constexpr uint32_t ID_S = idesc(1, 128, DK, false, true);        // (f o Unew)^T K
+    static constexpr uint32_t ID_O = idesc(1, 128, C, false, false);        // Unew^T P^T
+    static constexpr uint32_t ID_TK = idesc(1, 128, 128, false, true);      // T' K, 128 columns of d_k
+
+    static_assert(C == 32 || C == 64, "chunk");
+    static_assert(DK == 128 || DK == 256, "head dim");
+    static_assert(RING <= CTL_LINE, "ready flags of one ring fit one line");
+    static_assert(PP_STRIDE % 1024 == 0 && PP_AX % 1024 == 0 && PK_STRIDE % 1024 == 0, "swizzled operands need 1 KB alignment");
+    static_assert((uint32_t)C * 128 <= (uint32_t)C * AST * 4, "T' fits the solve buffer");
+    static_assert(TM_XO + 2 * XO_STRIDE <= 512, "TMEM columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+using Cfg64 = Cfg<64, 128>;
+using Cfg32 = Cfg<32, 128>;
+using Cfg32w = Cfg<32, 256>;
 
 // chain barriers
 enum {
@@ -125,11 +169,6 @@ enum {
 };
 // preparation barriers (per pipeline)
 enum { P_FULL = 0, P_G = 1, P_W = 2, P_DONE = 3, NBAR_PP = 4 };
-
-constexpr uint32_t ID_SS_N128 = idesc(1, 128, 128, false, false);
-constexpr uint32_t ID_SS_N64 = idesc(1, 128, 64, false, false);
-constexpr uint32_t ID_SS_N64_AMN = idesc(1, 128, 64, true, false);
-constexpr uint32_t ID_SS_N128_BMN = idesc(1, 128, 128, false, true);
 
 struct Params {
     const __nv_bfloat16 *beta;
@@ -140,9 +179,9 @@ struct Params {
     uint32_t *status;
     const int32_t *cu;       // packed offsets or null
     const int32_t *order;    // packed: sequences longest first (or null)
-    uint32_t *ctl;           // control block (ctl_words(Nc) words, see CTL_LINE)
-    uint8_t *ring;           // Nc x RING package slots
-    int H, T, N, items, Nc, Jmax_fixed;
+    uint32_t *ctl;           // control block (ctl_words(Nc, Ng) words, see CTL_LINE)
+    uint8_t *ring;           // Ng x RING package slots
+    int H, T, N, items, Nc, Ng, Jmax_fixed;   // Ng = Nc / NV chain groups, one ring each
     float scale, eps;
     int l2norm;
     int longhorn;           // step size beta / (1 + beta k^T k) instead of beta
@@ -157,6 +196,7 @@ struct Item {
     long long rowbase;
 };
 
+template <int C>
 __device__ __forceinline__ Item item_of(const Params &p, int it)
 {
     Item r;
@@ -177,23 +217,24 @@ __device__ __forceinline__ Item item_of(const Params &p, int it)
     return r;
 }
 
-// Walks the chunk stream of chain CTA c: its items c, c + Nc, ... (empty ones skipped),
-// each chunk in order.
+// Walks the chunk stream of chain group g: its items g, g + Ng, ... (empty ones
+// skipped), each chunk in order.
+template <int C>
 struct Stream {
     int it, n;
     Item cur;
     bool valid;
-    __device__ void start(const Params &p, int c)
+    __device__ void start(const Params &p, int g)
     {
-        it = c - p.Nc;
+        it = g - p.Ng;
         advance_item(p);
     }
     __device__ void advance_item(const Params &p)
     {
         while (true) {
-            it += p.Nc;
+            it += p.Ng;
             if (it >= p.items) { valid = false; return; }
-            cur = item_of(p, it);
+            cur = item_of<C>(p, it);
             if (cur.nch > 0) break;
         }
         n = 0;
@@ -209,28 +250,41 @@ struct Stream {
     __device__ long long row0() const { return cur.rowbase + (long long)n * C; }
 };
 
-__device__ __forceinline__ int stream_length(const Params &p, int c)
+template <int C>
+__device__ __forceinline__ int stream_length(const Params &p, int g)
 {
     int J = 0;
-    for (int it = c; it < p.items; it += p.Nc) J += item_of(p, it).nch;
+    for (int it = g; it < p.items; it += p.Ng) J += item_of<C>(p, it).nch;
     return J;
+}
+
+// r[0, 32 N) <- 32 N consecutive TMEM columns of this warp's lanes
+template <int N32>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t *r)
+{
+#pragma unroll
+    for (int i = 0; i < N32; ++i) tmem_ld32(taddr + 32 * i, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * i));
 }
 
 }  // namespace
 
 // ================================================================================= chain role
+template <class L>
 __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm_k,
                                           const CUtensorMap *tm_v, uint8_t *sm, int c)
 {
+    constexpr int C = L::C, DK = L::DK, DV = L::DV, NQ = L::NQ;
+    constexpr uint32_t PANEL = L::PANEL;
     const uint32_t sb = smem_u32(sm);
-    uint64_t *bar = (uint64_t *)(sm + CH_BAR);
-    volatile int *abort_flag = (volatile int *)(sm + CH_BAR + 32 * 8);
-    uint32_t *tmem_slot = (uint32_t *)(sm + CH_BAR + 32 * 8 + 8);
+    uint64_t *bar = (uint64_t *)(sm + L::CH_BAR);
+    volatile int *abort_flag = (volatile int *)(sm + L::CH_BAR + 32 * 8);
+    uint32_t *tmem_slot = (uint32_t *)(sm + L::CH_BAR + 32 * 8 + 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = c / L::NV, hv = c % L::NV;   // chain group (ring) and d_v half
     uint32_t *consumed = consumed_word(p.ctl, c);
-    uint32_t *ready = ready_words(p.ctl, p.Nc, c);
-    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc);
-    const uint8_t *ring = p.ring + (size_t)c * RING * PK_STRIDE;
+    uint32_t *ready = ready_words(p.ctl, p.Nc, grp);
+    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc, p.Ng);
+    const uint8_t *ring = p.ring + (size_t)grp * L::RING * L::PK_STRIDE;
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -254,7 +308,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int J = stream_length(p, c);
+    const int J = stream_length<C>(p, grp);
 
     auto fail = [&]() {
         if (!*abort_flag) {
@@ -272,21 +326,22 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     if (warp == 0) {
         // ---------------------------------------------------------------- K / V tiles (TMA)
         if (lane == 0) {
-            Stream st;
-            st.start(p, c);
+            Stream<C> st;
+            st.start(p, grp);
             int jk = -1, jv = -1;   // last chunk whose K / V copy was issued
             for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
                 const int s = j & 1;
                 const int row = (int)st.row0();
                 if (j >= 2 && !wait(B_KEMPTY + s, (uint32_t)((j >> 1) - 1))) break;
-                mbar_expect_tx(&bar[B_KFULL + s], 16384);
-                tma_load_2d(sm + CH_K + s * 16384, tm_k, &bar[B_KFULL + s], 0, row);
-                tma_load_2d(sm + CH_K + s * 16384 + 8192, tm_k, &bar[B_KFULL + s], 64, row);
+                mbar_expect_tx(&bar[B_KFULL + s], L::KTILE);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    tma_load_2d(sm + L::CH_K + s * L::KTILE + q * PANEL, tm_k, &bar[B_KFULL + s], 64 * q, row);
                 jk = j;
                 if (j >= 1 && !wait(B_VEMPTY, (uint32_t)(j - 1))) break;
-                mbar_expect_tx(&bar[B_VFULL], 16384);
-                tma_load_2d(sm + CH_V, tm_v, &bar[B_VFULL], 0, row);
-                tma_load_2d(sm + CH_V + 8192, tm_v, &bar[B_VFULL], 64, row);
+                mbar_expect_tx(&bar[B_VFULL], 2 * PANEL);
+                tma_load_2d(sm + L::CH_V, tm_v, &bar[B_VFULL], 128 * hv, row);
+                tma_load_2d(sm + L::CH_V + PANEL, tm_v, &bar[B_VFULL], 128 * hv + 64, row);
                 jv = j;
             }
             // the last copies issued into each buffer have landed before shared memory
@@ -304,7 +359,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             int issued = 0, landed = 0;
             bool ok = true;
             for (int j = 0; j < J && ok; ++j) {
-                const int s = j & 1, slot = j % RING;
+                const int s = j & 1, slot = j % L::RING;
                 // wait for the producer's flag
                 const long long t0 = clock64();
                 unsigned ns = 32;
@@ -317,8 +372,8 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 fence_async_global();
                 if (c == 0) CTR(j, 0);
                 if (j >= 2 && !(ok = wait(B_PEMPTY + s, (uint32_t)((j >> 1) - 1)))) break;
-                mbar_expect_tx(&bar[B_PFULL + s], PK_BYTES);
-                bulk_load(sm + CH_PK + s * PK_STRIDE, ring + (size_t)slot * PK_STRIDE, PK_BYTES,
+                mbar_expect_tx(&bar[B_PFULL + s], L::PK_BYTES);
+                bulk_load(sm + L::CH_PK + s * L::PK_STRIDE, ring + (size_t)slot * L::PK_STRIDE, L::PK_BYTES,
                           &bar[B_PFULL + s]);
                 issued = j + 1;
                 if (c == 0) CTR(j, 1);
@@ -340,19 +395,19 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0 && J > 0) {
-            const uint64_t dSB = sdesc(sb + CH_SB, 16, 1024);
-            const uint64_t dU1 = sdesc(sb + CH_U1, 16, 1024), dU2 = sdesc(sb + CH_U2, 16, 1024);
-            const uint64_t dK0 = sdesc(sb + CH_K, 8192, 1024), dK1 = sdesc(sb + CH_K + 16384, 8192, 1024);
-            const uint64_t dV = sdesc(sb + CH_V, 8192, 1024);
-            const uint64_t dPK0 = sdesc(sb + CH_PK, 16, 1024), dPK1 = sdesc(sb + CH_PK + PK_STRIDE, 16, 1024);
+            const uint64_t dSB = sdesc(sb + L::CH_SB, 16, 1024);
+            const uint64_t dU1 = sdesc(sb + L::CH_U1, 16, 1024), dU2 = sdesc(sb + L::CH_U2, 16, 1024);
+            const uint64_t dK0 = sdesc(sb + L::CH_K, PANEL, 1024), dK1 = sdesc(sb + L::CH_K + L::KTILE, PANEL, 1024);
+            const uint64_t dV = sdesc(sb + L::CH_V, PANEL, 1024);
+            const uint64_t dPK0 = sdesc(sb + L::CH_PK, 16, 1024), dPK1 = sdesc(sb + L::CH_PK + L::PK_STRIDE, 16, 1024);
             auto issue_U = [&](int m) {
                 // U^T = V^T T^T into X[m & 1]
                 tc_fence_after();
                 const uint64_t dpk = (m & 1) ? dPK1 : dPK0;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ss(tmem + TM_XO + (m & 1) * 128, dadd(dV, k * 2048), dadd(dpk, PK_T + k * 32),
-                                ID_SS_N64_AMN, k > 0);
+                for (int k = 0; k < C / 16; ++k)
+                    mma_bf16_ss(tmem + L::TM_XO + (m & 1) * L::XO_STRIDE, dadd(dV, k * 2048),
+                                dadd(dpk, L::PK_T + k * 32), L::ID_U, k > 0);
                 mma_commit(&bar[B_VEMPTY]);
             };
             bool ok = wait(B_VFULL, 0) && wait(B_PFULL, 0);
@@ -366,10 +421,9 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 if (!(ok = wait(B_OFREE + s, (uint32_t)(j >> 1)))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    mma_bf16_ss(tmem + TM_XO + s * 128, dadd(dSB, off), dadd(dpk, PK_WQ + off), ID_SS_N128, 1);
-                }
+                for (int k = 0; k < 4 * NQ; ++k)
+                    mma_bf16_ss(tmem + L::TM_XO + s * L::XO_STRIDE, dadd(dSB, (k >> 2) * 16384 + (k & 3) * 32),
+                                dadd(dpk, L::PK_WQ + (k >> 2) * L::WQ_PANEL + (k & 3) * 32), L::ID_XO, 1);
                 mma_commit(&bar[B_X + s]);
                 if (c == 0) CTR(j, 2);
                 // S_hat^T += U2^T K ; O^T += U1^T P^T
@@ -380,15 +434,15 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 {
                     const uint64_t dk = s ? dK1 : dK0;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16_ss(tmem + TM_S, dadd(dU2, k * 32), dadd(dk, k * 2048), ID_SS_N128_BMN, 1);
+                    for (int k = 0; k < C / 16; ++k)
+                        mma_bf16_ss(tmem + L::TM_S, dadd(dU2, k * 32), dadd(dk, k * 2048), L::ID_S, 1);
                 }
                 mma_commit(&bar[B_S]);
                 mma_commit(&bar[B_KEMPTY + s]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ss(tmem + TM_XO + s * 128 + 64, dadd(dU1, k * 32), dadd(dpk, PK_P + k * 32),
-                                ID_SS_N64, 1);
+                for (int k = 0; k < C / 16; ++k)
+                    mma_bf16_ss(tmem + L::TM_XO + s * L::XO_STRIDE + C, dadd(dU1, k * 32),
+                                dadd(dpk, L::PK_P + k * 32), L::ID_O, 1);
                 mma_commit(&bar[B_O + s]);
                 mma_commit(&bar[B_PEMPTY + s]);
                 if (c == 0) CTR(j, 4);
@@ -405,38 +459,41 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
         }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------- state and Unew, split in halves over two warpgroups
-        // warpgroup `half` owns S columns (d_k) [64 half, 64 half + 64) and chunk
-        // tokens [32 half, 32 half + 32); per chunk: state snapshot for the next
+        // warpgroup `half` owns S columns (d_k) [DK/2 half, DK/2 half + DK/2) and chunk
+        // tokens [C/2 half, C/2 half + C/2); per chunk: state snapshot for the next
         // MMA, then Unew -> U1, U2 once X is in TMEM; h0 in and h_T out at item ends
+        constexpr int KH = DK / 2, CH = C / 2;
         const int half = (warp >> 2) - 1;
-        const int dv = (warp & 3) * 32 + lane;
+        const int dvl = (warp & 3) * 32 + lane;   // TMEM lane: d_v column within this CTA's 128
+        const int dvg = 128 * hv + dvl;           // d_v column of the item
         const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
         const int tid_trace = 128 + 128 * half;
         // items without chunks pass their initial state straight through
-        for (int it = c; it < p.items; it += p.Nc) {
-            const Item I = item_of(p, it);
-            if (I.nch == 0 && p.hT) {
-                const size_t sidx = ((size_t)I.seq * p.H + I.h) * D * D;
-                for (int k = 64 * half; k < 64 * half + 64; ++k)
-                    p.hT[sidx + (size_t)k * D + dv] = p.h0 ? p.h0[sidx + (size_t)k * D + dv] : 0.f;
+        if (p.hT) {
+            for (int it = grp; it < p.items; it += p.Ng) {
+                const Item I = item_of<C>(p, it);
+                if (I.nch == 0) {
+                    const size_t sidx = ((size_t)I.seq * p.H + I.h) * DK * DV;
+                    for (int k = KH * half; k < KH * half + KH; ++k)
+                        p.hT[sidx + (size_t)k * DV + dvg] = p.h0 ? p.h0[sidx + (size_t)k * DV + dvg] : 0.f;
+                }
             }
         }
-        Stream st;
-        st.start(p, c);
+        Stream<C> st;
+        st.start(p, grp);
         float Gpend = 1.f;
-        uint8_t *sbp = sm + CH_SB + half * 16384;
         for (int j = 0; j < J && st.valid; ++j) {
             const int s = j & 1;
-            const size_t sidx = ((size_t)st.cur.seq * p.H + st.cur.h) * D * D;
+            const size_t sidx = ((size_t)st.cur.seq * p.H + st.cur.h) * DK * DV;
             if (st.first()) {
                 // S^T[dv][dk] = h0[dk][dv] into TMEM, pending scale 1
                 Gpend = 1.f;
-                for (int k0 = 64 * half; k0 < 64 * half + 64; k0 += 32) {
+                for (int k0 = KH * half; k0 < KH * half + KH; k0 += 32) {
                     uint32_t r[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k)
-                        r[k] = __float_as_uint(p.h0 ? p.h0[sidx + (size_t)(k0 + k) * D + dv] : 0.f);
-                    tmem_st32(tmem + lrow + TM_S + k0, r);
+                        r[k] = __float_as_uint(p.h0 ? p.h0[sidx + (size_t)(k0 + k) * DV + dvg] : 0.f);
+                    tmem_st32(tmem + lrow + L::TM_S + k0, r);
                 }
                 tmem_st_wait();
             } else {
@@ -444,7 +501,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             }
             wait(B_PFULL + s, (uint32_t)(j >> 1));
             tc_fence_after();
-            const float *vec = (const float *)(sm + CH_PK + s * PK_STRIDE + PK_VEC);
+            const float *vec = (const float *)(sm + L::CH_PK + s * L::PK_STRIDE + L::PK_VEC);
             const float GC = vec[64];
             if (c == 0 && tid == tid_trace) CTR(j, 8);
             const float Gn = Gpend;
@@ -452,10 +509,12 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             const bool renorm = Gnext < RENORM_BELOW;
             // bf16 snapshot of the true state S = G S_hat (A operand of the next MMA);
             // a renormalising chunk also rescales S_hat in TMEM to exp(gamma_C) S
-            {
+#pragma unroll 1
+            for (int pp = 0; pp < KH / 64; ++pp) {
+                const int panel = half * (KH / 64) + pp;
+                uint8_t *sbp = sm + L::CH_SB + panel * 16384;
                 uint32_t r[64];
-                tmem_ld32(tmem + lrow + TM_S + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld32(tmem + lrow + TM_S + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_ld_cols<2>(tmem + lrow + L::TM_S + 64 * panel, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
@@ -463,13 +522,13 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         w[e] = pack_bf16(Gn * __uint_as_float(r[c8 * 8 + 2 * e]), Gn * __uint_as_float(r[c8 * 8 + 2 * e + 1]));
-                    *(uint4 *)(sbp + sw128(dv, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(sbp + sw128(dvl, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 if (renorm) {
 #pragma unroll
                     for (int e = 0; e < 64; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * Gnext);
-                    tmem_st32(tmem + lrow + TM_S + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_st32(tmem + lrow + TM_S + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_st32(tmem + lrow + L::TM_S + 64 * panel, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_st32(tmem + lrow + L::TM_S + 64 * panel + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                     tmem_st_wait();
                 }
             }
@@ -480,18 +539,19 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_SNAP]);
             if (c == 0 && tid == tid_trace) CTR(j, 9);
-            // Unew (this warpgroup's 32 tokens) -> U1 = Unew^T, U2 = (f o Unew)^T / G, bf16
+            // Unew (this warpgroup's C/2 tokens) -> U1 = Unew^T, U2 = (f o Unew)^T / G, bf16
             if (!__all_sync(0xffffffffu, wait(B_X + s, (uint32_t)(j >> 1)))) break;
             if (c == 0 && tid == tid_trace) CTR(j, 6);
             tc_fence_after();
             {
-                uint32_t x[32];
-                tmem_ld32(tmem + lrow + TM_XO + s * 128 + 32 * half, x);
+                uint32_t x[CH];
+                if constexpr (CH == 32) tmem_ld32(tmem + lrow + L::TM_XO + s * L::XO_STRIDE + CH * half, x);
+                else tmem_ld16(tmem + lrow + L::TM_XO + s * L::XO_STRIDE + CH * half, x);
                 tmem_ld_wait();
-                uint8_t *u1 = sm + CH_U1, *u2 = sm + CH_U2;
-                const float *f0 = vec + 32 * half;
+                uint8_t *u1 = sm + L::CH_U1, *u2 = sm + L::CH_U2;
+                const float *f0 = vec + CH * half;
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
+                for (int c8 = 0; c8 < CH / 8; ++c8) {
                     uint32_t w1[4], w2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -500,7 +560,7 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                         w1[e] = pack_bf16(a, b);
                         w2[e] = pack_bf16(a * f0[i0] * fdiv, b * f0[i0 + 1] * fdiv);
                     }
-                    const uint32_t off = sw128(dv, (4 * half + c8) * 16);
+                    const uint32_t off = sw128(dvl, ((CH / 8) * half + c8) * 16);
                     *(uint4 *)(u1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                 }
@@ -515,13 +575,13 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 wait(B_S, (uint32_t)j);
                 tc_fence_after();
                 if (p.hT && !*abort_flag) {
-                    for (int k0 = 64 * half; k0 < 64 * half + 64; k0 += 32) {
+                    for (int k0 = KH * half; k0 < KH * half + KH; k0 += 32) {
                         uint32_t r[32];
-                        tmem_ld32(tmem + lrow + TM_S + k0, r);
+                        tmem_ld32(tmem + lrow + L::TM_S + k0, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
-                            p.hT[sidx + (size_t)(k0 + k) * D + dv] = Gpend * __uint_as_float(r[k]);
+                            p.hT[sidx + (size_t)(k0 + k) * DV + dvg] = Gpend * __uint_as_float(r[k]);
                     }
                 }
             }
@@ -530,16 +590,16 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
         }
     } else if (warp >= 12) {
         // ---------------------------------------------------------------- output
-        const int dv = (warp & 3) * 32 + lane;
+        const int dvl = (warp & 3) * 32 + lane;
+        const int dvg = 128 * hv + dvl;
         const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
         {
             uint32_t z[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) z[k] = 0u;
-            for (int s = 0; s < 2; ++s) {
-                tmem_st32(tmem + lrow + TM_XO + s * 128 + 64, z);
-                tmem_st32(tmem + lrow + TM_XO + s * 128 + 96, z);
-            }
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+                for (int cc = 0; cc < C; cc += 32) tmem_st32(tmem + lrow + L::TM_XO + s * L::XO_STRIDE + C + cc, z);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -548,31 +608,30 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 mbar_arrive(&bar[B_OFREE + 1]);
             }
         }
-        Stream st;
-        st.start(p, c);
+        Stream<C> st;
+        st.start(p, grp);
         for (int j = 0; j < J && st.valid; ++j, st.next(p)) {
             const int s = j & 1;
             if (!__all_sync(0xffffffffu, wait(B_O + s, (uint32_t)(j >> 1)))) break;
             if (c == 0 && tid == 384) CTR(j, 10);
             tc_fence_after();
-            uint32_t ov[64];
-            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-            tmem_ld32(tmem + lrow + TM_XO + s * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+            uint32_t ov[C];
+            tmem_ld_cols<C / 32>(tmem + lrow + L::TM_XO + s * L::XO_STRIDE + C, ov);
             tmem_ld_wait();
             uint32_t z[32];
 #pragma unroll
             for (int k = 0; k < 32; ++k) z[k] = 0u;
-            tmem_st32(tmem + lrow + TM_XO + s * 128 + 64, z);
-            tmem_st32(tmem + lrow + TM_XO + s * 128 + 96, z);
+#pragma unroll
+            for (int cc = 0; cc < C; cc += 32) tmem_st32(tmem + lrow + L::TM_XO + s * L::XO_STRIDE + C + cc, z);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_OFREE + s]);
             const int len = st.len();
-            __nv_bfloat16 *orow = p.o + st.row0() * D + dv;
+            __nv_bfloat16 *orow = p.o + st.row0() * DV + dvg;
 #pragma unroll
-            for (int r = 0; r < 64; ++r)
-                if (r < len) orow[(size_t)r * D] = __float2bfloat16_rn(p.scale * __uint_as_float(ov[r]));
+            for (int r = 0; r < C; ++r)
+                if (r < len) orow[(size_t)r * DV] = __float2bfloat16_rn(p.scale * __uint_as_float(ov[r]));
             if (c == 0 && tid == 384) CTR(j, 11);
         }
     }
@@ -588,11 +647,16 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
 // counter.  One task, for chunk n of item (seq, head):
 //   TMA K, Q -> [K;Q][K;Q]^T on the tensor cores (Gram rows, Q K^T rows, both
 //   norms on the diagonal) -> gates, scale vectors -> Qt in place, published at
-//   once -> A (warps 0, 1) while P is built (warps 2, 3) -> (I + A)^-1 in place ->
-//   T, T' -> -(T' K) on the tensor cores -> -W over K -> publish, ready flag.
+//   once -> A (warps [0, C/32)) while P is built (warps [C/32, C/16)) -> (I + A)^-1
+//   in place -> T, T' -> -(T' K) on the tensor cores, 128 columns of d_k at a
+//   time -> -W over K -> publish, ready flag.
+template <class L>
 __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, uint8_t *sm)
 {
+    constexpr int C = L::C, DK = L::DK, NQ = L::NQ, KW = L::KW, AST = (int)L::AST;
+    constexpr uint32_t PANEL = L::PANEL, WQP = L::WQ_PANEL;
+    constexpr int TPUB = 32 * KW;   // the thread that publishes (first thread of the P warps)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -602,8 +666,8 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         tmem_relinquish();
     }
     const int pipe = warp >> 2;
-    uint8_t *base = sm + pipe * PP_STRIDE;
-    uint64_t *bar = (uint64_t *)(base + PP_BAR);
+    uint8_t *base = sm + pipe * L::PP_STRIDE;
+    uint64_t *bar = (uint64_t *)(base + L::PP_BAR);
     if ((warp & 3) == 0 && lane == 0) {
         for (int i = 0; i < NBAR_PP; ++i) mbar_init(&bar[i], 1);
         fence_barrier_init();
@@ -617,21 +681,21 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
     const int t = tid & 127;   // thread within the pipeline
     const int q4 = warp & 3;   // warp within the pipeline = its TMEM lane quarter
     const int bar_id = 1 + pipe;            // the pipeline's four warps
-    const int bar_hi = 1 + PIPES + pipe;    // its warps 2 and 3
+    const int bar_hi = 1 + PIPES + pipe;    // its P warps
     const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tg = tmem + pipe * 128;  // [K;Q][K;Q]^T (128 columns), later T' K
+    const uint32_t tg = tmem + pipe * 128;  // [K;Q][K;Q]^T (2C columns), later T' K (128)
     const uint32_t sbase = smem_u32(base);
-    volatile int *task_word = (volatile int *)(base + PP_BAR + NBAR_PP * 8);
-    float *vb = (float *)(base + PP_VEC);
+    volatile int *task_word = (volatile int *)(base + L::PP_BAR + NBAR_PP * 8);
+    float *vb = (float *)(base + L::PP_VEC);
     float *s_beta = vb, *s_gl = vb + 64, *s_nk = vb + 128, *s_nq = vb + 192, *s_tc = vb + 256;
     float *s_qs = vb + 320, *s_ra = vb + 384, *s_cb = vb + 448, *s_f0 = vb + 512, *s_g = vb + 576;
     int *s_safe = (int *)(vb + 640);
     float *s_kk = vb + 704;             // k_hat_r^T k_hat_r (Longhorn's step size)
-    float *AX = (float *)(base + PP_AX);
-    uint8_t *tl = base + PP_TL;
+    float *AX = (float *)(base + L::PP_AX);
+    uint8_t *tl = base + L::PP_TL;
     const int Jmax = p.cu ? (int)p.ctl[1] : p.Jmax_fixed;
-    const long long ntasks = (long long)p.Nc * Jmax;
-    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc);
+    const long long ntasks = (long long)p.Ng * Jmax;
+    volatile uint32_t *gabort = abort_word(p.ctl, p.Nc, p.Ng);
     auto fail = [&]() {
         if (!*abort_flag) {
             *abort_flag = 1;
@@ -644,23 +708,24 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         fail();
         return false;
     };
-    // chunk j of chain CTA c: item and chunk within it (false if the stream is shorter)
-    auto locate = [&](int c, int j, Item &I, int &n) -> bool {
+    // chunk j of chain group g: item and chunk within it (false if the stream is shorter)
+    auto locate = [&](int g, int j, Item &I, int &n) -> bool {
         n = j;
-        for (int it = c; it < p.items; it += p.Nc) {
-            I = item_of(p, it);
+        for (int it = g; it < p.items; it += p.Ng) {
+            I = item_of<C>(p, it);
             if (n < I.nch) return true;
             n -= I.nch;
         }
         return false;
     };
     uint32_t k_task = 0;   // tasks this pipeline has run (barrier phases)
+    uint32_t k_w = 0;      // T' K products this pipeline has waited for (P_W phases)
     uint32_t tma_phase = 0;   // (t == 0) barrier phase of the K, Q copy last issued
     bool tma_pending = false, mma_issued = false;
-    uint32_t *pend_ready = nullptr;     // (t == 64) flag of a package still being written
+    uint32_t *pend_ready = nullptr;     // (t == TPUB) flag of a package still being written
     uint32_t pend_val = 0;
     while (true) {
-        if (t == 64 && pend_ready) {
+        if (t == TPUB && pend_ready) {
             // the previous package has landed: raise its ready flag (while thread 0 fetches a task)
             bulk_wait_all();
             fence_async_global();
@@ -677,83 +742,93 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         const int task = *task_word;
         named_bar(bar_id, 128);
         if (task >= ntasks) break;
-        const int c = task % p.Nc, j = task / p.Nc;
+        const int grp = task % p.Ng, j = task / p.Ng;
         Item I;
         int n;
-        if (!locate(c, j, I, n)) continue;
-        if (task == p.withhold) continue;   // test hook: the chain CTA's wait for it must run out
-        if (c == 0 && t == 0) CTR(j, 12);
+        if (!locate(grp, j, I, n)) continue;
+        if (task == p.withhold) continue;   // test hook: the chain CTAs' wait for it must run out
+        if (grp == 0 && t == 0) CTR(j, 12);
         const int len = min(C, I.L - n * C);
         const long long row0 = I.rowbase + (long long)n * C;
-        const int slot = j % RING;
-        uint32_t *consumed = consumed_word(p.ctl, c);
-        uint32_t *ready = ready_words(p.ctl, p.Nc, c) + slot;
-        uint8_t *dst = p.ring + ((size_t)c * RING + slot) * PK_STRIDE;
+        const int slot = j % L::RING;
+        uint32_t *ready = ready_words(p.ctl, p.Nc, grp) + slot;
+        uint8_t *dst = p.ring + ((size_t)grp * L::RING + slot) * L::PK_STRIDE;
         if (t == 0) {
-            // the ring slot must have been copied out by the chain CTA
+            // the ring slot must have been copied out by every chain CTA of the group
             const long long t0 = clock64();
             unsigned ns = 64;
-            while ((int)ld_acquire_gpu(consumed) < j - RING + 1) {
-                if (*gabort || clock64() - t0 > p.flag_budget) { fail(); break; }
-                __nanosleep(ns);
-                ns = ns < 256 ? 2 * ns : ns;   // a freed slot is seen within ~0.3 us
+            for (int hv = 0; hv < L::NV && !*abort_flag; ++hv) {
+                uint32_t *consumed = consumed_word(p.ctl, grp * L::NV + hv);
+                while ((int)ld_acquire_gpu(consumed) < j - L::RING + 1) {
+                    if (*gabort || clock64() - t0 > p.flag_budget) { fail(); break; }
+                    __nanosleep(ns);
+                    ns = ns < 256 ? 2 * ns : ns;   // a freed slot is seen within ~0.3 us
+                }
             }
             if (!*abort_flag) {
-                mbar_expect_tx(&bar[P_FULL], 32768);
-                tma_load_2d(tl, tm_k, &bar[P_FULL], 0, (int)row0);
-                tma_load_2d(tl + 16384, tm_k, &bar[P_FULL], 64, (int)row0);
-                tma_load_2d(tl + 8192, tm_q, &bar[P_FULL], 0, (int)row0);
-                tma_load_2d(tl + 24576, tm_q, &bar[P_FULL], 64, (int)row0);
+                mbar_expect_tx(&bar[P_FULL], NQ * WQP);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    tma_load_2d(tl + q * WQP, tm_k, &bar[P_FULL], 64 * q, (int)row0);
+                    tma_load_2d(tl + q * WQP + PANEL, tm_q, &bar[P_FULL], 64 * q, (int)row0);
+                }
                 tma_pending = true;
                 tma_phase = k_task;
-                if (c == 0) CTR(j, 13);
+                if (grp == 0) CTR(j, 13);
             }
         }
         if (q4 == 0) {
             // beta and g (zero past the chunk), gates scanned in log2 units
-            float g0 = 0.f, g1 = 0.f;
-            s_beta[lane] = lane < len ? __bfloat162float(p.beta[row0 + lane]) : 0.f;
-            s_beta[lane + 32] = lane + 32 < len ? __bfloat162float(p.beta[row0 + lane + 32]) : 0.f;
-            if (p.gate) {
-                g0 = lane < len ? p.gate[row0 + lane] : 0.f;
-                g1 = lane + 32 < len ? p.gate[row0 + lane + 32] : 0.f;
-                if (__any_sync(0xffffffffu, g0 > 0.f || g1 > 0.f) && lane == 0)
-                    raise_status(p.status, kStatusPositiveGate);
+            float gv[KW];
+            bool pos = false;
+#pragma unroll
+            for (int e = 0; e < KW; ++e) {
+                const int i = lane + 32 * e;
+                s_beta[i] = i < len ? __bfloat162float(p.beta[row0 + i]) : 0.f;
+                gv[e] = (p.gate && i < len) ? p.gate[row0 + i] : 0.f;
+                pos = pos || gv[e] > 0.f;
             }
+            if (p.gate && __any_sync(0xffffffffu, pos) && lane == 0) raise_status(p.status, kStatusPositiveGate);
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                float a0 = __shfl_up_sync(0xffffffffu, g0, o);
-                float a1 = __shfl_up_sync(0xffffffffu, g1, o);
-                if (lane >= o) { g0 += a0; g1 += a1; }
+#pragma unroll
+                for (int e = 0; e < KW; ++e) {
+                    const float a = __shfl_up_sync(0xffffffffu, gv[e], o);
+                    if (lane >= o) gv[e] += a;
+                }
             }
-            g1 += __shfl_sync(0xffffffffu, g0, 31);
-            g0 *= 1.4426950408889634f;
-            g1 *= 1.4426950408889634f;
-            s_gl[lane] = g0;
-            s_gl[lane + 32] = g1;
-            float mx = fmaxf(fabsf(g0), fabsf(g1));
+            float carry = 0.f, mx = 0.f;
+#pragma unroll
+            for (int e = 0; e < KW; ++e) {
+                gv[e] += carry;
+                carry = __shfl_sync(0xffffffffu, gv[e], 31);
+                gv[e] *= 1.4426950408889634f;
+                s_gl[lane + 32 * e] = gv[e];
+                mx = fmaxf(mx, fabsf(gv[e]));
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             if (lane == 0) *s_safe = mx < 100.f;
         }
         if (wait(P_FULL, k_task) && t == 0) tma_pending = false;
-        if (c == 0 && t == 0) CTR(j, 14);
+        if (grp == 0 && t == 0) CTR(j, 14);
         if (t == 0) {
             // [K;Q][K;Q]^T: Gram rows, Q K^T rows and both norms on the diagonals
+            // (C = 32: A rows 64..127 are the next panel's, their results unread)
             mma_issued = true;
             tc_fence_after();
-            const uint64_t d = sdesc(sbase + PP_TL, 16, 1024);
+            const uint64_t d = sdesc(sbase + L::PP_TL, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint64_t dk = dadd(d, (k >> 2) * 16384 + (k & 3) * 32);
-                mma_bf16_ss(tg, dk, dk, ID_SS_N128, k > 0);
+            for (int k = 0; k < 4 * NQ; ++k) {
+                const uint64_t dk = dadd(d, (k >> 2) * WQP + (k & 3) * 32);
+                mma_bf16_ss(tg, dk, dk, L::ID_XO, k > 0);
             }
             mma_commit(&bar[P_G]);
         }
         wait(P_G, k_task);
         tc_fence_after();
-        if (c == 0 && t == 0) CTR(j, 15);
-        {
+        if (grp == 0 && t == 0) CTR(j, 15);
+        if (q4 < 2 * KW) {
             // diagonal element of this lane's row: column 32 q4 + lane
             uint32_t v[32];
             tmem_ld32(tg + lrow + 32 * q4, v);
@@ -761,9 +836,9 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             float dg = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) dg = (i == lane) ? __uint_as_float(v[i]) : dg;
-            const int r = (q4 & 1) * 32 + lane;
+            const int r = (q4 % KW) * 32 + lane;
             const float nrm = r < len ? (p.l2norm ? rsqrtf(dg + p.eps) : 1.f) : 0.f;
-            if (q4 < 2) {
+            if (q4 < KW) {
                 s_nk[r] = nrm;
                 s_kk[r] = dg * nrm * nrm;
             } else {
@@ -773,7 +848,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         named_bar(bar_id, 128);
         const bool safe = *s_safe != 0;
         const float glC = s_gl[len - 1];
-        if (t < 64) {
+        if (t < C) {
             const float gl = s_gl[t];
             const float e = ex2f(gl);
             // the step size: beta, or Longhorn's beta / (1 + beta k^T k)
@@ -790,14 +865,14 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             if (t == 0) s_g[0] = ex2f(glC);
         }
         named_bar(bar_id, 128);
-        if (c == 0 && t == 0) CTR(j, 19);
+        if (grp == 0 && t == 0) CTR(j, 19);
         {
             // Qt = diag(exp(gamma) m) Q in place: 16-byte pieces, a warp covers 4 whole rows
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NQ * C / 16; ++u) {
                 const int idx = u * 128 + t;
-                const int hh = idx >> 9, r = (idx >> 3) & 63;
-                uint4 *qp = (uint4 *)(tl + hh * 16384 + 8192 + r * 128 + (idx & 7) * 16);
+                const int hh = idx / (C * 8), r = (idx >> 3) % C;
+                uint4 *qp = (uint4 *)(tl + hh * WQP + PANEL + r * 128 + (idx & 7) * 16);
                 const float f = s_qs[r];
                 uint4 a = *qp;
                 a.x = scale_pair(a.x, f); a.y = scale_pair(a.y, f);
@@ -807,13 +882,12 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         }
         fence_async_smem();
         named_bar(bar_id, 128);
-        if (c == 0 && t == 0) CTR(j, 22);
-        if (q4 < 2) {
+        if (grp == 0 && t == 0) CTR(j, 22);
+        if (q4 < KW) {
             // A = strict_lower(diag(beta n) (K K^T o D) diag(n)), full rows (zeros on and above the diagonal)
             const int r = q4 * 32 + lane;
-            uint32_t v[64];
-            tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            uint32_t v[C];
+            tmem_ld_cols<C / 32>(tg + lrow, v);
             tmem_ld_wait();
             float4 *arow = reinterpret_cast<float4 *>(AX + r * AST);
             if (safe) {
@@ -821,7 +895,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 const float ra = s_ra[r];
                 const float4 *cb4 = reinterpret_cast<const float4 *>(s_cb);
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
+                for (int c4 = 0; c4 < C / 4; ++c4) {
                     const float4 cb = cb4[c4];
                     const int i = 4 * c4;
                     arow[c4] = make_float4(i < r ? ra * cb.x * __uint_as_float(v[i]) : 0.f,
@@ -831,7 +905,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 }
             } else {
                 const float br = s_beta[r] * s_nk[r], gr = s_gl[r];
-                for (int c4 = 0; c4 < 16; ++c4) {
+                for (int c4 = 0; c4 < C / 4; ++c4) {
                     float a[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -841,29 +915,29 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                     arow[c4] = make_float4(a[0], a[1], a[2], a[3]);
                 }
             }
-            if (c == 0 && t == 0) CTR(j, 25);
-        } else {
+            if (grp == 0 && t == 0) CTR(j, 25);
+        } else if (q4 < 2 * KW) {
             // publish Qt now; once the copy has read it, its space takes T and P
-            if (t == 64 && !*abort_flag) {
-                bulk_store(dst + PK_WQ + 8192, tl + 8192, 8192);
-                bulk_store(dst + PK_WQ + 24576, tl + 24576, 8192);
+            if (t == TPUB && !*abort_flag) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) bulk_store(dst + L::PK_WQ + q * WQP + PANEL, tl + q * WQP + PANEL, PANEL);
                 bulk_commit();
                 bulk_wait_read();
             }
-            named_bar(bar_hi, 64);
-            if (c == 0 && t == 64) CTR(j, 26);
-            // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i], into Qt's second half
-            const int r = (q4 - 2) * 32 + lane;
-            uint32_t v[64];
-            tmem_ld32(tg + lrow, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(tg + lrow + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            named_bar(bar_hi, 32 * KW);
+            if (grp == 0 && t == TPUB) CTR(j, 26);
+            // P = lower(m_r n_i (q_r . k_i) D_ri), bf16 [r][i], into panel 1's Qt rows
+            uint8_t *pt = tl + WQP + PANEL;
+            const int r = (q4 - KW) * 32 + lane;
+            uint32_t v[C];
+            tmem_ld_cols<C / 32>(tg + lrow, v);
             tmem_ld_wait();
             const float mr = s_nq[r], gr = s_gl[r];
             if (safe) {
                 const float rp = mr * ex2f(gr);
                 const float4 *cb4 = reinterpret_cast<const float4 *>(s_cb);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 0; c8 < C / 8; ++c8) {
                     const float4 ca = cb4[2 * c8], cc = cb4[2 * c8 + 1];
                     const float cbv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
                     uint32_t w[4];
@@ -874,10 +948,10 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                         const float a1 = (i0 + 1 <= r) ? rp * cbv[2 * e + 1] * __uint_as_float(v[i0 + 1]) : 0.f;
                         w[e] = pack_bf16(a0, a1);
                     }
-                    *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(pt + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             } else {
-                for (int c8 = 0; c8 < 8; ++c8) {
+                for (int c8 = 0; c8 < C / 8; ++c8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -886,106 +960,113 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                         const float a1 = (i1 <= r) ? mr * s_nk[i1] * __uint_as_float(v[i1]) * ex2f(gr - s_gl[i1]) : 0.f;
                         w[e] = pack_bf16(a0, a1);
                     }
-                    *(uint4 *)(tl + 24576 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *(uint4 *)(pt + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (c == 0 && t == 64) CTR(j, 28);
+            if (grp == 0 && t == TPUB) CTR(j, 28);
         }
         tc_fence_before();   // G's last reads precede the MMA that reuses its columns
         named_bar(bar_id, 128);
-        if (c == 0 && t == 0) CTR(j, 20);
-        solve_unit_lower_64_packed<AST>(AX, lane, q4, bar_id);
-        if (c == 0 && t == 0) CTR(j, 16);
+        if (grp == 0 && t == 0) CTR(j, 20);
+        solve_unit_lower_packed<AST, C / 16>(AX, lane, q4, bar_id);
+        if (grp == 0 && t == 0) CTR(j, 16);
         {
-            // T = X diag(beta) (package, into Qt's first half) and T' = X diag(beta exp(gamma) n)
-            // (operand of the next MMA, over the solve buffer); X[r][i] = AX[i][r] for i <= r
-            const int r = t & 63, hh = t >> 6;
-            float x[32];
+            // T = X diag(beta) (package, into panel 0's Qt rows) and T' = X diag(beta exp(gamma) n)
+            // (operand of the next MMA, over the solve buffer); X[r][i] = AX[i][r] for i <= r.
+            // Thread t: row t % C, columns [CW (t / C), CW (t / C) + CW).
+            constexpr int CW = C * C / 128;
+            const int r = t % C, hh = t / C;
+            float x[CW];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int i = 32 * hh + e;
+            for (int e = 0; e < CW; ++e) {
+                const int i = CW * hh + e;
                 x[e] = (i <= r) ? AX[i * AST + r] : 0.f;
             }
             named_bar(bar_id, 128);   // all of X has been read before T' overwrites it
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
+            for (int c8 = 0; c8 < CW / 8; ++c8) {
                 uint32_t wt[4], wp[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int i0 = 32 * hh + 8 * c8 + 2 * e;
+                    const int i0 = CW * hh + 8 * c8 + 2 * e;
                     const float x0 = x[8 * c8 + 2 * e], x1 = x[8 * c8 + 2 * e + 1];
                     wt[e] = pack_bf16(x0 * s_beta[i0], x1 * s_beta[i0 + 1]);
                     wp[e] = pack_bf16(x0 * s_tc[i0], x1 * s_tc[i0 + 1]);
                 }
-                const uint32_t off = sw128(r, (hh * 4 + c8) * 16);
-                *(uint4 *)(tl + 8192 + off) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
-                *(uint4 *)(base + PP_AX + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+                const uint32_t off = sw128(r, (hh * (CW / 8) + c8) * 16);
+                *(uint4 *)(tl + PANEL + off) = make_uint4(wt[0], wt[1], wt[2], wt[3]);
+                *(uint4 *)(base + L::PP_AX + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
             }
-            if (c == 0 && t == 0) CTR(j, 29);
+            if (grp == 0 && t == 0) CTR(j, 29);
         }
         fence_async_smem();
         named_bar(bar_id, 128);
-        if (c == 0 && t == 0) CTR(j, 21);
-        if (t == 0) {
-            // (T' K)[r][dk] with r on TMEM lanes 0..63 (A rows 64..127 are don't-care)
+        if (grp == 0 && t == 0) CTR(j, 21);
+#pragma unroll 1
+        for (int hn = 0; hn < DK / 128; ++hn) {
+            if (t == 0) {
+                // (T' K)[r][dk], 128 columns of d_k from panel 2 hn on, with r on TMEM
+                // lanes 0..C-1 (A rows C..127 are don't-care)
+                tc_fence_after();
+                const uint64_t da = sdesc(sbase + L::PP_AX, 16, 1024);
+                const uint64_t db = sdesc(sbase + L::PP_TL + 2 * hn * WQP, WQP, 1024);
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    mma_bf16_ss(tg, dadd(da, k * 32), dadd(db, k * 2048), L::ID_TK, k > 0);
+                mma_commit(&bar[P_W]);
+                if (grp == 0) CTR(j, 24);
+            }
+            if (hn == 0 && t == TPUB && !*abort_flag) {
+                bulk_store(dst + L::PK_T, tl + PANEL, PANEL);
+                bulk_store(dst + L::PK_P, tl + WQP + PANEL, PANEL);
+                bulk_store(dst + L::PK_VEC, s_f0, L::VEC_BYTES);   // f0[64], exp(gamma_C)
+                bulk_commit();
+            }
+            wait(P_W, k_w++);
             tc_fence_after();
-            const uint64_t da = sdesc(sbase + PP_AX, 16, 1024);
-            const uint64_t db = sdesc(sbase + PP_TL, 16384, 1024);
+            if (grp == 0 && t == 0) CTR(j, 17);
+            if (q4 < KW) {
+                // -W rows over the K rows: token r, 128 columns
+                const int r = q4 * 32 + lane;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tg, dadd(da, k * 32), dadd(db, k * 2048), ID_SS_N128_BMN, k > 0);
-            mma_commit(&bar[P_W]);
-            if (c == 0) CTR(j, 24);
-        }
-        if (t == 64 && !*abort_flag) {
-            bulk_store(dst + PK_T, tl + 8192, 8192);
-            bulk_store(dst + PK_P, tl + 24576, 8192);
-            bulk_store(dst + PK_VEC, s_f0, 272);   // f0[64], exp(gamma_C)
-            bulk_commit();
-        }
-        wait(P_W, k_task);
-        tc_fence_after();
-        if (c == 0 && t == 0) CTR(j, 17);
-        if (q4 < 2) {
-            // -W rows over the K rows: token r, 128 columns
-            const int r = q4 * 32 + lane;
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[64];
+                    tmem_ld_cols<2>(tg + lrow + 64 * h, v);
+                    tmem_ld_wait();
+                    uint8_t *wrow = tl + (2 * hn + h) * WQP;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v[64];
-                tmem_ld32(tg + lrow + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(tg + lrow + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tmem_ld_wait();
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        uint32_t w[4];
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16(-__uint_as_float(v[8 * c8 + 2 * e]), -__uint_as_float(v[8 * c8 + 2 * e + 1]));
-                    *(uint4 *)(tl + h * 16384 + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack_bf16(-__uint_as_float(v[8 * c8 + 2 * e]), -__uint_as_float(v[8 * c8 + 2 * e + 1]));
+                        *(uint4 *)(wrow + sw128(r, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
                 }
             }
+            tc_fence_before();   // the columns' last reads precede the next product into them
+            if (hn + 1 < DK / 128) named_bar(bar_id, 128);
         }
-        tc_fence_before();
         fence_async_smem();
         named_bar(bar_id, 128);
-        if (c == 0 && t == 0) CTR(j, 23);
-        if (t == 64) {
+        if (grp == 0 && t == 0) CTR(j, 23);
+        if (t == TPUB) {
             // publish -W; the ready flag goes up at the top of the pipeline's next
             // task, once every copy of the package has landed
             if (!*abort_flag) {
-                bulk_store(dst + PK_WQ, tl, 8192);
-                bulk_store(dst + PK_WQ + 16384, tl + 16384, 8192);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) bulk_store(dst + L::PK_WQ + q * WQP, tl + q * WQP, PANEL);
                 bulk_commit();
                 pend_ready = ready;
                 pend_val = (uint32_t)(j + 1);
-                if (c == 0) CTR(j, 18);
+                if (grp == 0) CTR(j, 18);
             }
             bulk_wait_read();   // the buffers may be refilled
         }
         ++k_task;
         named_bar(bar_id, 128);
     }
-    if (t == 64) {
+    if (t == TPUB) {
         bulk_wait_all();
         if (pend_ready && !*abort_flag) {
             fence_async_global();
@@ -1009,19 +1090,21 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
 }
 
 // ================================================================================= kernel
+template <class L>
 __global__ void __launch_bounds__(NTHREADS, 1)
 k_coop_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    if ((int)blockIdx.x < p.Nc) chain_cta(p, &tm_k, &tm_v, sm, blockIdx.x);
-    else prep_cta(p, &tm_q, &tm_k, sm);
+    if ((int)blockIdx.x < p.Nc) chain_cta<L>(p, &tm_k, &tm_v, sm, blockIdx.x);
+    else prep_cta<L>(p, &tm_q, &tm_k, sm);
 }
 
 // Packed input: longest-first order of the sequences and the longest chunk stream of
-// any chain CTA (written to ctl[1]).  One block.
-__global__ void k_plan(const int32_t *cu, int N, int T, int H, int Nc, int32_t *order, uint32_t *ctl)
+// any chain group (written to ctl[1]).  One block.
+template <int C>
+__global__ void k_plan(const int32_t *cu, int N, int T, int H, int Ng, int32_t *order, uint32_t *ctl)
 {
     __shared__ int s_max;
     if (threadIdx.x == 0) s_max = 0;
@@ -1045,9 +1128,9 @@ __global__ void k_plan(const int32_t *cu, int N, int T, int H, int Nc, int32_t *
     }
     __syncthreads();
     const int items = N * H;
-    for (int c = threadIdx.x; c < Nc; c += blockDim.x) {
+    for (int g = threadIdx.x; g < Ng; g += blockDim.x) {
         int Jc = 0;
-        for (int it = c; it < items; it += Nc) {
+        for (int it = g; it < items; it += Ng) {
             const int sq = order[it / H];
             int a = cu[sq], b = cu[sq + 1];
             if (a < 0 || b < a || b > T) a = b = 0;
@@ -1083,13 +1166,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-bool make_map(CUtensorMap *m, const void *base, long long rows)
+// bf16 [rows][width] row-major, boxes of 64 columns x box_rows rows, 128-byte swizzle
+bool make_map(CUtensorMap *m, const void *base, long long rows, int width, int box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t gstr[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint64_t gdim[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    cuuint64_t gstr[1] = {(cuuint64_t)width * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim, gstr, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1104,26 +1188,120 @@ int num_sms()
     return n;
 }
 
-}  // namespace
-
-// Split of the SMs: chain CTAs (at most 64, at most one per item), the rest prepare.
+// Split of the SMs: chain CTAs (about 27 / 64 of them, at most NV per item, a
+// multiple of NV), the rest prepare.
+template <class L>
 int chain_ctas(const Geo &g, int sms)
 {
     const int items = g.N * g.H;
     int nc = (sms * 27 + 32) / 64;   // 64 of 152
-    if (nc > items) nc = items;
-    if (nc < 1) nc = 1;
+    if (nc > items * L::NV) nc = items * L::NV;
+    nc -= nc % L::NV;
+    if (nc < L::NV) nc = L::NV;
     return nc;
+}
+
+template <class L>
+size_t workspace_bytes_t(const Geo &g, int sms)
+{
+    if (sms <= 0) sms = 160;   // sizing without a device: an upper bound
+    const int nc = chain_ctas<L>(g, sms), ng = nc / L::NV;
+    const size_t ctl = ctl_words(nc, ng) * sizeof(uint32_t);
+    const size_t order = g.varlen ? sizeof(int32_t) * (size_t)(g.N + 1) : 0;
+    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    return al(ctl) + al(order) + (size_t)ng * L::RING * L::PK_STRIDE;
+}
+
+template <class L>
+cudaError_t fwd_t(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                  const __nv_bfloat16 *v, const __nv_bfloat16 *beta, const float *gate,
+                  const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
+                  uint32_t *status, cudaStream_t st)
+{
+    const int sms = num_sms();
+    if (sms < 2) return cudaErrorNotSupported;
+    if (ws_bytes < workspace_bytes_t<L>(g, sms)) return cudaErrorInvalidValue;
+    const int items = g.N * g.H;
+    if (items == 0) return cudaSuccess;
+    const int nc = chain_ctas<L>(g, sms), ng = nc / L::NV;
+    if (nc >= sms) return cudaErrorNotSupported;
+    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    uint8_t *w = (uint8_t *)ws;
+    const size_t ctl_bytes = ctl_words(nc, ng) * sizeof(uint32_t);
+    Params p;
+    p.beta = beta; p.gate = gate; p.h0 = h0; p.o = o; p.hT = hT; p.status = status;
+    p.cu = g.varlen ? g.cu : nullptr;
+    p.ctl = (uint32_t *)w;
+    p.order = g.varlen ? (const int32_t *)(w + al(ctl_bytes)) : nullptr;
+    p.ring = w + al(ctl_bytes) + (g.varlen ? al(sizeof(int32_t) * (size_t)(g.N + 1)) : 0);
+    p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc; p.Ng = ng;
+    p.Jmax_fixed = g.varlen ? 0 : ((items + ng - 1) / ng) * ((g.T + L::C - 1) / L::C);
+    p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm; p.longhorn = g.longhorn;
+    // Test hook (failure detection): GDN_DEBUG_WITHHOLD_TASK=n makes the preparation
+    // CTAs skip task n (chunk n / Ng of chain group n % Ng), so that group's bounded
+    // wait for the package runs out; every cross-CTA flag wait then gives up after
+    // about 1 ms, the launch winds down and the status word reports the timeout.
+    p.withhold = -1;
+    p.flag_budget = BUDGET;
+    if (const char *e = getenv("GDN_DEBUG_WITHHOLD_TASK")) {
+        if (e[0]) {
+            p.withhold = atoi(e);
+            p.flag_budget = HOOK_FLAG_BUDGET;
+        }
+    }
+    cudaError_t e = cudaMemsetAsync(p.ctl, 0, ctl_bytes, st);
+    if (e != cudaSuccess) return e;
+    if (g.varlen) {
+        k_plan<L::C><<<1, 1024, 0, st>>>(g.cu, g.N, g.T, g.H, ng, (int32_t *)p.order, p.ctl);
+        if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+    }
+    const long long rows = (long long)g.B * g.H * g.T;
+    CUtensorMap mq, mk, mv;
+    const long long maprows = rows > 0 ? rows : 1;
+    if (!make_map(&mq, q, maprows, L::DK, L::C) || !make_map(&mk, k, maprows, L::DK, L::C) ||
+        !make_map(&mv, v, maprows, L::DV, L::C))
+        return cudaErrorInvalidValue;
+    if ((e = cudaFuncSetAttribute(k_coop_fwd<L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)L::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_coop_fwd<L>, NTHREADS, L::SMEM_BYTES)) !=
+        cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    void *args[] = {(void *)&mq, (void *)&mk, (void *)&mv, (void *)&p};
+    e = cudaLaunchCooperativeKernel((const void *)k_coop_fwd<L>, dim3(sms), dim3(NTHREADS), args,
+                                    L::SMEM_BYTES, st);
+    if (e != cudaSuccess) return e;
+    return cudaPeekAtLastError();
+}
+
+// 0: (C 64, d 128), 1: (C 32, d 128), 2: (C 32, d 256), -1: none
+int instance(const Geo &g)
+{
+    if (g.dk != g.dv) return -1;
+    if (g.dk == 128 && g.C == 64) return 0;
+    if (g.dk == 128 && g.C == 32) return 1;
+    if (g.dk == 256 && g.C == 32) return 2;
+    return -1;
+}
+
+}  // namespace
+
+bool supports(const Geo &g, int dtype)
+{
+    return dtype == DN_BF16 && instance(g) >= 0 && (long long)g.B * g.H * (long long)g.T < (1LL << 31) &&
+           encode_fn() != nullptr;
 }
 
 size_t workspace_bytes(const Geo &g, int sms)
 {
-    if (sms <= 0) sms = 160;   // sizing without a device: an upper bound
-    const int nc = chain_ctas(g, sms);
-    const size_t ctl = ctl_words(nc) * sizeof(uint32_t);
-    const size_t order = g.varlen ? sizeof(int32_t) * (size_t)(g.N + 1) : 0;
-    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
-    return al(ctl) + al(order) + (size_t)nc * RING * PK_STRIDE;
+    switch (instance(g)) {
+    case 0: return workspace_bytes_t<Cfg64>(g, sms);
+    case 1: return workspace_bytes_t<Cfg32>(g, sms);
+    case 2: return workspace_bytes_t<Cfg32w>(g, sms);
+    }
+    return 0;
 }
 
 bool available()
@@ -1143,59 +1321,12 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                 const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
                 uint32_t *status, cudaStream_t st)
 {
-    const int sms = num_sms();
-    if (sms < 2) return cudaErrorNotSupported;
-    if (ws_bytes < workspace_bytes(g, sms)) return cudaErrorInvalidValue;
-    const int items = g.N * g.H;
-    if (items == 0) return cudaSuccess;
-    const int nc = chain_ctas(g, sms);
-    auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
-    uint8_t *w = (uint8_t *)ws;
-    const size_t ctl_bytes = ctl_words(nc) * sizeof(uint32_t);
-    Params p;
-    p.beta = beta; p.gate = gate; p.h0 = h0; p.o = o; p.hT = hT; p.status = status;
-    p.cu = g.varlen ? g.cu : nullptr;
-    p.ctl = (uint32_t *)w;
-    p.order = g.varlen ? (const int32_t *)(w + al(ctl_bytes)) : nullptr;
-    p.ring = w + al(ctl_bytes) + (g.varlen ? al(sizeof(int32_t) * (size_t)(g.N + 1)) : 0);
-    p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc;
-    p.Jmax_fixed = g.varlen ? 0 : ((items + nc - 1) / nc) * ((g.T + C - 1) / C);
-    p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm; p.longhorn = g.longhorn;
-    // Test hook (failure detection): GDN_DEBUG_WITHHOLD_TASK=n makes the preparation
-    // CTAs skip task n (chunk n / Nc of chain CTA n % Nc), so that chain CTA's bounded
-    // wait for the package runs out; every cross-CTA flag wait then gives up after
-    // about 1 ms, the launch winds down and the status word reports the timeout.
-    p.withhold = -1;
-    p.flag_budget = BUDGET;
-    if (const char *e = getenv("GDN_DEBUG_WITHHOLD_TASK")) {
-        if (e[0]) {
-            p.withhold = atoi(e);
-            p.flag_budget = HOOK_FLAG_BUDGET;
-        }
+    switch (instance(g)) {
+    case 0: return fwd_t<Cfg64>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
+    case 1: return fwd_t<Cfg32>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
+    case 2: return fwd_t<Cfg32w>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
     }
-    cudaError_t e = cudaMemsetAsync(p.ctl, 0, ctl_bytes, st);
-    if (e != cudaSuccess) return e;
-    if (g.varlen) {
-        k_plan<<<1, 1024, 0, st>>>(g.cu, g.N, g.T, g.H, nc, (int32_t *)p.order, p.ctl);
-        if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
-    }
-    const long long rows = (long long)g.B * g.H * g.T;
-    CUtensorMap mq, mk, mv;
-    const long long maprows = rows > 0 ? rows : 1;
-    if (!make_map(&mq, q, maprows) || !make_map(&mk, k, maprows) || !make_map(&mv, v, maprows))
-        return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(k_coop_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)) !=
-        cudaSuccess)
-        return e;
-    int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_coop_fwd, NTHREADS, SMEM_BYTES)) !=
-        cudaSuccess)
-        return e;
-    if (per_sm < 1) return cudaErrorNotSupported;
-    void *args[] = {(void *)&mq, (void *)&mk, (void *)&mv, (void *)&p};
-    e = cudaLaunchCooperativeKernel((const void *)k_coop_fwd, dim3(sms), dim3(NTHREADS), args, SMEM_BYTES, st);
-    if (e != cudaSuccess) return e;
-    return cudaPeekAtLastError();
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace coop

@@ -19,11 +19,15 @@ cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
 
 }  // namespace fast
 
-// Cooperative persistent forward (preparation CTAs + chain CTAs); same shapes as fast.
+// Cooperative persistent forward (preparation CTAs + chain CTAs): bf16 with
+// d_k = d_v = 128 and C = 64 or 32, or d_k = d_v = 256 and C = 32.
 namespace coop {
 
 // Whether this device can run it (cooperative launch, tensor-map encoder).
 bool available();
+
+// Whether it takes this geometry and dtype.
+bool supports(const Geo &g, int dtype);
 
 // Workspace it needs: control words, packed order, package ring.  sms <= 0 sizes
 // for an upper bound on the SM count.

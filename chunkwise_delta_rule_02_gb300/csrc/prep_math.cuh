@@ -146,7 +146,8 @@ __device__ __forceinline__ void solve_unit_lower_64(const float *Af, float *Xf, 
     sm100::named_bar(bar_id, 128);
 }
 
-// The same inverse computed in one buffer.  On entry AX holds the strictly lower
+// The same inverse computed in one buffer, for a 16 NB x 16 NB matrix (NB = 4:
+// 64 x 64, NB = 2: 32 x 32).  On entry AX holds the strictly lower
 // triangular A below its diagonal (fp32, row stride AST floats; what lies on and
 // above the diagonal is ignored).  On return the strictly lower blocks still hold
 // A, and X is stored transposed on and above the diagonal:
@@ -155,12 +156,14 @@ __device__ __forceinline__ void solve_unit_lower_64(const float *Af, float *Xf, 
 // zeros for the upper part of X_ii).  The off-diagonal blocks X_ij (i > j) go to
 // block (j, i); nothing reads or writes A's blocks after the diagonal phase, so
 // the column-parallel schedule of solve_unit_lower_64 carries over unchanged.
-// Called by the 128 threads of one warpgroup; synchronises it (named barrier
-// bar_id) between the phases and at the end.
-template <int AST>
-__device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, int q4, int bar_id)
+// Called by the 128 threads of one warpgroup (warps q4 >= NB idle in the diagonal
+// phase, warps q4 >= NB - 1 in the off-diagonal one); synchronises it (named
+// barrier bar_id) between the phases and at the end.
+template <int AST, int NB = 4>
+__device__ __forceinline__ void solve_unit_lower_packed(float *AX, int lane, int q4, int bar_id)
 {
-    {
+    static_assert(NB >= 1 && NB <= 4, "16 x 16 blocks, one warp each");
+    if (q4 < NB) {
         const int base = 16 * q4, c = lane & 15;
         float x[16];
 #pragma unroll
@@ -186,9 +189,9 @@ __device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, 
     }
     sm100::named_bar(bar_id, 128);
     const int g8 = lane >> 2, t4 = lane & 3;
-    if (q4 < 3) {
+    if (q4 < NB - 1) {
         const int j = q4;
-        for (int i = j + 1; i < 4; ++i) {
+        for (int i = j + 1; i < NB; ++i) {
             float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             for (int m = j; m < i; ++m) {
                 // Z = X_ii A_im
@@ -232,6 +235,12 @@ __device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, 
         }
     }
     sm100::named_bar(bar_id, 128);
+}
+
+template <int AST>
+__device__ __forceinline__ void solve_unit_lower_64_packed(float *AX, int lane, int q4, int bar_id)
+{
+    solve_unit_lower_packed<AST, 4>(AX, lane, q4, bar_id);
 }
 
 }  // namespace prep

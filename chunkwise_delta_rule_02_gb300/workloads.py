@@ -1,6 +1,6 @@
 """Seeded synthetic inputs for the (gated) delta-rule workloads.
 
-This module holds the shapes, seeds and value distributions of the five
+This module holds the shapes, seeds and value distributions of the
 workloads and nothing of the method's arithmetic: it draws q, k, v, beta, the
 log-gate g, the initial state, packed sequence lengths and upstream gradients.
 Both the CUDA path's tests/benchmark and the fp64 oracle take their inputs from
@@ -62,6 +62,13 @@ WORKLOADS: Dict[str, Workload] = {
     # Gated DeltaNet forward + backward, bf16, B8 H16 T4096 d128
     "gdn_fwdbwd_bf16_b8h16t4096d128": Workload("gdn_fwdbwd_bf16_b8h16t4096d128", 8, 16, 4096,
                                                128, "bf16", True, True, 4, backward=True),
+    # chunk 32 (the DeltaNet page's best chunk on A100) on the B4 H16 T8192 d128 forward
+    "gdn_fwd_bf16_b4h16t8192d128_c32_h0": Workload("gdn_fwd_bf16_b4h16t8192d128_c32_h0", 4, 16,
+                                                   8192, 128, "bf16", True, True, 5, chunk=32),
+    # head dim 256 (the Gated DeltaNet page's head size) at the same width, 8 heads x 256 =
+    # 16 x 128, chunk 32
+    "gdn_fwd_bf16_b4h8t8192d256_c32_h0": Workload("gdn_fwd_bf16_b4h8t8192d256_c32_h0", 4, 8, 8192,
+                                                  256, "bf16", True, True, 6, chunk=32),
 }
 
 WORKLOAD_ORDER: List[str] = list(WORKLOADS)

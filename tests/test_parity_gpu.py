@@ -160,12 +160,14 @@ def test_dn_fwd_f32_b1h2t256d64():
 @pytest.mark.parametrize("name,sel", [
     ("dn_fwd_bf16_b8h16t2048d128", [(0, 0), (3, 7), (7, 15), (5, 2)]),
     ("gdn_fwd_bf16_b4h16t8192d128_h0", [(0, 0), (1, 9), (3, 15), (2, 4)]),
+    ("gdn_fwd_bf16_b4h16t8192d128_c32_h0", [(0, 0), (2, 11), (3, 15)]),
+    ("gdn_fwd_bf16_b4h8t8192d256_c32_h0", [(0, 0), (1, 5), (3, 7)]),
 ])
 def test_full_size_forward_sampled(name, sel):
     """Full-size launch (the benchmark's configuration); the oracle recomputes sampled
     (batch, head) items, each over its whole sequence."""
     x = _gen(name)
-    o, hT = _run_fwd(x)
+    o, hT = _run_fwd(x, chunk=_w(name).chunk)
     refs = oracle_fwd(x, sel=sel)
     for (b, h), (ro, rh) in zip(sel, refs):
         _assert_close("o[%d,%d]" % (b, h), o[b:b + 1, h:h + 1], ro, TOL["bf16"])
