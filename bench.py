@@ -333,6 +333,35 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def record_traffic(csv_path: str, kernel: str, workload: str, capture: str, out: str = None) -> dict:
+    """Write profiles/traffic.json's entry for (kernel, workload) from the CSV of an ncu
+    capture of one launch (dram__bytes_read.sum, dram__bytes_write.sum), stamped with
+    the hash of the kernel's current sources.  Runs on any host (no GPU needed)."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hdr = next(r for r in rows if "Metric Name" in r)
+    start = rows.index(hdr) + 1
+    ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    got = {}
+    for r in rows[start:]:
+        if len(r) > vi and kernel in r[ki]:
+            got.setdefault(r[mi], float(r[vi].replace(",", "")))
+    if "dram__bytes_read.sum" not in got or "dram__bytes_write.sum" not in got:
+        raise SystemExit("no dram byte counters for %s in %s" % (kernel, csv_path))
+    rd, wr = int(got["dram__bytes_read.sum"]), int(got["dram__bytes_write.sum"])
+    p = out or os.path.join(ROOT, "profiles", "traffic.json")
+    d = json.load(open(p)) if os.path.exists(p) else {}
+    d[kernel + "@" + workload] = {
+        "dram_bytes_per_launch": rd + wr, "dram_read": rd, "dram_write": wr,
+        "source_sha": kernel_source_sha(kernel),
+        "sources": ", ".join(["csrc/" + f for f in KERNEL_SOURCES.get(kernel, [])] + ["include/gdn.h"]),
+        "capture": capture}
+    with open(p, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return d[kernel + "@" + workload]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture of this exact kernel source
     (profiles/traffic.json), scaled to the workload; None if absent or stale."""
@@ -625,7 +654,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="write profiles/traffic.json's entry for --workload from this ncu CSV and exit")
+    ap.add_argument("--capture", default="", help="with --record-traffic: the ncu command that made the CSV")
     args = ap.parse_args()
+
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, "k_coop_fwd", args.workload, args.capture)))
+        return
 
     if args.workload == DECODE_WORKLOAD:
         if args.impl == "ours":

@@ -222,3 +222,22 @@ def test_forward_counts_of_the_headline_workload():
     th = 4 * 16 * 128
     assert bench.algorithmic_flops(w, x) == th * (6 * 128 * 128 + 10 * 64 * 128) + 4 * 16 * 2 * (2 * 64 ** 3 // 3)
     assert bench.algorithmic_bytes(w, x) == th * 1030 + 2 * 4 * 16 * 128 * 128 * 4
+
+
+def test_record_traffic_reads_one_launch_and_stamps_the_source(tmp_path):
+    """The traffic entry is the read + write DRAM bytes of the named kernel's launch in
+    an ncu CSV, stamped with the hash of its current sources (so that a changed kernel
+    reads as unmeasured)."""
+    import bench
+    csv_path = tmp_path / "t.csv"
+    head = '"ID","Process ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+    rows = ['"0","1","k_other(int)","dram__bytes_read.sum","byte","5"\n',
+            '"1","1","k_coop_fwd<(anonymous namespace)::Cfg<64, 128>>(CUtensorMap_st)","dram__bytes_read.sum","byte","1,000"\n',
+            '"1","1","k_coop_fwd<(anonymous namespace)::Cfg<64, 128>>(CUtensorMap_st)","dram__bytes_write.sum","byte","24"\n']
+    csv_path.write_text("==PROF== noise\n" + head + "".join(rows))
+    out = tmp_path / "traffic.json"
+    e = bench.record_traffic(str(csv_path), "k_coop_fwd", "wl", "ncu ...", out=str(out))
+    assert e["dram_read"] == 1000 and e["dram_write"] == 24 and e["dram_bytes_per_launch"] == 1024
+    assert e["source_sha"] == bench.kernel_source_sha("k_coop_fwd")
+    import json
+    assert json.load(open(out))["k_coop_fwd@wl"]["capture"] == "ncu ..."
