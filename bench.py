@@ -770,8 +770,14 @@ def main():
     flops = algorithmic_flops(w, x) + (algorithmic_flops(w, x, backward=True) if w.backward else 0)
     path, launches_per_step = binding.dn_plan(shape, False)
     kname = {binding.DN_PATH_COOP: "k_coop_fwd", binding.DN_PATH_FUSED: "k_fast_fwd"}.get(path, "general_fwd")
+    bwd_desc = ""
     if w.backward:
-        launches_per_step += binding.dn_plan(shape, True)[1]
+        nb = binding.dn_plan(shape, True)[1]
+        launches_per_step += nb
+        coop_bwd = nb == 3 + (2 if d["cu_seqlens"] is not None else 0)
+        bwd_desc = ("; backward: the cooperative forward re-run writing every chunk's operands and"
+                    " states, the reverse scan over them, tcgen05 per-chunk gradients" if coop_bwd else
+                    "; backward: recompute, reverse scan and per-chunk kernels")
     if w.backward:
         # the timed region is the whole step: the forward plus the backward's kernels
         kdesc = "whole forward+backward step (%d kernels)" % launches_per_step
@@ -791,8 +797,7 @@ def main():
                        "path": {binding.DN_PATH_COOP: "cooperative tcgen05 kernel",
                                 binding.DN_PATH_FUSED: "fused tcgen05 kernel per (sequence, head)"}.get(
                                     path, "general fp32 kernels")
-                               + ("; backward: recompute, reverse scan and per-chunk kernels"
-                                  " (staged bf16 tensor-core products)" if w.backward else ""),
+                               + bwd_desc,
                        "l2": "no flush: inputs %.2f GB per step > 129 MB L2" % (abytes / 1e9),
                        "parallelism": "replicas over ranks" if world > 1 else "single GPU"},
             "roofline": roof, "clocks": clocks, "e2e": e2e,

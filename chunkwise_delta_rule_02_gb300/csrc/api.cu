@@ -66,6 +66,7 @@ int device_sms()
 struct Layout {
     size_t status, cstart, fast;
     size_t Kn, Qn, W, U, Unew, gam, eb, Sin, dSo, dUn, dQ, dK, dW, P, aux, M3;
+    size_t coop, coop_bytes, keep, Sin_b, Un_b, dSo_b, dUn_b;   // backward through the cooperative forward
     size_t total;
 };
 
@@ -89,6 +90,20 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, Fwd kind)
     }
     const size_t slots = (size_t)g.NC * g.H, C = g.C, dk = g.dk, dv = g.dv;
     auto take = [&](size_t nfloat) { size_t o = off; off += align256(nfloat * sizeof(float)); return o; };
+    if (for_backward && gen::bwd_uses_coop(g, s->dtype)) {
+        // the cooperative forward's ring, every chunk's package, and the bf16 states,
+        // Unew, dS_out, dUnew of the tcgen05 per-chunk backward
+        auto takeb = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
+        L.coop_bytes = coop::workspace_bytes(g, device_sms());
+        L.coop = takeb(L.coop_bytes);
+        L.keep = takeb(slots * coop::package_layout(g).stride);
+        L.Sin_b = takeb(slots * dk * dv * 2);
+        L.dSo_b = takeb(slots * dk * dv * 2);
+        L.Un_b = takeb(slots * C * dv * 2);
+        L.dUn_b = takeb(slots * C * dv * 2);
+        L.total = off;
+        return L;
+    }
     L.Kn = take(slots * C * dk);
     L.Qn = take(slots * C * dk);
     L.W = take(slots * C * dk);
@@ -121,6 +136,13 @@ gen::Ws general_ws(const Layout &L, char *base)
     w.gam = F(L.gam); w.eb = F(L.eb); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
     w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
     w.P = F(L.P); w.aux = F(L.aux); w.M3 = F(L.M3);
+    if (L.keep) {
+        auto B = [&](size_t o) { return (__nv_bfloat16 *)(base + o); };
+        w.keep = (uint8_t *)(base + L.keep);
+        w.coop_ws = base + L.coop;
+        w.coop_bytes = L.coop_bytes;
+        w.Sin_b = B(L.Sin_b); w.dSo_b = B(L.dSo_b); w.Un_b = B(L.Un_b); w.dUn_b = B(L.dUn_b);
+    }
     return w;
 }
 
@@ -276,10 +298,14 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
     int path, n;
     if (for_backward) {
         path = DN_PATH_GENERAL;
-        // k_prep, k_scan, k_bscan, then k_bwd_tc (tcgen05) or k_bbig, k_bchunk, k_bgrad;
-        // the pointer alignment the tcgen05 kernel also needs is not known here
+        // k_coop_fwd (+ k_plan), k_bscan_pk, k_bwd_tc; or k_prep, k_scan, k_bscan, then
+        // k_bwd_tc (tcgen05) or k_bbig, k_bchunk, k_bgrad (the entry point requires the
+        // 16-byte pointer alignment the tcgen05 kernel needs)
         const void *aligned = (const void *)(uintptr_t)256;
-        n = (gen::bwd_uses_tc(g, shape->dtype, aligned, aligned, aligned, aligned) ? 4 : 6) + offsets;
+        if (gen::bwd_uses_coop(g, shape->dtype))
+            n = 3 + 2 * offsets;
+        else
+            n = (gen::bwd_uses_tc(g, shape->dtype, aligned, aligned, aligned, aligned) ? 4 : 6) + offsets;
     } else if (fwd_kind(shape, g, 0, true) == Fwd::General) {
         path = DN_PATH_GENERAL;
         n = 3 + offsets;                    // k_prep, k_scan, k_out

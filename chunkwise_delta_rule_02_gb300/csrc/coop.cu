@@ -99,6 +99,9 @@ struct Cfg {
     // package ring depth: about 450 KB per ring (deeper rings spill packages from
     // L2 to HBM: 10 slots of the C = 64 package added 78 MB of DRAM traffic per launch)
     static constexpr int RING = C == 64 ? 9 : (DK == 128 ? 18 : 20);
+    // the backward's outputs (packages, S_in, Unew) are compiled into the instance the
+    // tcgen05 backward takes only
+    static constexpr bool EMIT = C == 64 && DK == 128;
 
     // package (ring slot in global memory and its copy in a chain CTA's shared memory)
     static constexpr uint32_t WQ_PANEL = 2 * PANEL;        // per panel [-W rows | Qt rows]
@@ -187,7 +190,22 @@ struct Params {
     int longhorn;           // step size beta / (1 + beta k^T k) instead of beta
     int withhold;           // test hook: this task's package is never published (-1: none)
     long long flag_budget;  // cycles a cross-CTA flag wait may take before it gives up
+    // for the backward (null otherwise): every package also into keep[slot], the bf16
+    // state entering each chunk into sin_out[slot][dk][dv] and Unew into
+    // unew_out[slot][C][dv], slot = chunk slot * H + head (chunk slots of a sequence
+    // from cstart, packed input, or nchs per sequence)
+    uint8_t *keep;
+    __nv_bfloat16 *sin_out, *unew_out;
+    const int32_t *cstart;
+    int nchs;
 };
+
+// workspace slot of chunk n of (sequence seq, head h), as the general kernels number them
+__device__ __forceinline__ size_t slot_of(const Params &p, int seq, int h, int n)
+{
+    const int j0 = p.cstart ? p.cstart[seq] : seq * p.nchs;
+    return (size_t)(j0 + n) * p.H + h;
+}
 
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
@@ -516,6 +534,9 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                 uint32_t r[64];
                 tmem_ld_cols<2>(tmem + lrow + L::TM_S + 64 * panel, r);
                 tmem_ld_wait();
+                uint16_t *sin = (L::EMIT && p.sin_out) ? reinterpret_cast<uint16_t *>(p.sin_out) +
+                                                slot_of(p, st.cur.seq, st.cur.h, st.n) * DK * DV + dvg
+                                          : nullptr;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     uint32_t w[4];
@@ -523,6 +544,15 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                     for (int e = 0; e < 4; ++e)
                         w[e] = pack_bf16(Gn * __uint_as_float(r[c8 * 8 + 2 * e]), Gn * __uint_as_float(r[c8 * 8 + 2 * e + 1]));
                     *(uint4 *)(sbp + sw128(dvl, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if (L::EMIT && sin) {
+                        // S_in[dk][dv] for this thread's d_v column (a warp writes 64 contiguous bytes)
+                        const int k0 = 64 * panel + c8 * 8;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sin[(size_t)(k0 + 2 * e) * DV] = (uint16_t)(w[e] & 0xFFFFu);
+                            sin[(size_t)(k0 + 2 * e + 1) * DV] = (uint16_t)(w[e] >> 16);
+                        }
+                    }
                 }
                 if (renorm) {
 #pragma unroll
@@ -563,6 +593,16 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                     const uint32_t off = sw128(dvl, ((CH / 8) * half + c8) * 16);
                     *(uint4 *)(u1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
                     *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                }
+                if (L::EMIT && p.unew_out) {
+                    // Unew[token][dv] (rows past the chunk's end are zeros here already)
+                    uint16_t *un = reinterpret_cast<uint16_t *>(p.unew_out) +
+                                   (slot_of(p, st.cur.seq, st.cur.h, st.n) * C + CH * half) * DV + dvg;
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        const uint32_t wb = pack_bf16(__uint_as_float(x[i]), 0.f);
+                        un[(size_t)i * DV] = (uint16_t)(wb & 0xFFFFu);
+                    }
                 }
             }
             fence_async_smem();
@@ -628,10 +668,12 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[B_OFREE + s]);
             const int len = st.len();
-            __nv_bfloat16 *orow = p.o + st.row0() * DV + dvg;
+            if (p.o) {
+                __nv_bfloat16 *orow = p.o + st.row0() * DV + dvg;
 #pragma unroll
-            for (int r = 0; r < C; ++r)
-                if (r < len) orow[(size_t)r * DV] = __float2bfloat16_rn(p.scale * __uint_as_float(ov[r]));
+                for (int r = 0; r < C; ++r)
+                    if (r < len) orow[(size_t)r * DV] = __float2bfloat16_rn(p.scale * __uint_as_float(ov[r]));
+            }
             if (c == 0 && tid == 384) CTR(j, 11);
         }
     }
@@ -753,6 +795,7 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
         const int slot = j % L::RING;
         uint32_t *ready = ready_words(p.ctl, p.Nc, grp) + slot;
         uint8_t *dst = p.ring + ((size_t)grp * L::RING + slot) * L::PK_STRIDE;
+        uint8_t *kdst = (L::EMIT && p.keep) ? p.keep + slot_of(p, I.seq, I.h, n) * L::PK_STRIDE : nullptr;
         if (t == 0) {
             // the ring slot must have been copied out by every chain CTA of the group
             const long long t0 = clock64();
@@ -920,7 +963,10 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             // publish Qt now; once the copy has read it, its space takes T and P
             if (t == TPUB && !*abort_flag) {
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) bulk_store(dst + L::PK_WQ + q * WQP + PANEL, tl + q * WQP + PANEL, PANEL);
+                for (int q = 0; q < NQ; ++q) {
+                    bulk_store(dst + L::PK_WQ + q * WQP + PANEL, tl + q * WQP + PANEL, PANEL);
+                    if (kdst) bulk_store(kdst + L::PK_WQ + q * WQP + PANEL, tl + q * WQP + PANEL, PANEL);
+                }
                 bulk_commit();
                 bulk_wait_read();
             }
@@ -1020,6 +1066,11 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
                 bulk_store(dst + L::PK_T, tl + PANEL, PANEL);
                 bulk_store(dst + L::PK_P, tl + WQP + PANEL, PANEL);
                 bulk_store(dst + L::PK_VEC, s_f0, L::VEC_BYTES);   // f0[64], exp(gamma_C)
+                if (kdst) {
+                    bulk_store(kdst + L::PK_T, tl + PANEL, PANEL);
+                    bulk_store(kdst + L::PK_P, tl + WQP + PANEL, PANEL);
+                    bulk_store(kdst + L::PK_VEC, s_f0, L::VEC_BYTES);
+                }
                 bulk_commit();
             }
             wait(P_W, k_w++);
@@ -1055,7 +1106,10 @@ __device__ __forceinline__ void prep_cta(const Params &p, const CUtensorMap *tm_
             // task, once every copy of the package has landed
             if (!*abort_flag) {
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) bulk_store(dst + L::PK_WQ + q * WQP, tl + q * WQP, PANEL);
+                for (int q = 0; q < NQ; ++q) {
+                    bulk_store(dst + L::PK_WQ + q * WQP, tl + q * WQP, PANEL);
+                    if (kdst) bulk_store(kdst + L::PK_WQ + q * WQP, tl + q * WQP, PANEL);
+                }
                 bulk_commit();
                 pend_ready = ready;
                 pend_val = (uint32_t)(j + 1);
@@ -1216,7 +1270,7 @@ template <class L>
 cudaError_t fwd_t(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                   const __nv_bfloat16 *v, const __nv_bfloat16 *beta, const float *gate,
                   const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
-                  uint32_t *status, cudaStream_t st)
+                  uint32_t *status, cudaStream_t st, const Emit *emit)
 {
     const int sms = num_sms();
     if (sms < 2) return cudaErrorNotSupported;
@@ -1237,6 +1291,12 @@ cudaError_t fwd_t(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
     p.H = g.H; p.T = g.T; p.N = g.N; p.items = items; p.Nc = nc; p.Ng = ng;
     p.Jmax_fixed = g.varlen ? 0 : ((items + ng - 1) / ng) * ((g.T + L::C - 1) / L::C);
     p.scale = g.scale; p.eps = g.eps; p.l2norm = g.l2norm; p.longhorn = g.longhorn;
+    p.keep = emit ? emit->keep : nullptr;
+    p.sin_out = emit ? emit->sin : nullptr;
+    p.unew_out = emit ? emit->unew : nullptr;
+    p.cstart = g.varlen ? g.cstart : nullptr;
+    p.nchs = (g.T + L::C - 1) / L::C;
+    if (emit && ((g.varlen && !g.cstart) || !L::EMIT)) return cudaErrorInvalidValue;
     // Test hook (failure detection): GDN_DEBUG_WITHHOLD_TASK=n makes the preparation
     // CTAs skip task n (chunk n / Ng of chain group n % Ng), so that group's bounded
     // wait for the package runs out; every cross-CTA flag wait then gives up after
@@ -1319,14 +1379,30 @@ bool available()
 cudaError_t fwd(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                 const __nv_bfloat16 *v, const __nv_bfloat16 *beta, const float *gate,
                 const float *h0, __nv_bfloat16 *o, float *hT, void *ws, size_t ws_bytes,
-                uint32_t *status, cudaStream_t st)
+                uint32_t *status, cudaStream_t st, const Emit *emit)
 {
     switch (instance(g)) {
-    case 0: return fwd_t<Cfg64>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
-    case 1: return fwd_t<Cfg32>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
-    case 2: return fwd_t<Cfg32w>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st);
+    case 0: return fwd_t<Cfg64>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st, emit);
+    case 1: return fwd_t<Cfg32>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st, emit);
+    case 2: return fwd_t<Cfg32w>(g, q, k, v, beta, gate, h0, o, hT, ws, ws_bytes, status, st, emit);
     }
     return cudaErrorInvalidValue;
+}
+
+PkLayout package_layout(const Geo &g)
+{
+    PkLayout r{};
+    auto fill = [&](auto cfg) {
+        using L = decltype(cfg);
+        r.stride = L::PK_STRIDE; r.wq = L::PK_WQ; r.wq_panel = L::WQ_PANEL; r.panel = L::PANEL;
+        r.t = L::PK_T; r.p = L::PK_P; r.vec = L::PK_VEC;
+    };
+    switch (instance(g)) {
+    case 0: fill(Cfg64{}); break;
+    case 1: fill(Cfg32{}); break;
+    case 2: fill(Cfg32w{}); break;
+    }
+    return r;
 }
 
 }  // namespace coop

@@ -43,6 +43,7 @@
 #include <stdlib.h>
 
 #include "bwd_tc.h"
+#include "fast.h"
 #include "prep_math.cuh"
 
 namespace gdn {
@@ -1007,6 +1008,159 @@ __global__ void __launch_bounds__(512) k_bscan_st(Geo g, const __nv_bfloat16 *__
         __syncthreads();
         // dS[kk][n] <- Gamma_C dS[kk][n] + sum_x G_x Q[x][kk] dO[x][n] - sum_x W[x][kk] dUnew[x][n]
         const float GC = expf(gC);
+        tiles(dk, ldv - 5,
+              [&](int m0, int n0, float (&acc)[2][4][4]) {
+                  tile_mma<true, true>(acc, GQ, LK, dOb, LV, m0, n0, C);
+                  tile_mma<true, true>(acc, Wn, LK, dUb, LV, m0, n0, C);
+              },
+              [&](int kk, int n, float a0, float a1) {
+                  float2 *sp = reinterpret_cast<float2 *>(sdS + kk * LS + n);
+                  const float2 o = *sp;
+                  const float v0 = fmaf(GC, o.x, a0), v1 = fmaf(GC, o.y, a1);
+                  *sp = make_float2(v0, v1);
+                  put_bf2(dSb + kk * LV + n, v0, v1);
+              });
+        __syncthreads();
+    }
+    if (dh0)
+        for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x) {
+            const int kk = idx >> ldv, n = idx & (dv - 1);
+            dh0[sidx + idx] = sdS[kk * LS + n];
+        }
+}
+
+// backward scan over the cooperative forward's packages (bf16 tiles in the 128-byte
+// swizzle: -W, Qt = diag(exp(gamma) m) Q, P, the vector f0 = exp(gamma_C - gamma) n and
+// exp(gamma_C)) and the raw keys, instead of the recompute's fp32 arrays:
+//   dUnew = P^T dO + diag(f0) K dS,   dS <- exp(gamma_C) dS + Qt^T dO - W^T dUnew
+// (diag(f0) K = diag(exp(gamma_C - gamma)) K~ and Qt = diag(exp(gamma)) Q~ of k_bscan_st).
+// Writes dS_out and dUnew as bf16 (the tcgen05 per-chunk backward's inputs).
+__global__ void __launch_bounds__(512) k_bscan_pk(Geo g, const __nv_bfloat16 *__restrict__ kin,
+                                                  const __nv_bfloat16 *__restrict__ dO,
+                                                  const float *__restrict__ dhT, float *__restrict__ dh0,
+                                                  const uint8_t *__restrict__ keep, coop::PkLayout pk, Ws w)
+{
+    const int s = blockIdx.x, h = blockIdx.y;
+    const int C = g.C, dk = g.dk, dv = g.dv;
+    const int LS = dv + 8, LC = spad(C), LK = spad(dk), LV = spad(dv), ldv = ilog2(dv);
+    int b, t0, L, j0, nch;
+    seq_of(g, s, b, t0, L, j0, nch);
+    extern __shared__ float sm[];
+    float *sdS = sm;                                         // [dk][LS] fp32
+    float *sF = sdS + dk * LS;                               // [C] f0
+    __nv_bfloat16 *Ps = reinterpret_cast<__nv_bfloat16 *>(sF + 128);   // P [C][LC]
+    __nv_bfloat16 *EK = Ps + C * LC;                         // diag(f0) K [C][LK]
+    __nv_bfloat16 *GQ = EK + C * LK;                         // Qt [C][LK]
+    __nv_bfloat16 *Wn = GQ + C * LK;                         // -W [C][LK]
+    __nv_bfloat16 *dOb = Wn + C * LK;                        // scale dO [C][LV]
+    __nv_bfloat16 *dUb = dOb + C * LV;                       // dUnew [C][LV]
+    __nv_bfloat16 *dSb = dUb + C * LV;                       // dS [dk][LV]
+    const size_t sidx = ((size_t)s * g.H + h) * dk * dv;
+    for (int idx = threadIdx.x; idx < dk * dv / 2; idx += blockDim.x) {
+        const int kk = (2 * idx) >> ldv, n = (2 * idx) & (dv - 1);
+        const float v0 = dhT ? dhT[sidx + 2 * idx] : 0.f, v1 = dhT ? dhT[sidx + 2 * idx + 1] : 0.f;
+        *reinterpret_cast<float2 *>(sdS + kk * LS + n) = make_float2(v0, v1);
+        put_bf2(dSb + kk * LV + n, v0, v1);
+    }
+    __syncthreads();
+    const uint8_t *pkg0 = keep + (size_t)h * pk.stride;   // + chunk slot * H * stride
+    auto pkg = [&](int c) { return pkg0 + (size_t)(j0 + c) * g.H * pk.stride; };
+    // chunk c's package, keys and dO into L2 two chunks ahead; at the top of the chunk
+    // every load of its operands is issued at once into registers
+    auto prefetch = [&](int c) {
+        if (threadIdx.x == 0 && c >= 0 && c < nch) {
+            const int ln = min(C, L - c * C);
+            const size_t rw = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
+            l2_prefetch(pkg(c), pk.stride);
+            l2_prefetch(kin + rw * dk, sizeof(__nv_bfloat16) * ln * dk);
+            l2_prefetch(dO + rw * dv, sizeof(__nv_bfloat16) * ln * dv);
+        }
+    };
+    // swizzled tile pieces: row r of a 64-column panel holds 16-byte chunks c ^ (r % 8)
+    auto swz = [](int r, int c8) { return (uint32_t)(r * 128 + (((c8 ^ (r & 7)) & 7) << 4)); };
+    constexpr int NB = 2;   // C * d / 8 <= 2 * 512 pieces of 16 bytes; C * C / 8 <= 512
+    uint4 rP, rK[NB], rQ[NB], rW[NB], rO[NB];
+    float rf = 0.f, rgC = 0.f;
+    const int nkp = (C * dk) >> 3, lk8 = ilog2(dk) - 3;   // pieces of a C x dk tile, per row
+    auto issue = [&](int c) {
+        const int ln = min(C, L - c * C);
+        const size_t rw = ((size_t)b * g.H + h) * g.T + t0 + (size_t)c * C;
+        const uint8_t *pg = pkg(c);
+        {
+            const int e = threadIdx.x;   // P: C rows x 8 pieces
+            rP = (e < C * 8) ? __ldg(reinterpret_cast<const uint4 *>(pg + pk.p + swz(e >> 3, e & 7)))
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+            const int e = threadIdx.x + u * blockDim.x;
+            const int r = e >> lk8, c16 = e & ((1 << lk8) - 1), q = c16 >> 3;
+            const uint8_t *tile = pg + pk.wq + q * pk.wq_panel + swz(r, c16 & 7);
+            const bool in = e < nkp;
+            rW[u] = in ? __ldg(reinterpret_cast<const uint4 *>(tile)) : make_uint4(0u, 0u, 0u, 0u);
+            rQ[u] = in ? __ldg(reinterpret_cast<const uint4 *>(tile + pk.panel)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        reg_load_bf(rK, kin + rw * dk, C, dk, ln);
+        reg_load_bf(rO, dO + rw * dv, C, dv, ln);
+        const float *vec = reinterpret_cast<const float *>(pg + pk.vec);
+        rf = (int)threadIdx.x < C ? __ldg(vec + threadIdx.x) : 0.f;
+        rgC = __ldg(vec + 64);
+    };
+    prefetch(nch - 1);
+    prefetch(nch - 2);
+    for (int c = nch - 1; c >= 0; --c) {
+        issue(c);
+        const int len = min(C, L - c * C);
+        const size_t slot = (size_t)(j0 + c) * g.H + h;
+        __nv_bfloat16 *dUb16 = w.dUn_b + slot * C * dv;
+        if ((int)threadIdx.x < C) sF[threadIdx.x] = rf;
+        {
+            __nv_bfloat16 *dS16 = w.dSo_b + slot * dk * dv;
+            for (int idx = threadIdx.x; idx < dk * dv / 4; idx += blockDim.x) {
+                const int kk = (4 * idx) >> ldv, n = (4 * idx) & (dv - 1);
+                put_bf4(dS16 + 4 * idx, *reinterpret_cast<const float4 *>(sdS + kk * LS + n), 1.f);
+            }
+        }
+        __syncthreads();
+        {
+            const int e = threadIdx.x;
+            if (e < C * 8) *reinterpret_cast<uint4 *>(Ps + (e >> 3) * LC + ((e & 7) << 3)) = rP;
+        }
+        reg_put_bf(rW, C, dk, [&](int r, int kk, uint4 v) { *reinterpret_cast<uint4 *>(Wn + r * LK + kk) = v; });
+        reg_put_bf(rQ, C, dk, [&](int r, int kk, uint4 v) { *reinterpret_cast<uint4 *>(GQ + r * LK + kk) = v; });
+        reg_put_bf(rK, C, dk, [&](int r, int kk, uint4 v) {
+            const float f = sF[r];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o[q] = bf16x2(f * __uint_as_float(wv[q] << 16), f * __uint_as_float(wv[q] & 0xFFFF0000u));
+            *reinterpret_cast<uint4 *>(EK + r * LK + kk) = make_uint4(o[0], o[1], o[2], o[3]);
+        });
+        reg_put_bf(rO, C, dv, [&](int r, int n, uint4 v) {
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                o[q] = bf16x2(g.scale * __uint_as_float(wv[q] << 16), g.scale * __uint_as_float(wv[q] & 0xFFFF0000u));
+            *reinterpret_cast<uint4 *>(dOb + r * LV + n) = make_uint4(o[0], o[1], o[2], o[3]);
+        });
+        __syncthreads();
+        prefetch(c - 2);
+        // dUnew[i][n] = sum_x P[x][i] dO[x][n] + sum_kk (f0 K)[i][kk] dS[kk][n]
+        tiles(C, ldv - 5,
+              [&](int m0, int n0, float (&acc)[2][4][4]) {
+                  tile_mma<true, true>(acc, Ps, LC, dOb, LV, m0, n0, C);
+                  tile_mma<false, true>(acc, EK, LK, dSb, LV, m0, n0, dk);
+              },
+              [&](int i, int n, float u0, float u1) {
+                  const bool live = i < len;
+                  put_bf2(dUb16 + i * dv + n, live ? u0 : 0.f, live ? u1 : 0.f);
+                  put_bf2(dUb + i * LV + n, live ? u0 : 0.f, live ? u1 : 0.f);
+              });
+        __syncthreads();
+        // dS[kk][n] <- exp(gamma_C) dS[kk][n] + sum_x Qt[x][kk] dO[x][n] - sum_x W[x][kk] dUnew[x][n]
+        const float GC = rgC;
         tiles(dk, ldv - 5,
               [&](int m0, int n0, float (&acc)[2][4][4]) {
                   tile_mma<true, true>(acc, GQ, LK, dOb, LV, m0, n0, C);
@@ -2436,6 +2590,17 @@ bool bwd_uses_tc(const Geo &g, int dtype, const void *q, const void *k, const vo
            ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)dO) & 15u) == 0);
 }
 
+bool bwd_uses_coop(const Geo &g, int dtype)
+{
+    for (const char *name : {"GDN_BWD_RECOMPUTE", "GDN_FORCE_GENERAL"}) {
+        const char *e = getenv(name);
+        if (e && e[0] && e[0] != '0') return false;
+    }
+    const void *aligned = (const void *)(uintptr_t)256;
+    return bwd_uses_tc(g, dtype, aligned, aligned, aligned, aligned) && g.C == 64 && g.dk == 128 &&
+           g.dv == 128 && coop::available() && coop::supports(g, dtype);
+}
+
 template <class Tin>
 cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,
                 const float *gate, const float *h0, const Tin *dO, const float *dhT, Tin *dq,
@@ -2444,6 +2609,21 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
 {
     cudaError_t e;
     if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        if (w.keep && bwd_uses_tc(g, DN_BF16, q, k, v, dO)) {
+            // the cooperative forward writes every chunk's package, S_in and Unew; the
+            // reverse scan reads the packages; then the tcgen05 per-chunk gradients
+            const coop::Emit em{w.keep, w.Sin_b, w.Un_b};
+            if ((e = coop::fwd(g, q, k, v, beta, gate, h0, nullptr, nullptr, w.coop_ws, w.coop_bytes, g.status,
+                               st, &em)) != cudaSuccess)
+                return e;
+            if ((e = set_smem(k_bscan_pk, smem_bscan_st(g))) != cudaSuccess) return e;
+            if (g.N > 0)
+                k_bscan_pk<<<dim3(g.N, g.H), 512, smem_bscan_st(g), st>>>(g, k, dO, dhT, dh0, w.keep,
+                                                                          coop::package_layout(g), w);
+            if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+            return btc::grads(g, q, k, v, beta, gate, dO, w.Sin_b, w.dSo_b, w.Un_b, w.dUn_b, dq, dk, dv,
+                              dbeta, dg, st);
+        }
         if (bwd_uses_tc(g, DN_BF16, q, k, v, dO)) {
             // recompute and the two staged scans, writing bf16 states and Unew / dUnew
             // (over the fp32 arrays they replace), then the tcgen05 per-chunk gradients

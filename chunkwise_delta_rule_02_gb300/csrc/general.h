@@ -23,6 +23,12 @@ struct Ws {
     // (backward scan), with the rows past a chunk's end as zeros
     __nv_bfloat16 *Sin_b, *dSo_b;   // [slots][dk][dv]
     __nv_bfloat16 *Un_b, *dUn_b;    // [slots][C][dv]
+    // when keep is set (bwd_uses_coop), the backward recomputes through the cooperative
+    // forward instead: its workspace (coop_ws, coop_bytes), every chunk's package in
+    // keep[slot], and the bf16 arrays above; the float arrays are then not used
+    uint8_t *keep;
+    void *coop_ws;
+    size_t coop_bytes;
 };
 
 template <class Tin>
@@ -32,6 +38,12 @@ cudaError_t fwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
 
 // Whether gdn_chunk_bwd takes the tcgen05 per-chunk backward for this call.
 bool bwd_uses_tc(const Geo &g, int dtype, const void *q, const void *k, const void *v, const void *dO);
+
+// Whether that backward gets its states, Unew and the reverse scan's operands from the
+// cooperative forward (bf16, d 128, chunk 64, a device that runs it; not with
+// GDN_BWD_RECOMPUTE=1, GDN_FORCE_GENERAL=1 or GDN_BWD_STAGED=1): kernels k_coop_fwd,
+// k_bscan_pk, k_bwd_tc.
+bool bwd_uses_coop(const Geo &g, int dtype);
 
 template <class Tin>
 cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Tin *beta,

@@ -126,7 +126,13 @@ dn_status gdn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, con
 
 /* Gated DeltaNet backward: gradients of L = <o, dO> + <hT, dhT>.
  * Recomputes the chunk states from q, k, v, beta, g, h0 (chunk states are
- * recomputed in the backward rather than kept — DeltaNet page, reply Q2).
+ * recomputed in the backward rather than kept — DeltaNet page, reply Q2).  For
+ * bf16 with dk = dv = 128 and chunk 64 the recompute is a run of the cooperative
+ * forward that also leaves every chunk's prepared operands and its state in the
+ * workspace (dn_workspace_size(shape, 1) counts them: about 145 KB per chunk and
+ * head); GDN_BWD_RECOMPUTE=1 or GDN_FORCE_GENERAL=1 recompute with the general
+ * kernels instead.  A bounded wait that runs out in that run is reported like the
+ * forward's (DN_ERR_TIMEOUT from dn_device_status).
  *   dO  [B,H,T,dv] (dtype), dhT [N,H,dk,dv] float32 or NULL (= 0)
  *   dq, dk [B,H,T,dk], dv [B,H,T,dv], dbeta [B,H,T]   (dtype), with respect to
  *   the raw q and k given (chained through the normalisation)

@@ -59,7 +59,7 @@ def _same(a, b, what, order_free=False):
 @pytest.mark.parametrize("dtype,d,C", [("bf16", 128, 64), ("bf16", 64, 32), ("f32", 64, 64)])
 def test_chunks_do_not_reach_each_other(dtype, d, C, monkeypatch):
     import chunkwise_delta_rule_02_gb300 as gdn
-    monkeypatch.setenv("GDN_FORCE_GENERAL", "1")   # the general kernels also for the bf16 forward
+    monkeypatch.setenv("GDN_FORCE_GENERAL", "1")   # the general kernels (forward and the backward's recompute)
     x = _inputs(dtype, d, C, seed=71 + d + C)
     f, s = _half(x, 0, C), _half(x, C, 2 * C)
     kw = dict(chunk=C)
