@@ -691,7 +691,13 @@ def main():
 
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     shape = gdn.make_shape(d["q"], d["v"], w.chunk, d["cu_seqlens"])
+    # fwd+bwd: the training step keeps the forward's per-chunk operands for the backward
+    # (gdn_chunk_fwd_save / gdn_chunk_bwd_saved) where the library has that path
+    saved = None
+    if w.backward and binding.dn_saved_size(shape) > 0:
+        saved = torch.empty(binding.dn_saved_size(shape), dtype=torch.uint8, device=dev)
     ws = binding.alloc_workspace(shape, w.backward, dev)
+    wsb = binding.alloc_workspace(shape, 2, dev) if saved is not None else None
     o = torch.empty_like(d["v"])
     N = shape.num_seqs if d["cu_seqlens"] is not None else w.B
     hT = torch.empty((N, w.H, w.d, w.d), dtype=torch.float32, device=dev)
@@ -703,6 +709,13 @@ def main():
     fast = binding.dn_uses_fast_path(shape, False) == 1
 
     def step():
+        if saved is not None:
+            binding.gdn_chunk_fwd_save(shape, d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], o, hT, saved,
+                                       ws, stream)
+            binding.gdn_chunk_bwd_saved(shape, d["q"], d["k"], d["v"], d["beta"], d["g"], d["do"], d["dhT"],
+                                        saved, grads["dq"], grads["dk"], grads["dv"], grads["dbeta"],
+                                        grads["dg"], grads["dh0"], wsb, stream)
+            return
         if d["g"] is None:
             binding.dn_chunk_fwd(shape, d["q"], d["k"], d["v"], d["beta"], d["h0"], o, hT, ws, stream)
         else:
@@ -721,7 +734,8 @@ def main():
     for _ in range(max(3, args.warmup)):
         step()
     barrier()
-    if binding.dn_device_status(ws, stream) != binding.DN_OK:
+    if binding.dn_device_status(ws, stream) != binding.DN_OK or (
+            wsb is not None and binding.dn_device_status(wsb, stream) != binding.DN_OK):
         raise RuntimeError("device status error after warm-up")
 
     per, clocks = run_timed(step, args.steps, stream, barrier, local)
@@ -771,7 +785,12 @@ def main():
     path, launches_per_step = binding.dn_plan(shape, False)
     kname = {binding.DN_PATH_COOP: "k_coop_fwd", binding.DN_PATH_FUSED: "k_fast_fwd"}.get(path, "general_fwd")
     bwd_desc = ""
-    if w.backward:
+    if w.backward and saved is not None:
+        launches_per_step += binding.dn_plan(shape, 2)[1]
+        bwd_desc = ("; the forward keeps every chunk's operands and states (gdn_chunk_fwd_save, %.2f GB);"
+                    " backward from them (gdn_chunk_bwd_saved): the reverse scan, tcgen05 per-chunk gradients"
+                    % (saved.numel() / 1e9))
+    elif w.backward:
         nb = binding.dn_plan(shape, True)[1]
         launches_per_step += nb
         coop_bwd = nb == 3 + (2 if d["cu_seqlens"] is not None else 0)

@@ -7,6 +7,7 @@ inputs.
 from . import workloads  # noqa: F401
 from .binding import (  # noqa: F401
     DnShape, GdnError, backward, decode_step, dn_chunk_fwd, dn_device_status, dn_host_arena_size,
-    dn_uses_fast_path, dn_workspace_size, forward, gdn_chunk_bwd, gdn_chunk_fwd,
-    gdn_chunk_fwd_host, gdn_chunk_fwd_noalloc, gdn_decode_step, make_shape,
+    dn_saved_size, dn_uses_fast_path, dn_workspace_size, forward, gdn_chunk_bwd, gdn_chunk_bwd_saved,
+    gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_noalloc, gdn_chunk_fwd_save, gdn_decode_step,
+    make_shape, saved_supported,
 )

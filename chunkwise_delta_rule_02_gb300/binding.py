@@ -6,9 +6,10 @@ library's CUDA kernels.  There is no fallback: if the library is missing, or a
 call returns an error status, these functions raise.
 
 The names match the C ABI: dn_workspace_size, dn_chunk_fwd, gdn_chunk_fwd,
-gdn_chunk_bwd, dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status,
-dn_uses_fast_path, dn_plan, gdn_chunk_fwd_noalloc, dn_noalloc_status,
-gdn_decode_step, dn_state_affine.  ``forward`` / ``backward`` additionally
+gdn_chunk_bwd, dn_saved_size, gdn_chunk_fwd_save, gdn_chunk_bwd_saved,
+dn_host_arena_size, gdn_chunk_fwd_host, dn_device_status, dn_uses_fast_path,
+dn_plan, gdn_chunk_fwd_noalloc, dn_noalloc_status, gdn_decode_step,
+dn_state_affine.  ``forward`` / ``backward`` additionally
 allocate outputs and the workspace with torch (device memory only) and, unless
 told not to, read the device status word after the call (which synchronises the
 stream) so that a bounded wait that ran out, malformed packed offsets or a
@@ -30,7 +31,8 @@ from ._build import LIB
 DN_F32, DN_BF16 = 0, 1
 DN_BETA_DELTA, DN_BETA_LONGHORN = 0, 1
 
-EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd",
+EXPORTS = ["dn_workspace_size", "dn_chunk_fwd", "gdn_chunk_fwd", "gdn_chunk_bwd", "dn_saved_size",
+           "gdn_chunk_fwd_save", "gdn_chunk_bwd_saved",
            "dn_host_arena_size", "gdn_chunk_fwd_host", "dn_device_status", "dn_status_str",
            "dn_uses_fast_path", "gdn_chunk_fwd_noalloc", "dn_noalloc_status", "dn_plan",
            "gdn_decode_step", "dn_state_affine"]
@@ -81,6 +83,12 @@ def lib():
             L.gdn_chunk_fwd.restype = I
             L.gdn_chunk_bwd.argtypes = [SP, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P]
             L.gdn_chunk_bwd.restype = I
+            L.dn_saved_size.argtypes = [SP]
+            L.dn_saved_size.restype = S
+            L.gdn_chunk_fwd_save.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P, S, P]
+            L.gdn_chunk_fwd_save.restype = I
+            L.gdn_chunk_bwd_saved.argtypes = [SP, P, P, P, P, P, P, P, P, S, P, P, P, P, P, P, P, S, P]
+            L.gdn_chunk_bwd_saved.restype = I
             L.dn_host_arena_size.argtypes = [SP, I, I]
             L.dn_host_arena_size.restype = S
             L.gdn_chunk_fwd_host.argtypes = [SP, P, P, P, P, P, P, P, P, P, S, P, S, P]
@@ -150,8 +158,9 @@ def make_shape(q: torch.Tensor, v: torch.Tensor, chunk: int = 64, cu_seqlens=Non
     return s
 
 
-def dn_workspace_size(shape: DnShape, for_backward: bool = False) -> int:
-    return int(lib().dn_workspace_size(ctypes.byref(shape), int(bool(for_backward))))
+def dn_workspace_size(shape: DnShape, for_backward=False) -> int:
+    """for_backward: False / True (gdn_chunk_bwd) or 2 (gdn_chunk_bwd_saved)."""
+    return int(lib().dn_workspace_size(ctypes.byref(shape), int(for_backward)))
 
 
 def dn_uses_fast_path(shape: DnShape, for_backward: bool = False) -> int:
@@ -162,10 +171,11 @@ DN_PATH_GENERAL, DN_PATH_FUSED, DN_PATH_COOP = 0, 1, 2
 PATH_NAMES = {DN_PATH_GENERAL: "general", DN_PATH_FUSED: "fused", DN_PATH_COOP: "coop"}
 
 
-def dn_plan(shape: DnShape, for_backward: bool = False):
-    """(path, kernels per call): DN_PATH_* and the number of library kernels one call launches."""
+def dn_plan(shape: DnShape, for_backward=False):
+    """(path, kernels per call): DN_PATH_* and the number of library kernels one call
+    launches; for_backward as in dn_workspace_size."""
     n = ctypes.c_int(0)
-    path = int(lib().dn_plan(ctypes.byref(shape), int(bool(for_backward)), ctypes.byref(n)))
+    path = int(lib().dn_plan(ctypes.byref(shape), int(for_backward), ctypes.byref(n)))
     return path, int(n.value)
 
 
@@ -192,6 +202,27 @@ def gdn_chunk_bwd(shape, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, d
                              _p(dO), _p(dhT), _p(dq), _p(dk), _p(dv), _p(dbeta), _p(dg),
                              _p(dh0), _p(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "gdn_chunk_bwd")
+
+
+def dn_saved_size(shape) -> int:
+    """Bytes of the buffer gdn_chunk_fwd_save fills (0: no saved path for the shape)."""
+    return int(lib().dn_saved_size(ctypes.byref(shape)))
+
+
+def gdn_chunk_fwd_save(shape, q, k, v, beta, g, h0, o, hT, saved, ws, stream=None):
+    rc = lib().gdn_chunk_fwd_save(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g), _p(h0),
+                                  _p(o), _p(hT), _p(saved), saved.numel() * saved.element_size(),
+                                  _p(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "gdn_chunk_fwd_save")
+
+
+def gdn_chunk_bwd_saved(shape, q, k, v, beta, g, dO, dhT, saved, dq, dk, dv, dbeta, dg, dh0, ws,
+                        stream=None):
+    rc = lib().gdn_chunk_bwd_saved(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(beta), _p(g), _p(dO),
+                                   _p(dhT), _p(saved), saved.numel() * saved.element_size(), _p(dq),
+                                   _p(dk), _p(dv), _p(dbeta), _p(dg), _p(dh0), _p(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "gdn_chunk_bwd_saved")
 
 
 def gdn_chunk_fwd_host(shape, q, k, v, beta, g, h0, o, hT, arena, ws, stream=None):
@@ -255,8 +286,9 @@ def dn_noalloc_status(stream=None) -> int:
     return int(lib().dn_noalloc_status(_stream(stream)))
 
 
-def alloc_workspace(shape: DnShape, for_backward: bool, device) -> torch.Tensor:
-    n = dn_workspace_size(shape, for_backward)
+def alloc_workspace(shape: DnShape, for_backward, device) -> torch.Tensor:
+    """for_backward: False / True (gdn_chunk_bwd) or 2 (gdn_chunk_bwd_saved)."""
+    n = dn_workspace_size(shape, int(for_backward))
     if n == 0:
         raise GdnError(DN_ERR_INVALID_ARG, "dn_workspace_size")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -266,13 +298,34 @@ def _nseq(q, cu_seqlens):
     return q.shape[0] if cu_seqlens is None else int(cu_seqlens.numel()) - 1
 
 
+def saved_supported(q, v, chunk=64, cu_seqlens=None, scale=1.0, qk_l2norm=True, eps=1e-6,
+                    longhorn=False) -> bool:
+    """Whether forward(save=True) / backward(saved=...) run for these inputs."""
+    return dn_saved_size(make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)) > 0
+
+
 def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0,
             qk_l2norm=True, eps=1e-6, want_state=True, ws=None, longhorn=False,
-            check_status=True):
+            check_status=True, save=False):
     """Allocate o (and hT) and run gdn_chunk_fwd / dn_chunk_fwd.  Returns (o, hT).
     check_status: read the device status word afterwards (synchronises the stream)
-    and raise GdnError if the kernels flagged anything."""
+    and raise GdnError if the kernels flagged anything.  save=True runs
+    gdn_chunk_fwd_save and returns (o, hT, saved) for backward(saved=saved)."""
     shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
+    if save:
+        n = dn_saved_size(shape)
+        if n == 0:
+            raise GdnError(DN_ERR_UNSUPPORTED, "gdn_chunk_fwd_save")
+        saved = torch.empty(n, dtype=torch.uint8, device=q.device)
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+        hT = torch.empty((_nseq(q, cu_seqlens), q.shape[1], q.shape[-1], v.shape[-1]), dtype=torch.float32,
+                         device=q.device) if want_state else None
+        if ws is None:
+            ws = alloc_workspace(shape, False, q.device)
+        gdn_chunk_fwd_save(shape, q, k, v, beta, g, h0, o, hT, saved, ws)
+        if check_status:
+            _check(dn_device_status(ws), "gdn_chunk_fwd_save (device status)")
+        return o, hT, saved
     o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     N = _nseq(q, cu_seqlens)
     hT = torch.empty((N, q.shape[1], q.shape[-1], v.shape[-1]), dtype=torch.float32,
@@ -289,15 +342,24 @@ def forward(q, k, v, beta, g=None, h0=None, cu_seqlens=None, chunk=64, scale=1.0
 
 
 def backward(q, k, v, beta, g, h0, dO, dhT, cu_seqlens=None, chunk=64, scale=1.0,
-             qk_l2norm=True, eps=1e-6, ws=None, longhorn=False, check_status=True):
-    """Allocate the gradients and run gdn_chunk_bwd.  Returns a dict.  check_status
-    as in forward."""
+             qk_l2norm=True, eps=1e-6, ws=None, longhorn=False, check_status=True, saved=None):
+    """Allocate the gradients and run gdn_chunk_bwd (or, with the buffer of
+    forward(save=True), gdn_chunk_bwd_saved).  Returns a dict.  check_status as in
+    forward."""
     shape = make_shape(q, v, chunk, cu_seqlens, scale, qk_l2norm, eps, longhorn)
     out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                dbeta=torch.empty_like(beta),
                dg=torch.empty_like(g) if g is not None else None,
                dh0=torch.empty((_nseq(q, cu_seqlens), q.shape[1], q.shape[-1], v.shape[-1]),
                                dtype=torch.float32, device=q.device))
+    if saved is not None:
+        if ws is None:
+            ws = alloc_workspace(shape, 2, q.device)
+        gdn_chunk_bwd_saved(shape, q, k, v, beta, g, dO, dhT, saved, out["dq"], out["dk"], out["dv"],
+                            out["dbeta"], out["dg"], out["dh0"], ws)
+        if check_status:
+            _check(dn_device_status(ws), "gdn_chunk_bwd_saved (device status)")
+        return out
     if ws is None:
         ws = alloc_workspace(shape, True, q.device)
     gdn_chunk_bwd(shape, q, k, v, beta, g, h0, dO, dhT, out["dq"], out["dk"], out["dv"],

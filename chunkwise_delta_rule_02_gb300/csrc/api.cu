@@ -92,8 +92,15 @@ Layout make_layout(const Geo &g, const dn_shape *s, int for_backward, Fwd kind)
     auto take = [&](size_t nfloat) { size_t o = off; off += align256(nfloat * sizeof(float)); return o; };
     if (for_backward && gen::bwd_uses_coop(g, s->dtype)) {
         // the cooperative forward's ring, every chunk's package, and the bf16 states,
-        // Unew, dS_out, dUnew of the tcgen05 per-chunk backward
+        // Unew, dS_out, dUnew of the tcgen05 per-chunk backward (for_backward = 2: the
+        // caller's saved buffer holds the packages, states and Unew)
         auto takeb = [&](size_t bytes) { size_t o = off; off += align256(bytes); return o; };
+        if (for_backward == 2) {
+            L.dSo_b = takeb(slots * dk * dv * 2);
+            L.dUn_b = takeb(slots * C * dv * 2);
+            L.total = off;
+            return L;
+        }
         L.coop_bytes = coop::workspace_bytes(g, device_sms());
         L.coop = takeb(L.coop_bytes);
         L.keep = takeb(slots * coop::package_layout(g).stride);
@@ -136,6 +143,10 @@ gen::Ws general_ws(const Layout &L, char *base)
     w.gam = F(L.gam); w.eb = F(L.eb); w.Sin = F(L.Sin); w.dSo = F(L.dSo); w.dUn = F(L.dUn);
     w.dQ = F(L.dQ); w.dK = F(L.dK); w.dW = F(L.dW);
     w.P = F(L.P); w.aux = F(L.aux); w.M3 = F(L.M3);
+    if (L.dSo_b) {
+        auto B = [&](size_t o) { return (__nv_bfloat16 *)(base + o); };
+        w.dSo_b = B(L.dSo_b); w.dUn_b = B(L.dUn_b);
+    }
     if (L.keep) {
         auto B = [&](size_t o) { return (__nv_bfloat16 *)(base + o); };
         w.keep = (uint8_t *)(base + L.keep);
@@ -144,6 +155,26 @@ gen::Ws general_ws(const Layout &L, char *base)
         w.Sin_b = B(L.Sin_b); w.dSo_b = B(L.dSo_b); w.Un_b = B(L.Un_b); w.dUn_b = B(L.dUn_b);
     }
     return w;
+}
+
+// The saved buffer of gdn_chunk_fwd_save / gdn_chunk_bwd_saved: every chunk's
+// package, then S_in and Unew in bf16 (offsets into the buffer; total 0 when the
+// shape has no such path).
+struct Saved {
+    size_t keep, sin, unew, total;
+};
+
+Saved saved_layout(const Geo &g, int dtype)
+{
+    Saved r{0, 0, 0, 0};
+    if (!gen::bwd_uses_coop(g, dtype)) return r;
+    const size_t slots = (size_t)g.NC * g.H;
+    size_t off = 0;
+    r.keep = off; off += align256(slots * coop::package_layout(g).stride);
+    r.sin = off; off += align256(slots * g.dk * g.dv * 2);
+    r.unew = off; off += align256(slots * g.C * g.dv * 2);
+    r.total = off;
+    return r;
 }
 
 // First chunk slot of every packed sequence; flags malformed offsets (which are
@@ -216,7 +247,7 @@ dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size
 dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *v,
                    const void *beta, const float *gate, const float *h0, void *o, float *hT,
                    void *ws, size_t ws_bytes, void *stream, bool allow_coop = true,
-                   bool honour_env = true)
+                   bool honour_env = true, const coop::Emit *emit = nullptr)
 {
     Geo g;
     dn_status rc = check_shape(s, &g);
@@ -229,6 +260,7 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
     Fwd kind;
+    if (emit && fwd_kind(s, g, 0, allow_coop, honour_env) != Fwd::Coop) return DN_ERR_UNSUPPORTED;
     if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, kind, allow_coop, honour_env)) != DN_OK) return rc;
     char *base = (char *)ws;
     cudaError_t e;
@@ -236,7 +268,7 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
         e = coop::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                       (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
                       (__nv_bfloat16 *)o, hT, base + L.fast, ws_bytes - L.fast,
-                      (uint32_t *)(base + L.status), st);
+                      (uint32_t *)(base + L.status), st, emit);
     } else if (kind == Fwd::PerItem) {
         e = fast::fwd(g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
                       (const __nv_bfloat16 *)v, (const __nv_bfloat16 *)beta, gate, h0,
@@ -280,6 +312,7 @@ size_t dn_workspace_size(const dn_shape *shape, int for_backward)
 {
     Geo g;
     if (check_shape(shape, &g) != DN_OK) return 0;
+    if (for_backward == 2 && !gen::bwd_uses_coop(g, shape->dtype)) return 0;
     return make_layout(g, shape, for_backward, fwd_kind(shape, g, for_backward, true)).total;
 }
 
@@ -296,7 +329,12 @@ int dn_plan(const dn_shape *shape, int for_backward, int *kernels)
     if (check_shape(shape, &g) != DN_OK) return -1;
     const int offsets = g.varlen ? 1 : 0;   // k_cstart
     int path, n;
-    if (for_backward) {
+    if (for_backward == 2) {
+        // gdn_chunk_bwd_saved: k_bscan_pk, k_bwd_tc (+ k_cstart)
+        if (!gen::bwd_uses_coop(g, shape->dtype)) return -1;
+        path = DN_PATH_GENERAL;
+        n = 2 + offsets;
+    } else if (for_backward) {
         path = DN_PATH_GENERAL;
         // k_coop_fwd (+ k_plan), k_bscan_pk, k_bwd_tc; or k_prep, k_scan, k_bscan, then
         // k_bwd_tc (tcgen05) or k_bbig, k_bchunk, k_bgrad (the entry point requires the
@@ -334,10 +372,16 @@ dn_status gdn_chunk_fwd(const dn_shape *shape, const void *q, const void *k, con
     return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, ws_bytes, stream);
 }
 
-dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, const void *v,
-                        const void *beta, const float *gate, const float *h0, const void *dO,
-                        const float *dhT, void *dq, void *dk, void *dv, void *dbeta, float *dg,
-                        float *dh0, void *ws, size_t ws_bytes, void *stream)
+}  // extern "C"
+
+namespace gdn {
+namespace {
+// gdn_chunk_bwd (saved == NULL) and gdn_chunk_bwd_saved
+dn_status bwd_impl(const dn_shape *shape, const void *q, const void *k, const void *v,
+                   const void *beta, const float *gate, const float *h0, const void *dO,
+                   const float *dhT, void *dq, void *dk, void *dv, void *dbeta, float *dg,
+                   float *dh0, void *ws, size_t ws_bytes, void *stream, void *saved,
+                   size_t saved_bytes)
 {
     Geo g;
     dn_status rc = check_shape(shape, &g);
@@ -345,14 +389,27 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
     if (dg && !gate) return DN_ERR_INVALID_ARG;
     if (g.T > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
         return DN_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, beta, gate, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0};
+    const void *ptrs[] = {q, k, v, beta, gate, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, saved};
     for (const void *p : ptrs)
         if (p && !is_aligned16(p)) return DN_ERR_INVALID_ARG;
+    Saved sv{0, 0, 0, 0};
+    if (saved) {
+        sv = saved_layout(g, shape->dtype);
+        if (sv.total == 0) return DN_ERR_UNSUPPORTED;
+        if (saved_bytes < sv.total) return DN_ERR_INVALID_ARG;
+    }
     cudaStream_t st = (cudaStream_t)stream;
     Layout L;
     Fwd kind;
-    if ((rc = begin_call(shape, g, 1, ws, ws_bytes, st, L, kind, false)) != DN_OK) return rc;
+    if ((rc = begin_call(shape, g, saved ? 2 : 1, ws, ws_bytes, st, L, kind, false)) != DN_OK) return rc;
     gen::Ws w = general_ws(L, (char *)ws);
+    if (saved) {
+        char *sb = (char *)saved;
+        w.keep = (uint8_t *)(sb + sv.keep);
+        w.Sin_b = (__nv_bfloat16 *)(sb + sv.sin);
+        w.Un_b = (__nv_bfloat16 *)(sb + sv.unew);
+        w.saved = true;
+    }
     cudaError_t e;
     if (shape->dtype == DN_F32)
         e = gen::bwd<float>(g, (const float *)q, (const float *)k, (const float *)v,
@@ -365,6 +422,54 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
             (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv,
             (__nv_bfloat16 *)dbeta, dg, dh0, w, st);
     return e == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, const void *v,
+                        const void *beta, const float *gate, const float *h0, const void *dO,
+                        const float *dhT, void *dq, void *dk, void *dv, void *dbeta, float *dg,
+                        float *dh0, void *ws, size_t ws_bytes, void *stream)
+{
+    return bwd_impl(shape, q, k, v, beta, gate, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, ws_bytes,
+                    stream, nullptr, 0);
+}
+
+size_t dn_saved_size(const dn_shape *shape)
+{
+    Geo g;
+    if (check_shape(shape, &g) != DN_OK) return 0;
+    if (fwd_kind(shape, g, 0, true) != Fwd::Coop) return 0;
+    return saved_layout(g, shape->dtype).total;
+}
+
+dn_status gdn_chunk_fwd_save(const dn_shape *shape, const void *q, const void *k, const void *v,
+                             const void *beta, const float *g, const float *h0, void *o, float *hT,
+                             void *saved, size_t saved_bytes, void *ws, size_t ws_bytes, void *stream)
+{
+    Geo geo;
+    dn_status rc = check_shape(shape, &geo);
+    if (rc != DN_OK) return rc;
+    const Saved sv = saved_layout(geo, shape->dtype);
+    if (sv.total == 0 || fwd_kind(shape, geo, 0, true) != Fwd::Coop) return DN_ERR_UNSUPPORTED;
+    if (!saved || !is_aligned16(saved) || saved_bytes < sv.total) return DN_ERR_INVALID_ARG;
+    char *sb = (char *)saved;
+    const coop::Emit em{(uint8_t *)(sb + sv.keep), (__nv_bfloat16 *)(sb + sv.sin),
+                        (__nv_bfloat16 *)(sb + sv.unew)};
+    return fwd_impl(shape, q, k, v, beta, g, h0, o, hT, ws, ws_bytes, stream, true, true, &em);
+}
+
+dn_status gdn_chunk_bwd_saved(const dn_shape *shape, const void *q, const void *k, const void *v,
+                              const void *beta, const float *gate, const void *dO, const float *dhT,
+                              const void *saved, size_t saved_bytes, void *dq, void *dk, void *dv,
+                              void *dbeta, float *dg, float *dh0, void *ws, size_t ws_bytes,
+                              void *stream)
+{
+    if (!saved) return DN_ERR_INVALID_ARG;
+    return bwd_impl(shape, q, k, v, beta, gate, nullptr, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, ws_bytes,
+                    stream, const_cast<void *>(saved), saved_bytes);
 }
 
 dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, const void *v,

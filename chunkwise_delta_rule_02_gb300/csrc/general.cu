@@ -2613,8 +2613,8 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
             // the cooperative forward writes every chunk's package, S_in and Unew; the
             // reverse scan reads the packages; then the tcgen05 per-chunk gradients
             const coop::Emit em{w.keep, w.Sin_b, w.Un_b};
-            if ((e = coop::fwd(g, q, k, v, beta, gate, h0, nullptr, nullptr, w.coop_ws, w.coop_bytes, g.status,
-                               st, &em)) != cudaSuccess)
+            if (!w.saved && (e = coop::fwd(g, q, k, v, beta, gate, h0, nullptr, nullptr, w.coop_ws,
+                                           w.coop_bytes, g.status, st, &em)) != cudaSuccess)
                 return e;
             if ((e = set_smem(k_bscan_pk, smem_bscan_st(g))) != cudaSuccess) return e;
             if (g.N > 0)

@@ -29,6 +29,9 @@ struct Ws {
     uint8_t *keep;
     void *coop_ws;
     size_t coop_bytes;
+    // keep, Sin_b and Un_b hold a cooperative forward's output already (the caller's
+    // saved buffer): the backward starts at the reverse scan
+    bool saved;
 };
 
 template <class Tin>

@@ -97,7 +97,8 @@ typedef struct {
 typedef enum { DN_BETA_DELTA = 0, DN_BETA_LONGHORN = 1 } dn_beta_mode;
 
 /* Bytes of device workspace the calls below need for `shape` (0 on bad
- * arguments).  for_backward = 1 sizes it for gdn_chunk_bwd. */
+ * arguments).  for_backward = 1 sizes it for gdn_chunk_bwd, 2 for
+ * gdn_chunk_bwd_saved (0 where the shape has no saved path). */
 size_t dn_workspace_size(const dn_shape *shape, int for_backward);
 
 /* DeltaNet forward (alpha = 1; Table 1 row "DeltaNet").
@@ -143,6 +144,28 @@ dn_status gdn_chunk_bwd(const dn_shape *shape, const void *q, const void *k, con
                         const void *beta, const float *g, const float *h0, const void *dO,
                         const float *dhT, void *dq, void *dk, void *dv, void *dbeta,
                         float *dg, float *dh0, void *ws, size_t ws_bytes, void *stream);
+
+/* Training step without the backward's recompute (bf16, dk = dv = 128, chunk 64,
+ * a device that runs the cooperative forward; DN_ERR_UNSUPPORTED otherwise, and
+ * dn_saved_size returns 0).  gdn_chunk_fwd_save is gdn_chunk_fwd that also fills
+ * `saved` (device, 16-byte aligned, >= dn_saved_size(shape) bytes: about 97 KB per
+ * chunk of 64 tokens and head) with every chunk's prepared operands, the state
+ * entering it and Unew, in bf16.  gdn_chunk_bwd_saved is gdn_chunk_bwd starting
+ * from that buffer: no recompute, h0 not needed (it is inside the saved states);
+ * the other arguments must be those of the forward call that filled it (the
+ * library does not check).  Workspaces: dn_workspace_size(shape, 0) and
+ * dn_workspace_size(shape, 2).  This keeps what the pages recompute (DeltaNet
+ * page, reply Q2): it trades the saved buffer's memory for one forward pass. */
+size_t dn_saved_size(const dn_shape *shape);
+dn_status gdn_chunk_fwd_save(const dn_shape *shape, const void *q, const void *k, const void *v,
+                             const void *beta, const float *g, const float *h0, void *o, float *hT,
+                             void *saved, size_t saved_bytes, void *ws, size_t ws_bytes,
+                             void *stream);
+dn_status gdn_chunk_bwd_saved(const dn_shape *shape, const void *q, const void *k, const void *v,
+                              const void *beta, const float *g, const void *dO, const float *dhT,
+                              const void *saved, size_t saved_bytes, void *dq, void *dk, void *dv,
+                              void *dbeta, float *dg, float *dh0, void *ws, size_t ws_bytes,
+                              void *stream);
 
 /* Recurrent decode step (one new token per sequence; the recurrence itself, as
  * in Table 1 of the Gated DeltaNet page, row "Gated DeltaNet", and the
@@ -251,7 +274,8 @@ int dn_uses_fast_path(const dn_shape *shape, int for_backward);
  * (the cooperative persistent tcgen05 kernel), or -1 for an invalid shape.  If
  * `kernels` is not null it receives the number of the library's own kernels the
  * call launches (memsets of the workspace are not counted).  for_backward as
- * above; the gdn_chunk_fwd_noalloc entry point never takes DN_PATH_COOP. */
+ * above (2: gdn_chunk_bwd_saved, -1 where it is not available); the
+ * gdn_chunk_fwd_noalloc entry point never takes DN_PATH_COOP. */
 enum { DN_PATH_GENERAL = 0, DN_PATH_FUSED = 1, DN_PATH_COOP = 2 };
 int dn_plan(const dn_shape *shape, int for_backward, int *kernels);
 

@@ -151,3 +151,54 @@ def test_timeout_in_the_recompute_is_reported():
     ref = oracle_bwd(x)
     for n in GRADS:
         assert rel(got[n], ref[n]) <= TOL["bf16"], n
+
+
+# ----------------------------------------------------------------------------- the saved path
+def _saved_case(x):
+    import chunkwise_delta_rule_02_gb300 as gdn
+    d = to_dev(x, DEV)
+    if not gdn.saved_supported(d["q"], d["v"], cu_seqlens=d["cu_seqlens"]):
+        pytest.skip("no saved path on this device")
+    return d
+
+
+@pytest.mark.parametrize("lengths", [None, [5, 64, 0, 130, 1, 63, 300]])
+def test_saved_path_equals_the_recompute(lengths):
+    """gdn_chunk_fwd_save writes what the backward's recompute writes (the same kernel on
+    the same inputs), so its o, h_T and the gradients of gdn_chunk_bwd_saved equal
+    gdn_chunk_fwd's and gdn_chunk_bwd's bit for bit (dg up to the order of its atomic
+    row sums); and they match the oracle."""
+    import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding
+    x = _gen(2, 3, 333, seed=34) if lengths is None else _gen(1, 3, 0, seed=35, lengths=lengths)
+    d = _saved_case(x)
+    kw = dict(cu_seqlens=d["cu_seqlens"])
+    o1, h1, saved = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], save=True, **kw)
+    o2, h2 = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], **kw)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    a = gdn.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], None, d["do"], d["dhT"], saved=saved, **kw)
+    b = gdn.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["do"], d["dhT"], **kw)
+    torch.cuda.synchronize()
+    for n in GRADS:
+        if n == "dg":
+            assert (a[n] - b[n]).abs().max() <= 1e-6 * b[n].abs().max()
+        else:
+            assert torch.equal(a[n], b[n]), n
+    ref = oracle_bwd(x)
+    for n in GRADS:
+        assert rel(a[n].float().cpu().numpy(), ref[n]) <= TOL["bf16"], n
+    shape = gdn.make_shape(d["q"], d["v"], 64, d["cu_seqlens"])
+    assert binding.dn_plan(shape, 2) == (binding.DN_PATH_GENERAL, 2 + (1 if lengths else 0))
+    assert binding.dn_workspace_size(shape, 2) < binding.dn_workspace_size(shape, 1)
+
+
+def test_saved_path_refuses_other_shapes():
+    """d 64: no saved path (dn_saved_size 0, DN_ERR_UNSUPPORTED)."""
+    import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding, workloads
+    w = workloads.Workload("ns", 1, 2, 64, 64, "bf16", True, True, 1, backward=True)
+    d = to_dev(workloads.generate(w), DEV)
+    assert not gdn.saved_supported(d["q"], d["v"])
+    with pytest.raises(gdn.GdnError) as err:
+        gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], save=True)
+    assert err.value.status == binding.DN_ERR_UNSUPPORTED
