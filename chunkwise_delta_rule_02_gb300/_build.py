@@ -12,7 +12,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn_gb300.so")
 ROOT = os.path.dirname(PKG)
 
-SOURCES = ["api.cu", "general.cu", "fast.cu", "coop.cu", "decode.cu", "affine.cu", "bwd_tc.cu"]
+SOURCES = ["api.cu", "general.cu", "fast.cu", "coop.cu", "decode.cu", "affine.cu", "bwd_tc.cu",
+           "bscan_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-extended-lambda", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "-I" + os.path.join(ROOT, "include")]

@@ -746,13 +746,16 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int bb = 16 * cg + e;
-                const float dA = (bb < a && a < len) ? -x[e] : 0.f;
+                const bool lower = bb < a && a < len;
+                const float dA = lower ? -x[e] : 0.f;
                 const float f = dA * kdI[e];
                 const float ev = fmaf(ba, f, gI[e]);
                 db += f;
                 rs += ev;
                 gI[e] = ev;
-                kdI[e] = dA * ba * Dri(a, bb);
+                // masked, not multiplied by zero: above the diagonal exp(gamma_a - gamma_b)
+                // overflows once the gates leave the factored range
+                kdI[e] = lower ? dA * ba * Dri(a, bb) : 0.f;
             }
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {

@@ -42,6 +42,7 @@
 
 #include <stdlib.h>
 
+#include "bscan_tc.h"
 #include "bwd_tc.h"
 #include "fast.h"
 #include "prep_math.cuh"
@@ -2590,6 +2591,14 @@ bool bwd_uses_tc(const Geo &g, int dtype, const void *q, const void *k, const vo
            ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)dO) & 15u) == 0);
 }
 
+// GDN_BSCAN_STAGED=1 keeps the warp-level reverse scan over the packages (k_bscan_pk)
+// where the tcgen05 one would run (used by the tests to compare the two).
+static bool staged_bscan()
+{
+    const char *e = getenv("GDN_BSCAN_STAGED");
+    return e && e[0] && e[0] != '0';
+}
+
 bool bwd_uses_coop(const Geo &g, int dtype)
 {
     for (const char *name : {"GDN_BWD_RECOMPUTE", "GDN_FORCE_GENERAL"}) {
@@ -2616,11 +2625,18 @@ cudaError_t bwd(const Geo &g, const Tin *q, const Tin *k, const Tin *v, const Ti
             if (!w.saved && (e = coop::fwd(g, q, k, v, beta, gate, h0, nullptr, nullptr, w.coop_ws,
                                            w.coop_bytes, g.status, st, &em)) != cudaSuccess)
                 return e;
-            if ((e = set_smem(k_bscan_pk, smem_bscan_st(g))) != cudaSuccess) return e;
-            if (g.N > 0)
-                k_bscan_pk<<<dim3(g.N, g.H), 512, smem_bscan_st(g), st>>>(g, k, dO, dhT, dh0, w.keep,
-                                                                          coop::package_layout(g), w);
-            if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+            if (bsc::supports(g, DN_BF16) && !staged_bscan()) {
+                // the reverse scan on tcgen05, dS resident in TMEM
+                if ((e = bsc::scan(g, k, dO, dhT, dh0, w.keep, coop::package_layout(g), w.dSo_b, w.dUn_b,
+                                   st)) != cudaSuccess)
+                    return e;
+            } else {
+                if ((e = set_smem(k_bscan_pk, smem_bscan_st(g))) != cudaSuccess) return e;
+                if (g.N > 0)
+                    k_bscan_pk<<<dim3(g.N, g.H), 512, smem_bscan_st(g), st>>>(g, k, dO, dhT, dh0, w.keep,
+                                                                              coop::package_layout(g), w);
+                if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+            }
             return btc::grads(g, q, k, v, beta, gate, dO, w.Sin_b, w.dSo_b, w.Un_b, w.dUn_b, dq, dk, dv,
                               dbeta, dg, st);
         }

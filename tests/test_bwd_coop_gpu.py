@@ -202,3 +202,32 @@ def test_saved_path_refuses_other_shapes():
     with pytest.raises(gdn.GdnError) as err:
         gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], save=True)
     assert err.value.status == binding.DN_ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------- the tcgen05 reverse scan
+def test_tc_reverse_scan_matches_the_warp_level_scan():
+    """k_bscan_tc (dS in TMEM) against k_bscan_pk (GDN_BSCAN_STAGED=1) on the same
+    packages, with more (sequence, head) items than SMs (a CTA takes several, each
+    from its last chunk to its first), and against the oracle on sampled items."""
+    x = _gen(8, 20, 300, seed=36)
+    a = _bwd(x)
+    b = _bwd(x, {"GDN_BSCAN_STAGED": "1"})
+    for n in GRADS:
+        assert rel(a[n], b[n]) <= 1e-2, (n, rel(a[n], b[n]))
+    sel = [(0, 0), (5, 13), (7, 19)]
+    for (bi, h), r in zip(sel, oracle_bwd(x, sel=sel)):
+        for n in GRADS:
+            assert rel(a[n][bi:bi + 1, h:h + 1], r[n]) <= TOL["bf16"], (n, bi, h)
+
+
+def test_tc_reverse_scan_strong_decay():
+    """Chunk decays near exp(-130): the reverse scan's pending scale renormalises the
+    TMEM state within a sequence."""
+    x = _gen(1, 2, 700, seed=37)
+    x["g"] = x["g"] * 40.0
+    x["beta"] = torch.ones_like(x["beta"])
+    got = _bwd(x)
+    ref = oracle_bwd(x)
+    for n in GRADS:
+        assert np.isfinite(got[n]).all(), n
+        assert rel(got[n], ref[n]) <= TOL["bf16"], (n, rel(got[n], ref[n]))
