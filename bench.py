@@ -773,6 +773,37 @@ def main():
         d2h = ho.numel() * ho.element_size() + hhT.numel() * hhT.element_size()
         e2e = {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
+    elif saved is not None:
+        # the training step end to end: its inputs (q, k, v, beta, g, h0, dO, dhT) from
+        # pinned host buffers, the forward and backward through the public calls, o, h_T
+        # and every gradient back to pinned host buffers, inside the timed region
+        names_in = ("q", "k", "v", "beta", "g", "h0", "do", "dhT")
+        hx = {k: x[k].pin_memory() for k in names_in}
+        outs_d = [o, hT] + [grads[k] for k in ("dq", "dk", "dv", "dbeta", "dg", "dh0")]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs_d]
+
+        def e2e_step():
+            for k in names_in:
+                d[k].copy_(hx[k], non_blocking=True)
+            step()
+            for hd, dd in zip(outs_h, outs_d):
+                hd.copy_(dd, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        t1.record(stream)
+        barrier()
+        ms_e2e = t0.elapsed_time(t1) / n_e2e
+        h2d = sum(hx[k].numel() * hx[k].element_size() for k in names_in)
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        e2e = {"value": tokens * world / (ms_e2e / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e}
 
     if rank != 0:
         if pg is not None:
