@@ -257,6 +257,10 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // base descriptors (the shared-memory base with each stride pair); an operand's descriptor
+    // is its base plus the operand's byte offset (>> 4), a constant at every MMA below
+    const uint64_t dKM = sdesc(sb, 16, 1024), dM16 = sdesc(sb, 16384, 1024), dM8 = sdesc(sb, 8192, 1024),
+                   dMU = sdesc(sb, UOD_HALF, 1024);
 
     // a bounded wait; a timeout is recorded and ends the CTA's work at the next task boundary
     auto wait = [&](int b, uint32_t phase) -> bool {
@@ -448,16 +452,17 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             // ---------------------------------------------------------- first products
             mma_issued = true;
             tc_fence_after();
+#pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t hk = (k & 3) * 32;
                 const uint32_t h16 = (k >> 2) * 16384, h24 = (k >> 2) * UOD_HALF;
-                const uint64_t dKQ = sdesc(sb + SM_KQ + h16 + hk, 16, 1024);
+                const uint64_t dKQ = dadd(dKM, SM_KQ + h16 + hk);
                 mma_bf16_ss(tmem + TM_A, dKQ, dKQ, ID_128_128, k > 0);                       // [K;Q][K;Q]^T
-                const uint64_t dOdU = sdesc(sb + SM_UOD + h24 + 8192 + hk, 16, 1024);
-                mma_bf16_ss(tmem + TM_YZ, dOdU, sdesc(sb + SM_S + h16 + hk, 16, 1024), ID_128_128, k > 0);   // [dO;dU] S^T
-                const uint64_t dUdO = sdesc(sb + SM_UOD + h24 + hk, 16, 1024);
-                mma_bf16_ss(tmem + TM_X, dUdO, sdesc(sb + SM_DS + h16 + hk, 16, 1024), ID_128_128, k > 0);   // [U;dO] dS^T
-                mma_bf16_ss(tmem + TM_DP, dOdU, sdesc(sb + SM_UOD + h24 + hk, 16, 1024), ID_128_64, k > 0);  // [dO;dU] U^T
+                const uint64_t dOdU = dadd(dKM, SM_UOD + h24 + 8192 + hk);
+                mma_bf16_ss(tmem + TM_YZ, dOdU, dadd(dKM, SM_S + h16 + hk), ID_128_128, k > 0);   // [dO;dU] S^T
+                const uint64_t dUdO = dadd(dKM, SM_UOD + h24 + hk);
+                mma_bf16_ss(tmem + TM_X, dUdO, dadd(dKM, SM_DS + h16 + hk), ID_128_128, k > 0);   // [U;dO] dS^T
+                mma_bf16_ss(tmem + TM_DP, dOdU, dadd(dKM, SM_UOD + h24 + hk), ID_128_64, k > 0);  // [dO;dU] U^T
             }
             mma_commit(&bar[B_M1]);
         }
@@ -578,12 +583,13 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         if (tid == 0) {
             // ---------------------------------------------------------- dT parts: Z K^T | dUnew V^T
             tc_fence_after();
+#pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t hk = (k & 3) * 32, h24 = (k >> 2) * UOD_HALF;
-                mma_bf16_ss(tmem + TM_A, sdesc(sb + T_Z + h24 + hk, 16, 1024),
-                            sdesc(sb + SM_KQ + (k >> 2) * 16384 + hk, 16, 1024), ID_128_64, k > 0);
-                mma_bf16_ss(tmem + TM_A + 64, sdesc(sb + SM_UOD + h24 + 16384 + hk, 16, 1024),
-                            sdesc(sb + SM_V + (k >> 2) * 8192 + hk, 16, 1024), ID_128_64, k > 0);
+                mma_bf16_ss(tmem + TM_A, dadd(dKM, T_Z + h24 + hk),
+                            dadd(dKM, SM_KQ + (k >> 2) * 16384 + hk), ID_128_64, k > 0);
+                mma_bf16_ss(tmem + TM_A + 64, dadd(dKM, SM_UOD + h24 + 16384 + hk),
+                            dadd(dKM, SM_V + (k >> 2) * 8192 + hk), ID_128_64, k > 0);
             }
             mma_commit(&bar[B_M4]);
         }
@@ -661,13 +667,15 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             // ---------------------------------------------------------- dQ2 = (dP o D) diag(n) K,
             // X2 = Linv^T (dT diag b)
             tc_fence_after();
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + TM_A, sdesc(sb + T_DP + k * 32, 16, 1024),
-                            dadd(sdesc(sb + SM_KQ, 16384, 1024), k * 2048), ID_128_128_BMN, k > 0);
+                mma_bf16_ss(tmem + TM_A, dadd(dKM, T_DP + k * 32),
+                            dadd(dM16, SM_KQ + k * 2048), ID_128_128_BMN, k > 0);
             mma_commit(&bar[B_M5]);
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + TM_ADJ, dadd(sdesc(sb + T_LI, 8192, 1024), k * 2048),
-                            dadd(sdesc(sb + T_ADJ, 8192, 1024), k * 2048), ID_128_64_ABMN, k > 0);
+                mma_bf16_ss(tmem + TM_ADJ, dadd(dM8, T_LI + k * 2048),
+                            dadd(dM8, T_ADJ + k * 2048), ID_128_64_ABMN, k > 0);
             mma_commit(&bar[B_X2]);
         }
         BTR(it, 6);
@@ -692,9 +700,10 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         named_bar(3, NCOMPUTE);
         if (tid == 0) {
             tc_fence_after();
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + TM_ADJ + 64, sdesc(sb + T_ADJ + k * 32, 16, 1024),
-                            sdesc(sb + T_LI + k * 32, 16, 1024), ID_128_64, k > 0);
+                mma_bf16_ss(tmem + TM_ADJ + 64, dadd(dKM, T_ADJ + k * 32),
+                            dadd(dKM, T_LI + k * 32), ID_128_64, k > 0);
             mma_commit(&bar[B_DA]);
         }
         BTR(it, 7);
@@ -799,15 +808,19 @@ k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         if (tid == 0) {
             // ---------------------------------------------------------- dK, T^T dW, T^T dUnew
             tc_fence_after();
-            const uint64_t dK = sdesc(sb + SM_KQ, 16384, 1024), dQ = sdesc(sb + SM_KQ + 8192, 16384, 1024);
-            const uint64_t dP2 = sdesc(sb + T_DP2, 8192, 1024), dLI = sdesc(sb + T_LI, 8192, 1024);
-            const uint64_t dZ = sdesc(sb + T_Z, UOD_HALF, 1024), dU = sdesc(sb + SM_UOD + 16384, UOD_HALF, 1024);
+            const uint64_t dK = dadd(dM16, SM_KQ), dQ = dadd(dM16, SM_KQ + 8192);
+            const uint64_t dP2 = dadd(dM8, T_DP2), dLI = dadd(dM8, T_LI);
+            const uint64_t dZ = dadd(dMU, T_Z), dU = dadd(dMU, SM_UOD + 16384);
+#pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16_ss(tmem + TM_A, dadd(dP2, k * 2048), dadd(dQ, k * 2048), ID_128_128_ABMN, k > 0);
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + TM_A, sdesc(sb + T_ADJ + k * 32, 16, 1024), dadd(dK, k * 2048), ID_128_128_BMN, 1);
+                mma_bf16_ss(tmem + TM_A, dadd(dKM, T_ADJ + k * 32), dadd(dK, k * 2048), ID_128_128_BMN, 1);
+#pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16_ss(tmem + TM_YZ, dadd(dLI, k * 2048), dadd(dZ, k * 2048), ID_128_128_ABMN, k > 0);
+#pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_bf16_ss(tmem + TM_DP, dadd(dLI, k * 2048), dadd(dU, k * 2048), ID_128_128_ABMN, k > 0);
             mma_commit(&bar[B_M6]);
