@@ -545,12 +545,16 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                         w[e] = pack_bf16(Gn * __uint_as_float(r[c8 * 8 + 2 * e]), Gn * __uint_as_float(r[c8 * 8 + 2 * e + 1]));
                     *(uint4 *)(sbp + sw128(dvl, c8 * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
                     if (L::EMIT && sin) {
-                        // S_in[dk][dv] for this thread's d_v column (a warp writes 64 contiguous bytes)
+                        // S_in[dk][dv]: w[e] holds rows k0 + 2e, k0 + 2e + 1 of this thread's d_v
+                        // column; with the neighbouring lane's word, the even lane stores row
+                        // k0 + 2e and the odd lane row k0 + 2e + 1, two d_v columns each
                         const int k0 = 64 * panel + c8 * 8;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            sin[(size_t)(k0 + 2 * e) * DV] = (uint16_t)(w[e] & 0xFFFFu);
-                            sin[(size_t)(k0 + 2 * e + 1) * DV] = (uint16_t)(w[e] >> 16);
+                            const uint32_t nb = __shfl_xor_sync(0xffffffffu, w[e], 1);
+                            const bool odd = lane & 1;
+                            const uint32_t pr = odd ? __byte_perm(nb, w[e], 0x7632u) : __byte_perm(w[e], nb, 0x5410u);
+                            *reinterpret_cast<uint32_t *>(sin + (size_t)(k0 + 2 * e + (odd ? 1 : 0)) * DV - (odd ? 1 : 0)) = pr;
                         }
                     }
                 }
@@ -595,13 +599,18 @@ __device__ __forceinline__ void chain_cta(const Params &p, const CUtensorMap *tm
                     *(uint4 *)(u2 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                 }
                 if (L::EMIT && p.unew_out) {
-                    // Unew[token][dv] (rows past the chunk's end are zeros here already)
+                    // Unew[token][dv] (rows past the chunk's end are zeros here already): token
+                    // pairs of this thread's d_v column, exchanged with the neighbouring lane so
+                    // that each lane stores one token row of two d_v columns
                     uint16_t *un = reinterpret_cast<uint16_t *>(p.unew_out) +
                                    (slot_of(p, st.cur.seq, st.cur.h, st.n) * C + CH * half) * DV + dvg;
+                    const bool odd = lane & 1;
 #pragma unroll
-                    for (int i = 0; i < CH; ++i) {
-                        const uint32_t wb = pack_bf16(__uint_as_float(x[i]), 0.f);
-                        un[(size_t)i * DV] = (uint16_t)(wb & 0xFFFFu);
+                    for (int i = 0; i < CH; i += 2) {
+                        const uint32_t wv = pack_bf16(__uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+                        const uint32_t nb = __shfl_xor_sync(0xffffffffu, wv, 1);
+                        const uint32_t pr = odd ? __byte_perm(nb, wv, 0x7632u) : __byte_perm(wv, nb, 0x5410u);
+                        *reinterpret_cast<uint32_t *>(un + (size_t)(i + (odd ? 1 : 0)) * DV - (odd ? 1 : 0)) = pr;
                     }
                 }
             }
