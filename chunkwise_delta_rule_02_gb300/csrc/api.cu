@@ -226,7 +226,8 @@ Fwd fwd_kind(const dn_shape *s, const Geo &g, int for_backward, bool allow_coop,
 }
 
 dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size_t ws_bytes,
-                     cudaStream_t st, Layout &L, Fwd &kind, bool allow_coop, bool honour_env = true)
+                     cudaStream_t st, Layout &L, Fwd &kind, bool allow_coop, bool honour_env = true,
+                     bool clear_status = true)
 {
     kind = fwd_kind(s, g, for_backward, allow_coop, honour_env);
     L = make_layout(g, s, for_backward, kind);
@@ -234,7 +235,8 @@ dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size
     if (ws_bytes < L.total) return DN_ERR_WORKSPACE;
     char *base = (char *)ws;
     g.status = (uint32_t *)(base + L.status);
-    if (cudaMemsetAsync(base + L.status, 0, sizeof(uint32_t), st) != cudaSuccess) return DN_ERR_CUDA;
+    if (clear_status && cudaMemsetAsync(base + L.status, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return DN_ERR_CUDA;
     if (g.varlen) {
         g.cstart = (const int32_t *)(base + L.cstart);
         k_cstart<<<1, 32, 0, st>>>(g.cu, g.N, g.T, g.C, (int32_t *)(base + L.cstart),
@@ -247,7 +249,7 @@ dn_status begin_call(const dn_shape *s, Geo &g, int for_backward, void *ws, size
 dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *v,
                    const void *beta, const float *gate, const float *h0, void *o, float *hT,
                    void *ws, size_t ws_bytes, void *stream, bool allow_coop = true,
-                   bool honour_env = true, const coop::Emit *emit = nullptr)
+                   bool honour_env = true, const coop::Emit *emit = nullptr, bool clear_status = true)
 {
     Geo g;
     dn_status rc = check_shape(s, &g);
@@ -261,7 +263,8 @@ dn_status fwd_impl(const dn_shape *s, const void *q, const void *k, const void *
     Layout L;
     Fwd kind;
     if (emit && fwd_kind(s, g, 0, allow_coop, honour_env) != Fwd::Coop) return DN_ERR_UNSUPPORTED;
-    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, kind, allow_coop, honour_env)) != DN_OK) return rc;
+    if ((rc = begin_call(s, g, 0, ws, ws_bytes, st, L, kind, allow_coop, honour_env, clear_status)) != DN_OK)
+        return rc;
     char *base = (char *)ws;
     cudaError_t e;
     if (kind == Fwd::Coop) {
@@ -534,8 +537,77 @@ size_t dn_host_arena_size(const dn_shape *s, int gated, int with_h0)
     if (gated) n += align256(tok * sizeof(float));
     if (with_h0) n += align256(st);
     n += align256(st);                            // hT
+    n += 2 * align256(st);                        // the state between time segments (two, in turn)
     return n;
 }
+
+// ---------------------------------------------------------------------------
+// The host entry point's pipeline.  Fixed-length input of at least 32 chunks is cut
+// along time into segments of whole chunks; the copies of segment i + 1 into the
+// arena overlap segment i's forward, and segment i's output goes back to the host
+// while later segments compute.  Each segment is a forward over [B][H][Ts] with the
+// state handed on through the arena, so the host link (the call's bound: about 0.2 TB/s
+// either way, the two directions concurrently) is busy throughout instead of in turns.
+// At most four segments: with eight, the strided copies of the two directions (rows of
+// 256 KB for T = 8192, d = 128) no longer overlapped on a GB300 (measured).
+namespace {
+CUcontext current_context();
+
+constexpr int kMaxSegments = 4;
+constexpr int kMinSegmentChunks = 16;
+constexpr int kMaxPipeDevices = 64;
+
+struct HostPipe {
+    CUcontext ctx;
+    cudaStream_t in, out;                 // copies to the arena, copies back
+    cudaEvent_t fork, join;
+    cudaEvent_t landed[kMaxSegments];     // segment i's inputs are in the arena
+    cudaEvent_t done[kMaxSegments];       // segment i's forward has completed
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxPipeDevices];
+
+// Segments of the time axis for the pipelined host path (1: no pipeline).
+int host_segments(const Geo &g)
+{
+    if (g.varlen || g.T <= 0) return 1;
+    const int nch = (g.T + g.C - 1) / g.C;
+    int n = nch / kMinSegmentChunks;
+    return n < 1 ? 1 : (n > kMaxSegments ? kMaxSegments : n);
+}
+
+// The device's streams and events for the pipeline, made on first use in each context.
+// Called with g_pipe_mu held.
+HostPipe *host_pipe()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxPipeDevices) return nullptr;
+    HostPipe &hp = g_pipe[dev];
+    const CUcontext ctx = current_context();
+    if (hp.in && hp.ctx == ctx) return &hp;
+    HostPipe fresh{};
+    bool ok = cudaStreamCreateWithFlags(&fresh.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&fresh.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&fresh.fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&fresh.join, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxSegments; ++i)
+        ok = cudaEventCreateWithFlags(&fresh.landed[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&fresh.done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;
+    fresh.ctx = ctx;
+    hp = fresh;
+    return &hp;
+}
+
+// [rows][width] bytes out of (or into) rows of `pitch` bytes, as one 2D copy.
+bool copy2d(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t rows,
+            cudaMemcpyKind kind, cudaStream_t st)
+{
+    if (width == 0 || rows == 0) return true;
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, st) == cudaSuccess;
+}
+
+}  // namespace
 
 dn_status gdn_chunk_fwd_host(const dn_shape *s, const void *q, const void *k, const void *v,
                              const void *beta, const float *gate, const float *h0, void *o,
@@ -560,6 +632,59 @@ dn_status gdn_chunk_fwd_host(const dn_shape *s, const void *q, const void *k, co
     char *dgate = gate ? carve(tok * sizeof(float)) : nullptr;
     char *dh0 = h0 ? carve(sbytes) : nullptr;
     char *dhT = carve(sbytes);
+    char *dst2[2] = {carve(sbytes), carve(sbytes)};   // the state between segments, in turn
+    const int nseg = host_segments(g);
+    if (nseg > 1) {
+        // segments of lch whole chunks: inputs of segment i land in its part of the arena
+        // (contiguous [B][H][Ts] rows, one strided copy per tensor), then its forward runs on
+        // `stream` from the state segment i - 1 left, then its output goes back
+        std::lock_guard<std::mutex> lock(g_pipe_mu);
+        HostPipe *hp = host_pipe();
+        if (!hp) return DN_ERR_CUDA;
+        const int nch = (g.T + g.C - 1) / g.C;
+        const int lch = (nch + nseg - 1) / nseg;
+        const size_t tseg = (size_t)lch * g.C;
+        const int S = (int)(((size_t)g.T + tseg - 1) / tseg);
+        const size_t BH = (size_t)g.B * g.H, T = (size_t)g.T;
+        const size_t kb = (size_t)g.dk * es, vb = (size_t)g.dv * es, gb = sizeof(float);
+        const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+        if (cudaEventRecord(hp->fork, st) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->out, hp->fork, 0) != cudaSuccess)
+            return DN_ERR_CUDA;
+        if (dh0 && cudaMemcpyAsync(dh0, h0, sbytes, H2D, hp->in) != cudaSuccess) return DN_ERR_CUDA;
+        for (int i = 0; i < S; ++i) {
+            const size_t t0 = (size_t)i * tseg, ts = T - t0 < tseg ? T - t0 : tseg;
+            const size_t off = BH * t0;   // tokens of the earlier segments in each arena tensor
+            const bool ok =
+                copy2d(dq + off * kb, ts * kb, (const char *)q + t0 * kb, T * kb, ts * kb, BH, H2D, hp->in) &&
+                copy2d(dk + off * kb, ts * kb, (const char *)k + t0 * kb, T * kb, ts * kb, BH, H2D, hp->in) &&
+                copy2d(dvv + off * vb, ts * vb, (const char *)v + t0 * vb, T * vb, ts * vb, BH, H2D, hp->in) &&
+                copy2d(db + off * es, ts * es, (const char *)beta + t0 * es, T * es, ts * es, BH, H2D, hp->in) &&
+                (!dgate ||
+                 copy2d(dgate + off * gb, ts * gb, (const char *)gate + t0 * gb, T * gb, ts * gb, BH, H2D, hp->in));
+            if (!ok || cudaEventRecord(hp->landed[i], hp->in) != cudaSuccess ||
+                cudaStreamWaitEvent(st, hp->landed[i], 0) != cudaSuccess)
+                return DN_ERR_CUDA;
+            dn_shape seg = *s;
+            seg.T = (int32_t)ts;
+            const float *h0i = i == 0 ? (const float *)dh0 : (const float *)dst2[(i - 1) & 1];
+            float *hTi = i == S - 1 ? (hT ? (float *)dhT : nullptr) : (float *)dst2[i & 1];
+            // the status word is cleared by the first segment only, so that it keeps what any
+            // segment flags
+            rc = fwd_impl(&seg, dq + off * kb, dk + off * kb, dvv + off * vb, db + off * es,
+                          dgate ? (const float *)(dgate + off * gb) : nullptr, h0i, dout + off * vb, hTi, ws,
+                          ws_bytes, stream, true, true, nullptr, i == 0);
+            if (rc != DN_OK) return rc;
+            if (cudaEventRecord(hp->done[i], st) != cudaSuccess || cudaStreamWaitEvent(hp->out, hp->done[i], 0) != cudaSuccess)
+                return DN_ERR_CUDA;
+            if (!copy2d((char *)o + t0 * vb, T * vb, dout + off * vb, ts * vb, ts * vb, BH, D2H, hp->out))
+                return DN_ERR_CUDA;
+        }
+        if (hT && cudaMemcpyAsync(hT, dhT, sbytes, D2H, hp->out) != cudaSuccess) return DN_ERR_CUDA;
+        if (cudaEventRecord(hp->join, hp->out) != cudaSuccess || cudaStreamWaitEvent(st, hp->join, 0) != cudaSuccess)
+            return DN_ERR_CUDA;
+        return DN_OK;
+    }
     struct { void *dst; const void *src; size_t n; } cp[] = {
         {dq, q, tok * g.dk * es}, {dk, k, tok * g.dk * es}, {dvv, v, tok * g.dv * es},
         {db, beta, tok * es}, {dgate, gate, tok * sizeof(float)}, {dh0, h0, sbytes}};

@@ -203,15 +203,32 @@ dn_status gdn_decode_step(const dn_shape *shape, const void *q, const void *k, c
 dn_status dn_state_affine(const float *A, const float *S, const float *B, float *out, int count,
                           int dk, int dv, void *stream);
 
-/* Bytes of the device staging arena gdn_chunk_fwd_host needs (0 on bad args). */
+/* Bytes of the device staging arena gdn_chunk_fwd_host needs (0 on bad args):
+ * the inputs, o, h0 and hT, and two more states for the time segments.      */
 size_t dn_host_arena_size(const dn_shape *shape, int gated, int with_h0);
 
 /* Gated DeltaNet forward on HOST buffers: copies q, k, v, beta, g, h0 (host,
  * pinned for asynchronous copies) into `arena` (device, >= dn_host_arena_size
- * bytes), runs gdn_chunk_fwd on `stream`, and copies o and hT back into the
+ * bytes), runs the forward on `stream`, and copies o and hT back into the
  * host buffers.  Returns once the work is enqueued: synchronise `stream`
  * before reading o / hT.  g, h0, hT may be NULL as in gdn_chunk_fwd; for
- * packed input shape->cu_seqlens must still be a DEVICE pointer.            */
+ * packed input shape->cu_seqlens must still be a DEVICE pointer.
+ * Fixed-length input of at least 32 chunks runs as up to 4 time segments of
+ * whole chunks, so that the copies over the host link overlap the compute:
+ *  - segment i's inputs go into the arena on a stream of the library's own;
+ *  - segment i's forward runs on `stream` from the state segment i - 1 left
+ *    (fp32, in the arena);
+ *  - segment i's o goes back on a second stream of the library's own.
+ * `stream` waits for those streams (events) before the call's work on it
+ * ends, so that completing `stream` means o and hT are on the host.
+ * Consequences:
+ *  - The results equal one forward over the whole sequence up to the fp32
+ *    rounding of the state between segments.
+ *  - The device status word (dn_device_status) keeps what any segment flags.
+ *  - The library's streams and events for this are made on the first such
+ *    call in each context; make that call before any stream capture.
+ *  - Calls from several host threads are enqueued one at a time.
+ * Packed input runs as one forward between the copies.                      */
 dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k,
                              const void *v, const void *beta, const float *g,
                              const float *h0, void *o, float *hT, void *arena,

@@ -1,7 +1,7 @@
 """gdn_chunk_fwd_host: the forward on host (pinned) buffers, against the oracle and
 against gdn_chunk_fwd on the same inputs, with and without gate, initial and
 final state, on the tcgen05 kernels (bf16, d = 128) and the general kernels
-(fp32)."""
+(fp32), as one forward and as time segments whose copies overlap the compute."""
 import numpy as np
 import pytest
 import torch
@@ -52,11 +52,16 @@ def _inputs(B, H, T, d, dtype, gated, with_h0, seed):
     return workloads.generate(w)
 
 
+# Fixed-length input of at least 32 chunks runs as time segments whose copies overlap the
+# compute (up to 4 segments of >= 16 chunks, the state handed on between them); shorter
+# input runs as one forward.
 @pytest.mark.parametrize("B,H,T,d,dtype,gated,with_h0", [
-    (2, 3, 4133, 128, "bf16", True, True),     # ragged last chunk
-    (1, 2, 2048, 128, "bf16", False, False),   # DeltaNet, zero initial state
-    (2, 2, 300, 128, "bf16", True, True),
-    (1, 2, 2100, 64, "f32", True, True),       # general fp32 kernels
+    (2, 3, 4133, 128, "bf16", True, True),     # ragged last chunk; 4 segments, the last ragged
+    (1, 2, 2048, 128, "bf16", False, False),   # DeltaNet, zero initial state; 2 segments
+    (2, 2, 300, 128, "bf16", True, True),      # one forward
+    (1, 2, 2100, 64, "f32", True, True),       # general fp32 kernels; 2 segments
+    (1, 2, 8229, 128, "bf16", True, True),     # 4 segments of 33 chunks, the last 1893 tokens
+    (1, 1, 4100, 64, "f32", True, False),      # fp32, 4 segments, zero initial state
 ])
 def test_host_forward_matches_oracle_and_device_path(B, H, T, d, dtype, gated, with_h0):
     x = _inputs(B, H, T, d, dtype, gated, with_h0, seed=T + d)
@@ -75,3 +80,28 @@ def test_host_forward_without_final_state():
     ho, _ = _host_forward(x, want_hT=False)
     do, _ = _device_forward(x)
     assert rel(ho, do) <= TOL["bf16"]
+
+
+def test_host_forward_reuses_its_arena():
+    """Two segmented calls in a row on the same arena and stream, the second on other
+    inputs: the second call's copies into the arena wait for the first call's work."""
+    xa = _inputs(1, 2, 4096, 128, "bf16", True, True, seed=11)
+    xb = _inputs(1, 2, 4096, 128, "bf16", True, True, seed=12)
+    from chunkwise_delta_rule_02_gb300 import binding
+    pins = [{k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("q", "k", "v", "beta", "g", "h0")
+                 else v) for k, v in x.items()} for x in (xa, xb)]
+    shape = binding.make_shape(pins[0]["q"], pins[0]["v"])
+    arena = torch.empty(binding.dn_host_arena_size(shape, True, True), dtype=torch.uint8, device=DEV)
+    ws = binding.alloc_workspace(shape, False, DEV)
+    outs = []
+    stream = torch.cuda.current_stream()
+    for pin in pins:
+        o = torch.full(tuple(pin["v"].shape), float("nan"), dtype=pin["v"].dtype).pin_memory()
+        hT = torch.full((1, 2, 128, 128), float("nan")).pin_memory()
+        binding.gdn_chunk_fwd_host(shape, pin["q"], pin["k"], pin["v"], pin["beta"], pin["g"], pin["h0"], o,
+                                   hT, arena, ws, stream)
+        outs.append((o, hT))
+    stream.synchronize()
+    for x, (o, hT) in zip((xa, xb), outs):
+        do, dh = _device_forward(x)
+        assert rel(o.float().numpy(), do) <= TOL["bf16"] and rel(hT.numpy(), dh) <= TOL["bf16"]
