@@ -105,3 +105,35 @@ def test_host_forward_reuses_its_arena():
     for x, (o, hT) in zip((xa, xb), outs):
         do, dh = _device_forward(x)
         assert rel(o.float().numpy(), do) <= TOL["bf16"] and rel(hT.numpy(), dh) <= TOL["bf16"]
+
+
+def test_segments_keep_a_timeout_flagged_by_an_earlier_segment(monkeypatch):
+    """The status word is cleared by the first segment only.  With T = 8229 the call runs
+    as segments of 33, 33, 33 and 30 chunks; with two heads the cooperative kernel numbers
+    its tasks 2 x chunk + head, so the test hook's task 62 (chunk 31 of head 0) is withheld
+    in the first three segments and does not exist in the last, which completes cleanly:
+    the call still reports the timeout, and the next call is correct."""
+    from chunkwise_delta_rule_02_gb300 import binding
+    x = _inputs(1, 2, 8229, 128, "bf16", True, True, seed=13)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) and k in ("q", "k", "v", "beta", "g", "h0")
+               else v) for k, v in x.items()}
+    shape = binding.make_shape(pin["q"], pin["v"])
+    if binding.dn_plan(shape)[0] != binding.DN_PATH_COOP:
+        pytest.skip("the cooperative kernel is not available on this device")
+    arena = torch.empty(binding.dn_host_arena_size(shape, True, True), dtype=torch.uint8, device=DEV)
+    ws = binding.alloc_workspace(shape, False, DEV)
+    o = torch.empty(tuple(x["v"].shape), dtype=x["v"].dtype).pin_memory()
+    hT = torch.empty((1, 2, 128, 128)).pin_memory()
+    stream = torch.cuda.current_stream()
+    monkeypatch.setenv("GDN_DEBUG_WITHHOLD_TASK", "62")
+    binding.gdn_chunk_fwd_host(shape, pin["q"], pin["k"], pin["v"], pin["beta"], pin["g"], pin["h0"], o, hT,
+                               arena, ws, stream)
+    stream.synchronize()
+    assert binding.dn_device_status(ws) == binding.DN_ERR_TIMEOUT
+    monkeypatch.delenv("GDN_DEBUG_WITHHOLD_TASK")
+    binding.gdn_chunk_fwd_host(shape, pin["q"], pin["k"], pin["v"], pin["beta"], pin["g"], pin["h0"], o, hT,
+                               arena, ws, stream)
+    stream.synchronize()
+    assert binding.dn_device_status(ws) == binding.DN_OK
+    do, dh = _device_forward(x)
+    assert rel(o.float().numpy(), do) <= TOL["bf16"] and rel(hT.numpy(), dh) <= TOL["bf16"]
