@@ -221,24 +221,69 @@ __device__ __forceinline__ void bgemm(int M, int N, int K, FA A, FB B, FS St)
         rgemm<TM, TN>(M, N, K, A, B, St);
 }
 
-// Column-parallel forward substitution: X = (I + A)^-1 diag(d), A strictly lower
-// (len x len, row stride ld).  Thread j solves column j on its own.
-__device__ __forceinline__ void unit_lower_solve(const float *A, float *X, const float *d,
-                                                 int len, int ld)
+// X = (I + A)^-1 diag(d) for the unit lower triangular I + A: A strictly lower in rows
+// and columns [0, len) (row stride ld, other entries ignored), d the column scales (or
+// null: none).  X is written on and below the diagonal and zero above it, rows and
+// columns [0, len).  Blocked by 16: the diagonal blocks Y_b = (I + A_bb)^-1 by
+// substitution (a thread per column), then block row b after block row, every block
+// left of the diagonal at once, X_bc = -Y_b sum_{k=c..b-1} A_bk X_kc (a thread per
+// column, the block's 16 rows in registers), all in fp32.  Every thread of the block
+// calls it (barriers inside).
+__device__ __noinline__ void unit_lower_solve(const float *A, float *X, const float *d, int len, int ld)
 {
-    for (int jc = threadIdx.x; jc < len; jc += blockDim.x) {
-        for (int r = 0; r < len; ++r) {
+    const int nb = (len + 15) >> 4;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int t = tid; t < nb * 16; t += nt) {
+        const int b = t >> 4, c = (b << 4) + (t & 15);
+        if (c >= len) continue;
+        const int r1 = min(len, (b + 1) << 4);
+        for (int r = b << 4; r < r1; ++r) {
             float x;
-            if (r < jc) {
+            if (r < c) {
                 x = 0.f;
-            } else if (r == jc) {
-                x = d ? d[jc] : 1.f;
+            } else if (r == c) {
+                x = 1.f;
             } else {
                 float s = 0.f;
-                for (int i = jc; i < r; ++i) s = fmaf(A[r * ld + i], X[i * ld + jc], s);
+                for (int i = c; i < r; ++i) s = fmaf(A[r * ld + i], X[i * ld + c], s);
                 x = -s;
             }
-            X[r * ld + jc] = x;
+            X[r * ld + c] = x;
+        }
+    }
+    for (int t = tid; t < len * len; t += nt) {
+        const int r = t / len, c = t - r * len;
+        if ((c >> 4) > (r >> 4)) X[r * ld + c] = 0.f;
+    }
+    __syncthreads();
+    for (int b = 1; b < nb; ++b) {
+        const int r0 = b << 4, rows = min(16, len - r0);
+        for (int c = tid; c < r0; c += nt) {
+            float z[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) z[rr] = 0.f;
+            for (int i = c; i < r0; ++i) {
+                const float xi = X[i * ld + c];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr)
+                    if (rr < rows) z[rr] = fmaf(A[(r0 + rr) * ld + i], xi, z[rr]);
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                if (rr < rows) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int m = 0; m <= rr; ++m) s = fmaf(X[(r0 + rr) * ld + r0 + m], z[m], s);
+                    X[(r0 + rr) * ld + c] = -s;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (d) {
+        for (int t = tid; t < len * len; t += nt) {
+            const int r = t / len, c = t - r * len;
+            if (c <= r) X[r * ld + c] *= d[c];
         }
     }
 }
