@@ -576,6 +576,19 @@ int host_segments(const Geo &g)
     return n < 1 ? 1 : (n > kMaxSegments ? kMaxSegments : n);
 }
 
+// Head groups for the pipelined host path with packed input (1: none).  Packed tensors
+// are [H][T] rows, so a group of heads is one contiguous block of each, and heads are
+// independent: each group is a forward over its heads, its copies overlapping the
+// others' compute.  (Packed input cannot be cut along time here: its sequence bounds are
+// on the device.)  A group's beta rows must start 16-byte aligned in the arena.
+int host_head_groups(const Geo &g)
+{
+    if (!g.varlen || g.T <= 0 || (g.T + g.C - 1) / g.C < 2 * kMinSegmentChunks) return 1;
+    for (int G = kMaxSegments; G >= 2; --G)
+        if (g.H % G == 0 && ((size_t)g.T * (g.H / G)) % 8 == 0) return G;
+    return 1;
+}
+
 // The device's streams and events for the pipeline, made on first use in each context.
 // Called with g_pipe_mu held.
 HostPipe *host_pipe()
@@ -681,6 +694,55 @@ dn_status gdn_chunk_fwd_host(const dn_shape *s, const void *q, const void *k, co
                 return DN_ERR_CUDA;
         }
         if (hT && cudaMemcpyAsync(hT, dhT, sbytes, D2H, hp->out) != cudaSuccess) return DN_ERR_CUDA;
+        if (cudaEventRecord(hp->join, hp->out) != cudaSuccess || cudaStreamWaitEvent(st, hp->join, 0) != cudaSuccess)
+            return DN_ERR_CUDA;
+        return DN_OK;
+    }
+    const int ngrp = host_head_groups(g);
+    if (ngrp > 1) {
+        // packed input: group i is heads [i Hg, (i + 1) Hg), contiguous in every [H][T] tensor;
+        // its states are [N][Hg][dk][dv] in the arena, strided [N][H][dk][dv] on the host
+        std::lock_guard<std::mutex> lock(g_pipe_mu);
+        HostPipe *hp = host_pipe();
+        if (!hp) return DN_ERR_CUDA;
+        const int Hg = g.H / ngrp;
+        const size_t per = (size_t)Hg * g.T;   // token rows of a group
+        const size_t kb = (size_t)g.dk * es, vb = (size_t)g.dv * es, gb = sizeof(float);
+        const size_t srow = (size_t)g.dk * g.dv * sizeof(float);   // one (sequence, head) state
+        const size_t sgrp = (size_t)g.N * Hg * srow;
+        const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+        if (cudaEventRecord(hp->fork, st) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->out, hp->fork, 0) != cudaSuccess)
+            return DN_ERR_CUDA;
+        for (int i = 0; i < ngrp; ++i) {
+            const size_t t0 = per * i;
+            const bool ok =
+                cudaMemcpyAsync(dq + t0 * kb, (const char *)q + t0 * kb, per * kb, H2D, hp->in) == cudaSuccess &&
+                cudaMemcpyAsync(dk + t0 * kb, (const char *)k + t0 * kb, per * kb, H2D, hp->in) == cudaSuccess &&
+                cudaMemcpyAsync(dvv + t0 * vb, (const char *)v + t0 * vb, per * vb, H2D, hp->in) == cudaSuccess &&
+                cudaMemcpyAsync(db + t0 * es, (const char *)beta + t0 * es, per * es, H2D, hp->in) == cudaSuccess &&
+                (!dgate || cudaMemcpyAsync(dgate + t0 * gb, (const char *)gate + t0 * gb, per * gb, H2D, hp->in) ==
+                               cudaSuccess) &&
+                (!dh0 || copy2d(dh0 + i * sgrp, Hg * srow, (const char *)h0 + (size_t)i * Hg * srow, (size_t)g.H * srow,
+                                Hg * srow, (size_t)g.N, H2D, hp->in));
+            if (!ok || cudaEventRecord(hp->landed[i], hp->in) != cudaSuccess ||
+                cudaStreamWaitEvent(st, hp->landed[i], 0) != cudaSuccess)
+                return DN_ERR_CUDA;
+            dn_shape sub = *s;
+            sub.H = Hg;
+            // the status word is cleared by the first group only
+            rc = fwd_impl(&sub, dq + t0 * kb, dk + t0 * kb, dvv + t0 * vb, db + t0 * es,
+                          dgate ? (const float *)(dgate + t0 * gb) : nullptr, dh0 ? (const float *)(dh0 + i * sgrp) : nullptr,
+                          dout + t0 * vb, hT ? (float *)(dhT + i * sgrp) : nullptr, ws, ws_bytes, stream, true, true,
+                          nullptr, i == 0);
+            if (rc != DN_OK) return rc;
+            if (cudaEventRecord(hp->done[i], st) != cudaSuccess || cudaStreamWaitEvent(hp->out, hp->done[i], 0) != cudaSuccess)
+                return DN_ERR_CUDA;
+            if (cudaMemcpyAsync((char *)o + t0 * vb, dout + t0 * vb, per * vb, D2H, hp->out) != cudaSuccess ||
+                (hT && !copy2d((char *)hT + (size_t)i * Hg * srow, (size_t)g.H * srow, dhT + i * sgrp, Hg * srow,
+                               Hg * srow, (size_t)g.N, D2H, hp->out)))
+                return DN_ERR_CUDA;
+        }
         if (cudaEventRecord(hp->join, hp->out) != cudaSuccess || cudaStreamWaitEvent(st, hp->join, 0) != cudaSuccess)
             return DN_ERR_CUDA;
         return DN_OK;

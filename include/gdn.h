@@ -228,7 +228,11 @@ size_t dn_host_arena_size(const dn_shape *shape, int gated, int with_h0);
  *  - The library's streams and events for this are made on the first such
  *    call in each context; make that call before any stream capture.
  *  - Calls from several host threads are enqueued one at a time.
- * Packed input runs as one forward between the copies.                      */
+ * Packed input of at least 32 chunks runs instead as up to 4 groups of heads
+ * (H divisible by their number), each group's rows of every [H][T] tensor one
+ * contiguous copy and its states copied from and into their [N][H] places;
+ * heads are independent, so the results equal one forward's.  Other packed
+ * input runs as one forward between the copies.                            */
 dn_status gdn_chunk_fwd_host(const dn_shape *shape, const void *q, const void *k,
                              const void *v, const void *beta, const float *g,
                              const float *h0, void *o, float *hT, void *arena,

@@ -137,3 +137,36 @@ def test_segments_keep_a_timeout_flagged_by_an_earlier_segment(monkeypatch):
     assert binding.dn_device_status(ws) == binding.DN_OK
     do, dh = _device_forward(x)
     assert rel(o.float().numpy(), do) <= TOL["bf16"] and rel(hT.numpy(), dh) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("H,lengths", [(4, [1000, 64, 0, 3000, 5, 1123]), (6, [2048, 2048])])
+def test_host_forward_packed_runs_as_head_groups(H, lengths):
+    """Packed input of >= 32 chunks runs as groups of heads whose copies overlap the
+    compute (H 4: four groups of one head; H 6: three groups of two), the states copied
+    per group from and into their [N][H] places; against the device path and the oracle,
+    with an empty and a one-token sequence among them."""
+    import chunkwise_delta_rule_02_gb300 as gdn
+    from chunkwise_delta_rule_02_gb300 import binding, workloads
+    w = workloads.Workload("hostv", 1, H, 0, 128, "bf16", True, True, 21, varlen_total=1, varlen_n=1)
+    x = workloads.generate(w, lengths=lengths)
+    pin = {k: x[k].pin_memory() for k in ("q", "k", "v", "beta", "g", "h0")}
+    cu = x["cu_seqlens"].to(DEV)
+    shape = binding.make_shape(pin["q"], pin["v"], 64, cu)
+    N = len(lengths)
+    o = torch.full(tuple(x["v"].shape), float("nan"), dtype=x["v"].dtype).pin_memory()
+    hT = torch.full((N, H, 128, 128), float("nan")).pin_memory()
+    arena = torch.empty(binding.dn_host_arena_size(shape, True, True), dtype=torch.uint8, device=DEV)
+    ws = binding.alloc_workspace(shape, False, DEV)
+    stream = torch.cuda.current_stream()
+    binding.gdn_chunk_fwd_host(shape, pin["q"], pin["k"], pin["v"], pin["beta"], pin["g"], pin["h0"], o, hT,
+                               arena, ws, stream)
+    stream.synchronize()
+    assert binding.dn_device_status(ws) == binding.DN_OK
+    d = to_dev(x, DEV)
+    od, hd = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    ho, hh = o.float().numpy(), hT.numpy()
+    assert np.isfinite(ho).all() and np.isfinite(hh).all()
+    assert rel(ho, od.float().cpu().numpy()) <= TOL["bf16"] and rel(hh, hd.cpu().numpy()) <= TOL["bf16"]
+    ro, rh = oracle_fwd(x)
+    assert rel(ho, ro) <= TOL["bf16"] and rel(hh, rh) <= TOL["bf16"]
