@@ -192,6 +192,26 @@ def test_saved_path_equals_the_recompute(lengths):
     assert binding.dn_workspace_size(shape, 2) < binding.dn_workspace_size(shape, 1)
 
 
+def test_saved_path_ungated_without_initial_state():
+    """DeltaNet (no gate) from a zero initial state through the saved path: dg is absent;
+    the other gradients (dh0 with respect to the zero state among them) equal the
+    recompute path's and match the oracle."""
+    import chunkwise_delta_rule_02_gb300 as gdn
+    x = _gen(2, 2, 200, seed=38, gated=False, with_h0=False)
+    d = _saved_case(x)
+    o, hT, saved = gdn.forward(d["q"], d["k"], d["v"], d["beta"], None, None, save=True)
+    a = gdn.backward(d["q"], d["k"], d["v"], d["beta"], None, None, d["do"], d["dhT"], saved=saved)
+    b = gdn.backward(d["q"], d["k"], d["v"], d["beta"], None, None, d["do"], d["dhT"])
+    torch.cuda.synchronize()
+    assert a["dg"] is None
+    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+        assert torch.equal(a[n], b[n]), n
+    ref = oracle_bwd(x)
+    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+        if ref[n] is not None:
+            assert rel(a[n].float().cpu().numpy(), ref[n]) <= TOL["bf16"], n
+
+
 def test_saved_path_refuses_other_shapes():
     """d 64: no saved path (dn_saved_size 0, DN_ERR_UNSUPPORTED)."""
     import chunkwise_delta_rule_02_gb300 as gdn

@@ -166,6 +166,35 @@ def test_longhorn_backward_varlen():
         _check(n, got[n], ref[n], TOL["bf16"])
 
 
+@pytest.mark.parametrize("l2,lengths", [(True, None), (False, [70, 1, 0, 190])])
+def test_longhorn_saved_path(l2, lengths):
+    """Longhorn's step size through the training path: forward(save=True) keeps the
+    chunk operands the cooperative forward prepared with it, backward(saved=...) starts
+    at the reverse scan over them.  The gradients equal the recompute path's (dg up to
+    the order of its atomic row sums) and match the oracle."""
+    import chunkwise_delta_rule_02_gb300 as gdn
+    x = _gen(2, 2, 333, 128, "bf16", seed=71, backward=True, l2=l2) if lengths is None else \
+        _gen(1, 2, 0, 128, "bf16", seed=72, backward=True, l2=l2, lengths=lengths)
+    d = to_dev(x, DEV)
+    kw = dict(cu_seqlens=d["cu_seqlens"], qk_l2norm=l2, longhorn=True)
+    if not gdn.saved_supported(d["q"], d["v"], cu_seqlens=d["cu_seqlens"]):
+        pytest.skip("no saved path on this device")
+    o1, h1, saved = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], save=True, **kw)
+    o2, h2 = gdn.forward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], **kw)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    a = gdn.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], None, d["do"], d["dhT"], saved=saved, **kw)
+    b = gdn.backward(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["do"], d["dhT"], **kw)
+    torch.cuda.synchronize()
+    for n in GRADS:
+        if n == "dg":
+            assert (a[n] - b[n]).abs().max() <= 1e-6 * b[n].abs().max()
+        else:
+            assert torch.equal(a[n], b[n]), n
+    ref = _oracle_bwd(x, l2=l2)
+    for n in GRADS:
+        _check(n, a[n].float().cpu().numpy(), ref[n], TOL["bf16"])
+
+
 @pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 64), ("bf16", 96, 30)])
 @pytest.mark.parametrize("l2", [True, False])
 def test_longhorn_decode_steps(dtype, dk, dv, l2):
