@@ -66,6 +66,21 @@ def test_workspace_size_and_validation(gdn):
     assert gdn.dn_workspace_size(_shape(gdn, B=1, cu=16, N=3), False) > 0
 
 
+def test_host_arena_size(gdn):
+    """gdn_chunk_fwd_host's device arena: q, k, v, o, beta, g and the states each in a
+    256-byte aligned block, the states being h0, h_T and the two that carry the state
+    between the time segments of the pipelined call; 0 on bad arguments."""
+    a256 = lambda n: (n + 255) // 256 * 256
+    B, H, T, d = 2, 3, 1000, 128
+    s = _shape(gdn, B=B, H=H, T=T, d=d)
+    tok, st = B * H * T, B * H * d * d * 4
+    base = 4 * a256(tok * d * 2) + a256(tok * 2) + 3 * a256(st)   # q k v o, beta, hT + 2 between
+    assert gdn.dn_host_arena_size(s, False, False) == base
+    assert gdn.dn_host_arena_size(s, True, False) == base + a256(tok * 4)
+    assert gdn.dn_host_arena_size(s, True, True) == base + a256(tok * 4) + a256(st)
+    assert gdn.dn_host_arena_size(_shape(gdn, B=0), True, True) == 0
+
+
 def test_beta_mode_is_validated(gdn):
     """DN_BETA_DELTA and DN_BETA_LONGHORN are the two step-size modes; any other value
     is rejected before any device work, and Longhorn's needs no extra workspace
