@@ -362,6 +362,47 @@ def record_traffic(csv_path: str, kernel: str, workload: str, capture: str, out:
     return d[kernel + "@" + workload]
 
 
+STEP_KERNELS = ("k_coop_fwd", "k_bscan_tc", "k_bwd_tc")   # one step of the training path
+
+
+def record_step_traffic(csv_path: str, workload: str, capture: str, out: str = None) -> dict:
+    """Write profiles/traffic.json's entry for one whole forward+backward step: the read +
+    write DRAM bytes of one launch of each of STEP_KERNELS in an ncu CSV (exactly one each),
+    stamped with the hash of every kernel source ("step@workload")."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hdr = next(r for r in rows if "Metric Name" in r)
+    start = rows.index(hdr) + 1
+    ii, ki, mi, vi = hdr.index("ID"), hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    launches = {}   # launch id -> (step kernel, {metric: value})
+    for r in rows[start:]:
+        if len(r) <= vi:
+            continue
+        name = next((k for k in STEP_KERNELS if k in r[ki]), None)
+        if name is None:
+            continue
+        launches.setdefault(r[ii], (name, {}))[1][r[mi]] = float(r[vi].replace(",", ""))
+    names = sorted(n for n, _ in launches.values())
+    if names != sorted(STEP_KERNELS):
+        raise SystemExit("need exactly one launch of each of %s in %s, found %s" % (STEP_KERNELS, csv_path, names))
+    rd = wr = 0
+    for _, m in launches.values():
+        if "dram__bytes_read.sum" not in m or "dram__bytes_write.sum" not in m:
+            raise SystemExit("no dram byte counters in %s" % csv_path)
+        rd += int(m["dram__bytes_read.sum"])
+        wr += int(m["dram__bytes_write.sum"])
+    p = out or os.path.join(ROOT, "profiles", "traffic.json")
+    d = json.load(open(p)) if os.path.exists(p) else {}
+    d["step@" + workload] = {
+        "dram_bytes_per_launch": rd + wr, "dram_read": rd, "dram_write": wr,
+        "source_sha": kernel_source_sha("step"), "sources": "csrc/*, include/gdn.h",
+        "kernels": ", ".join(STEP_KERNELS), "capture": capture}
+    with open(p, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return d["step@" + workload]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch recorded from an ncu capture of this exact kernel source
     (profiles/traffic.json), scaled to the workload; None if absent or stale."""
@@ -660,7 +701,11 @@ def main():
     args = ap.parse_args()
 
     if args.record_traffic:
-        print(json.dumps(record_traffic(args.record_traffic, "k_coop_fwd", args.workload, args.capture)))
+        from chunkwise_delta_rule_02_gb300 import workloads
+        if workloads.WORKLOADS[args.workload].backward:
+            print(json.dumps(record_step_traffic(args.record_traffic, args.workload, args.capture)))
+        else:
+            print(json.dumps(record_traffic(args.record_traffic, "k_coop_fwd", args.workload, args.capture)))
         return
 
     if args.workload == DECODE_WORKLOAD:
@@ -836,7 +881,7 @@ def main():
     # a single forward kernel is timed back to back on its own (burst tensor peak); the
     # forward+backward step is a sequence of kernels (sustained tensor peak)
     roof = roofline(abytes, flops, ms, pk, src, sustained=w.backward)
-    roof["traffic"] = None if w.backward else recorded_traffic(kname, w.name)
+    roof["traffic"] = recorded_traffic("step", w.name) if w.backward else recorded_traffic(kname, w.name)
     roof["kernel"] = kdesc
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

@@ -6,6 +6,8 @@ import os
 import socket
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -222,6 +224,31 @@ def test_forward_counts_of_the_headline_workload():
     th = 4 * 16 * 128
     assert bench.algorithmic_flops(w, x) == th * (6 * 128 * 128 + 10 * 64 * 128) + 4 * 16 * 2 * (2 * 64 ** 3 // 3)
     assert bench.algorithmic_bytes(w, x) == th * 1030 + 2 * 4 * 16 * 128 * 128 * 4
+
+
+def test_record_step_traffic_sums_one_launch_of_each_kernel(tmp_path):
+    """The forward+backward step's traffic entry sums one launch each of the cooperative
+    forward, the reverse scan and the per-chunk gradients, stamped with the hash of every
+    kernel source; a capture with a kernel missing or repeated is refused."""
+    import bench
+    head = '"ID","Process ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+    def row(i, k, m, v):
+        return '"%d","1","%s","%s","byte","%s"\n' % (i, k, m, v)
+    rows = [row(0, "k_other(int)", "dram__bytes_read.sum", "5")]
+    for i, (k, rd, wr) in enumerate((("coop::k_coop_fwd<Cfg<64, 128>>(x)", "1,000", "24"),
+                                     ("gdn::bsc::k_bscan_tc(x)", "300", "200"),
+                                     ("gdn::btc::k_bwd_tc(x)", "2,000", "100")), start=1):
+        rows += [row(i, k, "dram__bytes_read.sum", rd), row(i, k, "dram__bytes_write.sum", wr)]
+    csv_path = tmp_path / "s.csv"
+    csv_path.write_text("==PROF== noise\n" + head + "".join(rows))
+    out = tmp_path / "traffic.json"
+    e = bench.record_step_traffic(str(csv_path), "fb", "ncu ...", out=str(out))
+    assert e["dram_read"] == 3300 and e["dram_write"] == 324 and e["dram_bytes_per_launch"] == 3624
+    assert e["source_sha"] == bench.kernel_source_sha("step")
+    bad = tmp_path / "b.csv"
+    bad.write_text(head + "".join(rows[:5]))   # the gradients kernel missing
+    with pytest.raises(SystemExit):
+        bench.record_step_traffic(str(bad), "fb", "ncu ...", out=str(out))
 
 
 def test_record_traffic_reads_one_launch_and_stamps_the_source(tmp_path):
